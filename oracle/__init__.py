@@ -1,0 +1,151 @@
+"""CPU oracle for the FP16 TN GEMM ``D = A @ B.T`` and the M=1 GEMV ``y = x @ W.T``.
+
+TEST INFRASTRUCTURE ONLY.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline / reference leg of ``bench.py`` may import this package.  It shares
+no code with the CUDA library in ``tma_pipelined_tensor_tn_gb300`` and imports
+nothing from it.
+
+The arithmetic lives in ``oracle.c`` (plain C, FP64 accumulation, k ascending,
+one IEEE 754 round-to-nearest-even to binary16 at the end).  This module builds
+that file with gcc and marshals numpy ``uint16`` (raw binary16 bits) arrays to it.
+
+Definition followed (see the header of ``oracle.c`` for the passages):
+"使用 TMA 为 GEMM 建立 Pipeline", step 4 "完整 Kernel" (A (M,K), B (N,K), D (M,N),
+FP32 accumulate, FP16 out); "Learning TileLang with GEMV", §01 GEMV (y = x W^T,
+W N x K row-major, FP32 accumulate).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile ``oracle.c`` into ``liboracle.so`` (gcc, -O2, OpenMP if available)."""
+    if (not force and os.path.exists(_LIB)
+            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+        return _LIB
+    base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", _SRC, "-o", _LIB + ".tmp", "-lm"]
+    # -fno-fast-math keeps IEEE semantics; no -march flags so x86 and Arm agree.
+    try:
+        subprocess.run(base[:1] + ["-fopenmp", "-fno-fast-math"] + base[1:],
+                       check=True, capture_output=True)
+    except subprocess.CalledProcessError:
+        subprocess.run(base[:1] + ["-fno-fast-math"] + base[1:], check=True,
+                       capture_output=True)
+    os.replace(_LIB + ".tmp", _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            i64, p = ctypes.c_int64, ctypes.c_void_p
+            lib.oracle_half_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_half_to_double.restype = ctypes.c_double
+            lib.oracle_double_to_half.argtypes = [ctypes.c_double]
+            lib.oracle_double_to_half.restype = ctypes.c_uint16
+            lib.oracle_max_threads.argtypes = []
+            lib.oracle_max_threads.restype = ctypes.c_int
+            lib.oracle_gemm_f16.argtypes = [i64, i64, i64, p, p, p, p, ctypes.c_int]
+            lib.oracle_gemm_f16.restype = ctypes.c_int
+            lib.oracle_gemm_f16_at.argtypes = [i64, i64, i64, p, p, i64, p, p, p, p,
+                                               ctypes.c_int]
+            lib.oracle_gemm_f16_at.restype = ctypes.c_int
+            lib.oracle_gemv_f16.argtypes = [i64, i64, p, p, p, p, ctypes.c_int]
+            lib.oracle_gemv_f16.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def _bits(a: np.ndarray) -> np.ndarray:
+    """Accept float16 or uint16 arrays; return a C-contiguous uint16 view."""
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float16:
+        a = a.view(np.uint16)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected float16/uint16 bits, got {a.dtype}")
+    return a
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def max_threads() -> int:
+    return int(_load().oracle_max_threads())
+
+
+def half_to_double(h: int) -> float:
+    """Decode one binary16 bit pattern."""
+    return float(_load().oracle_half_to_double(int(h) & 0xFFFF))
+
+
+def double_to_half(x: float) -> int:
+    """Encode one double to binary16 bits, round to nearest, ties to even."""
+    return int(_load().oracle_double_to_half(float(x)))
+
+
+def gemm_f16(A, B, *, return_sum: bool = False, threads: int = 0):
+    """D = fp16_rne(A @ B.T) with FP64 accumulation.
+
+    A: (M, K) and B: (N, K) binary16 arrays (float16 or uint16 bits).
+    Returns D as float16 (M, N); with ``return_sum`` also the FP64 sums.
+    """
+    A, B = _bits(A), _bits(B)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("A and B must share K")
+    D = np.empty((M, N), dtype=np.uint16)
+    S = np.empty((M, N), dtype=np.float64) if return_sum else None
+    _load().oracle_gemm_f16(M, N, K, _ptr(A), _ptr(B), _ptr(D),
+                            _ptr(S) if S is not None else None, int(threads))
+    D = D.view(np.float16)
+    return (D, S) if return_sum else D
+
+
+def gemm_f16_at(A, B, ms, ns, *, return_sum: bool = False, threads: int = 0):
+    """D[ms[i], ns[i]] for sampled positions (same definition as ``gemm_f16``)."""
+    A, B = _bits(A), _bits(B)
+    M, K = A.shape
+    N, _ = B.shape
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    if ms.shape != ns.shape or ms.ndim != 1:
+        raise ValueError("ms and ns must be 1-D and equally long")
+    if ms.size and (ms.min() < 0 or ms.max() >= M or ns.min() < 0 or ns.max() >= N):
+        raise IndexError("sample position out of range")
+    out = np.empty(ms.shape, dtype=np.uint16)
+    S = np.empty(ms.shape, dtype=np.float64) if return_sum else None
+    _load().oracle_gemm_f16_at(M, N, K, _ptr(A), _ptr(B), ms.size, _ptr(ms), _ptr(ns),
+                               _ptr(out), _ptr(S) if S is not None else None, int(threads))
+    out = out.view(np.float16)
+    return (out, S) if return_sum else out
+
+
+def gemv_f16(x, W, *, return_sum: bool = False, threads: int = 0):
+    """y = fp16_rne(x @ W.T) with FP64 accumulation; x: (K,), W: (N, K)."""
+    x, W = _bits(x), _bits(W)
+    N, K = W.shape
+    if x.shape != (K,):
+        raise ValueError("x must have length K")
+    y = np.empty((N,), dtype=np.uint16)
+    S = np.empty((N,), dtype=np.float64) if return_sum else None
+    _load().oracle_gemv_f16(N, K, _ptr(x), _ptr(W), _ptr(y),
+                            _ptr(S) if S is not None else None, int(threads))
+    y = y.view(np.float16)
+    return (y, S) if return_sum else y
