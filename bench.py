@@ -1,0 +1,405 @@
+#!/usr/bin/env python
+"""Benchmark of the hot path: FP16 TN GEMM at M=N=K=4096 and the M=1 GEMV
+(N=4096, K=14336), both through the C ABI of libtmagemm.so.
+
+One step = one gemm_f16 launch (4096^3) + one gemv_f16 launch (4096 x 14336).
+Inputs are resident in HBM before timing; each kernel rotates through enough
+distinct input sets (> 2x L2) that every launch reads its operands from HBM.
+Per-kernel times come from CUDA events on the launching stream.
+
+Prints ONE JSON line (rank 0).  `value` is the GEMM's TFLOP/s over all ranks;
+the GEMV's GB/s is in `gemv`.  `--impl reference` times the CPU oracle instead
+(the only reference that exists for this path) on a bounded sample.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "FP16 GEMM TFLOP/s at 4096³ (% of dense peak); M=1 GEMV HBM GB/s"
+GEMM_M = GEMM_N = GEMM_K = 4096
+GEMV_N, GEMV_K = 4096, 14336
+WORKLOAD = ("gemm_f16 TN D=A*B^T M=N=K=4096, A,B ~ U[-1,1] fp16, fp32 accumulate, fp16 out; "
+            "+ gemv_f16 y=x*W^T N=4096 K=14336, x,W ~ N(0,0.02) fp16")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+KERNEL_SOURCES = ["tma_pipelined_tensor_tn_gb300/csrc/gemm_tn.cu",
+                  "tma_pipelined_tensor_tn_gb300/csrc/gemv.cu",
+                  "tma_pipelined_tensor_tn_gb300/csrc/ptx.cuh",
+                  "tma_pipelined_tensor_tn_gb300/csrc/tile_sched.cuh"]
+
+
+def gemm_flops(M=GEMM_M, N=GEMM_N, K=GEMM_K):
+    return 2.0 * M * N * K
+
+
+def gemm_bytes(M=GEMM_M, N=GEMM_N, K=GEMM_K):
+    return 2.0 * (M * K + N * K + M * N)
+
+
+def gemv_bytes(N=GEMV_N, K=GEMV_K):
+    """Algorithmic bytes: W (N*K) + x (K) + y (N) fp16 elements, each once."""
+    return 2.0 * (N * K + K + N)
+
+
+def sources_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(key):
+    """DRAM bytes per launch from a committed ncu summary, if the kernel sources
+    have not changed since it was taken."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    e = d.get(key)
+    if not e or e.get("sources_hash") != sources_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks ----
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.err = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError as e:
+            self.err = str(e)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": self.err or "no nvidia-smi"}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+                power.append(float(parts[3]))
+            except ValueError:
+                continue
+            for name, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "no samples"}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------- CPU oracle ----
+
+def oracle_gemm_sample(rows, A_np, B_np, threads=0):
+    """Oracle on the first `rows` rows of the 4096^3 GEMM; returns (s, threads)."""
+    import oracle
+    oracle.build()
+    t0 = time.perf_counter()
+    oracle.gemm_f16(A_np[:rows], B_np, threads=threads)
+    dt = time.perf_counter() - t0
+    return dt, oracle.max_threads() if threads <= 0 else threads
+
+
+def cpu_baseline(target_s=12.0):
+    """Time the oracle, as it stands, on a bounded sample of the 4096^3 GEMM."""
+    import oracle
+    from tma_pipelined_tensor_tn_gb300 import inputs
+    A, B = inputs.gemm_inputs(GEMM_M, GEMM_N, GEMM_K, seed=0)
+    A_np, B_np = A.numpy(), B.numpy()
+    dt, cores = oracle_gemm_sample(8, A_np, B_np)            # calibrate
+    rows = int(max(8, min(GEMM_M, 8 * target_s / max(dt, 1e-3))))
+    dt, cores = oracle_gemm_sample(rows, A_np, B_np)
+    tflops = gemm_flops(rows, GEMM_N, GEMM_K) / dt / 1e12
+    return {"value": tflops, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {rows} of 4096 rows of D for the 4096^3 GEMM "
+                      f"({rows}x4096x4096 FP64 MACs, {dt:.1f} s)"}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the CPU oracle, as it stands, on a bounded sample."""
+    if rank != 0:
+        return 0
+    import oracle
+    from tma_pipelined_tensor_tn_gb300 import inputs
+    oracle.build()
+    A, B = inputs.gemm_inputs(GEMM_M, GEMM_N, GEMM_K, seed=0)
+    A_np, B_np = A.numpy(), B.numpy()
+    x, W = inputs.gemv_inputs(GEMV_N, GEMV_K, seed=0)
+    x_np, W_np = x.numpy(), W.numpy()
+    # size a step at about 1.5 s of oracle work
+    dt, cores = oracle_gemm_sample(8, A_np, B_np)
+    rows = int(max(8, min(GEMM_M, 8 * 1.5 / max(dt, 1e-3))))
+    for _ in range(args.warmup):
+        oracle.gemm_f16(A_np[:rows], B_np)
+    gemm_t = gemv_t = 0.0
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.gemm_f16(A_np[:rows], B_np)
+        t1 = time.perf_counter()
+        oracle.gemv_f16(x_np, W_np)
+        t2 = time.perf_counter()
+        gemm_t += t1 - t0
+        gemv_t += t2 - t1
+    value = args.steps * gemm_flops(rows, GEMM_N, GEMM_K) / gemm_t / 1e12
+    gemv_gbs = args.steps * gemv_bytes() / gemv_t / 1e9
+    sample = (f"each step: rows 0..{rows - 1} of D for the 4096^3 GEMM ({rows}x4096x4096 FP64 MACs) "
+              f"+ the full 4096x14336 GEMV")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * (gemm_t + gemv_t) / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "reference": "CPU oracle (FP64, plain loops)",
+                   "sample_rows": rows},
+        "gemv": {"value": gemv_gbs, "unit": "GB/s"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- ours ----
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import tma_pipelined_tensor_tn_gb300 as tg
+    from tma_pipelined_tensor_tn_gb300 import inputs
+
+    tg.build()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    props = torch.cuda.get_device_properties(dev)
+    l2 = int(getattr(props, "L2_cache_size", 0) or 0) or 129 * 1024 * 1024
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+
+    # ---- resident inputs, rotated so that every launch misses L2 ----
+    A, B = inputs.gemm_inputs(GEMM_M, GEMM_N, GEMM_K, seed=rank)
+    x, W = inputs.gemv_inputs(GEMV_N, GEMV_K, seed=rank)
+    r_gemm = inputs.l2_rotation_count(int(gemm_bytes()), l2)
+    r_gemv = inputs.l2_rotation_count(int(gemv_bytes()), l2)
+    dA, dB = A.to(dev), B.to(dev)
+    gemm_sets = [(dA, dB, torch.empty((GEMM_M, GEMM_N), dtype=torch.float16, device=dev))]
+    for _ in range(r_gemm - 1):
+        gemm_sets.append((dA.clone(), dB.clone(),
+                          torch.empty((GEMM_M, GEMM_N), dtype=torch.float16, device=dev)))
+    dx, dW = x.to(dev), W.to(dev)
+    gemv_sets = [(dx, dW, torch.empty((GEMV_N,), dtype=torch.float16, device=dev))]
+    for _ in range(r_gemv - 1):
+        gemv_sets.append((dx.clone(), dW.clone(), torch.empty((GEMV_N,), dtype=torch.float16, device=dev)))
+    torch.cuda.synchronize(dev)
+
+    def step(i):
+        a, b, d = gemm_sets[i % r_gemm]
+        s1 = tg.gemm_f16(GEMM_M, GEMM_N, GEMM_K, a.data_ptr(), b.data_ptr(), d.data_ptr(), sh)
+        return s1
+
+    def step_gemv(i):
+        xv, wv, yv = gemv_sets[i % r_gemv]
+        return tg.gemv_f16(GEMV_N, GEMV_K, xv.data_ptr(), wv.data_ptr(), yv.data_ptr(), sh)
+
+    for i in range(args.warmup):
+        assert step(i) == 0 and step_gemv(i) == 0
+    tg.check(stream)
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    launches = 0
+    for i in range(args.steps):
+        ev[i][0].record(stream)
+        s1 = step(i)
+        ev[i][1].record(stream)
+        s2 = step_gemv(i)
+        ev[i][2].record(stream)
+        launches += 2
+        if s1 or s2:
+            raise RuntimeError(f"launch failed: {tg.strerror(s1 or s2)}")
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    wall = time.perf_counter() - t0
+    clk = clocks.stop()
+    tg.check(stream)
+
+    gemm_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    gemv_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    times = [sum(gemm_ms), sum(gemv_ms), wall]
+    if world > 1:
+        t = torch.tensor(times, dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        times = t.tolist()
+    gemm_total_ms, gemv_total_ms, wall = times
+
+    # ---- end to end through the C ABI: host buffers, copies inside the region ----
+    e2e_steps = max(3, min(args.steps, 10))
+    hA = A.pin_memory()
+    hB = B.pin_memory()
+    hD = torch.empty((GEMM_M, GEMM_N), dtype=torch.float16).pin_memory()
+    eA = torch.empty_like(dA)
+    eB = torch.empty_like(dB)
+    eD = torch.empty((GEMM_M, GEMM_N), dtype=torch.float16, device=dev)
+    for _ in range(2):   # warm-up of the copy path
+        eA.copy_(hA, non_blocking=True)
+        eB.copy_(hB, non_blocking=True)
+        tg.gemm_f16(GEMM_M, GEMM_N, GEMM_K, eA.data_ptr(), eB.data_ptr(), eD.data_ptr(), sh)
+        hD.copy_(eD, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        eA.copy_(hA, non_blocking=True)
+        eB.copy_(hB, non_blocking=True)
+        s = tg.gemm_f16(GEMM_M, GEMM_N, GEMM_K, eA.data_ptr(), eB.data_ptr(), eD.data_ptr(), sh)
+        if s:
+            raise RuntimeError(tg.strerror(s))
+        hD.copy_(eD, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = e0.elapsed_time(e1)
+    tg.check(stream)
+
+    peaks, peak_src = load_peaks()
+    gemm_avg_s = gemm_total_ms / 1e3 / args.steps
+    gemv_avg_s = gemv_total_ms / 1e3 / args.steps
+    value = world * args.steps * gemm_flops() / (gemm_total_ms / 1e3) / 1e12
+    achieved = gemm_flops() / gemm_avg_s / 1e12
+    peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    gemv_gbs = gemv_bytes() / gemv_avg_s / 1e9
+    peak_h = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": (gemm_total_ms + gemv_total_ms) / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f16", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "gemm": [GEMM_M, GEMM_N, GEMM_K],
+                   "gemv": [GEMV_N, GEMV_K],
+                   "l2": f"inputs larger than L2: {r_gemm} rotating GEMM sets and {r_gemv} "
+                         f"rotating GEMV sets ({l2 // 2**20} MiB L2)",
+                   "parallelism": f"replicas x{world}", "seed": "rank"},
+        "gemm": {"value": achieved, "unit": "TFLOP/s", "us_per_launch": gemm_avg_s * 1e6,
+                 "pct_of_dense_peak": 100.0 * achieved / peak_t},
+        "gemv": {"value": gemv_gbs, "unit": "GB/s", "us_per_launch": gemv_avg_s * 1e6,
+                 "pct_of_hbm_peak": 100.0 * gemv_gbs / peak_h},
+        "roofline": {"bound": "tensor", "kernel": "gemm_tn_f16_kernel", "achieved": achieved,
+                     "peak": peak_t, "unit": "TFLOP/s", "frac": achieved / peak_t,
+                     "traffic": load_traffic("gemm_tn_f16_kernel@gemm_4096"),
+                     "peak_source": f"{peak_src} bf16_tflops (burst; fp16 dense = bf16 dense)",
+                     "flops_per_launch": gemm_flops()},
+        "roofline_gemv": {"bound": "hbm", "kernel": "gemv_f16_kernel", "achieved": gemv_gbs,
+                          "peak": peak_h, "unit": "GB/s", "frac": gemv_gbs / peak_h,
+                          "traffic": load_traffic("gemv_f16_kernel@gemv_4096x14336"),
+                          "peak_source": f"{peak_src} hbm_gbs",
+                          "bytes_per_launch": gemv_bytes()},
+        "e2e": {"value": e2e_steps * gemm_flops() / (e2e_ms / 1e3) / 1e12 * world, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": int(hA.numel() * 2 + hB.numel() * 2),
+                "d2h_bytes_per_step": int(hD.numel() * 2),
+                "steps": e2e_steps, "what": "pinned host A,B -> device, gemm_f16, D -> pinned host"},
+        "gpu_launches": launches,
+        "wall_s_timed_region": wall,
+        "clocks": clk,
+        "device": props.name,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    try:
+        return run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch
+            torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,147 @@
+/*
+ * tmagemm — FP16 "TN" GEMM D = A * B^T and M = 1 GEMV for sm_103a (GB300).
+ *
+ * C ABI of libtmagemm.so.  Plain pointers and sizes only.  All matrices are
+ * dense row-major binary16 (IEEE fp16) with no padding between rows.
+ *
+ * Operation (both entry points): FP32 accumulation inside the kernel and one
+ * round-to-nearest-even conversion to fp16 per output element.
+ *   - GEMM and its operand layout: "使用 TMA 为 GEMM 建立 Pipeline" (Modern GPU
+ *     programming for MLSys), step 4 "完整 Kernel": A (M, K), B (N, K),
+ *     D (M, N), float32 accumulator, float16 output; the Croqtile chapter
+ *     "高级数据搬运：TMA、Swizzle 与不规则访问", section "示例：流水线矩阵乘法中的
+ *     TMA": matmul(lhs [M, K], rhs [N, K], output [M, N]).
+ *   - GEMV: "Learning TileLang with GEMV", §01 GEMV: y = x * W^T with W N x K
+ *     row-major (the nn.Linear weight layout), FP32 accumulation.
+ *   - Ragged edges: out-of-range operand elements are read as zero and
+ *     out-of-range outputs are never written ("高级数据搬运…", section
+ *     "零填充：.zfill"; TensorCore_GEMM_with_TMA §2.1: OOB fill NONE = zeros).
+ *
+ * Ownership: the caller owns every buffer.  The library allocates no device
+ * memory in any call.  A, B and D must not overlap.
+ *
+ * Execution: gemm_f16 / gemv_f16 validate their arguments on the host, enqueue
+ * one kernel on `stream` and return without synchronising.  A CUDA launch
+ * error is reported as TMAGEMM_ERR_CUDA.  A device-side wait that exceeds its
+ * time limit (a pipeline handshake that never completes) makes the kernel stop
+ * early and record a sticky error; tmagemm_check() reports it.
+ *
+ * Thread safety: all entry points may be called from several host threads.
+ */
+#ifndef TMAGEMM_H
+#define TMAGEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+typedef enum {
+    TMAGEMM_OK = 0,
+    TMAGEMM_ERR_INVALID = -1,      /* M, N or K <= 0, or a NULL pointer          */
+    TMAGEMM_ERR_ALIGN = -2,        /* pointer not 16-byte aligned, or K % 8 != 0,
+                                      or N % 8 != 0 (GEMM with M > 1): the TMA
+                                      row strides must be multiples of 16 bytes  */
+    TMAGEMM_ERR_UNSUPPORTED = -3,  /* a dimension >= 2^31, or no sm_100-family
+                                      device                                     */
+    TMAGEMM_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed          */
+    TMAGEMM_ERR_TIMEOUT = -5       /* a device-side pipeline wait timed out      */
+} tmagemm_status;
+
+/*
+ * D = fp16(A * B^T), accumulated in FP32.
+ *   M, N, K : sizes (> 0).
+ *   A       : device pointer, M x K fp16, row-major (K contiguous).
+ *   B       : device pointer, N x K fp16, row-major (K contiguous).
+ *   D       : device pointer, M x N fp16, row-major; written, never read.
+ *   stream  : cudaStream_t (NULL = legacy default stream).
+ * Requirements: A, B, D 16-byte aligned; K % 8 == 0; N % 8 == 0 when M > 1.
+ * M == 1 is computed by the GEMV kernel (x = A, W = B, y = D).
+ * Kernel: persistent, warp-specialised: a TMA producer warp feeding a
+ * multi-stage mbarrier ring of 128B-swizzled tiles, one thread issuing
+ * tcgen05.mma into a double-buffered TMEM accumulator, and four epilogue warps
+ * (tcgen05.ld -> fp16 -> swizzled SMEM -> TMA store).  Tiles are visited in an
+ * L2-grouped order ("使用 TMA 为 GEMM 建立 Pipeline", 第 6 步 Persistent
+ * Scheduling; TensorCore_GEMM_with_TMA §2.3 block swizzle).
+ * Returns a tmagemm_status.
+ */
+int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+             void* stream);
+
+/*
+ * y = fp16(x * W^T), accumulated in FP32 ("Learning TileLang with GEMV",
+ * §01 GEMV; loads as in §4.5 thread_vectorized_split_k, reduction as in
+ * §4.6 Reduction).
+ *   N, K   : sizes (> 0).
+ *   x      : device pointer, K fp16.
+ *   W      : device pointer, N x K fp16, row-major.
+ *   y      : device pointer, N fp16; written, never read.
+ *   stream : cudaStream_t (NULL = legacy default stream).
+ * Requirements: x, W, y 16-byte aligned; K % 8 == 0.
+ * Returns a tmagemm_status.
+ */
+int gemv_f16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream);
+
+/*
+ * Synchronises `stream`, then reads and clears the current device's sticky
+ * device-side error word.  Returns TMAGEMM_OK, TMAGEMM_ERR_TIMEOUT (a kernel
+ * stopped after a pipeline wait ran out of time) or TMAGEMM_ERR_CUDA.
+ */
+int tmagemm_check(void* stream);
+
+/*
+ * Detail of the last device-side error on the current device (0 = none):
+ * bits 0..7 the wait site, bits 8..31 the block index.  Does not clear it.
+ */
+int tmagemm_last_error_detail(void);
+
+/* Static text for a status code (never NULL). */
+const char* tmagemm_strerror(int status);
+
+/* Library version, (major << 16) | (minor << 8) | patch. */
+int tmagemm_version(void);
+
+/*
+ * Diagnostics for the failure path: enqueues a one-block kernel whose only
+ * thread waits, with the same bounded wait the GEMM roles use, on an mbarrier
+ * that nothing ever arrives on.  After `limit_ms` (1..10000) the wait gives up
+ * and records a timeout in the device error word; the kernel then returns
+ * normally and the context stays usable.  tmagemm_check() afterwards must
+ * return TMAGEMM_ERR_TIMEOUT.  No TMA or tensor-core work is involved.
+ */
+int tmagemm_selftest_wait_timeout(int64_t limit_ms, void* stream);
+
+/* ---- host-side introspection of the kernels' schedule (no GPU needed) ---- */
+
+/*
+ * Output tile visited as linear id `tile` of a grid of grid_m x grid_n tiles
+ * with `group_m` tile rows per L2 group: *m_blk, *n_blk receive the tile's row
+ * and column.  This is the same function the GEMM kernel runs.  Returns
+ * TMAGEMM_ERR_INVALID for out-of-range input.
+ */
+int tmagemm_tile_coord(int64_t tile, int64_t grid_m, int64_t grid_n, int64_t group_m,
+                       int64_t* m_blk, int64_t* n_blk);
+
+/*
+ * Position of k-block iteration `it` (counted over the whole life of a CTA,
+ * across tiles) in a ring of `stages` SMEM stages: *stage = it % stages and
+ * *phase = parity of the stage's mbarrier phase for that use.  Same function
+ * as the kernel's producer and MMA loops.
+ */
+int tmagemm_ring_position(int64_t it, int64_t stages, int64_t* stage, int64_t* phase);
+
+/*
+ * The GEMM launch configuration for (M, N, K) on a device with `num_sms` SMs:
+ * tile sizes, pipeline stages, tile count, grid size, threads per block and
+ * dynamic shared memory bytes, written to out[0..7] in that order
+ * (BM, BN, BK, STAGES, tiles, grid, threads, smem).  No GPU needed.
+ */
+int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t* out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TMAGEMM_H */

@@ -1,0 +1,199 @@
+"""GPU parity of the tcgen05 GEMM (through the C ABI) against the CPU oracle.
+
+Sizes: the four GEMM workloads (256^3, 4096^3, ragged 4000x3000x4160 and
+8192^3, the last checked on samples), integer-valued inputs (bit-exact), the
+identity / rank-1 closed forms, edge shapes next to the tile boundaries and an
+out-of-bounds write guard.
+"""
+import numpy as np
+import pytest
+
+import oracle
+from tma_pipelined_tensor_tn_gb300 import inputs
+from tests.parity_util import assert_bitexact, compare
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tg():
+    import tma_pipelined_tensor_tn_gb300 as m
+    m.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return m
+
+
+def run_gemm(tg, A, B, stream=None):
+    """A, B: CPU fp16 tensors -> D (CPU fp16 numpy) computed by gemm_f16."""
+    dA, dB = A.cuda(), B.cuda()
+    D = tg.gemm(dA, dB, stream=stream)
+    tg.check(stream)
+    return D.cpu().numpy()
+
+
+@pytest.mark.parametrize("name,seed", [
+    ("gemm_256", 0), ("gemm_256", 1),
+    ("gemm_ragged_4000x3000x4160", 0), ("gemm_ragged_4000x3000x4160", 1),
+    ("gemm_4096", 0),
+])
+def test_gemm_parity_full(tg, name, seed):
+    w = inputs.WORKLOADS[name]
+    A, B = inputs.gemm_inputs(w["M"], w["N"], w["K"], seed=seed)
+    D = run_gemm(tg, A, B)
+    ref = oracle.gemm_f16(A.numpy(), B.numpy())
+    stats = compare(D, ref, f"{name} seed {seed}")
+    print(name, seed, stats)
+
+
+def sample_positions(M, N, BM, BN, rng, n_random=20000):
+    """Every element of one interior and the last row/column tile bands, tile
+    corners, plus random positions."""
+    ms, ns = [], []
+    last_m, last_n = ((M - 1) // BM) * BM, ((N - 1) // BN) * BN
+    for m in (0, BM + 5, last_m, M - 1):
+        ms.append(np.full(N, m))
+        ns.append(np.arange(N))
+    for n in (0, BN + 7, last_n, N - 1):
+        ms.append(np.arange(M))
+        ns.append(np.full(M, n))
+    tm = np.arange(0, M, BM)
+    tn = np.arange(0, N, BN)
+    cm, cn = np.meshgrid(tm, tn, indexing="ij")
+    for dm, dn in ((0, 0), (BM - 1, 0), (0, BN - 1), (BM - 1, BN - 1)):
+        ms.append(np.minimum(cm.ravel() + dm, M - 1))
+        ns.append(np.minimum(cn.ravel() + dn, N - 1))
+    ms.append(rng.integers(0, M, n_random))
+    ns.append(rng.integers(0, N, n_random))
+    return np.concatenate(ms), np.concatenate(ns)
+
+
+def test_gemm_8192_sampled(tg):
+    w = inputs.WORKLOADS["gemm_8192"]
+    M, N, K = w["M"], w["N"], w["K"]
+    A, B = inputs.gemm_inputs(M, N, K, seed=0)
+    D = run_gemm(tg, A, B)
+    plan = tg.tmagemm_gemm_plan(M, N, K, 148)
+    ms, ns = sample_positions(M, N, plan["BM"], plan["BN"], np.random.default_rng(0))
+    ref = oracle.gemm_f16_at(A.numpy(), B.numpy(), ms, ns)
+    print("gemm_8192 sampled", ms.size, compare(D[ms, ns], ref, "8192^3 sampled"))
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (4000, 3000, 4160), (4096, 4096, 4096)])
+def test_gemm_integer_bitexact(tg, M, N, K):
+    # Entries in {-2..2}: every product and partial sum is an integer below 2^24,
+    # so FP32 accumulation is exact and both sides round the same integer.
+    A = inputs.integer_f16((M, K), seed=10)
+    B = inputs.integer_f16((N, K), seed=11)
+    D = run_gemm(tg, A, B)
+    assert_bitexact(D, oracle.gemm_f16(A.numpy(), B.numpy()), f"integer {M}x{N}x{K}")
+
+
+def test_gemm_8192_integer_sampled_bitexact(tg):
+    M = N = K = 8192
+    A = inputs.integer_f16((M, K), seed=12)
+    B = inputs.integer_f16((N, K), seed=13)
+    D = run_gemm(tg, A, B)
+    ms, ns = sample_positions(M, N, 128, 256, np.random.default_rng(1), n_random=5000)
+    assert_bitexact(D[ms, ns], oracle.gemm_f16_at(A.numpy(), B.numpy(), ms, ns), "integer 8192")
+
+
+def test_gemm_identity_closed_forms(tg):
+    g = torch.Generator().manual_seed(5)
+    K, N, M = 512, 384, 640
+    B = (torch.rand((N, K), generator=g) * 2 - 1).half()
+    A = (torch.rand((M, K), generator=g) * 2 - 1).half()
+    I = torch.eye(K, dtype=torch.float16)
+    assert_bitexact(run_gemm(tg, I, B), B.numpy().T, "A = I gives B^T")
+    assert_bitexact(run_gemm(tg, A, I), A.numpy(), "B = I gives A")
+
+
+def test_gemm_rank1_powers_of_two(tg):
+    rng = np.random.default_rng(21)
+    M, N, K = 300, 264, 192
+    a = rng.choice([-1, 1], M) * 2.0 ** rng.integers(-5, 3, M)
+    b = rng.choice([-1, 1], N) * 2.0 ** rng.integers(-5, 3, N)
+    A = torch.from_numpy(np.repeat(a[:, None], K, axis=1).astype(np.float16))
+    B = torch.from_numpy(np.repeat(b[:, None], K, axis=1).astype(np.float16))
+    D = run_gemm(tg, A, B)
+    assert np.array_equal(D.astype(np.float64), K * np.outer(a, b))
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (2, 8, 8), (127, 120, 64), (129, 136, 72), (200, 200, 24), (1000, 264, 296),
+    (128, 256, 64), (129, 264, 8), (513, 1032, 1000), (3, 2056, 136),
+])
+def test_gemm_edge_shapes(tg, M, N, K):
+    A, B = inputs.gemm_inputs(M, N, K, seed=M + N + K)
+    D = run_gemm(tg, A, B)
+    compare(D, oracle.gemm_f16(A.numpy(), B.numpy()), f"edge {M}x{N}x{K}")
+
+
+def test_gemm_out_of_bounds_guard(tg):
+    """D sits inside a larger buffer filled with a sentinel: after a ragged run
+    the guard regions still hold it and every D element was written."""
+    M, N, K = 4000, 3000, 4160
+    A, B = inputs.gemm_inputs(M, N, K, seed=3)
+    guard = 4096  # elements (8 KB) on each side, keeps D 16-byte aligned
+    sentinel = np.uint16(0x7E01)  # a NaN pattern the kernel never produces
+    buf = torch.full((guard + M * N + guard,), 0, dtype=torch.int16)
+    buf.fill_(int(sentinel.view(np.int16)))
+    dbuf = buf.cuda()
+    D = dbuf[guard:guard + M * N].view(torch.float16).view(M, N)
+    tg.gemm(A.cuda(), B.cuda(), out=D)
+    tg.check()
+    host = dbuf.cpu().numpy().view(np.uint16)
+    assert np.all(host[:guard] == sentinel) and np.all(host[guard + M * N:] == sentinel)
+    body = host[guard:guard + M * N]
+    assert not np.any(body == sentinel), "some D elements were not written"
+    compare(body.view(np.float16).reshape(M, N), oracle.gemm_f16(A.numpy(), B.numpy()), "guarded")
+
+
+def test_gemm_m1_routes_to_gemv(tg):
+    x, W = inputs.gemv_inputs(1000, 1024, seed=4)
+    A = x.reshape(1, -1)
+    D = run_gemm(tg, A, W)
+    y = tg.gemv(x.cuda(), W.cuda())
+    tg.check()
+    assert_bitexact(D[0], y.cpu().numpy(), "M=1 GEMM vs GEMV")
+    compare(D, oracle.gemm_f16(A.numpy(), W.numpy()), "M=1")
+
+
+def test_gemm_transpose_symmetry(tg):
+    A, B = inputs.gemm_inputs(640, 512, 1024, seed=6)
+    D1 = run_gemm(tg, A, B)
+    D2 = run_gemm(tg, B, A)
+    compare(D2, D1.T, "gemm(B, A) vs gemm(A, B)^T")
+    print("transpose symmetry bit-exact:", np.array_equal(D2.view(np.uint16), D1.T.view(np.uint16)))
+
+
+def test_gemm_side_stream_and_repeat(tg):
+    A, B = inputs.gemm_inputs(1024, 768, 512, seed=8)
+    s = torch.cuda.Stream()
+    dA, dB = A.cuda(), B.cuda()
+    torch.cuda.synchronize()
+    with torch.cuda.stream(s):
+        D1 = tg.gemm(dA, dB, stream=s)
+        D2 = tg.gemm(dA, dB, stream=s)
+    tg.check(s)
+    assert_bitexact(D1.cpu().numpy(), D2.cpu().numpy(), "repeatable")
+    compare(D1.cpu().numpy(), oracle.gemm_f16(A.numpy(), B.numpy()), "side stream")
+
+
+def test_gemm_misaligned_device_pointer_rejected(tg):
+    buf = torch.zeros(256 * 256 + 8, dtype=torch.float16, device="cuda")
+    p = buf.data_ptr()
+    assert tg.gemm_f16(256, 256, 256, p + 2, p, p, None) == tg.TMAGEMM_ERR_ALIGN
+    assert tg.gemm_f16(256, 256, 260, p, p, p, None) == tg.TMAGEMM_ERR_ALIGN
+
+
+def test_wait_timeout_is_reported_and_context_survives(tg):
+    """A wait that nobody completes ends with a TIMEOUT status, not a hang; the
+    next GEMM on the same context still works."""
+    assert tg.tmagemm_check(None) == tg.TMAGEMM_OK
+    assert tg.tmagemm_selftest_wait_timeout(200, None) == tg.TMAGEMM_OK
+    assert tg.tmagemm_check(None) == tg.TMAGEMM_ERR_TIMEOUT
+    assert tg.tmagemm_last_error_detail() & 0xFF == 7
+    assert tg.tmagemm_check(None) == tg.TMAGEMM_OK          # cleared
+    A, B = inputs.gemm_inputs(256, 256, 256, seed=9)
+    compare(run_gemm(tg, A, B), oracle.gemm_f16(A.numpy(), B.numpy()), "after timeout")

@@ -1,0 +1,191 @@
+"""Host-side tests of the CUDA library that need no GPU.
+
+* the library loads and exports every symbol include/tmagemm.h declares;
+* argument validation returns status codes before any CUDA call;
+* the persistent schedule and the pipeline ring (the same functions the
+  kernel runs, exported for introspection) against the pages' worked examples.
+"""
+import json
+import os
+import re
+
+import pytest
+
+import tma_pipelined_tensor_tn_gb300 as tg
+from tma_pipelined_tensor_tn_gb300 import _build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLDEN = os.path.join(ROOT, "tests", "golden")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    _build.build()
+    return tg.lib()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "tmagemm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s+\**(\w+)\s*\(", text, flags=re.M)))
+
+
+def test_library_exports_every_header_symbol():
+    names = header_functions()
+    assert "gemm_f16" in names and "gemv_f16" in names
+    L = tg.lib()
+    for n in names:
+        assert hasattr(L, n), n
+        assert n in tg.SIGNATURES, n
+
+
+def test_strerror_covers_all_codes():
+    for code in (0, -1, -2, -3, -4, -5):
+        assert tg.strerror(code) and tg.strerror(code) != "unknown status"
+    assert tg.strerror(12345) == "unknown status"
+
+
+@pytest.mark.parametrize("M,N,K,expect", [
+    (0, 256, 256, tg.TMAGEMM_ERR_INVALID),
+    (256, -1, 256, tg.TMAGEMM_ERR_INVALID),
+    (256, 256, 0, tg.TMAGEMM_ERR_INVALID),
+    (256, 256, 260, tg.TMAGEMM_ERR_ALIGN),      # K % 8
+    (256, 250, 256, tg.TMAGEMM_ERR_ALIGN),      # N % 8 (M > 1)
+    (1 << 31, 256, 256, tg.TMAGEMM_ERR_UNSUPPORTED),
+])
+def test_gemm_validation_codes(M, N, K, expect):
+    p = 1 << 20   # aligned fake address: validation fails before it is touched
+    assert tg.gemm_f16(M, N, K, p, p, p, None) == expect
+
+
+def test_gemm_null_and_misaligned_pointers():
+    p = 1 << 20
+    assert tg.gemm_f16(256, 256, 256, None, p, p, None) == tg.TMAGEMM_ERR_INVALID
+    assert tg.gemm_f16(256, 256, 256, p, p, None, None) == tg.TMAGEMM_ERR_INVALID
+    assert tg.gemm_f16(256, 256, 256, p + 2, p, p, None) == tg.TMAGEMM_ERR_ALIGN
+    assert tg.gemm_f16(256, 256, 256, p, p + 8, p, None) == tg.TMAGEMM_ERR_ALIGN
+    # M == 1 goes to the GEMV rules: N need not be a multiple of 8, K must be.
+    assert tg.gemm_f16(1, 250, 260, p, p, p, None) == tg.TMAGEMM_ERR_ALIGN
+    assert tg.gemv_f16(4096, 14336, p, p, p + 4, None) == tg.TMAGEMM_ERR_ALIGN
+    assert tg.gemv_f16(4096, 0, p, p, p, None) == tg.TMAGEMM_ERR_INVALID
+
+
+def test_group_m_order_golden():
+    g = json.load(open(os.path.join(GOLDEN, "persistent_schedule.json")))
+    for c in g["cases"]:
+        assert tg.tmagemm_tile_coord(c["tile"], c["grid_m"], c["grid_n"], g["group_m"]) == (c["m"], c["n"]), c
+
+
+@pytest.mark.parametrize("grid_m,grid_n", [(32, 32), (2, 2), (10, 3), (32, 12), (63, 17), (1, 5)])
+def test_group_m_order_is_a_bijection(grid_m, grid_n):
+    seen = set()
+    for t in range(grid_m * grid_n):
+        m, n = tg.tmagemm_tile_coord(t, grid_m, grid_n, 8)
+        assert 0 <= m < grid_m and 0 <= n < grid_n
+        seen.add((m, n))
+    assert len(seen) == grid_m * grid_n
+
+
+def test_tile_coord_rejects_out_of_range():
+    with pytest.raises(tg.TmaGemmError):
+        tg.tmagemm_tile_coord(4, 2, 2, 8)
+
+
+def test_ring_reduces_to_pipeline_trace():
+    g = json.load(open(os.path.join(GOLDEN, "pipeline_depth2_k5.json")))
+    S, KT = g["pipe_depth"], g["k_tiles"]
+    stages, tma_ph, mma_ph, refill = [], [], [], []
+    for it in range(KT):
+        s, ph = tg.tmagemm_ring_position(it, S)
+        stages.append(s)
+        tma_ph.append(ph)
+        # one barrier reused every iteration (the page's single MMA barrier)
+        mma_ph.append(tg.tmagemm_ring_position(it, 1)[1])
+        # a producer refills a stage with load it + S once iteration it freed it
+        refill.append(it + S if it + S < KT else None)
+    assert stages == g["stage"]
+    assert tma_ph == g["phase_tma"]
+    assert mma_ph == g["phase_mma"]
+    assert refill == g["refill_tile"]
+
+
+class MBarrierModel:
+    """Phase counter of an mbarrier with arrival count 1."""
+
+    def __init__(self):
+        self.completed = 0
+
+    def arrive(self):
+        self.completed += 1
+
+    def wait_ok(self, parity):
+        # try_wait.parity(P) succeeds once the phase with parity P completed,
+        # i.e. when the current (incomplete) phase has the other parity.
+        return (self.completed & 1) != parity
+
+
+@pytest.mark.parametrize("k_tiles,stages", [(64, 2), (65, 4), (4, 4), (65, 2), (3, 5)])
+def test_running_ring_counter_matches_barrier_phases(k_tiles, stages):
+    """Consumer waits issued with the kernel's ring parity always match the
+    barrier's state across tiles, for any K_TILES (odd ones included)."""
+    full = [MBarrierModel() for _ in range(stages)]
+    it = 0
+    for _tile in range(3):
+        for _kb in range(k_tiles):
+            s, ph = tg.tmagemm_ring_position(it, stages)
+            assert not full[s].wait_ok(ph)      # not complete before the load lands
+            full[s].arrive()                    # TMA completes the phase
+            assert full[s].wait_ok(ph)
+            it += 1
+
+
+def test_per_tile_phase_reset_breaks_with_odd_barrier_counts():
+    """The page's per-tile reset of phases needs every barrier to be used an even
+    number of times per tile; with 65 k-blocks the reset parity is wrong."""
+    g = json.load(open(os.path.join(GOLDEN, "persistent_schedule.json")))
+    kt, S = g["k_tiles"], g["pipe_depth"]
+    uses = [0] * S
+    for it in range(kt):
+        uses[tg.tmagemm_ring_position(it, S)[0]] += 1
+    assert uses == [g["tma_bar_uses_per_stage_per_tile"]] * S
+    assert kt == g["mma_bar_uses_per_tile"]
+    # odd count: after one tile of 65 uses the single MMA barrier has odd parity
+    bar = MBarrierModel()
+    for _ in range(65):
+        bar.arrive()
+    assert bar.completed & 1 == 1          # resetting the expected parity to 0 would be wrong
+    assert tg.tmagemm_ring_position(65, 1)[1] == 1   # the running counter gets it right
+
+
+def test_plan_for_the_workloads():
+    g = json.load(open(os.path.join(GOLDEN, "persistent_schedule.json")))
+    # The page's exercise: 4096^2 output, 128x128 tiles -> 1024 tiles.
+    assert (4096 // 128) * (4096 // 128) == g["tiles_4096_128x128"]
+    p = tg.tmagemm_gemm_plan(4096, 4096, 4096, 152)
+    assert (p["BM"], p["BK"]) == (128, 64)
+    assert p["tiles"] == (4096 // p["BM"]) * (4096 // p["BN"])
+    assert p["grid"] == min(p["tiles"], 152)
+    assert p["smem"] <= 232448
+    r = tg.tmagemm_gemm_plan(4000, 3000, 4160, 152)
+    assert r["tiles"] == -(-4000 // r["BM"]) * -(-3000 // r["BN"])
+    s = tg.tmagemm_gemm_plan(256, 256, 256, 152)
+    assert s["grid"] == s["tiles"] <= 4
+
+
+def test_persistent_schedule_visits_every_tile_once():
+    p = tg.tmagemm_gemm_plan(4000, 3000, 4160, 152)
+    grid_m, grid_n = -(-4000 // p["BM"]), -(-3000 // p["BN"])
+    visits = {}
+    for cta in range(p["grid"]):
+        for t in range(cta, p["tiles"], p["grid"]):
+            mn = tg.tmagemm_tile_coord(t, grid_m, grid_n, 8)
+            visits[mn] = visits.get(mn, 0) + 1
+    assert len(visits) == grid_m * grid_n and set(visits.values()) == {1}
+
+
+def test_no_gpu_returns_cuda_error_not_crash():
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    p = 1 << 20
+    assert tg.gemm_f16(256, 256, 256, p, p, p, None) == tg.TMAGEMM_ERR_CUDA

@@ -1,0 +1,36 @@
+"""FP16 TN GEMM (D = A @ B.T) and M=1 GEMV for GB300 (sm_103a).
+
+The compute path is the CUDA library ``libtmagemm.so`` built from ``csrc/``;
+this package only marshals arguments to its C ABI (``include/tmagemm.h``).
+"""
+from ._binding import (  # noqa: F401
+    LIB_PATH,
+    SIGNATURES,
+    TMAGEMM_ERR_ALIGN,
+    TMAGEMM_ERR_CUDA,
+    TMAGEMM_ERR_INVALID,
+    TMAGEMM_ERR_TIMEOUT,
+    TMAGEMM_ERR_UNSUPPORTED,
+    TMAGEMM_OK,
+    TmaGemmError,
+    check,
+    gemm,
+    gemm_f16,
+    gemv,
+    gemv_f16,
+    lib,
+    strerror,
+    tmagemm_check,
+    tmagemm_gemm_plan,
+    tmagemm_last_error_detail,
+    tmagemm_ring_position,
+    tmagemm_selftest_wait_timeout,
+    tmagemm_tile_coord,
+    tmagemm_version,
+)
+
+
+def build(force: bool = False) -> str:
+    """Compile libtmagemm.so in-tree (nvcc, sm_103a)."""
+    from ._build import build as _b
+    return _b(force=force)

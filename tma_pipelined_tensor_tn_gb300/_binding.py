@@ -1,0 +1,189 @@
+"""Thin ctypes binding to libtmagemm.so (C ABI in include/tmagemm.h).
+
+Argument marshalling only: every step of the GEMM/GEMV runs in the library's
+CUDA kernels.  If the library is missing this module raises; there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libtmagemm.so")
+
+TMAGEMM_OK = 0
+TMAGEMM_ERR_INVALID = -1
+TMAGEMM_ERR_ALIGN = -2
+TMAGEMM_ERR_UNSUPPORTED = -3
+TMAGEMM_ERR_CUDA = -4
+TMAGEMM_ERR_TIMEOUT = -5
+
+# Every symbol include/tmagemm.h declares, with (argtypes, restype).
+_i64, _p, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
+_P64 = ctypes.POINTER(ctypes.c_int64)
+SIGNATURES = {
+    "gemm_f16": ([_i64, _i64, _i64, _p, _p, _p, _p], _int),
+    "gemv_f16": ([_i64, _i64, _p, _p, _p, _p], _int),
+    "tmagemm_check": ([_p], _int),
+    "tmagemm_last_error_detail": ([], _int),
+    "tmagemm_strerror": ([_int], ctypes.c_char_p),
+    "tmagemm_version": ([], _int),
+    "tmagemm_selftest_wait_timeout": ([_i64, _p], _int),
+    "tmagemm_tile_coord": ([_i64, _i64, _i64, _i64, _P64, _P64], _int),
+    "tmagemm_ring_position": ([_i64, _i64, _P64, _P64], _int),
+    "tmagemm_gemm_plan": ([_i64, _i64, _i64, _i64, _P64], _int),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class TmaGemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {strerror(status)} (status {status})" if what else strerror(status))
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(
+                    f"{LIB_PATH} not found: build it first (python -c "
+                    "'import __graft_entry__ as g; g.build()')")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (argt, rest) in SIGNATURES.items():
+                fn = getattr(L, name)
+                fn.argtypes = argt
+                fn.restype = rest
+            _lib = L
+    return _lib
+
+
+def strerror(status: int) -> str:
+    return lib().tmagemm_strerror(int(status)).decode()
+
+
+# ---- raw C-ABI calls (same names as the header) ------------------------------
+
+def gemm_f16(M, N, K, A, B, D, stream=None) -> int:
+    return lib().gemm_f16(M, N, K, A, B, D, stream)
+
+
+def gemv_f16(N, K, x, W, y, stream=None) -> int:
+    return lib().gemv_f16(N, K, x, W, y, stream)
+
+
+def tmagemm_check(stream=None) -> int:
+    return lib().tmagemm_check(stream)
+
+
+def tmagemm_last_error_detail() -> int:
+    return lib().tmagemm_last_error_detail()
+
+
+def tmagemm_version() -> int:
+    return lib().tmagemm_version()
+
+
+def tmagemm_selftest_wait_timeout(limit_ms, stream=None) -> int:
+    return lib().tmagemm_selftest_wait_timeout(limit_ms, stream)
+
+
+def tmagemm_tile_coord(tile, grid_m, grid_n, group_m):
+    m, n = ctypes.c_int64(), ctypes.c_int64()
+    s = lib().tmagemm_tile_coord(tile, grid_m, grid_n, group_m, ctypes.byref(m), ctypes.byref(n))
+    if s != TMAGEMM_OK:
+        raise TmaGemmError(s, "tmagemm_tile_coord")
+    return m.value, n.value
+
+
+def tmagemm_ring_position(it, stages):
+    st, ph = ctypes.c_int64(), ctypes.c_int64()
+    s = lib().tmagemm_ring_position(it, stages, ctypes.byref(st), ctypes.byref(ph))
+    if s != TMAGEMM_OK:
+        raise TmaGemmError(s, "tmagemm_ring_position")
+    return st.value, ph.value
+
+
+def tmagemm_gemm_plan(M, N, K, num_sms):
+    out = (ctypes.c_int64 * 8)()
+    s = lib().tmagemm_gemm_plan(M, N, K, num_sms, out)
+    if s != TMAGEMM_OK:
+        raise TmaGemmError(s, "tmagemm_gemm_plan")
+    keys = ("BM", "BN", "BK", "STAGES", "tiles", "grid", "threads", "smem")
+    return dict(zip(keys, list(out)))
+
+
+# ---- torch-tensor conveniences (marshalling only) ----------------------------
+
+def _stream_handle(stream, device):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check_f16_cuda(name, t):
+    import torch
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != torch.float16:
+        raise TypeError(f"{name} must be float16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous (row-major)")
+
+
+def gemm(A, B, out=None, stream=None):
+    """D = A @ B.T for CUDA fp16 tensors A (M, K), B (N, K); returns D (M, N)."""
+    import torch
+    _check_f16_cuda("A", A)
+    _check_f16_cuda("B", B)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("A and B must share K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    _check_f16_cuda("out", out)
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must be (M, N)")
+    with torch.cuda.device(A.device):
+        s = lib().gemm_f16(M, N, K, A.data_ptr(), B.data_ptr(), out.data_ptr(),
+                           _stream_handle(stream, A.device))
+    if s != TMAGEMM_OK:
+        raise TmaGemmError(s, "gemm_f16")
+    return out
+
+
+def gemv(x, W, out=None, stream=None):
+    """y = x @ W.T for CUDA fp16 tensors x (K,), W (N, K); returns y (N,)."""
+    import torch
+    _check_f16_cuda("x", x)
+    _check_f16_cuda("W", W)
+    N, K = W.shape
+    if tuple(x.shape) != (K,):
+        raise ValueError("x must be (K,)")
+    if out is None:
+        out = torch.empty((N,), dtype=torch.float16, device=W.device)
+    _check_f16_cuda("out", out)
+    with torch.cuda.device(W.device):
+        s = lib().gemv_f16(N, K, x.data_ptr(), W.data_ptr(), out.data_ptr(),
+                           _stream_handle(stream, W.device))
+    if s != TMAGEMM_OK:
+        raise TmaGemmError(s, "gemv_f16")
+    return out
+
+
+def check(stream=None, device=None):
+    """Synchronise and raise if a kernel recorded a device-side timeout."""
+    import torch
+    dev = device if device is not None else torch.cuda.current_device()
+    with torch.cuda.device(dev):
+        s = lib().tmagemm_check(_stream_handle(stream, dev))
+    if s != TMAGEMM_OK:
+        raise TmaGemmError(s, f"tmagemm_check (detail 0x{tmagemm_last_error_detail():x})")

@@ -1,0 +1,265 @@
+// C ABI of libtmagemm.so (declared in include/tmagemm.h): argument
+// validation, TMA tensor-map encoding, per-device state, kernel dispatch and
+// the sticky device-side error word.
+//
+// Tensor maps follow "TensorCore_GEMM_with_TMA" §2.1 init tensor map: a rank-2
+// map per operand with sizes {inner, outer} (fastest first), one byte stride
+// for the outer dimension, a box of {64 fp16, rows} and 128-byte swizzle for a
+// 64-element fp16 row; out-of-range elements read as zero (OOB fill NONE).
+// Unlike the page, errors are returned as status codes, never printed.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/tmagemm.h"
+#include "launch.h"
+#include "ptx.cuh"
+#include "tile_sched.cuh"
+
+namespace tmagemm {
+
+// Sticky per-device error word written by the kernels' bounded waits.
+__device__ uint32_t g_err_word = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool ready = false;
+    int sms = 0;
+    int cc_major = 0;
+    uint32_t* err_word = nullptr;
+};
+
+std::mutex g_mutex;
+DeviceState g_dev[kMaxDevices];
+std::atomic<int> g_last_detail{0};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+uint64_t wait_limit_ns() {
+    static const uint64_t v = [] {
+        const char* s = std::getenv("TMAGEMM_WAIT_LIMIT_MS");
+        long ms = s ? std::strtol(s, nullptr, 10) : 0;
+        if (ms <= 0) ms = 2000;
+        return static_cast<uint64_t>(ms) * 1000000ull;
+    }();
+    return v;
+}
+
+// Per-device set-up, once, with that device current.
+int device_state(DeviceState** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return TMAGEMM_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return TMAGEMM_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    DeviceState& d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return TMAGEMM_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) !=
+            cudaSuccess)
+            return TMAGEMM_ERR_CUDA;
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return TMAGEMM_ERR_CUDA;
+        d.err_word = static_cast<uint32_t*>(p);
+        if (!g_encode) {
+            cudaDriverEntryPointQueryResult q{};
+            void* fn = nullptr;
+            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                 cudaEnableDefault, &q) != cudaSuccess ||
+                q != cudaDriverEntryPointSuccess || fn == nullptr)
+                return TMAGEMM_ERR_CUDA;
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+        }
+        d.ready = true;
+    }
+    if (d.cc_major != 10) return TMAGEMM_ERR_UNSUPPORTED;   // sm_100 family only
+    *out = &d;
+    return TMAGEMM_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Row-major fp16 matrix of `rows` x `cols` (cols contiguous) as a rank-2 map.
+int encode_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
+              uint32_t box_rows, CUtensorMapSwizzle swz, CUtensorMapL2promotion l2) {
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {cols * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
+}
+
+int validate_common(int64_t a, int64_t b, int64_t c) {
+    if (a <= 0 || b <= 0 || c <= 0) return TMAGEMM_ERR_INVALID;
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    if (a > lim || b > lim || c > lim) return TMAGEMM_ERR_UNSUPPORTED;
+    return TMAGEMM_OK;
+}
+
+int gemv_impl(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream) {
+    if (!x || !W || !y) return TMAGEMM_ERR_INVALID;
+    if (int s = validate_common(N, K, 1)) return s;
+    if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (K % 8) != 0) return TMAGEMM_ERR_ALIGN;
+    DeviceState* d = nullptr;
+    if (int s = device_state(&d)) return s;
+    cudaError_t e = launch_gemv(N, K, x, W, y, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace tmagemm
+
+using namespace tmagemm;
+
+extern "C" {
+
+int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+             void* stream) {
+    if (!A || !B || !D) return TMAGEMM_ERR_INVALID;
+    if (int s = validate_common(M, N, K)) return s;
+    if (M == 1) return gemv_impl(N, K, A, B, D, stream);
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
+        return TMAGEMM_ERR_ALIGN;
+    DeviceState* d = nullptr;
+    if (int s = device_state(&d)) return s;
+    const GemmPlan plan = plan_gemm(M, N, K, d->sms);
+    CUtensorMap tmA, tmB, tmD;
+    if (int s = encode_2d(&tmA, A, K, M, plan.bk, plan.bm, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+        return s;
+    if (int s = encode_2d(&tmB, B, K, N, plan.bk, plan.bn, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+        return s;
+    if (int s = encode_2d(&tmD, D, N, M, plan.epi_cols, plan.bm, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE))
+        return s;
+    GemmArgs args;
+    args.M = static_cast<int32_t>(M);
+    args.N = static_cast<int32_t>(N);
+    args.K = static_cast<int32_t>(K);
+    args.wait_limit_ns = wait_limit_ns();
+    args.err_word = d->err_word;
+    cudaError_t e = launch_gemm_tn(plan, tmA, tmB, tmD, args, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
+}
+
+int gemv_f16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream) {
+    return gemv_impl(N, K, x, W, y, stream);
+}
+
+int tmagemm_check(void* stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TMAGEMM_ERR_CUDA;
+    DeviceState* d = nullptr;
+    if (int s = device_state(&d)) return s;
+    uint32_t v = 0;
+    if (cudaMemcpy(&v, d->err_word, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return TMAGEMM_ERR_CUDA;
+    if (v == 0) return TMAGEMM_OK;
+    g_last_detail.store(static_cast<int>(v));
+    const uint32_t zero = 0;
+    if (cudaMemcpy(d->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+        return TMAGEMM_ERR_CUDA;
+    return TMAGEMM_ERR_TIMEOUT;
+}
+
+int tmagemm_last_error_detail(void) { return g_last_detail.load(); }
+
+const char* tmagemm_strerror(int status) {
+    switch (status) {
+        case TMAGEMM_OK: return "ok";
+        case TMAGEMM_ERR_INVALID: return "invalid argument (non-positive size or NULL pointer)";
+        case TMAGEMM_ERR_ALIGN:
+            return "alignment: pointers must be 16-byte aligned, K % 8 == 0 and N % 8 == 0";
+        case TMAGEMM_ERR_UNSUPPORTED: return "unsupported size or device";
+        case TMAGEMM_ERR_CUDA: return "CUDA runtime or driver call failed";
+        case TMAGEMM_ERR_TIMEOUT: return "device-side pipeline wait timed out";
+        default: return "unknown status";
+    }
+}
+
+int tmagemm_version(void) { return (0 << 16) | (1 << 8) | 0; }
+
+int tmagemm_tile_coord(int64_t tile, int64_t grid_m, int64_t grid_n, int64_t group_m,
+                       int64_t* m_blk, int64_t* n_blk) {
+    if (!m_blk || !n_blk || grid_m <= 0 || grid_n <= 0 || group_m <= 0 || tile < 0 ||
+        tile >= grid_m * grid_n)
+        return TMAGEMM_ERR_INVALID;
+    const TileCoord c = tile_coord(tile, grid_m, grid_n, group_m);
+    *m_blk = c.m_blk;
+    *n_blk = c.n_blk;
+    return TMAGEMM_OK;
+}
+
+int tmagemm_ring_position(int64_t it, int64_t stages, int64_t* stage, int64_t* phase) {
+    if (!stage || !phase || it < 0 || it > 0xffffffffll || stages <= 0 || stages > 64)
+        return TMAGEMM_ERR_INVALID;
+    *stage = ring_stage(static_cast<uint32_t>(it), static_cast<uint32_t>(stages));
+    *phase = ring_phase(static_cast<uint32_t>(it), static_cast<uint32_t>(stages));
+    return TMAGEMM_OK;
+}
+
+int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t* out) {
+    if (!out || num_sms <= 0) return TMAGEMM_ERR_INVALID;
+    if (int s = validate_common(M, N, K)) return s;
+    const GemmPlan p = plan_gemm(M, N, K, static_cast<int>(num_sms));
+    out[0] = p.bm;
+    out[1] = p.bn;
+    out[2] = p.bk;
+    out[3] = p.stages;
+    out[4] = p.tiles;
+    out[5] = p.grid;
+    out[6] = p.threads;
+    out[7] = p.smem_bytes;
+    return TMAGEMM_OK;
+}
+
+int tmagemm_selftest_wait_timeout(int64_t limit_ms, void* stream) {
+    if (limit_ms <= 0 || limit_ms > 10000) return TMAGEMM_ERR_INVALID;
+    DeviceState* d = nullptr;
+    if (int s = device_state(&d)) return s;
+    cudaError_t e = launch_wait_timeout_probe(static_cast<uint64_t>(limit_ms) * 1000000ull,
+                                              d->err_word, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
+}
+
+}  // extern "C"
+
+namespace tmagemm {
+namespace {
+
+// One block; thread 0 inits an mbarrier expecting one arrival that never
+// comes and waits on it with the same bounded wait the GEMM roles use.
+__global__ void wait_timeout_probe_kernel(uint64_t limit_ns, uint32_t* err) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        mbar_init(smem_u32(&bar), 1);
+        fence_mbarrier_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        (void)wait_or_abort(smem_u32(&bar), 0, &abort_flag, err, kSiteTest, limit_ns);
+    }
+    __syncthreads();
+}
+
+}  // namespace
+
+cudaError_t launch_wait_timeout_probe(uint64_t limit_ns, uint32_t* err_word, cudaStream_t stream) {
+    wait_timeout_probe_kernel<<<1, 32, 0, stream>>>(limit_ns, err_word);
+    return cudaGetLastError();
+}
+
+}  // namespace tmagemm

@@ -1,0 +1,42 @@
+// Internal host-side interface between the C ABI (abi.cu) and the kernels'
+// translation units.  Not installed; the public interface is include/tmagemm.h.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace tmagemm {
+
+// GEMM tile configuration used by the persistent tcgen05 kernel.
+struct GemmPlan {
+    int bm, bn, bk, stages;
+    int64_t tiles, grid_m, grid_n, k_blocks;
+    int grid, threads;
+    int smem_bytes;
+    int epi_cols;      // columns per epilogue TMA store box
+};
+
+// Pure function of the problem shape and the SM count (no CUDA calls).
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms);
+
+struct GemmArgs {
+    int32_t M, N, K;
+    uint64_t wait_limit_ns;
+    uint32_t* err_word;   // device address of the sticky error word
+};
+
+// Enqueue the GEMM kernel.  Tensor maps: A {K, M} box {bk, bm}; B {K, N} box
+// {bk, bn}; D {N, M} box {epi_cols, bm}; all 128B-swizzled.
+cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream);
+
+// Enqueue the GEMV kernel: y[n] = sum_k x[k] * W[n][k].
+cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y,
+                        cudaStream_t stream);
+
+// Enqueue a one-block kernel that waits on an mbarrier nobody arrives on, with
+// the given limit; it must end by recording kSiteTest in the error word.
+cudaError_t launch_wait_timeout_probe(uint64_t limit_ns, uint32_t* err_word, cudaStream_t stream);
+
+}  // namespace tmagemm
