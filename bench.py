@@ -88,60 +88,115 @@ def load_traffic(key):
 # ---------------------------------------------------------------- clocks ----
 
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples SM clock, power and clock-event reasons during the timed region.
 
-    def __init__(self, gpu_index):
-        self.gpu = gpu_index
-        self.proc = None
-        self.lines = []
-        self.err = None
+    Reads NVML through ctypes (about every millisecond) and falls back to
+    ``nvidia-smi -lms 100`` when NVML cannot be loaded.  Read-only.
+    """
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device):
+        self.dev = torch_device
+        self.samples = []          # (t, sm_mhz, max_mhz, power_w, reasons_mask)
+        self.stop_evt = threading.Event()
+        self.thread = None
+        self.source = None
+        self.note = None
+        self.window = None
+
+    def _nvml_handle(self):
+        import ctypes
+        nv = ctypes.CDLL("libnvidia-ml.so.1")
+        if nv.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        uuid = None
+        try:
+            import torch
+            u = getattr(torch.cuda.get_device_properties(self.dev), "uuid", None)
+            if u is not None:
+                uuid = ("GPU-" + str(u)).encode()
+        except Exception:
+            uuid = None
+        if uuid is None or nv.nvmlDeviceGetHandleByUUID(uuid, ctypes.byref(h)) != 0:
+            if nv.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(self.dev.index or 0), ctypes.byref(h)) != 0:
+                raise OSError("no NVML handle")
+        return nv, h
+
+    def _run_nvml(self, nv, h):
+        import ctypes
+        clk, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+        nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+        get_reasons = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(nv, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        while not self.stop_evt.is_set():
+            t = time.perf_counter()
+            if nv.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk)) == 0:
+                p = pw.value / 1000.0 if nv.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw)) == 0 else None
+                r = rs.value if get_reasons(h, ctypes.byref(rs)) == 0 else 0
+                self.samples.append((t, float(clk.value), float(mx.value), p, int(r)))
+            time.sleep(0.001)
+
+    def _run_smi(self):
+        fields = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                  "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                  "clocks_event_reasons.sw_power_cap")
+        proc = subprocess.Popen(["nvidia-smi", f"--id={self.dev.index or 0}", f"--query-gpu={fields}",
+                                 "--format=csv,noheader,nounits", "-lms", "100"],
+                                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        bits = (0x8, 0x40, 0x20, 0x4)
+        try:
+            for line in proc.stdout:
+                if self.stop_evt.is_set():
+                    break
+                parts = [x.strip() for x in line.split(",")]
+                try:
+                    mask = sum(b for b, v in zip(bits, parts[3:7]) if v.lower().startswith("active"))
+                    self.samples.append((time.perf_counter(), float(parts[0]), float(parts[1]),
+                                         float(parts[2]), mask))
+                except (ValueError, IndexError):
+                    continue
+        finally:
+            proc.terminate()
 
     def start(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.t = threading.Thread(target=self._read, daemon=True)
-            self.t.start()
+            nv, h = self._nvml_handle()
+            self.source = "nvml"
+            self.thread = threading.Thread(target=self._run_nvml, args=(nv, h), daemon=True)
         except OSError as e:
-            self.err = str(e)
+            self.note = f"nvml unavailable ({e}); nvidia-smi at 100 ms"
+            self.source = "nvidia-smi"
+            self.thread = threading.Thread(target=self._run_smi, daemon=True)
+        self.thread.start()
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
 
     def stop(self):
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": self.err or "no nvidia-smi"}
-        time.sleep(0.25)
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.t.join(timeout=2)
-        sm, smax, power, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
-            parts = [p.strip() for p in ln.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-                power.append(float(parts[3]))
-            except ValueError:
-                continue
-            for name, v in zip(names, parts[5:9]):
-                if v.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": "no samples"}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "power_w_max": max(power), "samples": len(sm), "reasons": sorted(reasons)}
+        time.sleep(0.05)
+        self.stop_evt.set()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        t0, t1 = self.window or (float("-inf"), float("inf"))
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        used = inside if len(inside) >= 3 else self.samples
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "note": self.note or "no samples"}
+        mask = 0
+        for s in used:
+            mask |= s[4]
+        out = {"sm_mhz": statistics.median(s[1] for s in used),
+               "sm_max_mhz": max(s[2] for s in used),
+               "sm_mhz_min": min(s[1] for s in used),
+               "power_w_max": max((s[3] for s in used if s[3] is not None), default=None),
+               "samples": len(used), "samples_in_timed_region": len(inside),
+               "source": self.source,
+               "reasons": sorted(n for b, n in self.REASONS.items() if mask & b)}
+        if self.note:
+            out["note"] = self.note
+        return out
 
 
 # ------------------------------------------------------------- CPU oracle ----
@@ -261,35 +316,42 @@ def run_ours(args, rank, world, local_rank):
         assert step(i) == 0 and step_gemv(i) == 0
     tg.check(stream)
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    clocks = ClockSampler(local_rank)
+    # Timed region: K GEMM launches back to back, then K GEMV launches, each
+    # batch between one pair of CUDA events on the launching stream (event
+    # pairs around every single launch would add their own overhead to these
+    # 20-100 us kernels).
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+    clocks = ClockSampler(dev)
     clocks.start()
-    time.sleep(0.3)
+    time.sleep(0.05)
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
     t0 = time.perf_counter()
     launches = 0
+    evs[0].record(stream)
     for i in range(args.steps):
-        ev[i][0].record(stream)
         s1 = step(i)
-        ev[i][1].record(stream)
+        launches += 1
+        if s1:
+            raise RuntimeError(f"gemm launch failed: {tg.strerror(s1)}")
+    evs[1].record(stream)
+    for i in range(args.steps):
         s2 = step_gemv(i)
-        ev[i][2].record(stream)
-        launches += 2
-        if s1 or s2:
-            raise RuntimeError(f"launch failed: {tg.strerror(s1 or s2)}")
+        launches += 1
+        if s2:
+            raise RuntimeError(f"gemv launch failed: {tg.strerror(s2)}")
+    evs[2].record(stream)
     torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
-    wall = time.perf_counter() - t0
+    t1 = time.perf_counter()
+    wall = t1 - t0
+    clocks.mark(t0, t1)
     clk = clocks.stop()
     tg.check(stream)
 
-    gemm_ms = [e[0].elapsed_time(e[1]) for e in ev]
-    gemv_ms = [e[1].elapsed_time(e[2]) for e in ev]
-    times = [sum(gemm_ms), sum(gemv_ms), wall]
+    times = [evs[0].elapsed_time(evs[1]), evs[1].elapsed_time(evs[2]), wall]
     if world > 1:
         t = torch.tensor(times, dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -377,8 +439,8 @@ def run_ours(args, rank, world, local_rank):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -113,6 +113,16 @@ int tmagemm_version(void);
  */
 int tmagemm_selftest_wait_timeout(int64_t limit_ms, void* stream);
 
+/*
+ * Tuning/test override of the GEMM's tile width N: 256, 224 or 192 forces that
+ * tile shape for every later gemm_f16 call in the process; 0 restores the
+ * automatic choice (the width that minimises the number of tile rounds on
+ * the device's SMs, weighted by tile cost).  Results are the same for every
+ * width up to FP32 accumulation order.  Returns TMAGEMM_ERR_INVALID for other
+ * values.
+ */
+int tmagemm_set_tile_n(int bn);
+
 /* ---- host-side introspection of the kernels' schedule (no GPU needed) ---- */
 
 /*

@@ -129,6 +129,21 @@ def test_gemm_edge_shapes(tg, M, N, K):
     compare(D, oracle.gemm_f16(A.numpy(), B.numpy()), f"edge {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("bn", [256, 224, 192])
+@pytest.mark.parametrize("M,N,K", [(1031, 1000, 1032), (300, 2056, 4160)])
+def test_gemm_each_tile_width(tg, bn, M, N, K):
+    """Every tile shape the plan can pick, on ragged shapes, real and integer inputs."""
+    try:
+        assert tg.tmagemm_set_tile_n(bn) == tg.TMAGEMM_OK
+        A, B = inputs.gemm_inputs(M, N, K, seed=bn)
+        compare(run_gemm(tg, A, B), oracle.gemm_f16(A.numpy(), B.numpy()), f"BN={bn} {M}x{N}x{K}")
+        Ai = inputs.integer_f16((M, K), seed=bn + 1)
+        Bi = inputs.integer_f16((N, K), seed=bn + 2)
+        assert_bitexact(run_gemm(tg, Ai, Bi), oracle.gemm_f16(Ai.numpy(), Bi.numpy()), f"BN={bn} int")
+    finally:
+        tg.tmagemm_set_tile_n(0)
+
+
 def test_gemm_out_of_bounds_guard(tg):
     """D sits inside a larger buffer filled with a sentinel: after a ragged run
     the guard regions still hold it and every D element was written."""

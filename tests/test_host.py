@@ -163,13 +163,33 @@ def test_plan_for_the_workloads():
     assert (4096 // 128) * (4096 // 128) == g["tiles_4096_128x128"]
     p = tg.tmagemm_gemm_plan(4096, 4096, 4096, 152)
     assert (p["BM"], p["BK"]) == (128, 64)
-    assert p["tiles"] == (4096 // p["BM"]) * (4096 // p["BN"])
+    assert p["tiles"] == -(-4096 // p["BM"]) * -(-4096 // p["BN"])
     assert p["grid"] == min(p["tiles"], 152)
     assert p["smem"] <= 232448
     r = tg.tmagemm_gemm_plan(4000, 3000, 4160, 152)
     assert r["tiles"] == -(-4000 // r["BM"]) * -(-3000 // r["BN"])
     s = tg.tmagemm_gemm_plan(256, 256, 256, 152)
     assert s["grid"] == s["tiles"] <= 4
+
+
+def test_plan_balances_waves_on_gb300():
+    # 4096^3 on 152 SMs: 128x224 tiles give 32 x 19 = 608 = 4 x 152 tiles, so
+    # every SM runs exactly four tiles (128x256 would leave a partial 4th wave).
+    p = tg.tmagemm_gemm_plan(4096, 4096, 4096, 152)
+    assert p["BN"] == 224 and p["tiles"] == 4 * 152
+    assert tg.tmagemm_gemm_plan(8192, 8192, 8192, 152)["BN"] == 256
+
+
+def test_tile_width_override():
+    try:
+        assert tg.tmagemm_set_tile_n(256) == tg.TMAGEMM_OK
+        assert tg.tmagemm_gemm_plan(4096, 4096, 4096, 152)["BN"] == 256
+        assert tg.tmagemm_set_tile_n(192) == tg.TMAGEMM_OK
+        assert tg.tmagemm_gemm_plan(4096, 4096, 4096, 152)["BN"] == 192
+        assert tg.tmagemm_set_tile_n(100) == tg.TMAGEMM_ERR_INVALID
+    finally:
+        assert tg.tmagemm_set_tile_n(0) == tg.TMAGEMM_OK
+    assert tg.tmagemm_gemm_plan(4096, 4096, 4096, 152)["BN"] == 224
 
 
 def test_persistent_schedule_visits_every_tile_once():

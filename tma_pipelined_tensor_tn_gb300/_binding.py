@@ -34,6 +34,7 @@ SIGNATURES = {
     "tmagemm_tile_coord": ([_i64, _i64, _i64, _i64, _P64, _P64], _int),
     "tmagemm_ring_position": ([_i64, _i64, _P64, _P64], _int),
     "tmagemm_gemm_plan": ([_i64, _i64, _i64, _i64, _P64], _int),
+    "tmagemm_set_tile_n": ([_int], _int),
 }
 
 _lock = threading.Lock()
@@ -92,6 +93,10 @@ def tmagemm_version() -> int:
 
 def tmagemm_selftest_wait_timeout(limit_ms, stream=None) -> int:
     return lib().tmagemm_selftest_wait_timeout(limit_ms, stream)
+
+
+def tmagemm_set_tile_n(bn) -> int:
+    return lib().tmagemm_set_tile_n(bn)
 
 
 def tmagemm_tile_coord(tile, grid_m, grid_n, group_m):

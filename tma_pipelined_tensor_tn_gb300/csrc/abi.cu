@@ -140,7 +140,10 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void
     if (int s = encode_2d(&tmB, B, K, N, plan.bk, plan.bn, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
         return s;
-    if (int s = encode_2d(&tmD, D, N, M, plan.epi_cols, plan.bm, CU_TENSOR_MAP_SWIZZLE_128B,
+    // Store boxes are one swizzle span wide: 64 columns (128 B) or 32 columns (64 B).
+    const CUtensorMapSwizzle dswz =
+        plan.epi_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    if (int s = encode_2d(&tmD, D, N, M, plan.epi_cols, plan.bm, dswz,
                           CU_TENSOR_MAP_L2_PROMOTION_NONE))
         return s;
     GemmArgs args;
@@ -189,6 +192,12 @@ const char* tmagemm_strerror(int status) {
 }
 
 int tmagemm_version(void) { return (0 << 16) | (1 << 8) | 0; }
+
+int tmagemm_set_tile_n(int bn) {
+    if (bn != 0 && bn != 256 && bn != 224 && bn != 192) return TMAGEMM_ERR_INVALID;
+    __atomic_store_n(&g_force_tile_n, bn, __ATOMIC_RELEASE);
+    return TMAGEMM_OK;
+}
 
 int tmagemm_tile_coord(int64_t tile, int64_t grid_m, int64_t grid_n, int64_t group_m,
                        int64_t* m_blk, int64_t* n_blk) {

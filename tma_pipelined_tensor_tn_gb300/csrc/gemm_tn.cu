@@ -43,19 +43,22 @@ namespace tmagemm {
 
 namespace {
 
-template <int BM_, int BN_, int BK_, int STAGES_>
+template <int BN_, int EPI_COLS_, int STAGES_>
 struct Cfg {
-    static constexpr int BM = BM_, BN = BN_, BK = BK_, STAGES = STAGES_;
+    static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_;
     static constexpr int kThreads = 192;            // 6 warps
     static constexpr int kEpiThreads = 128;         // warps 2..5
-    static constexpr int kEpiCols = 64;             // one 128-byte row of fp16 per box row
+    static constexpr int kEpiCols = EPI_COLS_;      // columns per TMA store box
+    static constexpr uint32_t kEpiRowBytes = kEpiCols * 2;       // = the box's swizzle span
+    static constexpr uint32_t kEpiChunks = kEpiRowBytes / 16;    // 16-byte chunks per box row
     static constexpr int kGroupM = 8;               // L2 group height in tiles
     static constexpr uint32_t kABytes = BM * BK * 2;
     static constexpr uint32_t kBBytes = BN * BK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
-    static constexpr uint32_t kEpiBufBytes = BM * kEpiCols * 2;
+    static constexpr uint32_t kEpiBufBytes = BM * kEpiRowBytes;
     static constexpr int kEpiBufs = 2;
-    static constexpr uint32_t kTmemCols = 512;      // two BN-column fp32 accumulators
+    static constexpr uint32_t kTmemCols = 512;      // two accumulators, 256 columns apart
+    static constexpr uint32_t kAccStride = 256;
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + STAGES * kABytes;
     static constexpr uint32_t kOffD = kOffB + STAGES * kBBytes;
@@ -65,17 +68,20 @@ struct Cfg {
     static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + base alignment slack
     static constexpr uint32_t kIdesc = umma_idesc_f16_f32(BM, BN);
 
-    static_assert(BM == 128, "one CTA-wide MMA covers 128 TMEM lanes");
     static_assert(BK * 2 == 128, "a K-major row of one k-block is one 128-byte swizzle atom");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
+    static_assert(kEpiCols == 32 || kEpiCols == 64, "store boxes are 64 or 128 bytes wide");
     static_assert(BN % kEpiCols == 0, "epilogue boxes tile BN");
-    static_assert(2 * BN <= (int)kTmemCols, "two accumulators fit in TMEM");
+    static_assert(kAccStride + BN <= kTmemCols, "two accumulators fit in TMEM");
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "stages stay 1024-B aligned");
     static_assert(kEpiBufBytes % 1024 == 0, "epilogue boxes stay 1024-B aligned");
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in shared memory");
 };
 
-using MainCfg = Cfg<128, 256, 64, 4>;
+// Tile shapes the host plan chooses from (all 128 rows x BN columns x 64 K).
+using Cfg256 = Cfg<256, 64, 4>;
+using Cfg224 = Cfg<224, 32, 4>;
+using Cfg192 = Cfg<192, 64, 4>;
 
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
@@ -172,7 +178,7 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                                    kSiteMmaAccEmpty, limit_ns))
                     break;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * C::BN;
+                const uint32_t d_tmem = tmem_base + acc * C::kAccStride;
                 for (int32_t kb = 0; kb < k_blocks; ++kb) {
                     const uint32_t s = ring_stage(it, C::STAGES);
                     const uint32_t ph = ring_phase(it, C::STAGES);
@@ -217,13 +223,14 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             // All 128 epilogue threads take the same decision.
             if (!named_bar_and(1, C::kEpiThreads, ok)) break;
             tc_fence_after();
-            const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + acc * C::BN;
+            const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + acc * C::kAccStride;
 #pragma unroll 1
             for (int c = 0; c < C::BN / C::kEpiCols; ++c, ++box) {
-                uint32_t v[64];
-                tmem_ld_32x32b_x32(t_row + c * C::kEpiCols, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
-                tmem_ld_32x32b_x32(t_row + c * C::kEpiCols + 32,
-                                   *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                uint32_t v[C::kEpiCols];
+#pragma unroll
+                for (int h = 0; h < C::kEpiCols / 32; ++h)
+                    tmem_ld_32x32b_x32(t_row + c * C::kEpiCols + 32 * h,
+                                       *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
                 tmem_ld_wait();
                 if (c == C::BN / C::kEpiCols - 1) {
                     // Whole accumulator read: give it back to the MMA warp.
@@ -235,16 +242,19 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 // The store that last read this buffer (two boxes ago) must be done.
                 if (leader) bulk_wait_group_read<1>();
                 named_bar_sync(1, C::kEpiThreads);
-                // Row `row` of the box: 128 bytes = 8 x 16-byte chunks; the
-                // 128B swizzle puts chunk j at position j ^ (row % 8).
-                const uint32_t row_addr = buf + row * 128u;
+                // Row `row` of the box holds kEpiChunks 16-byte chunks.  The
+                // TMA swizzle whose span equals the row width (64B or 128B)
+                // XORs the chunk index with address bits 7.. of the row start:
+                // chunk j of row r lands at j ^ ((r * row_bytes / 128) % chunks).
+                const uint32_t row_addr = buf + row * C::kEpiRowBytes;
+                const uint32_t xr = ((row * C::kEpiRowBytes) >> 7) & (C::kEpiChunks - 1);
 #pragma unroll
-                for (uint32_t j = 0; j < 8; ++j) {
+                for (uint32_t j = 0; j < C::kEpiChunks; ++j) {
                     const uint32_t p0 = pack_half2_rn(v[8 * j + 0], v[8 * j + 1]);
                     const uint32_t p1 = pack_half2_rn(v[8 * j + 2], v[8 * j + 3]);
                     const uint32_t p2 = pack_half2_rn(v[8 * j + 4], v[8 * j + 5]);
                     const uint32_t p3 = pack_half2_rn(v[8 * j + 6], v[8 * j + 7]);
-                    st_shared_v4(row_addr + ((j ^ (row & 7u)) << 4), p0, p1, p2, p3);
+                    st_shared_v4(row_addr + ((j ^ xr) << 4), p0, p1, p2, p3);
                 }
                 fence_proxy_async_smem();
                 named_bar_sync(1, C::kEpiThreads);
@@ -269,8 +279,10 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 
 }  // namespace
 
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms) {
-    using C = MainCfg;
+namespace {
+
+template <class C>
+GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms) {
     GemmPlan p{};
     p.bm = C::BM;
     p.bn = C::BN;
@@ -281,16 +293,23 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms) {
     p.grid_n = ceil_div(N, C::BN);
     p.k_blocks = ceil_div(K, C::BK);
     p.tiles = p.grid_m * p.grid_n;
-    const int64_t sms = num_sms > 0 ? num_sms : 1;
     p.grid = static_cast<int>(p.tiles < sms ? p.tiles : sms);
     p.threads = C::kThreads;
     p.smem_bytes = static_cast<int>(C::kSmemBytes);
     return p;
 }
 
-cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream) {
-    using C = MainCfg;
+// Modelled time of a plan: the busiest CTA runs ceil(tiles / grid) tiles, and
+// a tile's mainloop costs about BN + 32 units (MMA time grows with BN, the A
+// operand traffic per k-block does not).
+int64_t plan_cost(const GemmPlan& p) {
+    const int64_t rounds = ceil_div(p.tiles, p.grid);
+    return rounds * (p.bn + 32);
+}
+
+template <class C>
+cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                       const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream) {
     auto kernel = gemm_tn_f16_kernel<C>;
     // Per-device opt-in to > 48 KB dynamic shared memory, once per device.
     static std::atomic<bool> attr_done[64];
@@ -308,6 +327,36 @@ cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const C
         static_cast<int32_t>(plan.tiles), static_cast<int32_t>(plan.k_blocks), args.wait_limit_ns,
         args.err_word);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+int g_force_tile_n = 0;
+
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms) {
+    const int64_t sms = num_sms > 0 ? num_sms : 1;
+    const GemmPlan cands[3] = {plan_for<Cfg256>(M, N, K, sms), plan_for<Cfg224>(M, N, K, sms),
+                               plan_for<Cfg192>(M, N, K, sms)};
+    const int forced = __atomic_load_n(&g_force_tile_n, __ATOMIC_ACQUIRE);
+    GemmPlan best = cands[0];
+    for (const GemmPlan& c : cands) {
+        if (forced != 0) {
+            if (c.bn == forced) return c;
+            continue;
+        }
+        if (plan_cost(c) < plan_cost(best)) best = c;
+    }
+    return best;
+}
+
+cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream) {
+    switch (plan.bn) {
+        case 256: return launch_cfg<Cfg256>(plan, tmA, tmB, tmD, args, stream);
+        case 224: return launch_cfg<Cfg224>(plan, tmA, tmB, tmD, args, stream);
+        case 192: return launch_cfg<Cfg192>(plan, tmA, tmB, tmD, args, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace tmagemm

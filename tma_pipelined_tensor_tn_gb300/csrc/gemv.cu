@@ -2,18 +2,23 @@
 //
 // The shape reads each W element exactly once (117,440,512 of the 117,477,376
 // algorithmic bytes at N = 4096, K = 14336), so the bound is HBM bandwidth, not
-// arithmetic ("Learning TileLang with GEMV", §02 Bandwidth Bound).  Following
-// the page's lessons for bandwidth-bound kernels (§07 Summary):
-//   - each output row is owned by one warp, so there are N warps in flight;
-//   - at every step the 32 lanes of a warp read 32 adjacent 16-byte chunks of
-//     the row: fully coalesced, 512 contiguous bytes (§4.3 Coalescing);
-//   - every load is 128 bits = 8 fp16 (§4.5 thread_vectorized_split_k), and
-//     UNROLL independent loads per lane are issued before any is consumed, to
-//     keep enough bytes in flight per SM to cover HBM latency;
-//   - the per-lane partial sums are combined with warp shuffles
-//     (§4.6 Reduction: thread all-reduce lowered to shuffles).
-// W is streamed with L1::no_allocate so it does not evict x, which every warp
-// re-reads from L1.
+// arithmetic ("Learning TileLang with GEMV", §02 Bandwidth Bound).  The page's
+// rules for a bandwidth-bound kernel (§07 Summary) decide the design:
+//   - enough independent work: one warp per output row gives N warps (4096 at
+//     the Llama-3-8B down-projection shape, about 27 per SM), all resident at
+//     once, so every warp gets the same HBM share and no SM tail remains;
+//   - coalesced: at every step the 32 lanes of a warp read 32 adjacent 16-byte
+//     chunks of the row, 512 contiguous bytes (§4.3 Coalescing);
+//   - wide: every load is 128 bits = 8 fp16 (§4.5 thread_vectorized_split_k).
+// What the page leaves implicit, and what sets the achieved bandwidth here, is
+// the number of bytes in flight per SM (HBM latency x per-SM bandwidth, about
+// 40 KB).  Each lane keeps two groups of GROUP 16-byte loads in flight: the
+// loads of group g+1 are issued before group g is consumed (explicit double
+// buffering), so a warp always has 4-8 KB outstanding.
+// The per-lane FP32 partial sums are combined with warp shuffles (§4.6
+// Reduction: thread all-reduce lowered to shuffles) and y[n] is written once
+// with cvt.rn.  W is streamed with L1::no_allocate so it does not evict x,
+// which every warp re-reads from L1.  No atomics: results are deterministic.
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -24,12 +29,12 @@ namespace tmagemm {
 
 namespace {
 
-constexpr int kGemvWarps = 4;     // rows per block
-constexpr int kGemvUnroll = 8;    // 16-byte loads in flight per lane
+constexpr int kGvWarps = 8;      // rows per block
+constexpr int kGvGroup = 4;      // 16-byte loads per lane per group
 
 __device__ __forceinline__ uint4 ld_stream_v4(const uint4* p) {
     uint4 r;
-    asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+    asm volatile("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
                  : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
                  : "l"(p));
     return r;
@@ -48,32 +53,48 @@ __device__ __forceinline__ float dot8(const uint4& w, const uint4& x, float acc)
     return acc;
 }
 
-template <int WARPS, int UNROLL>
-__global__ void __launch_bounds__(WARPS * 32)
+// This lane's chunks idx0 + 32*u, u < GROUP.
+__device__ __forceinline__ void load_group(const uint4* wrow, int32_t idx0, uint4 (&w)[kGvGroup]) {
+#pragma unroll
+    for (int u = 0; u < kGvGroup; ++u) w[u] = ld_stream_v4(wrow + idx0 + 32 * u);
+}
+
+__device__ __forceinline__ void consume_group(const uint4* __restrict__ x, int32_t idx0,
+                                              const uint4 (&w)[kGvGroup], float (&acc)[kGvGroup]) {
+#pragma unroll
+    for (int u = 0; u < kGvGroup; ++u) acc[u] = dot8(w[u], __ldg(x + idx0 + 32 * u), acc[u]);
+}
+
+__global__ void __launch_bounds__(kGvWarps * 32)
 gemv_f16_kernel(const uint4* __restrict__ x, const uint4* __restrict__ W, __half* __restrict__ y,
                 int32_t N, int32_t K8) {
     const int lane = threadIdx.x & 31;
-    const int32_t n = blockIdx.x * WARPS + (threadIdx.x >> 5);
+    const int32_t n = blockIdx.x * kGvWarps + (threadIdx.x >> 5);
     if (n >= N) return;
     const uint4* wrow = W + static_cast<int64_t>(n) * K8;
-    float acc = 0.f;
-    // Main part: whole groups of 32 * UNROLL chunks, no predicates.
-    const int32_t k_main = (K8 / (32 * UNROLL)) * (32 * UNROLL);
-    for (int32_t base = lane; base < k_main; base += 32 * UNROLL) {
-        uint4 wv[UNROLL], xv[UNROLL];
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) wv[u] = ld_stream_v4(wrow + base + 32 * u);
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) xv[u] = __ldg(x + base + 32 * u);
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) acc = dot8(wv[u], xv[u], acc);
+    float acc[kGvGroup] = {};
+    // Whole groups: group g covers this lane's chunks lane + 32*(g*GROUP + u).
+    constexpr int32_t kStep = 32 * kGvGroup;
+    const int32_t groups = K8 / kStep;
+    uint4 wa[kGvGroup], wb[kGvGroup];
+    if (groups > 0) load_group(wrow, lane, wa);
+    for (int32_t g = 0; g < groups; g += 2) {
+        const int32_t ia = lane + g * kStep;
+        const int32_t ib = ia + kStep;
+        if (g + 1 < groups) load_group(wrow, ib, wb);
+        consume_group(x, ia, wa, acc);
+        if (g + 2 < groups) load_group(wrow, ib + kStep, wa);
+        if (g + 1 < groups) consume_group(x, ib, wb, acc);
     }
-    // Tail: the remaining (< 32 * UNROLL) chunks, one per lane per step.
-    for (int32_t idx = k_main + lane; idx < K8; idx += 32)
-        acc = dot8(ld_stream_v4(wrow + idx), __ldg(x + idx), acc);
+    // Tail: the remaining (< 32 * GROUP) chunks, one per lane per step.
+    for (int32_t idx = groups * kStep + lane; idx < K8; idx += 32)
+        acc[0] = dot8(ld_stream_v4(wrow + idx), __ldg(x + idx), acc[0]);
+    float s = acc[0];
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) y[n] = __float2half_rn(acc);
+    for (int u = 1; u < kGvGroup; ++u) s += acc[u];
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if (lane == 0) y[n] = __float2half_rn(s);
 }
 
 }  // namespace
@@ -81,9 +102,8 @@ gemv_f16_kernel(const uint4* __restrict__ x, const uint4* __restrict__ W, __half
 cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y,
                         cudaStream_t stream) {
     const int32_t K8 = static_cast<int32_t>(K / 8);
-    const int64_t blocks = (N + kGemvWarps - 1) / kGemvWarps;
-    gemv_f16_kernel<kGemvWarps, kGemvUnroll><<<static_cast<unsigned>(blocks), kGemvWarps * 32, 0,
-                                               stream>>>(
+    const int64_t blocks = (N + kGvWarps - 1) / kGvWarps;
+    gemv_f16_kernel<<<static_cast<unsigned>(blocks), kGvWarps * 32, 0, stream>>>(
         static_cast<const uint4*>(x), static_cast<const uint4*>(W), static_cast<__half*>(y),
         static_cast<int32_t>(N), K8);
     return cudaGetLastError();

@@ -31,9 +31,12 @@ struct GemmArgs {
 cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream);
 
-// Enqueue the GEMV kernel: y[n] = sum_k x[k] * W[n][k].
+// Enqueue the GEMV kernel: y[n] = sum_k x[k] * W[n][k]; one warp per row.
 cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y,
                         cudaStream_t stream);
+
+// Tile-N override for the GEMM plan (0 = automatic); a tuning/test knob.
+extern int g_force_tile_n;
 
 // Enqueue a one-block kernel that waits on an mbarrier nobody arrives on, with
 // the given limit; it must end by recording kSiteTest in the error word.

@@ -27,12 +27,6 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-__device__ __forceinline__ uint64_t globaltimer_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
 // One lane of the (fully active) warp returns true.
 __device__ __forceinline__ bool elect_one() {
     uint32_t pred = 0;
@@ -98,6 +92,19 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
+// Non-blocking probe: true once the phase with parity `parity` has completed.
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P;\n\t"
+        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 P, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, P;\n\t}"
+        : "=r"(ok)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // ----------------------------------------------------------- error word ----
 
 // Wait-site ids recorded in the error word (bits 0..7).
@@ -109,6 +116,8 @@ enum WaitSite : uint32_t {
     kSiteDrainFull = 5,
     kSiteDrainMma = 6,
     kSiteTest = 7,
+    kSiteGemvFull = 8,
+    kSiteGemvX = 9,
 };
 
 // Sticky per-device error word: 0 = fine, otherwise site | (block << 8).
@@ -117,6 +126,12 @@ __device__ __forceinline__ void record_error(uint32_t* err_word, uint32_t site) 
     atomicCAS(err_word, 0u, code == 0u ? 1u : code);
 }
 
+// Waits are timed with the SM cycle counter (cheap to read, unlike the global
+// timer).  A limit in nanoseconds is converted at 2.5 cycles/ns, above the
+// maximum SM clock, so the real time before giving up is never shorter than
+// the limit (about 1.2x at the 2.07 GHz maximum, more at lower clocks).
+__device__ __forceinline__ uint64_t limit_cycles(uint64_t limit_ns) { return limit_ns * 5u / 2u; }
+
 // Polls `bar` for `parity`.  Gives up (returns false) when the CTA-wide abort
 // flag is raised by another role, or after `limit_ns`, in which case it raises
 // the flag itself and records `site` in the device error word.
@@ -124,11 +139,32 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               volatile int* abort_flag, uint32_t* err_word,
                                               uint32_t site, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const uint64_t t0 = clock64();
+    const uint64_t lim = limit_cycles(limit_ns);
     for (uint32_t spin = 0;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
-        if ((spin & 15u) == 15u && globaltimer_ns() - t0 > limit_ns) {
+        if ((spin & 15u) == 15u && static_cast<uint64_t>(clock64()) - t0 > lim) {
+            *abort_flag = 1;
+            record_error(err_word, site);
+            return false;
+        }
+    }
+}
+
+// Like wait_or_abort, but polls with the non-blocking test_wait instead of
+// letting try_wait suspend the thread: for waits on the critical path of a
+// latency-bound loop, where the wake-up delay of a suspended thread shows.
+__device__ __forceinline__ bool poll_or_abort(uint32_t bar, uint32_t parity,
+                                              volatile int* abort_flag, uint32_t* err_word,
+                                              uint32_t site, uint64_t limit_ns) {
+    if (mbar_test_wait(bar, parity)) return true;
+    const uint64_t t0 = clock64();
+    const uint64_t lim = limit_cycles(limit_ns);
+    for (uint32_t spin = 0;; ++spin) {
+        if (mbar_test_wait(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if ((spin & 63u) == 63u && static_cast<uint64_t>(clock64()) - t0 > lim) {
             *abort_flag = 1;
             record_error(err_word, site);
             return false;
@@ -141,10 +177,11 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ bool wait_bounded(uint32_t bar, uint32_t parity, uint32_t* err_word,
                                              uint32_t site, uint64_t limit_ns) {
     if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
+    const uint64_t t0 = clock64();
+    const uint64_t lim = limit_cycles(limit_ns);
     for (uint32_t spin = 0;; ++spin) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((spin & 15u) == 15u && globaltimer_ns() - t0 > limit_ns) {
+        if ((spin & 15u) == 15u && static_cast<uint64_t>(clock64()) - t0 > lim) {
             record_error(err_word, site);
             return false;
         }
