@@ -386,6 +386,8 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1)
     tg.check(stream)
 
+    extras = measure_extras(tg, dev, stream, l2)
+
     peaks, peak_src = load_peaks()
     gemm_avg_s = gemm_total_ms / 1e3 / args.steps
     gemv_avg_s = gemv_total_ms / 1e3 / args.steps
@@ -425,6 +427,7 @@ def run_ours(args, rank, world, local_rank):
                 "d2h_bytes_per_step": int(hD.numel() * 2),
                 "steps": e2e_steps, "what": "pinned host A,B -> device, gemm_f16, D -> pinned host"},
         "gpu_launches": launches,
+        "extras": extras,
         "wall_s_timed_region": wall,
         "clocks": clk,
         "device": props.name,
@@ -434,6 +437,61 @@ def run_ours(args, rank, world, local_rank):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def _time_launches(fn, reps, stream):
+    """Average device time of `fn` over `reps` back-to-back launches (events on `stream`)."""
+    import torch
+    for _ in range(3):
+        fn(0)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(reps):
+        fn(i)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) * 1e3 / reps
+
+
+def measure_extras(tg, dev, stream, l2):
+    """Rows beyond the headline path, each against the plain kernel on the same
+    shape: split-K GEMM on a shape with few output tiles and a long K."""
+    import torch
+    from tma_pipelined_tensor_tn_gb300 import inputs
+    sh = stream.cuda_stream
+    out = {}
+    M, N, K = 1024, 1024, 16384
+    A, B = inputs.gemm_inputs(M, N, K, seed=7)
+    sets = inputs.l2_rotation_count(2 * (M * K + N * K), l2)
+    ops = [(A.to(dev), B.to(dev)) if i == 0 else None for i in range(sets)]
+    for i in range(1, sets):
+        ops[i] = (ops[0][0].clone(), ops[0][1].clone())
+    D = torch.empty((M, N), dtype=torch.float16, device=dev)
+    need = tg.gemm_f16_splitk_workspace_size(M, N, K, 0)
+    ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+    plan = tg.tmagemm_gemm_plan(M, N, K, torch.cuda.get_device_properties(dev).multi_processor_count, 0)
+
+    def plain(i):
+        a, b = ops[i % sets]
+        assert tg.gemm_f16(M, N, K, a.data_ptr(), b.data_ptr(), D.data_ptr(), sh) == 0
+
+    def split(i):
+        a, b = ops[i % sets]
+        assert tg.gemm_f16_splitk(M, N, K, a.data_ptr(), b.data_ptr(), D.data_ptr(), 0,
+                                  ws.data_ptr(), need, sh) == 0
+
+    t_plain = _time_launches(plain, 50, stream)
+    t_split = _time_launches(split, 50, stream)
+    tg.check(stream)
+    fl = gemm_flops(M, N, K)
+    out["splitk_1024x1024x16384"] = {
+        "splits": plan["splits"], "units": plan["units"], "tile_n": plan["BN"],
+        "us_splitk": t_split, "us_plain": t_plain,
+        "tflops_splitk": fl / t_split / 1e6, "tflops_plain": fl / t_plain / 1e6,
+        "speedup": t_plain / t_split, "workspace_bytes": need,
+        "note": "split-K time includes the FP32 partial reduction kernel"}
+    return out
 
 
 def main(argv=None):

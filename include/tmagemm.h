@@ -47,7 +47,9 @@ typedef enum {
     TMAGEMM_ERR_UNSUPPORTED = -3,  /* a dimension >= 2^31, or no sm_100-family
                                       device                                     */
     TMAGEMM_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed          */
-    TMAGEMM_ERR_TIMEOUT = -5       /* a device-side pipeline wait timed out      */
+    TMAGEMM_ERR_TIMEOUT = -5,      /* a device-side pipeline wait timed out      */
+    TMAGEMM_ERR_WORKSPACE = -6     /* split-K workspace missing, misaligned or
+                                      smaller than required                      */
 } tmagemm_status;
 
 /*
@@ -69,6 +71,36 @@ typedef enum {
  */
 int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
              void* stream);
+
+/*
+ * Split-K form of gemm_f16 for shapes with too few output tiles to fill the
+ * GPU (e.g. small M x N with long K): the K range is cut into `splits` parts,
+ * each (tile, part) is one work unit of the same persistent tcgen05 kernel,
+ * every unit writes its FP32 partial tile to `workspace`, and a second kernel
+ * adds the partials in part order and rounds once to fp16.  Partial sums
+ * across blocks need an FP32 destination and one final conversion
+ * ("Learning TileLang with GEMV", §5.2 block_split_k).
+ *   splits         : 0 = choose automatically; otherwise the requested count,
+ *                    clamped so that every part has at least one 64-wide
+ *                    k-block.  If the plan ends with one part, the plain
+ *                    kernel runs and the workspace is not touched.
+ *   workspace      : device pointer, 16-byte aligned, at least
+ *                    gemm_f16_splitk_workspace_size(M, N, K, splits) bytes;
+ *                    caller-owned scratch, overwritten, no initial contents
+ *                    needed.  Calls that overlap on the GPU must not share it.
+ *   workspace_bytes: its size.
+ * Other arguments, requirements and status codes as gemm_f16, plus
+ * TMAGEMM_ERR_WORKSPACE.  Results are deterministic (fixed summation order).
+ */
+int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+                    int64_t splits, void* workspace, int64_t workspace_bytes, void* stream);
+
+/*
+ * Bytes of workspace gemm_f16_splitk needs for (M, N, K, splits) on the
+ * current device (splits = 0: the automatic choice): parts x M x N x 4, or 0
+ * when no split is made.  Negative values are status codes.
+ */
+int64_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int64_t splits);
 
 /*
  * y = fp16(x * W^T), accumulated in FP32 ("Learning TileLang with GEMV",
@@ -143,12 +175,13 @@ int tmagemm_tile_coord(int64_t tile, int64_t grid_m, int64_t grid_n, int64_t gro
 int tmagemm_ring_position(int64_t it, int64_t stages, int64_t* stage, int64_t* phase);
 
 /*
- * The GEMM launch configuration for (M, N, K) on a device with `num_sms` SMs:
- * tile sizes, pipeline stages, tile count, grid size, threads per block and
- * dynamic shared memory bytes, written to out[0..7] in that order
- * (BM, BN, BK, STAGES, tiles, grid, threads, smem).  No GPU needed.
+ * The GEMM launch configuration for (M, N, K) on a device with `num_sms` SMs
+ * and a split request (1 = gemm_f16, 0 = automatic split-K, > 1 = that many
+ * parts): written to out[0..10] in the order BM, BN, BK, STAGES, tiles, grid,
+ * threads, smem bytes, parts, k-blocks per part, work units.  No GPU needed.
  */
-int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t* out);
+int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t splits,
+                      int64_t* out);
 
 #ifdef __cplusplus
 }

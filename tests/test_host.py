@@ -40,7 +40,7 @@ def test_library_exports_every_header_symbol():
 
 
 def test_strerror_covers_all_codes():
-    for code in (0, -1, -2, -3, -4, -5):
+    for code in (0, -1, -2, -3, -4, -5, -6):
         assert tg.strerror(code) and tg.strerror(code) != "unknown status"
     assert tg.strerror(12345) == "unknown status"
 
@@ -68,6 +68,8 @@ def test_gemm_null_and_misaligned_pointers():
     assert tg.gemm_f16(1, 250, 260, p, p, p, None) == tg.TMAGEMM_ERR_ALIGN
     assert tg.gemv_f16(4096, 14336, p, p, p + 4, None) == tg.TMAGEMM_ERR_ALIGN
     assert tg.gemv_f16(4096, 0, p, p, p, None) == tg.TMAGEMM_ERR_INVALID
+    assert tg.gemm_f16_splitk(256, 256, 256, p, p, p, -1, p, 1 << 20, None) == tg.TMAGEMM_ERR_INVALID
+    assert tg.gemm_f16_splitk(256, 256, 260, p, p, p, 2, p, 1 << 20, None) == tg.TMAGEMM_ERR_ALIGN
 
 
 def test_group_m_order_golden():
@@ -190,6 +192,26 @@ def test_tile_width_override():
     finally:
         assert tg.tmagemm_set_tile_n(0) == tg.TMAGEMM_OK
     assert tg.tmagemm_gemm_plan(4096, 4096, 4096, 152)["BN"] == 224
+
+
+@pytest.mark.parametrize("M,N,K,splits", [(1024, 1024, 16384, 0), (256, 256, 256, 8),
+                                          (129, 264, 1000, 5), (4000, 3000, 4160, 2),
+                                          (300, 520, 8, 3), (1000, 1000, 4160, 3)])
+def test_splitk_plan_has_no_empty_part(M, N, K, splits):
+    p = tg.tmagemm_gemm_plan(M, N, K, 152, splits)
+    kb = -(-K // p["BK"])
+    assert 1 <= p["splits"] <= kb
+    assert (p["splits"] - 1) * p["kb_per_unit"] < kb <= p["splits"] * p["kb_per_unit"]
+    assert p["units"] == p["tiles"] * p["splits"]
+    assert p["grid"] == min(p["units"], 152)
+    if splits > 1:
+        assert p["splits"] == min(splits, -(-kb // p["kb_per_unit"]))
+
+
+def test_splitk_auto_plan_fills_the_gpu():
+    p = tg.tmagemm_gemm_plan(1024, 1024, 16384, 152, 0)
+    assert p["splits"] > 1 and p["units"] <= 152 and p["units"] > 152 // 2
+    assert tg.tmagemm_gemm_plan(4096, 4096, 4096, 152, 0)["splits"] == 1
 
 
 def test_persistent_schedule_visits_every_tile_once():

@@ -11,11 +11,15 @@ from ._binding import (  # noqa: F401
     TMAGEMM_ERR_INVALID,
     TMAGEMM_ERR_TIMEOUT,
     TMAGEMM_ERR_UNSUPPORTED,
+    TMAGEMM_ERR_WORKSPACE,
     TMAGEMM_OK,
     TmaGemmError,
     check,
     gemm,
     gemm_f16,
+    gemm_f16_splitk,
+    gemm_f16_splitk_workspace_size,
+    gemm_splitk,
     gemv,
     gemv_f16,
     lib,

@@ -19,6 +19,7 @@ TMAGEMM_ERR_ALIGN = -2
 TMAGEMM_ERR_UNSUPPORTED = -3
 TMAGEMM_ERR_CUDA = -4
 TMAGEMM_ERR_TIMEOUT = -5
+TMAGEMM_ERR_WORKSPACE = -6
 
 # Every symbol include/tmagemm.h declares, with (argtypes, restype).
 _i64, _p, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
@@ -26,6 +27,8 @@ _P64 = ctypes.POINTER(ctypes.c_int64)
 SIGNATURES = {
     "gemm_f16": ([_i64, _i64, _i64, _p, _p, _p, _p], _int),
     "gemv_f16": ([_i64, _i64, _p, _p, _p, _p], _int),
+    "gemm_f16_splitk": ([_i64, _i64, _i64, _p, _p, _p, _i64, _p, _i64, _p], _int),
+    "gemm_f16_splitk_workspace_size": ([_i64, _i64, _i64, _i64], _i64),
     "tmagemm_check": ([_p], _int),
     "tmagemm_last_error_detail": ([], _int),
     "tmagemm_strerror": ([_int], ctypes.c_char_p),
@@ -33,7 +36,7 @@ SIGNATURES = {
     "tmagemm_selftest_wait_timeout": ([_i64, _p], _int),
     "tmagemm_tile_coord": ([_i64, _i64, _i64, _i64, _P64, _P64], _int),
     "tmagemm_ring_position": ([_i64, _i64, _P64, _P64], _int),
-    "tmagemm_gemm_plan": ([_i64, _i64, _i64, _i64, _P64], _int),
+    "tmagemm_gemm_plan": ([_i64, _i64, _i64, _i64, _i64, _P64], _int),
     "tmagemm_set_tile_n": ([_int], _int),
 }
 
@@ -73,6 +76,14 @@ def strerror(status: int) -> str:
 
 def gemm_f16(M, N, K, A, B, D, stream=None) -> int:
     return lib().gemm_f16(M, N, K, A, B, D, stream)
+
+
+def gemm_f16_splitk(M, N, K, A, B, D, splits, workspace, workspace_bytes, stream=None) -> int:
+    return lib().gemm_f16_splitk(M, N, K, A, B, D, splits, workspace, workspace_bytes, stream)
+
+
+def gemm_f16_splitk_workspace_size(M, N, K, splits) -> int:
+    return lib().gemm_f16_splitk_workspace_size(M, N, K, splits)
 
 
 def gemv_f16(N, K, x, W, y, stream=None) -> int:
@@ -115,12 +126,13 @@ def tmagemm_ring_position(it, stages):
     return st.value, ph.value
 
 
-def tmagemm_gemm_plan(M, N, K, num_sms):
-    out = (ctypes.c_int64 * 8)()
-    s = lib().tmagemm_gemm_plan(M, N, K, num_sms, out)
+def tmagemm_gemm_plan(M, N, K, num_sms, splits=1):
+    out = (ctypes.c_int64 * 11)()
+    s = lib().tmagemm_gemm_plan(M, N, K, num_sms, splits, out)
     if s != TMAGEMM_OK:
         raise TmaGemmError(s, "tmagemm_gemm_plan")
-    keys = ("BM", "BN", "BK", "STAGES", "tiles", "grid", "threads", "smem")
+    keys = ("BM", "BN", "BK", "STAGES", "tiles", "grid", "threads", "smem", "splits",
+            "kb_per_unit", "units")
     return dict(zip(keys, list(out)))
 
 
@@ -162,6 +174,33 @@ def gemm(A, B, out=None, stream=None):
                            _stream_handle(stream, A.device))
     if s != TMAGEMM_OK:
         raise TmaGemmError(s, "gemm_f16")
+    return out
+
+
+def gemm_splitk(A, B, workspace=None, splits=0, out=None, stream=None):
+    """Split-K D = A @ B.T; `workspace` is a CUDA tensor of at least
+    gemm_f16_splitk_workspace_size(...) bytes (allocated here if None)."""
+    import torch
+    _check_f16_cuda("A", A)
+    _check_f16_cuda("B", B)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("A and B must share K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=A.device)
+    _check_f16_cuda("out", out)
+    with torch.cuda.device(A.device):
+        need = lib().gemm_f16_splitk_workspace_size(M, N, K, splits)
+        if need < 0:
+            raise TmaGemmError(int(need), "gemm_f16_splitk_workspace_size")
+        if workspace is None:
+            workspace = torch.empty((max(int(need), 16),), dtype=torch.uint8, device=A.device)
+        s = lib().gemm_f16_splitk(M, N, K, A.data_ptr(), B.data_ptr(), out.data_ptr(), splits,
+                                  workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                  _stream_handle(stream, A.device))
+    if s != TMAGEMM_OK:
+        raise TmaGemmError(s, "gemm_f16_splitk")
     return out
 
 

@@ -99,6 +99,19 @@ int encode_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, 
     return r == CUDA_SUCCESS ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 
+// FP32 split-K workspace [splits][rows][cols] as a rank-3 map, box {32, box_rows, 1}.
+int encode_ws_3d(CUtensorMap* map, void* base, uint64_t cols, uint64_t rows, uint64_t splits,
+                 uint32_t box_rows) {
+    cuuint64_t dims[3] = {cols, rows, splits};
+    cuuint64_t strides[2] = {cols * 4, cols * rows * 4};
+    cuuint32_t box[3] = {32, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
+}
+
 int validate_common(int64_t a, int64_t b, int64_t c) {
     if (a <= 0 || b <= 0 || c <= 0) return TMAGEMM_ERR_INVALID;
     const int64_t lim = (int64_t(1) << 31) - 1;
@@ -113,6 +126,40 @@ int gemv_impl(int64_t N, int64_t K, const void* x, const void* W, void* y, void*
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
     cudaError_t e = launch_gemv(N, K, x, W, y, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
+}
+
+// Encodes the tensor maps for `plan` and launches it; for a split-K plan also
+// the reduction of the workspace into D.
+int run_gemm(const GemmPlan& plan, DeviceState* d, int64_t M, int64_t N, int64_t K, const void* A,
+             const void* B, void* D, void* workspace, void* stream) {
+    CUtensorMap tmA, tmB, tmD;
+    if (int s = encode_2d(&tmA, A, K, M, plan.bk, plan.bm, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+        return s;
+    if (int s = encode_2d(&tmB, B, K, N, plan.bk, plan.bn, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+        return s;
+    if (plan.out_f32) {
+        if (int s = encode_ws_3d(&tmD, workspace, N, M, plan.splits, plan.bm)) return s;
+    } else {
+        // Store boxes are one swizzle span wide: 64 columns (128 B) or 32 columns (64 B).
+        const CUtensorMapSwizzle dswz =
+            plan.epi_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+        if (int s = encode_2d(&tmD, D, N, M, plan.epi_cols, plan.bm, dswz,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE))
+            return s;
+    }
+    GemmArgs args;
+    args.M = static_cast<int32_t>(M);
+    args.N = static_cast<int32_t>(N);
+    args.K = static_cast<int32_t>(K);
+    args.wait_limit_ns = wait_limit_ns();
+    args.err_word = d->err_word;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_gemm_tn(plan, tmA, tmB, tmD, args, st);
+    if (e == cudaSuccess && plan.out_f32)
+        e = launch_splitk_reduce(workspace, D, M, N, plan.splits, d->sms, st);
     return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 
@@ -132,28 +179,36 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void
         return TMAGEMM_ERR_ALIGN;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    const GemmPlan plan = plan_gemm(M, N, K, d->sms);
-    CUtensorMap tmA, tmB, tmD;
-    if (int s = encode_2d(&tmA, A, K, M, plan.bk, plan.bm, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
-        return s;
-    if (int s = encode_2d(&tmB, B, K, N, plan.bk, plan.bn, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
-        return s;
-    // Store boxes are one swizzle span wide: 64 columns (128 B) or 32 columns (64 B).
-    const CUtensorMapSwizzle dswz =
-        plan.epi_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    if (int s = encode_2d(&tmD, D, N, M, plan.epi_cols, plan.bm, dswz,
-                          CU_TENSOR_MAP_L2_PROMOTION_NONE))
-        return s;
-    GemmArgs args;
-    args.M = static_cast<int32_t>(M);
-    args.N = static_cast<int32_t>(N);
-    args.K = static_cast<int32_t>(K);
-    args.wait_limit_ns = wait_limit_ns();
-    args.err_word = d->err_word;
-    cudaError_t e = launch_gemm_tn(plan, tmA, tmB, tmD, args, static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
+    return run_gemm(plan_gemm(M, N, K, d->sms, 1), d, M, N, K, A, B, D, nullptr, stream);
+}
+
+int64_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int64_t splits) {
+    if (splits < 0 || splits > 4096) return TMAGEMM_ERR_INVALID;
+    if (int s = validate_common(M, N, K)) return s;
+    if (M == 1) return 0;
+    DeviceState* d = nullptr;
+    if (int s = device_state(&d)) return s;
+    const GemmPlan p = plan_gemm(M, N, K, d->sms, splits == 0 ? 0 : splits);
+    if (p.splits <= 1) return 0;
+    return p.splits * M * N * 4;
+}
+
+int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+                    int64_t splits, void* workspace, int64_t workspace_bytes, void* stream) {
+    if (!A || !B || !D) return TMAGEMM_ERR_INVALID;
+    if (splits < 0 || splits > 4096) return TMAGEMM_ERR_INVALID;
+    if (int s = validate_common(M, N, K)) return s;
+    if (M == 1) return gemv_impl(N, K, A, B, D, stream);
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
+        return TMAGEMM_ERR_ALIGN;
+    DeviceState* d = nullptr;
+    if (int s = device_state(&d)) return s;
+    const GemmPlan p = plan_gemm(M, N, K, d->sms, splits == 0 ? 0 : splits);
+    if (p.splits <= 1)   // nothing to split: the plain kernel, no workspace needed
+        return run_gemm(plan_gemm(M, N, K, d->sms, 1), d, M, N, K, A, B, D, nullptr, stream);
+    if (!workspace || !aligned16(workspace) || workspace_bytes < p.splits * M * N * 4)
+        return TMAGEMM_ERR_WORKSPACE;
+    return run_gemm(p, d, M, N, K, A, B, D, workspace, stream);
 }
 
 int gemv_f16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream) {
@@ -187,6 +242,8 @@ const char* tmagemm_strerror(int status) {
         case TMAGEMM_ERR_UNSUPPORTED: return "unsupported size or device";
         case TMAGEMM_ERR_CUDA: return "CUDA runtime or driver call failed";
         case TMAGEMM_ERR_TIMEOUT: return "device-side pipeline wait timed out";
+        case TMAGEMM_ERR_WORKSPACE:
+            return "split-K workspace missing, not 16-byte aligned, or smaller than required";
         default: return "unknown status";
     }
 }
@@ -218,10 +275,11 @@ int tmagemm_ring_position(int64_t it, int64_t stages, int64_t* stage, int64_t* p
     return TMAGEMM_OK;
 }
 
-int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t* out) {
-    if (!out || num_sms <= 0) return TMAGEMM_ERR_INVALID;
+int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t splits,
+                      int64_t* out) {
+    if (!out || num_sms <= 0 || splits < 0 || splits > 4096) return TMAGEMM_ERR_INVALID;
     if (int s = validate_common(M, N, K)) return s;
-    const GemmPlan p = plan_gemm(M, N, K, static_cast<int>(num_sms));
+    const GemmPlan p = plan_gemm(M, N, K, static_cast<int>(num_sms), splits);
     out[0] = p.bm;
     out[1] = p.bn;
     out[2] = p.bk;
@@ -230,6 +288,9 @@ int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t*
     out[5] = p.grid;
     out[6] = p.threads;
     out[7] = p.smem_bytes;
+    out[8] = p.splits;
+    out[9] = p.kb_per_unit;
+    out[10] = p.units;
     return TMAGEMM_OK;
 }
 

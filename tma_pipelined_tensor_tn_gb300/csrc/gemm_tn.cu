@@ -27,6 +27,14 @@
 // of "高级数据搬运…", 零填充) and clamps out-of-range stores, so interior and
 // edge tiles run the same code.
 //
+// Split-K: the same kernel runs work units (tile, k-split).  With FP32 output
+// (OUT_F32) each unit stores its partial accumulator to a caller-provided
+// workspace [splits][M][N] through a 3-D tensor map, and splitk_reduce sums the
+// partials in split order and rounds to fp16 ("Learning TileLang with GEMV",
+// §5.2 block_split_k: partial sums across blocks need an FP32 destination and
+// one final conversion).  The reduction order is fixed, so results are
+// deterministic.
+//
 // Every mbarrier wait is bounded (see ptx.cuh): on a timeout the CTA raises a
 // shared abort flag, all roles leave their loops, in-flight TMA loads and
 // MMAs are drained, TMEM is freed, and the error word records the site.
@@ -43,13 +51,16 @@ namespace tmagemm {
 
 namespace {
 
-template <int BN_, int EPI_COLS_, int STAGES_>
+template <int BN_, int EPI_COLS_, int STAGES_, bool OUT_F32_>
 struct Cfg {
     static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_;
+    static constexpr bool kOutF32 = OUT_F32_;
     static constexpr int kThreads = 192;            // 6 warps
     static constexpr int kEpiThreads = 128;         // warps 2..5
-    static constexpr int kEpiCols = EPI_COLS_;      // columns per TMA store box
-    static constexpr uint32_t kEpiRowBytes = kEpiCols * 2;       // = the box's swizzle span
+    // One store box row is one swizzle span: 32 or 64 fp16 columns, or 32 fp32.
+    static constexpr int kEpiCols = OUT_F32_ ? 32 : EPI_COLS_;
+    static constexpr uint32_t kEpiElemBytes = OUT_F32_ ? 4 : 2;
+    static constexpr uint32_t kEpiRowBytes = kEpiCols * kEpiElemBytes;
     static constexpr uint32_t kEpiChunks = kEpiRowBytes / 16;    // 16-byte chunks per box row
     static constexpr int kGroupM = 8;               // L2 group height in tiles
     static constexpr uint32_t kABytes = BM * BK * 2;
@@ -70,8 +81,8 @@ struct Cfg {
 
     static_assert(BK * 2 == 128, "a K-major row of one k-block is one 128-byte swizzle atom");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
-    static_assert(kEpiCols == 32 || kEpiCols == 64, "store boxes are 64 or 128 bytes wide");
-    static_assert(BN % kEpiCols == 0, "epilogue boxes tile BN");
+    static_assert(kEpiRowBytes == 64 || kEpiRowBytes == 128, "store boxes are 64 or 128 bytes wide");
+    static_assert(kEpiCols % 32 == 0 && BN % kEpiCols == 0, "epilogue boxes tile BN");
     static_assert(kAccStride + BN <= kTmemCols, "two accumulators fit in TMEM");
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "stages stay 1024-B aligned");
     static_assert(kEpiBufBytes % 1024 == 0, "epilogue boxes stay 1024-B aligned");
@@ -79,16 +90,26 @@ struct Cfg {
 };
 
 // Tile shapes the host plan chooses from (all 128 rows x BN columns x 64 K).
-using Cfg256 = Cfg<256, 64, 4>;
-using Cfg224 = Cfg<224, 32, 4>;
-using Cfg192 = Cfg<192, 64, 4>;
+using Cfg256 = Cfg<256, 64, 4, false>;
+using Cfg224 = Cfg<224, 32, 4, false>;
+using Cfg192 = Cfg<192, 64, 4, false>;
+// Split-K partial-tile variants (FP32 output boxes of 32 columns).
+using Cfg256F = Cfg<256, 32, 4, true>;
+using Cfg224F = Cfg<224, 32, 4, true>;
+using Cfg192F = Cfg<192, 32, 4, true>;
+
+// Work decomposition passed to the kernel.  Unit u covers output tile
+// u % num_tiles and k-blocks [split * kb_per_unit, min(k_blocks, ...)) with
+// split = u / num_tiles.  Without split-K, kb_per_unit = k_blocks.
+struct Work {
+    int32_t N, grid_m, grid_n, num_tiles, num_units, k_blocks, kb_per_unit;
+};
 
 template <class C>
 __global__ void __launch_bounds__(C::kThreads, 1)
 gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmD, const int32_t N, const int32_t grid_m,
-                   const int32_t grid_n, const int32_t num_tiles, const int32_t k_blocks,
-                   const uint64_t limit_ns, uint32_t* __restrict__ err) {
+                   const __grid_constant__ CUtensorMap tmD, const Work w, const uint64_t limit_ns,
+                   uint32_t* __restrict__ err) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Dynamic shared memory is only guaranteed 16-byte aligned: round up.
     const uint32_t raw = smem_u32(smem_raw);
@@ -140,11 +161,14 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         if (elect_one()) {
             uint32_t it = 0;
             bool ok = true;
-            for (int32_t tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const TileCoord tc = tile_coord(tile, grid_m, grid_n, C::kGroupM);
+            for (int32_t u = blockIdx.x; ok && u < w.num_units; u += gridDim.x) {
+                const int32_t tile = u % w.num_tiles;
+                const int32_t kb0 = (u / w.num_tiles) * w.kb_per_unit;
+                const int32_t kb1 = min(w.k_blocks, kb0 + w.kb_per_unit);
+                const TileCoord tc = tile_coord(tile, w.grid_m, w.grid_n, C::kGroupM);
                 const int32_t m0 = tc.m_blk * C::BM;
                 const int32_t n0 = tc.n_blk * C::BN;
-                for (int32_t kb = 0; kb < k_blocks; ++kb) {
+                for (int32_t kb = kb0; kb < kb1; ++kb) {
                     const uint32_t s = ring_stage(it, C::STAGES);
                     const uint32_t ph = ring_phase(it, C::STAGES);
                     if (!wait_or_abort(empty_bar(s), ph ^ 1u, abort_flag, err, kSiteProducerEmpty,
@@ -171,7 +195,9 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         if (elect_one()) {
             uint32_t it = 0, tcount = 0;
             bool ok = true;
-            for (int32_t tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++tcount) {
+            for (int32_t u = blockIdx.x; ok && u < w.num_units; u += gridDim.x, ++tcount) {
+                const int32_t kb0 = (u / w.num_tiles) * w.kb_per_unit;
+                const int32_t kb1 = min(w.k_blocks, kb0 + w.kb_per_unit);
                 const uint32_t acc = tcount & 1u;
                 const uint32_t acc_ph = (tcount >> 1) & 1u;
                 if (!wait_or_abort(acc_empty_bar(acc), acc_ph ^ 1u, abort_flag, err,
@@ -179,7 +205,7 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     break;
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * C::kAccStride;
-                for (int32_t kb = 0; kb < k_blocks; ++kb) {
+                for (int32_t kb = kb0; kb < kb1; ++kb) {
                     const uint32_t s = ring_stage(it, C::STAGES);
                     const uint32_t ph = ring_phase(it, C::STAGES);
                     if (!wait_or_abort(full_bar(s), ph, abort_flag, err, kSiteMmaFull, limit_ns)) {
@@ -193,7 +219,7 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                     for (int j = 0; j < C::BK / 16; ++j) {
                         mma_f16_ss(d_tmem, umma_desc_sw128_kmajor(a_addr + 32u * j),
                                    umma_desc_sw128_kmajor(b_addr + 32u * j), C::kIdesc,
-                                   (kb | j) != 0 ? 1u : 0u);
+                                   (kb != kb0 || j != 0) ? 1u : 0u);
                     }
                     mma_commit(empty_bar(s));   // stage s free once these MMAs finish
                     ++it;
@@ -212,8 +238,10 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         const uint32_t row = quarter * 32u + static_cast<uint32_t>(lane);  // row in tile
         const bool leader = threadIdx.x == 64;
         uint32_t tcount = 0, box = 0;
-        for (int32_t tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++tcount) {
-            const TileCoord tc = tile_coord(tile, grid_m, grid_n, C::kGroupM);
+        for (int32_t u = blockIdx.x; u < w.num_units; u += gridDim.x, ++tcount) {
+            const int32_t tile = u % w.num_tiles;
+            const int32_t split = u / w.num_tiles;
+            const TileCoord tc = tile_coord(tile, w.grid_m, w.grid_n, C::kGroupM);
             const int32_t m0 = tc.m_blk * C::BM;
             const int32_t n0 = tc.n_blk * C::BN;
             const uint32_t acc = tcount & 1u;
@@ -250,17 +278,27 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 const uint32_t xr = ((row * C::kEpiRowBytes) >> 7) & (C::kEpiChunks - 1);
 #pragma unroll
                 for (uint32_t j = 0; j < C::kEpiChunks; ++j) {
-                    const uint32_t p0 = pack_half2_rn(v[8 * j + 0], v[8 * j + 1]);
-                    const uint32_t p1 = pack_half2_rn(v[8 * j + 2], v[8 * j + 3]);
-                    const uint32_t p2 = pack_half2_rn(v[8 * j + 4], v[8 * j + 5]);
-                    const uint32_t p3 = pack_half2_rn(v[8 * j + 6], v[8 * j + 7]);
-                    st_shared_v4(row_addr + ((j ^ xr) << 4), p0, p1, p2, p3);
+                    if constexpr (C::kOutF32) {
+                        st_shared_v4(row_addr + ((j ^ xr) << 4), v[4 * j + 0], v[4 * j + 1],
+                                     v[4 * j + 2], v[4 * j + 3]);
+                    } else {
+                        const uint32_t p0 = pack_half2_rn(v[8 * j + 0], v[8 * j + 1]);
+                        const uint32_t p1 = pack_half2_rn(v[8 * j + 2], v[8 * j + 3]);
+                        const uint32_t p2 = pack_half2_rn(v[8 * j + 4], v[8 * j + 5]);
+                        const uint32_t p3 = pack_half2_rn(v[8 * j + 6], v[8 * j + 7]);
+                        st_shared_v4(row_addr + ((j ^ xr) << 4), p0, p1, p2, p3);
+                    }
                 }
                 fence_proxy_async_smem();
                 named_bar_sync(1, C::kEpiThreads);
                 if (leader) {
                     const int32_t x = n0 + c * C::kEpiCols;
-                    if (x < N) tma_store_2d(&tmD, buf, x, m0);
+                    if (x < w.N) {
+                        if constexpr (C::kOutF32)
+                            tma_store_3d(&tmD, buf, x, m0, split);
+                        else
+                            tma_store_2d(&tmD, buf, x, m0);
+                    }
                     bulk_commit_group();
                 }
             }
@@ -277,12 +315,32 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
 }
 
-}  // namespace
-
-namespace {
+// D[m][n] = fp16( sum_{s < S} P[s][m][n] ), summed in split order (deterministic).
+// Each thread handles 8 consecutive outputs: two 16-byte loads per split and one
+// 16-byte store.  Grid-stride over M*N/8 (N % 8 == 0).
+__global__ void __launch_bounds__(256)
+splitk_reduce_kernel(const float4* __restrict__ P, uint4* __restrict__ D, int64_t groups8,
+                     int64_t mn4, int32_t splits) {
+    for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < groups8;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        float4 a = P[2 * g], b = P[2 * g + 1];
+        for (int32_t s = 1; s < splits; ++s) {
+            const float4 pa = P[s * mn4 + 2 * g];
+            const float4 pb = P[s * mn4 + 2 * g + 1];
+            a.x += pa.x; a.y += pa.y; a.z += pa.z; a.w += pa.w;
+            b.x += pb.x; b.y += pb.y; b.z += pb.z; b.w += pb.w;
+        }
+        uint4 o;
+        o.x = pack_half2_rn(__float_as_uint(a.x), __float_as_uint(a.y));
+        o.y = pack_half2_rn(__float_as_uint(a.z), __float_as_uint(a.w));
+        o.z = pack_half2_rn(__float_as_uint(b.x), __float_as_uint(b.y));
+        o.w = pack_half2_rn(__float_as_uint(b.z), __float_as_uint(b.w));
+        D[g] = o;
+    }
+}
 
 template <class C>
-GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms) {
+GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) {
     GemmPlan p{};
     p.bm = C::BM;
     p.bn = C::BN;
@@ -293,18 +351,31 @@ GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms) {
     p.grid_n = ceil_div(N, C::BN);
     p.k_blocks = ceil_div(K, C::BK);
     p.tiles = p.grid_m * p.grid_n;
-    p.grid = static_cast<int>(p.tiles < sms ? p.tiles : sms);
+    if (splits <= 0) {
+        // Automatic: enough units to cover the SMs, at least 4 k-blocks each.
+        splits = sms / p.tiles;
+        const int64_t max_by_k = p.k_blocks / 4 > 0 ? p.k_blocks / 4 : 1;
+        if (splits > max_by_k) splits = max_by_k;
+        if (splits > 16) splits = 16;
+        if (splits < 1) splits = 1;
+    }
+    if (splits > p.k_blocks) splits = p.k_blocks;
+    p.kb_per_unit = ceil_div(p.k_blocks, splits);
+    p.splits = ceil_div(p.k_blocks, p.kb_per_unit);   // no empty split
+    p.units = p.tiles * p.splits;
+    p.grid = static_cast<int>(p.units < sms ? p.units : sms);
     p.threads = C::kThreads;
     p.smem_bytes = static_cast<int>(C::kSmemBytes);
+    p.out_f32 = C::kOutF32;
     return p;
 }
 
-// Modelled time of a plan: the busiest CTA runs ceil(tiles / grid) tiles, and
-// a tile's mainloop costs about BN + 32 units (MMA time grows with BN, the A
-// operand traffic per k-block does not).
+// Modelled time of a plan: the busiest CTA runs ceil(units / grid) units of
+// kb_per_unit k-blocks, and a k-block costs about BN + 32 units of time (MMA
+// time grows with BN, the A operand traffic per k-block does not).
 int64_t plan_cost(const GemmPlan& p) {
-    const int64_t rounds = ceil_div(p.tiles, p.grid);
-    return rounds * (p.bn + 32);
+    const int64_t rounds = ceil_div(p.units, p.grid);
+    return rounds * p.kb_per_unit * (p.bn + 32);
 }
 
 template <class C>
@@ -322,10 +393,16 @@ cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUten
         if (e != cudaSuccess) return e;
         if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
     }
-    kernel<<<plan.grid, C::kThreads, C::kSmemBytes, stream>>>(
-        tmA, tmB, tmD, args.N, static_cast<int32_t>(plan.grid_m), static_cast<int32_t>(plan.grid_n),
-        static_cast<int32_t>(plan.tiles), static_cast<int32_t>(plan.k_blocks), args.wait_limit_ns,
-        args.err_word);
+    Work w;
+    w.N = args.N;
+    w.grid_m = static_cast<int32_t>(plan.grid_m);
+    w.grid_n = static_cast<int32_t>(plan.grid_n);
+    w.num_tiles = static_cast<int32_t>(plan.tiles);
+    w.num_units = static_cast<int32_t>(plan.units);
+    w.k_blocks = static_cast<int32_t>(plan.k_blocks);
+    w.kb_per_unit = static_cast<int32_t>(plan.kb_per_unit);
+    kernel<<<plan.grid, C::kThreads, C::kSmemBytes, stream>>>(tmA, tmB, tmD, w, args.wait_limit_ns,
+                                                             args.err_word);
     return cudaGetLastError();
 }
 
@@ -333,10 +410,18 @@ cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUten
 
 int g_force_tile_n = 0;
 
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms) {
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits) {
     const int64_t sms = num_sms > 0 ? num_sms : 1;
-    const GemmPlan cands[3] = {plan_for<Cfg256>(M, N, K, sms), plan_for<Cfg224>(M, N, K, sms),
-                               plan_for<Cfg192>(M, N, K, sms)};
+    GemmPlan cands[3];
+    if (splits == 1) {
+        cands[0] = plan_for<Cfg256>(M, N, K, sms, 1);
+        cands[1] = plan_for<Cfg224>(M, N, K, sms, 1);
+        cands[2] = plan_for<Cfg192>(M, N, K, sms, 1);
+    } else {
+        cands[0] = plan_for<Cfg256F>(M, N, K, sms, splits);
+        cands[1] = plan_for<Cfg224F>(M, N, K, sms, splits);
+        cands[2] = plan_for<Cfg192F>(M, N, K, sms, splits);
+    }
     const int forced = __atomic_load_n(&g_force_tile_n, __ATOMIC_ACQUIRE);
     GemmPlan best = cands[0];
     for (const GemmPlan& c : cands) {
@@ -351,12 +436,33 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms) {
 
 cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream) {
+    if (!plan.out_f32) {
+        switch (plan.bn) {
+            case 256: return launch_cfg<Cfg256>(plan, tmA, tmB, tmD, args, stream);
+            case 224: return launch_cfg<Cfg224>(plan, tmA, tmB, tmD, args, stream);
+            case 192: return launch_cfg<Cfg192>(plan, tmA, tmB, tmD, args, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (plan.bn) {
-        case 256: return launch_cfg<Cfg256>(plan, tmA, tmB, tmD, args, stream);
-        case 224: return launch_cfg<Cfg224>(plan, tmA, tmB, tmD, args, stream);
-        case 192: return launch_cfg<Cfg192>(plan, tmA, tmB, tmD, args, stream);
+        case 256: return launch_cfg<Cfg256F>(plan, tmA, tmB, tmD, args, stream);
+        case 224: return launch_cfg<Cfg224F>(plan, tmA, tmB, tmD, args, stream);
+        case 192: return launch_cfg<Cfg192F>(plan, tmA, tmB, tmD, args, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_splitk_reduce(const void* partials, void* D, int64_t M, int64_t N,
+                                 int64_t splits, int num_sms, cudaStream_t stream) {
+    const int64_t groups8 = M * N / 8;
+    int64_t blocks = (groups8 + 255) / 256;
+    const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const float4*>(partials), static_cast<uint4*>(D), groups8, M * N / 4,
+        static_cast<int32_t>(splits));
+    return cudaGetLastError();
 }
 
 }  // namespace tmagemm

@@ -12,13 +12,23 @@ namespace tmagemm {
 struct GemmPlan {
     int bm, bn, bk, stages;
     int64_t tiles, grid_m, grid_n, k_blocks;
+    int64_t splits;        // k-splits (1 = plain GEMM, fp16 output)
+    int64_t kb_per_unit;   // k-blocks per work unit
+    int64_t units;         // tiles * splits
     int grid, threads;
     int smem_bytes;
-    int epi_cols;      // columns per epilogue TMA store box
+    int epi_cols;          // columns per epilogue TMA store box
+    bool out_f32;          // split-K partials (FP32 workspace) instead of fp16 D
 };
 
 // Pure function of the problem shape and the SM count (no CUDA calls).
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms);
+// splits == 1: the plain GEMM; splits == 0: choose the split count; else that
+// many splits (clamped so that no split is empty).
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits = 1);
+
+// D = fp16(sum of `splits` FP32 partial M x N matrices laid out back to back).
+cudaError_t launch_splitk_reduce(const void* partials, void* D, int64_t M, int64_t N,
+                                 int64_t splits, int num_sms, cudaStream_t stream);
 
 struct GemmArgs {
     int32_t M, N, K;
@@ -27,7 +37,8 @@ struct GemmArgs {
 };
 
 // Enqueue the GEMM kernel.  Tensor maps: A {K, M} box {bk, bm}; B {K, N} box
-// {bk, bn}; D {N, M} box {epi_cols, bm}; all 128B-swizzled.
+// {bk, bn}; D {N, M} box {epi_cols, bm} (fp16), or for split-K the FP32
+// workspace {N, M, splits} box {32, bm, 1}.
 cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream);
 

@@ -214,6 +214,15 @@ __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int
         : "memory");
 }
 
+// 3-D tiled store (x inner, then y, then z), same rules as the 2-D store.
+__device__ __forceinline__ void tma_store_3d(const void* tmap, uint32_t src, int32_t x, int32_t y,
+                                             int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
+        ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(src)
+        : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
