@@ -48,8 +48,10 @@ typedef enum {
                                       device                                     */
     TMAGEMM_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed          */
     TMAGEMM_ERR_TIMEOUT = -5,      /* a device-side pipeline wait timed out      */
-    TMAGEMM_ERR_WORKSPACE = -6     /* split-K workspace missing, misaligned or
+    TMAGEMM_ERR_WORKSPACE = -6,    /* split-K workspace missing, misaligned or
                                       smaller than required                      */
+    TMAGEMM_ERR_SCRATCH_LIMIT = -7 /* gemm_f16_splitk_noalloc: the problem needs
+                                      more than its fixed 32 MiB scratch         */
 } tmagemm_status;
 
 /*
@@ -94,6 +96,30 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void
  */
 int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
                     int64_t splits, void* workspace, int64_t workspace_bytes, void* stream);
+
+/*
+ * gemm_f16_splitk for callers that cannot allocate device memory — code past a
+ * no-allocation point (cudaMalloc synchronises the device and would stall a
+ * latency-critical loop), plugins whose host framework owns all device memory
+ * and exposes no allocator, or users with a fixed budget set at start-up.
+ * The pages have no counterpart of this entry point: it exists only so that
+ * such callers can use split-K without providing a workspace.
+ *   Same arguments, requirements and results as gemm_f16_splitk, without the
+ *   workspace: the library uses its own fixed array of 32 MiB in device memory
+ *   (part of its device module, so every GPU that loads this entry point holds
+ *   it until the process exits).  The caller still passes A, B and D.
+ *   Problems whose split-K workspace (gemm_f16_splitk_workspace_size) exceeds
+ *   32 MiB are rejected with TMAGEMM_ERR_SCRATCH_LIMIT; nothing is launched.
+ *   No call allocates: no cudaMalloc, cudaFree or allocating library routine.
+ *   The first call on each device looks up the array's device address on
+ *   that device; make that first call before any stream capture.
+ *   Every call shares the one array.  Calls whose kernels may overlap on the
+ *   GPU (different streams, or several host threads) race on it; order them
+ *   on one stream.  Its contents between calls do not matter: each call
+ *   writes every partial it later reads.
+ */
+int gemm_f16_splitk_noalloc(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+                            int64_t splits, void* stream);
 
 /*
  * Bytes of workspace gemm_f16_splitk needs for (M, N, K, splits) on the

@@ -11,6 +11,7 @@ from ._binding import (  # noqa: F401
     TMAGEMM_ERR_INVALID,
     TMAGEMM_ERR_TIMEOUT,
     TMAGEMM_ERR_UNSUPPORTED,
+    TMAGEMM_ERR_SCRATCH_LIMIT,
     TMAGEMM_ERR_WORKSPACE,
     TMAGEMM_OK,
     TmaGemmError,
@@ -18,6 +19,7 @@ from ._binding import (  # noqa: F401
     gemm,
     gemm_f16,
     gemm_f16_splitk,
+    gemm_f16_splitk_noalloc,
     gemm_f16_splitk_workspace_size,
     gemm_splitk,
     gemv,

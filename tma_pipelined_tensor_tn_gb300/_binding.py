@@ -20,6 +20,7 @@ TMAGEMM_ERR_UNSUPPORTED = -3
 TMAGEMM_ERR_CUDA = -4
 TMAGEMM_ERR_TIMEOUT = -5
 TMAGEMM_ERR_WORKSPACE = -6
+TMAGEMM_ERR_SCRATCH_LIMIT = -7
 
 # Every symbol include/tmagemm.h declares, with (argtypes, restype).
 _i64, _p, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
@@ -29,6 +30,7 @@ SIGNATURES = {
     "gemv_f16": ([_i64, _i64, _p, _p, _p, _p], _int),
     "gemm_f16_splitk": ([_i64, _i64, _i64, _p, _p, _p, _i64, _p, _i64, _p], _int),
     "gemm_f16_splitk_workspace_size": ([_i64, _i64, _i64, _i64], _i64),
+    "gemm_f16_splitk_noalloc": ([_i64, _i64, _i64, _p, _p, _p, _i64, _p], _int),
     "tmagemm_check": ([_p], _int),
     "tmagemm_last_error_detail": ([], _int),
     "tmagemm_strerror": ([_int], ctypes.c_char_p),
@@ -80,6 +82,11 @@ def gemm_f16(M, N, K, A, B, D, stream=None) -> int:
 
 def gemm_f16_splitk(M, N, K, A, B, D, splits, workspace, workspace_bytes, stream=None) -> int:
     return lib().gemm_f16_splitk(M, N, K, A, B, D, splits, workspace, workspace_bytes, stream)
+
+
+def gemm_f16_splitk_noalloc(M, N, K, A, B, D, splits, stream=None) -> int:
+    """Split-K GEMM using the library's fixed device scratch (no allocation)."""
+    return lib().gemm_f16_splitk_noalloc(M, N, K, A, B, D, splits, stream)
 
 
 def gemm_f16_splitk_workspace_size(M, N, K, splits) -> int:

@@ -244,6 +244,9 @@ const char* tmagemm_strerror(int status) {
         case TMAGEMM_ERR_TIMEOUT: return "device-side pipeline wait timed out";
         case TMAGEMM_ERR_WORKSPACE:
             return "split-K workspace missing, not 16-byte aligned, or smaller than required";
+        case TMAGEMM_ERR_SCRATCH_LIMIT:
+            return "problem needs more split-K scratch than the fixed 32 MiB of the "
+                   "no-allocation entry point";
         default: return "unknown status";
     }
 }
