@@ -67,6 +67,14 @@ def _load():
             lib.oracle_gemm_f16_at.restype = ctypes.c_int
             lib.oracle_gemv_f16.argtypes = [i64, i64, p, p, p, p, ctypes.c_int]
             lib.oracle_gemv_f16.restype = ctypes.c_int
+            lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+            lib.oracle_bf16_to_double.restype = ctypes.c_double
+            lib.oracle_double_to_bf16.argtypes = [ctypes.c_double]
+            lib.oracle_double_to_bf16.restype = ctypes.c_uint16
+            lib.oracle_gemm_bf16.argtypes = [i64, i64, i64, p, p, p, p, ctypes.c_int]
+            lib.oracle_gemm_bf16.restype = ctypes.c_int
+            lib.oracle_gemv_bf16.argtypes = [i64, i64, p, p, p, p, ctypes.c_int]
+            lib.oracle_gemv_bf16.restype = ctypes.c_int
             _lib = lib
     return _lib
 
@@ -149,3 +157,57 @@ def gemv_f16(x, W, *, return_sum: bool = False, threads: int = 0):
                             _ptr(S) if S is not None else None, int(threads))
     y = y.view(np.float16)
     return (y, S) if return_sum else y
+
+
+# ---- bfloat16 forms (operands and results as raw uint16 bit patterns) --------
+
+def _bits16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"expected uint16 bf16 bit patterns, got {a.dtype}")
+    return a
+
+
+def bf16_to_double(h: int) -> float:
+    """Decode one bfloat16 bit pattern."""
+    return float(_load().oracle_bf16_to_double(int(h) & 0xFFFF))
+
+
+def double_to_bf16(x: float) -> int:
+    """Encode one double to bfloat16 bits, round to nearest, ties to even."""
+    return int(_load().oracle_double_to_bf16(float(x)))
+
+
+def gemm_bf16(A, B, *, return_sum: bool = False, threads: int = 0):
+    """D = bf16_rne(A @ B.T), FP64 accumulation; A (M, K), B (N, K) as uint16
+    bf16 bit patterns.  Returns D as uint16 bit patterns (M, N)."""
+    A, B = _bits16(A), _bits16(B)
+    M, K = A.shape
+    N, K2 = B.shape
+    if K != K2:
+        raise ValueError("A and B must share K")
+    D = np.empty((M, N), dtype=np.uint16)
+    S = np.empty((M, N), dtype=np.float64) if return_sum else None
+    _load().oracle_gemm_bf16(M, N, K, _ptr(A), _ptr(B), _ptr(D),
+                             _ptr(S) if S is not None else None, int(threads))
+    return (D, S) if return_sum else D
+
+
+def gemv_bf16(x, W, *, return_sum: bool = False, threads: int = 0):
+    """y = bf16_rne(x @ W.T), FP64 accumulation; uint16 bf16 bit patterns."""
+    x, W = _bits16(x), _bits16(W)
+    N, K = W.shape
+    if x.shape != (K,):
+        raise ValueError("x must have length K")
+    y = np.empty((N,), dtype=np.uint16)
+    S = np.empty((N,), dtype=np.float64) if return_sum else None
+    _load().oracle_gemv_bf16(N, K, _ptr(x), _ptr(W), _ptr(y),
+                             _ptr(S) if S is not None else None, int(threads))
+    return (y, S) if return_sum else y
+
+
+def bf16_bits_to_float64(a) -> np.ndarray:
+    """Decode an array of bf16 bit patterns through the oracle's codec table."""
+    a = _bits16(a)
+    lut = np.array([bf16_to_double(h) for h in range(65536)])
+    return lut[a]

@@ -29,10 +29,15 @@
  * (1 sign bit, 5 exponent bits with bias 15, 10 fraction bits; exponent 0 =
  * zero/subnormal, exponent 31 = inf/NaN).
  *
+ * The bfloat16 forms (oracle_gemm_bf16, oracle_gemv_bf16) follow the same
+ * definition with bf16 operands and a bf16 result ("TensorCore_GEMM_with_TMA"
+ * runs its TN GEMM in bf16 with FP32 accumulation).
+ *
  * Parity status: every function here is pinned by the CPU tests (exact
  * rational arithmetic on tiny shapes, integer-valued inputs against an exact
  * integer matmul, identity / rank-1 / unit-vector closed forms, transpose
- * symmetry, and the full binary16 decode/encode tables against numpy).
+ * symmetry, the full binary16 decode/encode tables against numpy, and the
+ * bf16 codec against float32 bit patterns and exact rationals).
  */
 #include <math.h>
 #include <stdint.h>
@@ -92,15 +97,62 @@ uint16_t oracle_double_to_half(double x)
     return (uint16_t)(sign | (uint16_t)((e + 15) << 10) | (uint16_t)(q - 1024.0));
 }
 
-/* ---- decode table (a pure function of the codec above) ------------------ */
+/* ---- bfloat16 codec ------------------------------------------------------
+ * bfloat16 keeps the top 16 bits of an IEEE binary32: 1 sign bit, 8 exponent
+ * bits with bias 127, 7 fraction bits (exponent 0 = zero/subnormal, 255 =
+ * inf/NaN).  Decoding and encoding are written from that format, the same
+ * way as the binary16 codec above. */
+
+double oracle_bf16_to_double(uint16_t h)
+{
+    const int sign = (h >> 15) & 1;
+    const int expo = (h >> 7) & 0xff;
+    const int frac = h & 0x7f;
+    double v;
+    if (expo == 0) {
+        v = ldexp((double)frac, -133);                 /* 0.f * 2^-126 */
+    } else if (expo == 255) {
+        v = frac ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(128 + frac), expo - 134);   /* 1.f * 2^(e-127) */
+    }
+    return sign ? -v : v;
+}
+
+uint16_t oracle_double_to_bf16(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    if (isnan(x)) return (uint16_t)(sign | 0x7fc0);
+    double a = fabs(x);
+    if (isinf(a)) return (uint16_t)(sign | 0x7f80);
+    if (a < ldexp(1.0, -126)) {
+        /* subnormal range: value = q * 2^-133, q in [0, 128]; q == 128 is the
+         * smallest normal, which the bit pattern q also encodes. */
+        double q = round_half_even(ldexp(a, 133));
+        return (uint16_t)(sign | (uint16_t)q);
+    }
+    int e2;
+    (void)frexp(a, &e2);
+    int e = e2 - 1;                                 /* 2^e <= a < 2^(e+1) */
+    double q = round_half_even(ldexp(a, 7 - e));    /* in [128, 256] */
+    if (q == 256.0) { q = 128.0; e += 1; }
+    if (e > 127) return (uint16_t)(sign | 0x7f80);  /* overflow -> inf */
+    return (uint16_t)(sign | (uint16_t)((e + 127) << 7) | (uint16_t)(q - 128.0));
+}
+
+/* ---- decode tables (pure functions of the codecs above) ----------------- */
 
 static double g_lut[65536];
+static double g_lut_bf16[65536];
 static int g_lut_ready = 0;
 
 static void build_lut(void)
 {
     if (g_lut_ready) return;
-    for (int h = 0; h < 65536; ++h) g_lut[h] = oracle_half_to_double((uint16_t)h);
+    for (int h = 0; h < 65536; ++h) {
+        g_lut[h] = oracle_half_to_double((uint16_t)h);
+        g_lut_bf16[h] = oracle_bf16_to_double((uint16_t)h);
+    }
     g_lut_ready = 1;
 }
 
@@ -119,6 +171,13 @@ static double dot_f16(const uint16_t* a, const uint16_t* b, int64_t K)
 {
     double acc = 0.0;
     for (int64_t k = 0; k < K; ++k) acc += g_lut[a[k]] * g_lut[b[k]];
+    return acc;
+}
+
+static double dot_bf16(const uint16_t* a, const uint16_t* b, int64_t K)
+{
+    double acc = 0.0;
+    for (int64_t k = 0; k < K; ++k) acc += g_lut_bf16[a[k]] * g_lut_bf16[b[k]];
     return acc;
 }
 
@@ -186,6 +245,49 @@ int oracle_gemv_f16(int64_t N, int64_t K, const uint16_t* x, const uint16_t* W,
         double s = dot_f16(x, W + n * K, K);
         if (sum64) sum64[n] = s;
         y[n] = oracle_double_to_half(s);
+    }
+    return used;
+}
+
+/* ---- bfloat16 forms: the same definitions with bf16 operands and output --
+ * ("TensorCore_GEMM_with_TMA" runs the same TN GEMM in bf16 with FP32
+ * accumulation and a round-to-nearest conversion of the result). */
+
+int oracle_gemm_bf16(int64_t M, int64_t N, int64_t K,
+                     const uint16_t* A, const uint16_t* B,
+                     uint16_t* D, double* sum64, int nthreads)
+{
+    build_lut();
+    int used = 1;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+    used = nthreads;
+    #pragma omp parallel for schedule(dynamic, 1) num_threads(nthreads)
+#endif
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double s = dot_bf16(A + m * K, B + n * K, K);
+            if (sum64) sum64[m * N + n] = s;
+            D[m * N + n] = oracle_double_to_bf16(s);
+        }
+    }
+    return used;
+}
+
+int oracle_gemv_bf16(int64_t N, int64_t K, const uint16_t* x, const uint16_t* W,
+                     uint16_t* y, double* sum64, int nthreads)
+{
+    build_lut();
+    int used = 1;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+    used = nthreads;
+    #pragma omp parallel for schedule(static) num_threads(nthreads)
+#endif
+    for (int64_t n = 0; n < N; ++n) {
+        double s = dot_bf16(x, W + n * K, K);
+        if (sum64) sum64[n] = s;
+        y[n] = oracle_double_to_bf16(s);
     }
     return used;
 }
