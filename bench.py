@@ -491,6 +491,37 @@ def measure_extras(tg, dev, stream, l2):
         "tflops_splitk": fl / t_split / 1e6, "tflops_plain": fl / t_plain / 1e6,
         "speedup": t_plain / t_split, "workspace_bytes": need,
         "note": "split-K time includes the FP32 partial reduction kernel"}
+
+    # bf16 forms of the two headline kernels, same shapes and rotation rules.
+    Mh = Nh = Kh = 4096
+    Ab, Bb = inputs.gemm_inputs(Mh, Nh, Kh, seed=8)
+    Ab, Bb = Ab.to(torch.bfloat16), Bb.to(torch.bfloat16)
+    rs = inputs.l2_rotation_count(int(gemm_bytes()), l2)
+    bsets = [(Ab.to(dev), Bb.to(dev))]
+    for _ in range(rs - 1):
+        bsets.append((bsets[0][0].clone(), bsets[0][1].clone()))
+    Dh = torch.empty((Mh, Nh), dtype=torch.bfloat16, device=dev)
+
+    def gemm_b(i):
+        a, b = bsets[i % rs]
+        assert tg.gemm_bf16(Mh, Nh, Kh, a.data_ptr(), b.data_ptr(), Dh.data_ptr(), sh) == 0
+
+    t_gb = _time_launches(gemm_b, 100, stream)
+    xg, Wg = inputs.gemv_inputs(GEMV_N, GEMV_K, seed=9)
+    rv = inputs.l2_rotation_count(int(gemv_bytes()), l2)
+    vsets = [(xg.to(torch.bfloat16).to(dev), Wg.to(torch.bfloat16).to(dev))]
+    for _ in range(rv - 1):
+        vsets.append((vsets[0][0].clone(), vsets[0][1].clone()))
+    yb = torch.empty((GEMV_N,), dtype=torch.bfloat16, device=dev)
+
+    def gemv_b(i):
+        xv, wv = vsets[i % rv]
+        assert tg.gemv_bf16(GEMV_N, GEMV_K, xv.data_ptr(), wv.data_ptr(), yb.data_ptr(), sh) == 0
+
+    t_vb = _time_launches(gemv_b, 100, stream)
+    tg.check(stream)
+    out["bf16_gemm_4096"] = {"us": t_gb, "tflops": gemm_flops() / t_gb / 1e6}
+    out["bf16_gemv_4096x14336"] = {"us": t_vb, "gbs": gemv_bytes() / t_vb / 1e3}
     return out
 
 

@@ -143,6 +143,19 @@ int64_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int64_t 
 int gemv_f16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream);
 
 /*
+ * bfloat16 forms of gemm_f16 and gemv_f16: A, B, D (x, W, y) hold bf16
+ * values; accumulation is FP32 and each output is rounded once to bf16
+ * (nearest even).  Same kernels, tiles, requirements and status codes; only
+ * the element type of the tensor maps, the MMA operand format and the final
+ * conversion change.  "TensorCore_GEMM_with_TMA" runs this TN GEMM in bf16
+ * (§2.1 init tensor map: CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; §2.3: bf16 output
+ * rounded to nearest).
+ */
+int gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+              void* stream);
+int gemv_bf16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream);
+
+/*
  * Synchronises `stream`, then reads and clears the current device's sticky
  * device-side error word.  Returns TMAGEMM_OK, TMAGEMM_ERR_TIMEOUT (a kernel
  * stopped after a pipeline wait ran out of time) or TMAGEMM_ERR_CUDA.

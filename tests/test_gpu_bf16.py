@@ -1,0 +1,114 @@
+"""GPU parity of the bf16 GEMM and GEMV (gemm_bf16 / gemv_bf16, through the C
+ABI) against the oracle's bf16 definitions.
+
+Tolerance: bf16 keeps 8 significant bits, so one rounding of the result moves
+it by up to 2^-8 relative (half a step of 2^-7).  The fp16 rule's relative
+term (2e-3) is below that, so the bf16 rule is |err| <= 1e-2 + 8e-3*|ref|
+(one bf16 step relative), with the internal gate |err| <= 1 bf16 step of ref
++ 2^-11 as for fp16.  Integer-valued inputs must still match bit for bit."""
+import numpy as np
+import pytest
+
+import oracle
+from tma_pipelined_tensor_tn_gb300 import inputs
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+ATOL, RTOL, SLACK = 1e-2, 8e-3, 2.0 ** -11
+
+
+@pytest.fixture(scope="module")
+def tg():
+    import tma_pipelined_tensor_tn_gb300 as m
+    m.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return m
+
+
+def to_bits(t):
+    return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def bits_value(b):
+    with np.errstate(invalid="ignore"):
+        return (np.asarray(b, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_step(v):
+    a = np.abs(v)
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return 2.0 ** (e - 7)
+
+
+def compare_bf16(gpu_bits, ref_bits, what):
+    g, r = bits_value(gpu_bits), bits_value(ref_bits)
+    assert np.all(np.isfinite(g)), what
+    err = np.abs(g - r)
+    assert np.all(err <= ATOL + RTOL * np.abs(r)), (what, float(err.max()))
+    assert np.all(err <= bf16_step(r) + SLACK), (what, float((err - bf16_step(r)).max()))
+
+
+def uniform_bf16(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.rand(shape, generator=g) * 2 - 1).to(torch.bfloat16)
+
+
+def run(tg, A, B):
+    D = tg.gemm(A.cuda(), B.cuda())
+    tg.check()
+    return to_bits(D)
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 256, 256), (4000, 3000, 4160), (4096, 4096, 4096)])
+def test_gemm_bf16_parity(tg, M, N, K):
+    A, B = uniform_bf16((M, K), M), uniform_bf16((N, K), N + 1)
+    compare_bf16(run(tg, A, B), oracle.gemm_bf16(to_bits(A), to_bits(B)), f"bf16 {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("bn", [256, 224, 192])
+def test_gemm_bf16_each_tile_width(tg, bn):
+    M, N, K = 1031, 1000, 1032
+    A, B = uniform_bf16((M, K), bn), uniform_bf16((N, K), bn + 1)
+    try:
+        assert tg.tmagemm_set_tile_n(bn) == tg.TMAGEMM_OK
+        D = run(tg, A, B)
+    finally:
+        tg.tmagemm_set_tile_n(0)
+    compare_bf16(D, oracle.gemm_bf16(to_bits(A), to_bits(B)), f"bf16 BN={bn}")
+
+
+def test_gemm_bf16_integer_bitexact(tg):
+    M, N, K = 1000, 1024, 4160
+    A = inputs.integer_f16((M, K), seed=70).to(torch.bfloat16)
+    B = inputs.integer_f16((N, K), seed=71).to(torch.bfloat16)
+    assert np.array_equal(run(tg, A, B), oracle.gemm_bf16(to_bits(A), to_bits(B)))
+
+
+def test_gemm_bf16_identity(tg):
+    K, N = 512, 264
+    B = uniform_bf16((N, K), 72)
+    I = torch.eye(K, dtype=torch.bfloat16)
+    assert np.array_equal(run(tg, I, B), np.ascontiguousarray(to_bits(B).T))
+
+
+def test_gemv_bf16_parity_and_m1_route(tg):
+    N, K = 4096, 14336
+    g = torch.Generator().manual_seed(73)
+    x = (torch.randn(K, generator=g) * 0.02).to(torch.bfloat16)
+    W = (torch.randn((N, K), generator=g) * 0.02).to(torch.bfloat16)
+    y = tg.gemv(x.cuda(), W.cuda())
+    tg.check()
+    ref = oracle.gemv_bf16(to_bits(x), to_bits(W))
+    compare_bf16(to_bits(y), ref, "gemv bf16")
+    D = run(tg, x.reshape(1, -1), W)
+    assert np.array_equal(D[0], to_bits(y))
+
+
+def test_gemv_bf16_integer_bitexact(tg):
+    N, K = 1000, 2056
+    x = inputs.integer_f16((K,), seed=74).to(torch.bfloat16)
+    W = inputs.integer_f16((N, K), seed=75).to(torch.bfloat16)
+    y = tg.gemv(x.cuda(), W.cuda())
+    tg.check()
+    assert np.array_equal(to_bits(y), oracle.gemv_bf16(to_bits(x), to_bits(W)))

@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     TmaGemmError,
     check,
     gemm,
+    gemm_bf16,
     gemm_f16,
     gemm_f16_splitk,
     gemm_f16_splitk_noalloc,
@@ -24,6 +25,7 @@ from ._binding import (  # noqa: F401
     gemm_splitk,
     gemv,
     gemv_f16,
+    gemv_bf16,
     lib,
     strerror,
     tmagemm_check,

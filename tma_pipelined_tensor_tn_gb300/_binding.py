@@ -28,6 +28,8 @@ _P64 = ctypes.POINTER(ctypes.c_int64)
 SIGNATURES = {
     "gemm_f16": ([_i64, _i64, _i64, _p, _p, _p, _p], _int),
     "gemv_f16": ([_i64, _i64, _p, _p, _p, _p], _int),
+    "gemm_bf16": ([_i64, _i64, _i64, _p, _p, _p, _p], _int),
+    "gemv_bf16": ([_i64, _i64, _p, _p, _p, _p], _int),
     "gemm_f16_splitk": ([_i64, _i64, _i64, _p, _p, _p, _i64, _p, _i64, _p], _int),
     "gemm_f16_splitk_workspace_size": ([_i64, _i64, _i64, _i64], _i64),
     "gemm_f16_splitk_noalloc": ([_i64, _i64, _i64, _p, _p, _p, _i64, _p], _int),
@@ -78,6 +80,14 @@ def strerror(status: int) -> str:
 
 def gemm_f16(M, N, K, A, B, D, stream=None) -> int:
     return lib().gemm_f16(M, N, K, A, B, D, stream)
+
+
+def gemm_bf16(M, N, K, A, B, D, stream=None) -> int:
+    return lib().gemm_bf16(M, N, K, A, B, D, stream)
+
+
+def gemv_bf16(N, K, x, W, y, stream=None) -> int:
+    return lib().gemv_bf16(N, K, x, W, y, stream)
 
 
 def gemm_f16_splitk(M, N, K, A, B, D, splits, workspace, workspace_bytes, stream=None) -> int:
@@ -152,35 +162,37 @@ def _stream_handle(stream, device):
     return ctypes.c_void_p(stream.cuda_stream)
 
 
-def _check_f16_cuda(name, t):
+def _check_f16_cuda(name, t, dtype=None):
     import torch
+    dtype = dtype or torch.float16
     if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
         raise TypeError(f"{name} must be a CUDA tensor")
-    if t.dtype != torch.float16:
-        raise TypeError(f"{name} must be float16, got {t.dtype}")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous (row-major)")
 
 
 def gemm(A, B, out=None, stream=None):
-    """D = A @ B.T for CUDA fp16 tensors A (M, K), B (N, K); returns D (M, N)."""
+    """D = A @ B.T for CUDA fp16 or bf16 tensors A (M, K), B (N, K); returns D (M, N)."""
     import torch
-    _check_f16_cuda("A", A)
-    _check_f16_cuda("B", B)
+    dt = A.dtype if A.dtype in (torch.float16, torch.bfloat16) else torch.float16
+    _check_f16_cuda("A", A, dt)
+    _check_f16_cuda("B", B, dt)
     M, K = A.shape
     N, K2 = B.shape
     if K != K2:
         raise ValueError("A and B must share K")
     if out is None:
-        out = torch.empty((M, N), dtype=torch.float16, device=A.device)
-    _check_f16_cuda("out", out)
+        out = torch.empty((M, N), dtype=dt, device=A.device)
+    _check_f16_cuda("out", out, dt)
     if tuple(out.shape) != (M, N):
         raise ValueError("out must be (M, N)")
+    fn = lib().gemm_bf16 if dt == torch.bfloat16 else lib().gemm_f16
     with torch.cuda.device(A.device):
-        s = lib().gemm_f16(M, N, K, A.data_ptr(), B.data_ptr(), out.data_ptr(),
-                           _stream_handle(stream, A.device))
+        s = fn(M, N, K, A.data_ptr(), B.data_ptr(), out.data_ptr(), _stream_handle(stream, A.device))
     if s != TMAGEMM_OK:
-        raise TmaGemmError(s, "gemm_f16")
+        raise TmaGemmError(s, "gemm_bf16" if dt == torch.bfloat16 else "gemm_f16")
     return out
 
 
@@ -212,21 +224,22 @@ def gemm_splitk(A, B, workspace=None, splits=0, out=None, stream=None):
 
 
 def gemv(x, W, out=None, stream=None):
-    """y = x @ W.T for CUDA fp16 tensors x (K,), W (N, K); returns y (N,)."""
+    """y = x @ W.T for CUDA fp16 or bf16 tensors x (K,), W (N, K); returns y (N,)."""
     import torch
-    _check_f16_cuda("x", x)
-    _check_f16_cuda("W", W)
+    dt = W.dtype if W.dtype in (torch.float16, torch.bfloat16) else torch.float16
+    _check_f16_cuda("x", x, dt)
+    _check_f16_cuda("W", W, dt)
     N, K = W.shape
     if tuple(x.shape) != (K,):
         raise ValueError("x must be (K,)")
     if out is None:
-        out = torch.empty((N,), dtype=torch.float16, device=W.device)
-    _check_f16_cuda("out", out)
+        out = torch.empty((N,), dtype=dt, device=W.device)
+    _check_f16_cuda("out", out, dt)
+    fn = lib().gemv_bf16 if dt == torch.bfloat16 else lib().gemv_f16
     with torch.cuda.device(W.device):
-        s = lib().gemv_f16(N, K, x.data_ptr(), W.data_ptr(), out.data_ptr(),
-                           _stream_handle(stream, W.device))
+        s = fn(N, K, x.data_ptr(), W.data_ptr(), out.data_ptr(), _stream_handle(stream, W.device))
     if s != TMAGEMM_OK:
-        raise TmaGemmError(s, "gemv_f16")
+        raise TmaGemmError(s, "gemv_bf16" if dt == torch.bfloat16 else "gemv_f16")
     return out
 
 

@@ -86,15 +86,19 @@ int device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Row-major fp16 matrix of `rows` x `cols` (cols contiguous) as a rank-2 map.
+// Row-major 16-bit (fp16 or bf16) matrix of `rows` x `cols` (cols contiguous)
+// as a rank-2 map.
 int encode_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, uint32_t box_cols,
-              uint32_t box_rows, CUtensorMapSwizzle swz, CUtensorMapL2promotion l2) {
+              uint32_t box_rows, CUtensorMapSwizzle swz, CUtensorMapL2promotion l2,
+              bool bf16 = false) {
     cuuint64_t dims[2] = {cols, rows};
     cuuint64_t strides[1] = {cols * 2};
     cuuint32_t box[2] = {box_cols, box_rows};
     cuuint32_t estr[2] = {1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims,
-                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2,
+    const CUtensorMapDataType dt =
+        bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    CUresult r = g_encode(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, l2,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
@@ -119,13 +123,14 @@ int validate_common(int64_t a, int64_t b, int64_t c) {
     return TMAGEMM_OK;
 }
 
-int gemv_impl(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream) {
+int gemv_impl(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream,
+              bool bf16 = false) {
     if (!x || !W || !y) return TMAGEMM_ERR_INVALID;
     if (int s = validate_common(N, K, 1)) return s;
     if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (K % 8) != 0) return TMAGEMM_ERR_ALIGN;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    cudaError_t e = launch_gemv(N, K, x, W, y, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_gemv(N, K, x, W, y, bf16, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 
@@ -135,10 +140,10 @@ int run_gemm(const GemmPlan& plan, DeviceState* d, int64_t M, int64_t N, int64_t
              const void* B, void* D, void* workspace, void* stream) {
     CUtensorMap tmA, tmB, tmD;
     if (int s = encode_2d(&tmA, A, K, M, plan.bk, plan.bm, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, plan.bf16))
         return s;
     if (int s = encode_2d(&tmB, B, K, N, plan.bk, plan.bn, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, plan.bf16))
         return s;
     if (plan.out_f32) {
         if (int s = encode_ws_3d(&tmD, workspace, N, M, plan.splits, plan.bm)) return s;
@@ -147,7 +152,7 @@ int run_gemm(const GemmPlan& plan, DeviceState* d, int64_t M, int64_t N, int64_t
         const CUtensorMapSwizzle dswz =
             plan.epi_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
         if (int s = encode_2d(&tmD, D, N, M, plan.epi_cols, plan.bm, dswz,
-                              CU_TENSOR_MAP_L2_PROMOTION_NONE))
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE, plan.bf16))
             return s;
     }
     GemmArgs args;
@@ -159,7 +164,7 @@ int run_gemm(const GemmPlan& plan, DeviceState* d, int64_t M, int64_t N, int64_t
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_gemm_tn(plan, tmA, tmB, tmD, args, st);
     if (e == cudaSuccess && plan.out_f32)
-        e = launch_splitk_reduce(workspace, D, M, N, plan.splits, d->sms, st);
+        e = launch_splitk_reduce(workspace, D, M, N, plan.splits, plan.bf16, d->sms, st);
     return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 
@@ -213,6 +218,22 @@ int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void* A, const void* 
 
 int gemv_f16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream) {
     return gemv_impl(N, K, x, W, y, stream);
+}
+
+int gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+              void* stream) {
+    if (!A || !B || !D) return TMAGEMM_ERR_INVALID;
+    if (int s = validate_common(M, N, K)) return s;
+    if (M == 1) return gemv_impl(N, K, A, B, D, stream, true);
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
+        return TMAGEMM_ERR_ALIGN;
+    DeviceState* d = nullptr;
+    if (int s = device_state(&d)) return s;
+    return run_gemm(plan_gemm(M, N, K, d->sms, 1, true), d, M, N, K, A, B, D, nullptr, stream);
+}
+
+int gemv_bf16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream) {
+    return gemv_impl(N, K, x, W, y, stream, true);
 }
 
 int tmagemm_check(void* stream) {

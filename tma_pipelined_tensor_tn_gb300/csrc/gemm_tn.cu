@@ -51,10 +51,11 @@ namespace tmagemm {
 
 namespace {
 
-template <int BN_, int EPI_COLS_, int STAGES_, bool OUT_F32_>
+template <int BN_, int EPI_COLS_, int STAGES_, bool OUT_F32_, bool BF16_>
 struct Cfg {
     static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_;
     static constexpr bool kOutF32 = OUT_F32_;
+    static constexpr bool kBF16 = BF16_;           // operands (and D) bf16 instead of fp16
     static constexpr int kThreads = 192;            // 6 warps
     static constexpr int kEpiThreads = 128;         // warps 2..5
     // One store box row is one swizzle span: 32 or 64 fp16 columns, or 32 fp32.
@@ -77,7 +78,7 @@ struct Cfg {
     static constexpr uint32_t kNumBars = 2 * STAGES + 5;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + base alignment slack
-    static constexpr uint32_t kIdesc = umma_idesc_f16_f32(BM, BN);
+    static constexpr uint32_t kIdesc = umma_idesc_16bit_f32(BM, BN, BF16_);
 
     static_assert(BK * 2 == 128, "a K-major row of one k-block is one 128-byte swizzle atom");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
@@ -89,14 +90,15 @@ struct Cfg {
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in shared memory");
 };
 
-// Tile shapes the host plan chooses from (all 128 rows x BN columns x 64 K).
-using Cfg256 = Cfg<256, 64, 4, false>;
-using Cfg224 = Cfg<224, 32, 4, false>;
-using Cfg192 = Cfg<192, 64, 4, false>;
+// Tile shapes the host plan chooses from (all 128 rows x BN columns x 64 K),
+// for fp16 (T = false) and bf16 (T = true) operands.
+template <bool T> using Cfg256 = Cfg<256, 64, 4, false, T>;
+template <bool T> using Cfg224 = Cfg<224, 32, 4, false, T>;
+template <bool T> using Cfg192 = Cfg<192, 64, 4, false, T>;
 // Split-K partial-tile variants (FP32 output boxes of 32 columns).
-using Cfg256F = Cfg<256, 32, 4, true>;
-using Cfg224F = Cfg<224, 32, 4, true>;
-using Cfg192F = Cfg<192, 32, 4, true>;
+template <bool T> using Cfg256F = Cfg<256, 32, 4, true, T>;
+template <bool T> using Cfg224F = Cfg<224, 32, 4, true, T>;
+template <bool T> using Cfg192F = Cfg<192, 32, 4, true, T>;
 
 // Work decomposition passed to the kernel.  Unit u covers output tile
 // u % num_tiles and k-blocks [split * kb_per_unit, min(k_blocks, ...)) with
@@ -282,10 +284,10 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                         st_shared_v4(row_addr + ((j ^ xr) << 4), v[4 * j + 0], v[4 * j + 1],
                                      v[4 * j + 2], v[4 * j + 3]);
                     } else {
-                        const uint32_t p0 = pack_half2_rn(v[8 * j + 0], v[8 * j + 1]);
-                        const uint32_t p1 = pack_half2_rn(v[8 * j + 2], v[8 * j + 3]);
-                        const uint32_t p2 = pack_half2_rn(v[8 * j + 4], v[8 * j + 5]);
-                        const uint32_t p3 = pack_half2_rn(v[8 * j + 6], v[8 * j + 7]);
+                        const uint32_t p0 = pack2_rn<C::kBF16>(v[8 * j + 0], v[8 * j + 1]);
+                        const uint32_t p1 = pack2_rn<C::kBF16>(v[8 * j + 2], v[8 * j + 3]);
+                        const uint32_t p2 = pack2_rn<C::kBF16>(v[8 * j + 4], v[8 * j + 5]);
+                        const uint32_t p3 = pack2_rn<C::kBF16>(v[8 * j + 6], v[8 * j + 7]);
                         st_shared_v4(row_addr + ((j ^ xr) << 4), p0, p1, p2, p3);
                     }
                 }
@@ -315,9 +317,10 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
     }
 }
 
-// D[m][n] = fp16( sum_{s < S} P[s][m][n] ), summed in split order (deterministic).
-// Each thread handles 8 consecutive outputs: two 16-byte loads per split and one
-// 16-byte store.  Grid-stride over M*N/8 (N % 8 == 0).
+// D[m][n] = fp16/bf16( sum_{s < S} P[s][m][n] ), summed in split order
+// (deterministic).  Each thread handles 8 consecutive outputs: two 16-byte
+// loads per split and one 16-byte store.  Grid-stride over M*N/8 (N % 8 == 0).
+template <bool BF16>
 __global__ void __launch_bounds__(256)
 splitk_reduce_kernel(const float4* __restrict__ P, uint4* __restrict__ D, int64_t groups8,
                      int64_t mn4, int32_t splits) {
@@ -331,10 +334,10 @@ splitk_reduce_kernel(const float4* __restrict__ P, uint4* __restrict__ D, int64_
             b.x += pb.x; b.y += pb.y; b.z += pb.z; b.w += pb.w;
         }
         uint4 o;
-        o.x = pack_half2_rn(__float_as_uint(a.x), __float_as_uint(a.y));
-        o.y = pack_half2_rn(__float_as_uint(a.z), __float_as_uint(a.w));
-        o.z = pack_half2_rn(__float_as_uint(b.x), __float_as_uint(b.y));
-        o.w = pack_half2_rn(__float_as_uint(b.z), __float_as_uint(b.w));
+        o.x = pack2_rn<BF16>(__float_as_uint(a.x), __float_as_uint(a.y));
+        o.y = pack2_rn<BF16>(__float_as_uint(a.z), __float_as_uint(a.w));
+        o.z = pack2_rn<BF16>(__float_as_uint(b.x), __float_as_uint(b.y));
+        o.w = pack2_rn<BF16>(__float_as_uint(b.z), __float_as_uint(b.w));
         D[g] = o;
     }
 }
@@ -367,6 +370,7 @@ GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) 
     p.threads = C::kThreads;
     p.smem_bytes = static_cast<int>(C::kSmemBytes);
     p.out_f32 = C::kOutF32;
+    p.bf16 = C::kBF16;
     return p;
 }
 
@@ -410,17 +414,19 @@ cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUten
 
 int g_force_tile_n = 0;
 
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits) {
-    const int64_t sms = num_sms > 0 ? num_sms : 1;
+namespace {
+
+template <bool T>
+GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) {
     GemmPlan cands[3];
     if (splits == 1) {
-        cands[0] = plan_for<Cfg256>(M, N, K, sms, 1);
-        cands[1] = plan_for<Cfg224>(M, N, K, sms, 1);
-        cands[2] = plan_for<Cfg192>(M, N, K, sms, 1);
+        cands[0] = plan_for<Cfg256<T>>(M, N, K, sms, 1);
+        cands[1] = plan_for<Cfg224<T>>(M, N, K, sms, 1);
+        cands[2] = plan_for<Cfg192<T>>(M, N, K, sms, 1);
     } else {
-        cands[0] = plan_for<Cfg256F>(M, N, K, sms, splits);
-        cands[1] = plan_for<Cfg224F>(M, N, K, sms, splits);
-        cands[2] = plan_for<Cfg192F>(M, N, K, sms, splits);
+        cands[0] = plan_for<Cfg256F<T>>(M, N, K, sms, splits);
+        cands[1] = plan_for<Cfg224F<T>>(M, N, K, sms, splits);
+        cands[2] = plan_for<Cfg192F<T>>(M, N, K, sms, splits);
     }
     const int forced = __atomic_load_n(&g_force_tile_n, __ATOMIC_ACQUIRE);
     GemmPlan best = cands[0];
@@ -434,32 +440,47 @@ GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits)
     return best;
 }
 
-cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                           const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream) {
+template <bool T>
+cudaError_t launch_typed(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                         const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream) {
     if (!plan.out_f32) {
         switch (plan.bn) {
-            case 256: return launch_cfg<Cfg256>(plan, tmA, tmB, tmD, args, stream);
-            case 224: return launch_cfg<Cfg224>(plan, tmA, tmB, tmD, args, stream);
-            case 192: return launch_cfg<Cfg192>(plan, tmA, tmB, tmD, args, stream);
+            case 256: return launch_cfg<Cfg256<T>>(plan, tmA, tmB, tmD, args, stream);
+            case 224: return launch_cfg<Cfg224<T>>(plan, tmA, tmB, tmD, args, stream);
+            case 192: return launch_cfg<Cfg192<T>>(plan, tmA, tmB, tmD, args, stream);
             default: return cudaErrorInvalidValue;
         }
     }
     switch (plan.bn) {
-        case 256: return launch_cfg<Cfg256F>(plan, tmA, tmB, tmD, args, stream);
-        case 224: return launch_cfg<Cfg224F>(plan, tmA, tmB, tmD, args, stream);
-        case 192: return launch_cfg<Cfg192F>(plan, tmA, tmB, tmD, args, stream);
+        case 256: return launch_cfg<Cfg256F<T>>(plan, tmA, tmB, tmD, args, stream);
+        case 224: return launch_cfg<Cfg224F<T>>(plan, tmA, tmB, tmD, args, stream);
+        case 192: return launch_cfg<Cfg192F<T>>(plan, tmA, tmB, tmD, args, stream);
         default: return cudaErrorInvalidValue;
     }
 }
 
+}  // namespace
+
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits, bool bf16) {
+    const int64_t sms = num_sms > 0 ? num_sms : 1;
+    return bf16 ? plan_typed<true>(M, N, K, sms, splits) : plan_typed<false>(M, N, K, sms, splits);
+}
+
+cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                           const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream) {
+    return plan.bf16 ? launch_typed<true>(plan, tmA, tmB, tmD, args, stream)
+                     : launch_typed<false>(plan, tmA, tmB, tmD, args, stream);
+}
+
 cudaError_t launch_splitk_reduce(const void* partials, void* D, int64_t M, int64_t N,
-                                 int64_t splits, int num_sms, cudaStream_t stream) {
+                                 int64_t splits, bool bf16, int num_sms, cudaStream_t stream) {
     const int64_t groups8 = M * N / 8;
     int64_t blocks = (groups8 + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
-    splitk_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+    auto kernel = bf16 ? splitk_reduce_kernel<true> : splitk_reduce_kernel<false>;
+    kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
         static_cast<const float4*>(partials), static_cast<uint4*>(D), groups8, M * N / 4,
         static_cast<int32_t>(splits));
     return cudaGetLastError();

@@ -1,4 +1,5 @@
-// M = 1 GEMV on CUDA cores: y[n] = fp16( sum_k x[k] * W[n][k] ), FP32 accumulation.
+// M = 1 GEMV on CUDA cores: y[n] = fp16( sum_k x[k] * W[n][k] ), FP32 accumulation
+// (and the same with bf16 operands and output).
 //
 // The shape reads each W element exactly once (117,440,512 of the 117,477,376
 // algorithmic bytes at N = 4096, K = 14336), so the bound is HBM bandwidth, not
@@ -19,6 +20,7 @@
 // Reduction: thread all-reduce lowered to shuffles) and y[n] is written once
 // with cvt.rn.  W is streamed with L1::no_allocate so it does not evict x,
 // which every warp re-reads from L1.  No atomics: results are deterministic.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -40,13 +42,23 @@ __device__ __forceinline__ uint4 ld_stream_v4(const uint4* p) {
     return r;
 }
 
+// Two packed 16-bit values -> two floats (exact for fp16 and bf16).
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t v) {
+    if constexpr (BF16)
+        return __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v));
+    else
+        return __half22float2(*reinterpret_cast<const __half2*>(&v));
+}
+
+template <bool BF16>
 __device__ __forceinline__ float dot8(const uint4& w, const uint4& x, float acc) {
-    const __half2* wh = reinterpret_cast<const __half2*>(&w);
-    const __half2* xh = reinterpret_cast<const __half2*>(&x);
+    const uint32_t wv[4] = {w.x, w.y, w.z, w.w};
+    const uint32_t xv[4] = {x.x, x.y, x.z, x.w};
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-        const float2 wf = __half22float2(wh[i]);
-        const float2 xf = __half22float2(xh[i]);
+        const float2 wf = unpack2<BF16>(wv[i]);
+        const float2 xf = unpack2<BF16>(xv[i]);
         acc = fmaf(wf.x, xf.x, acc);
         acc = fmaf(wf.y, xf.y, acc);
     }
@@ -59,14 +71,16 @@ __device__ __forceinline__ void load_group(const uint4* wrow, int32_t idx0, uint
     for (int u = 0; u < kGvGroup; ++u) w[u] = ld_stream_v4(wrow + idx0 + 32 * u);
 }
 
+template <bool BF16>
 __device__ __forceinline__ void consume_group(const uint4* __restrict__ x, int32_t idx0,
                                               const uint4 (&w)[kGvGroup], float (&acc)[kGvGroup]) {
 #pragma unroll
-    for (int u = 0; u < kGvGroup; ++u) acc[u] = dot8(w[u], __ldg(x + idx0 + 32 * u), acc[u]);
+    for (int u = 0; u < kGvGroup; ++u) acc[u] = dot8<BF16>(w[u], __ldg(x + idx0 + 32 * u), acc[u]);
 }
 
+template <bool BF16>
 __global__ void __launch_bounds__(kGvWarps * 32)
-gemv_f16_kernel(const uint4* __restrict__ x, const uint4* __restrict__ W, __half* __restrict__ y,
+gemv_f16_kernel(const uint4* __restrict__ x, const uint4* __restrict__ W, uint16_t* __restrict__ y,
                 int32_t N, int32_t K8) {
     const int lane = threadIdx.x & 31;
     const int32_t n = blockIdx.x * kGvWarps + (threadIdx.x >> 5);
@@ -82,29 +96,35 @@ gemv_f16_kernel(const uint4* __restrict__ x, const uint4* __restrict__ W, __half
         const int32_t ia = lane + g * kStep;
         const int32_t ib = ia + kStep;
         if (g + 1 < groups) load_group(wrow, ib, wb);
-        consume_group(x, ia, wa, acc);
+        consume_group<BF16>(x, ia, wa, acc);
         if (g + 2 < groups) load_group(wrow, ib + kStep, wa);
-        if (g + 1 < groups) consume_group(x, ib, wb, acc);
+        if (g + 1 < groups) consume_group<BF16>(x, ib, wb, acc);
     }
     // Tail: the remaining (< 32 * GROUP) chunks, one per lane per step.
     for (int32_t idx = groups * kStep + lane; idx < K8; idx += 32)
-        acc[0] = dot8(ld_stream_v4(wrow + idx), __ldg(x + idx), acc[0]);
+        acc[0] = dot8<BF16>(ld_stream_v4(wrow + idx), __ldg(x + idx), acc[0]);
     float s = acc[0];
 #pragma unroll
     for (int u = 1; u < kGvGroup; ++u) s += acc[u];
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
-    if (lane == 0) y[n] = __float2half_rn(s);
+    if (lane == 0) {
+        if constexpr (BF16)
+            y[n] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+        else
+            y[n] = __half_as_ushort(__float2half_rn(s));
+    }
 }
 
 }  // namespace
 
-cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y,
+cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y, bool bf16,
                         cudaStream_t stream) {
     const int32_t K8 = static_cast<int32_t>(K / 8);
     const int64_t blocks = (N + kGvWarps - 1) / kGvWarps;
-    gemv_f16_kernel<<<static_cast<unsigned>(blocks), kGvWarps * 32, 0, stream>>>(
-        static_cast<const uint4*>(x), static_cast<const uint4*>(W), static_cast<__half*>(y),
+    auto kernel = bf16 ? gemv_f16_kernel<true> : gemv_f16_kernel<false>;
+    kernel<<<static_cast<unsigned>(blocks), kGvWarps * 32, 0, stream>>>(
+        static_cast<const uint4*>(x), static_cast<const uint4*>(W), static_cast<uint16_t*>(y),
         static_cast<int32_t>(N), K8);
     return cudaGetLastError();
 }

@@ -19,16 +19,18 @@ struct GemmPlan {
     int smem_bytes;
     int epi_cols;          // columns per epilogue TMA store box
     bool out_f32;          // split-K partials (FP32 workspace) instead of fp16 D
+    bool bf16;             // bf16 operands and output instead of fp16
 };
 
 // Pure function of the problem shape and the SM count (no CUDA calls).
 // splits == 1: the plain GEMM; splits == 0: choose the split count; else that
 // many splits (clamped so that no split is empty).
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits = 1);
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits = 1,
+                   bool bf16 = false);
 
-// D = fp16(sum of `splits` FP32 partial M x N matrices laid out back to back).
+// D = fp16/bf16(sum of `splits` FP32 partial M x N matrices laid out back to back).
 cudaError_t launch_splitk_reduce(const void* partials, void* D, int64_t M, int64_t N,
-                                 int64_t splits, int num_sms, cudaStream_t stream);
+                                 int64_t splits, bool bf16, int num_sms, cudaStream_t stream);
 
 struct GemmArgs {
     int32_t M, N, K;
@@ -42,8 +44,9 @@ struct GemmArgs {
 cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream);
 
-// Enqueue the GEMV kernel: y[n] = sum_k x[k] * W[n][k]; one warp per row.
-cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y,
+// Enqueue the GEMV kernel: y[n] = sum_k x[k] * W[n][k]; one warp per row;
+// fp16 or bf16 operands and output.
+cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y, bool bf16,
                         cudaStream_t stream);
 
 // Tile-N override for the GEMM plan (0 = automatic); a tuning/test knob.

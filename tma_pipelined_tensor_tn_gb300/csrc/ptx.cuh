@@ -17,6 +17,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 namespace tmagemm {
@@ -330,22 +331,37 @@ __device__ __forceinline__ uint64_t umma_desc_sw128_kmajor(uint32_t smem_addr) {
     return d;
 }
 
-// Instruction descriptor for kind::f16: D fp32, A and B fp16, both K-major,
-// shape M x N (M in {64,128}, N multiple of 16 up to 256).
-__host__ __device__ constexpr uint32_t umma_idesc_f16_f32(uint32_t M, uint32_t N) {
-    return (1u << 4)            // D format: F32
-         | (0u << 7)            // A format: F16
-         | (0u << 10)           // B format: F16
-         | (0u << 15)           // A K-major
-         | (0u << 16)           // B K-major
-         | ((N >> 3) << 17)     // N / 8
-         | ((M >> 4) << 24);    // M / 16
+// Instruction descriptor for kind::f16: D fp32, A and B both fp16 or both
+// bf16 (never mixed), both K-major, shape M x N (M in {64,128}, N multiple of
+// 16 up to 256).
+__host__ __device__ constexpr uint32_t umma_idesc_16bit_f32(uint32_t M, uint32_t N, bool bf16) {
+    return (1u << 4)                    // D format: F32
+         | ((bf16 ? 1u : 0u) << 7)      // A format: F16 (0) or BF16 (1)
+         | ((bf16 ? 1u : 0u) << 10)     // B format: the same as A
+         | (0u << 15)                   // A K-major
+         | (0u << 16)                   // B K-major
+         | ((N >> 3) << 17)             // N / 8
+         | ((M >> 4) << 24);            // M / 16
 }
 
 // Two fp32 -> one packed half2, round to nearest even.
 __device__ __forceinline__ uint32_t pack_half2_rn(uint32_t lo_bits, uint32_t hi_bits) {
     __half2 h = __floats2half2_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
     return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Two fp32 -> one packed bfloat162, round to nearest even.
+__device__ __forceinline__ uint32_t pack_bf162_rn(uint32_t lo_bits, uint32_t hi_bits) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(lo_bits), __uint_as_float(hi_bits));
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t pack2_rn(uint32_t lo_bits, uint32_t hi_bits) {
+    if constexpr (BF16)
+        return pack_bf162_rn(lo_bits, hi_bits);
+    else
+        return pack_half2_rn(lo_bits, hi_bits);
 }
 
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
