@@ -522,6 +522,26 @@ def measure_extras(tg, dev, stream, l2):
     tg.check(stream)
     out["bf16_gemm_4096"] = {"us": t_gb, "tflops": gemm_flops() / t_gb / 1e6}
     out["bf16_gemv_4096x14336"] = {"us": t_vb, "gbs": gemv_bytes() / t_vb / 1e3}
+
+    # Skinny decode GEMMs at the GEMV's weight shape: M tokens x (4096 x 14336).
+    for Ms in (8, 16):
+        Xs = (torch.randn((Ms, GEMV_K), generator=torch.Generator().manual_seed(Ms)) * 0.02).half()
+        xsets = [Xs.to(dev)] * rv
+        Ds = torch.empty((Ms, GEMV_N), dtype=torch.float16, device=dev)
+        wsets = [(vsets[i][1].view(torch.float16)) for i in range(rv)]
+        need_s = tg.gemm_f16_small_m_workspace_size(Ms, GEMV_N, GEMV_K)
+        ws_s = torch.empty((max(need_s, 16),), dtype=torch.uint8, device=dev)
+
+        def small(i, Ms=Ms, Ds=Ds, ws_s=ws_s, need_s=need_s):
+            assert tg.gemm_f16_small_m(Ms, GEMV_N, GEMV_K, xsets[i % rv].data_ptr(),
+                                       wsets[i % rv].data_ptr(), Ds.data_ptr(), ws_s.data_ptr(),
+                                       need_s, sh) == 0
+
+        t_s = _time_launches(small, 100, stream)
+        tg.check(stream)
+        by = 2.0 * (GEMV_N * GEMV_K + Ms * GEMV_K + Ms * GEMV_N)
+        out[f"small_m{Ms}_4096x14336"] = {"us": t_s, "gbs": by / t_s / 1e3,
+                                          "tflops": 2.0 * Ms * GEMV_N * GEMV_K / t_s / 1e6}
     return out
 
 

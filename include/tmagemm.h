@@ -143,6 +143,31 @@ int64_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int64_t 
 int gemv_f16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream);
 
 /*
+ * Skinny GEMM for a few rows of activations, D = fp16(X * W^T) with
+ * 2 <= M <= 64: the decode step of "Learning TileLang with GEMV" (§01 GEMV:
+ * every linear layer is a GEMV when tokens are decoded one by one) for a
+ * batch of M tokens.  Like the GEMV it is bound by reading W once.  The
+ * tcgen05 kernel runs with the roles swapped — W is the 128-row MMA operand
+ * and X (rows past M read as zero) the 16/32/64-wide one — and with K split
+ * so that enough SMs stream W; FP32 partials go to `workspace` and a second
+ * kernel adds them in fixed order, transposes and rounds to fp16.
+ *   X         : device pointer, M x K fp16 row-major (activations).
+ *   W         : device pointer, N x K fp16 row-major (weights).
+ *   D         : device pointer, M x N fp16 row-major.
+ *   workspace : device pointer, 16-byte aligned, at least
+ *               gemm_f16_small_m_workspace_size(M, N, K) bytes; scratch,
+ *               overwritten, no initial contents needed; not shared by calls
+ *               that overlap on the GPU.
+ * Requirements as gemm_f16; M outside [2, 64] returns TMAGEMM_ERR_UNSUPPORTED
+ * (M = 1 is gemv_f16, larger M is gemm_f16).  Deterministic.
+ */
+int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void* W, void* D,
+                     void* workspace, int64_t workspace_bytes, void* stream);
+
+/* Workspace bytes gemm_f16_small_m needs on the current device (negative = status). */
+int64_t gemm_f16_small_m_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
  * bfloat16 forms of gemm_f16 and gemv_f16: A, B, D (x, W, y) hold bf16
  * values; accumulation is FP32 and each output is rounded once to bf16
  * (nearest even).  Same kernels, tiles, requirements and status codes; only

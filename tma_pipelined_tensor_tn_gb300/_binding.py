@@ -29,6 +29,8 @@ SIGNATURES = {
     "gemm_f16": ([_i64, _i64, _i64, _p, _p, _p, _p], _int),
     "gemv_f16": ([_i64, _i64, _p, _p, _p, _p], _int),
     "gemm_bf16": ([_i64, _i64, _i64, _p, _p, _p, _p], _int),
+    "gemm_f16_small_m": ([_i64, _i64, _i64, _p, _p, _p, _p, _i64, _p], _int),
+    "gemm_f16_small_m_workspace_size": ([_i64, _i64, _i64], _i64),
     "gemv_bf16": ([_i64, _i64, _p, _p, _p, _p], _int),
     "gemm_f16_splitk": ([_i64, _i64, _i64, _p, _p, _p, _i64, _p, _i64, _p], _int),
     "gemm_f16_splitk_workspace_size": ([_i64, _i64, _i64, _i64], _i64),
@@ -80,6 +82,40 @@ def strerror(status: int) -> str:
 
 def gemm_f16(M, N, K, A, B, D, stream=None) -> int:
     return lib().gemm_f16(M, N, K, A, B, D, stream)
+
+
+def gemm_f16_small_m(M, N, K, X, W, D, workspace, workspace_bytes, stream=None) -> int:
+    return lib().gemm_f16_small_m(M, N, K, X, W, D, workspace, workspace_bytes, stream)
+
+
+def gemm_f16_small_m_workspace_size(M, N, K) -> int:
+    return lib().gemm_f16_small_m_workspace_size(M, N, K)
+
+
+def gemm_small_m(X, W, workspace=None, out=None, stream=None):
+    """D = X @ W.T for CUDA fp16 X (M, K) with 2 <= M <= 64 and W (N, K)."""
+    import torch
+    _check_f16_cuda("X", X)
+    _check_f16_cuda("W", W)
+    M, K = X.shape
+    N, K2 = W.shape
+    if K != K2:
+        raise ValueError("X and W must share K")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.float16, device=X.device)
+    _check_f16_cuda("out", out)
+    with torch.cuda.device(X.device):
+        need = lib().gemm_f16_small_m_workspace_size(M, N, K)
+        if need < 0:
+            raise TmaGemmError(int(need), "gemm_f16_small_m_workspace_size")
+        if workspace is None:
+            workspace = torch.empty((max(int(need), 16),), dtype=torch.uint8, device=X.device)
+        s = lib().gemm_f16_small_m(M, N, K, X.data_ptr(), W.data_ptr(), out.data_ptr(),
+                                   workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                   _stream_handle(stream, X.device))
+    if s != TMAGEMM_OK:
+        raise TmaGemmError(s, "gemm_f16_small_m")
+    return out
 
 
 def gemm_bf16(M, N, K, A, B, D, stream=None) -> int:

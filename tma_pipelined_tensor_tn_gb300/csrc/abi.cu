@@ -103,16 +103,19 @@ int encode_2d(CUtensorMap* map, const void* base, uint64_t cols, uint64_t rows, 
     return r == CUDA_SUCCESS ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 
-// FP32 split-K workspace [splits][rows][cols] as a rank-3 map, box {32, box_rows, 1}.
+// FP32 split-K workspace [splits][rows][cols] as a rank-3 map, box
+// {box_cols, box_rows, 1}; the swizzle span equals the box row (64 or 128 B).
 int encode_ws_3d(CUtensorMap* map, void* base, uint64_t cols, uint64_t rows, uint64_t splits,
-                 uint32_t box_rows) {
+                 uint32_t box_rows, uint32_t box_cols = 32) {
     cuuint64_t dims[3] = {cols, rows, splits};
     cuuint64_t strides[2] = {cols * 4, cols * rows * 4};
-    cuuint32_t box[3] = {32, box_rows, 1};
+    cuuint32_t box[3] = {box_cols, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
+    const CUtensorMapSwizzle swz =
+        box_cols * 4 == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
-                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 
@@ -218,6 +221,49 @@ int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void* A, const void* 
 
 int gemv_f16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream) {
     return gemv_impl(N, K, x, W, y, stream);
+}
+
+int64_t gemm_f16_small_m_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (int s = validate_common(M, N, K)) return s;
+    if (M < 2 || M > 64) return TMAGEMM_ERR_UNSUPPORTED;
+    DeviceState* d = nullptr;
+    if (int s = device_state(&d)) return s;
+    const GemmPlan p = plan_small_m(M, N, K, d->sms, 0);
+    return p.splits * N * p.bn * 4;
+}
+
+int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void* W, void* D,
+                     void* workspace, int64_t workspace_bytes, void* stream) {
+    if (!X || !W || !D) return TMAGEMM_ERR_INVALID;
+    if (int s = validate_common(M, N, K)) return s;
+    if (M < 2 || M > 64) return TMAGEMM_ERR_UNSUPPORTED;
+    if (!aligned16(X) || !aligned16(W) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
+        return TMAGEMM_ERR_ALIGN;
+    DeviceState* d = nullptr;
+    if (int s = device_state(&d)) return s;
+    const GemmPlan p = plan_small_m(M, N, K, d->sms, 0);
+    const int64_t need = p.splits * N * p.bn * 4;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < need) return TMAGEMM_ERR_WORKSPACE;
+    // Swapped roles: the weights are the 128-row operand, the activations the
+    // narrow one (rows past M read as zero), partials [splits][N][Mp].
+    CUtensorMap tmW, tmX, tmP;
+    if (int s = encode_2d(&tmW, W, K, N, p.bk, p.bm, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+        return s;
+    if (int s = encode_2d(&tmX, X, K, M, p.bk, p.bn, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+        return s;
+    if (int s = encode_ws_3d(&tmP, workspace, p.bn, N, p.splits, p.bm, p.epi_cols)) return s;
+    GemmArgs args;
+    args.M = static_cast<int32_t>(N);
+    args.N = static_cast<int32_t>(p.bn);
+    args.K = static_cast<int32_t>(K);
+    args.wait_limit_ns = wait_limit_ns();
+    args.err_word = d->err_word;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_small_m(p, tmW, tmX, tmP, args, st);
+    if (e == cudaSuccess) e = launch_small_m_reduce(workspace, D, M, N, p.bn, p.splits, st);
+    return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 
 int gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,

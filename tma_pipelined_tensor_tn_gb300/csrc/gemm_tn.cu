@@ -58,8 +58,9 @@ struct Cfg {
     static constexpr bool kBF16 = BF16_;           // operands (and D) bf16 instead of fp16
     static constexpr int kThreads = 192;            // 6 warps
     static constexpr int kEpiThreads = 128;         // warps 2..5
-    // One store box row is one swizzle span: 32 or 64 fp16 columns, or 32 fp32.
-    static constexpr int kEpiCols = OUT_F32_ ? 32 : EPI_COLS_;
+    // One store box row is one swizzle span: 32 or 64 fp16 columns, or 32 fp32
+    // (16 fp32 when the whole tile is only 16 columns wide).
+    static constexpr int kEpiCols = OUT_F32_ ? (BN_ < 32 ? BN_ : 32) : EPI_COLS_;
     static constexpr uint32_t kEpiElemBytes = OUT_F32_ ? 4 : 2;
     static constexpr uint32_t kEpiRowBytes = kEpiCols * kEpiElemBytes;
     static constexpr uint32_t kEpiChunks = kEpiRowBytes / 16;    // 16-byte chunks per box row
@@ -83,7 +84,7 @@ struct Cfg {
     static_assert(BK * 2 == 128, "a K-major row of one k-block is one 128-byte swizzle atom");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
     static_assert(kEpiRowBytes == 64 || kEpiRowBytes == 128, "store boxes are 64 or 128 bytes wide");
-    static_assert(kEpiCols % 32 == 0 && BN % kEpiCols == 0, "epilogue boxes tile BN");
+    static_assert(kEpiCols % 16 == 0 && BN % kEpiCols == 0, "epilogue boxes tile BN");
     static_assert(kAccStride + BN <= kTmemCols, "two accumulators fit in TMEM");
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "stages stay 1024-B aligned");
     static_assert(kEpiBufBytes % 1024 == 0, "epilogue boxes stay 1024-B aligned");
@@ -99,6 +100,14 @@ template <bool T> using Cfg192 = Cfg<192, 64, 4, false, T>;
 template <bool T> using Cfg256F = Cfg<256, 32, 4, true, T>;
 template <bool T> using Cfg224F = Cfg<224, 32, 4, true, T>;
 template <bool T> using Cfg192F = Cfg<192, 32, 4, true, T>;
+
+// Swap-AB tiles for skinny GEMMs (M = 2..64 rows of activations): the weight
+// matrix is the 128-row "A" operand, the activations the narrow "B" operand,
+// so the MMA is 128 x Mp x 16 with Mp in {16, 32, 64}.  Stages are small, so
+// the ring is deeper to keep more of the weight stream in flight.
+using CfgS16 = Cfg<16, 16, 10, true, false>;
+using CfgS32 = Cfg<32, 32, 9, true, false>;
+using CfgS64 = Cfg<64, 32, 8, true, false>;
 
 // Work decomposition passed to the kernel.  Unit u covers output tile
 // u % num_tiles and k-blocks [split * kb_per_unit, min(k_blocks, ...)) with
@@ -257,10 +266,15 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
 #pragma unroll 1
             for (int c = 0; c < C::BN / C::kEpiCols; ++c, ++box) {
                 uint32_t v[C::kEpiCols];
+                if constexpr (C::kEpiCols == 16) {
+                    tmem_ld_32x32b_x16(t_row + c * C::kEpiCols,
+                                       *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
+                } else {
 #pragma unroll
-                for (int h = 0; h < C::kEpiCols / 32; ++h)
-                    tmem_ld_32x32b_x32(t_row + c * C::kEpiCols + 32 * h,
-                                       *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
+                    for (int h = 0; h < C::kEpiCols / 32; ++h)
+                        tmem_ld_32x32b_x32(t_row + c * C::kEpiCols + 32 * h,
+                                           *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
+                }
                 tmem_ld_wait();
                 if (c == C::BN / C::kEpiCols - 1) {
                     // Whole accumulator read: give it back to the MMA warp.
@@ -470,6 +484,54 @@ cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const C
                            const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream) {
     return plan.bf16 ? launch_typed<true>(plan, tmA, tmB, tmD, args, stream)
                      : launch_typed<false>(plan, tmA, tmB, tmD, args, stream);
+}
+
+GemmPlan plan_small_m(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits) {
+    const int64_t sms = num_sms > 0 ? num_sms : 1;
+    // The swapped problem: rows = N (weights), columns = Mp, same K.
+    if (M <= 16) return plan_for<CfgS16>(N, 16, K, sms, splits);
+    if (M <= 32) return plan_for<CfgS32>(N, 32, K, sms, splits);
+    return plan_for<CfgS64>(N, 64, K, sms, splits);
+}
+
+cudaError_t launch_small_m(const GemmPlan& plan, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                           const CUtensorMap& tmP, const GemmArgs& args, cudaStream_t stream) {
+    switch (plan.bn) {
+        case 16: return launch_cfg<CfgS16>(plan, tmW, tmX, tmP, args, stream);
+        case 32: return launch_cfg<CfgS32>(plan, tmW, tmX, tmP, args, stream);
+        case 64: return launch_cfg<CfgS64>(plan, tmW, tmX, tmP, args, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+namespace {
+
+// D[m][n] = fp16( sum_{s < S} P[s][n][m] ) for m < M: the partials of the
+// swapped problem are N x Mp (weights' rows by padded activation rows).  A
+// thread owns one n and reads its Mp contiguous partials per split; for a
+// fixed m, consecutive threads write consecutive n (coalesced).
+__global__ void __launch_bounds__(256)
+small_m_reduce_kernel(const float* __restrict__ P, __half* __restrict__ D, int32_t M, int32_t N,
+                      int32_t Mp, int32_t splits) {
+    const int32_t n = blockIdx.x * blockDim.x + threadIdx.x;
+    if (n >= N) return;
+    const int64_t part = static_cast<int64_t>(N) * Mp;
+    for (int32_t m = 0; m < M; ++m) {
+        float acc = P[static_cast<int64_t>(n) * Mp + m];
+        for (int32_t s = 1; s < splits; ++s) acc += P[s * part + static_cast<int64_t>(n) * Mp + m];
+        D[static_cast<int64_t>(m) * N + n] = __float2half_rn(acc);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_small_m_reduce(const void* partials, void* D, int64_t M, int64_t N, int64_t Mp,
+                                  int64_t splits, cudaStream_t stream) {
+    const int64_t blocks = (N + 255) / 256;
+    small_m_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        static_cast<const float*>(partials), static_cast<__half*>(D), static_cast<int32_t>(M),
+        static_cast<int32_t>(N), static_cast<int32_t>(Mp), static_cast<int32_t>(splits));
+    return cudaGetLastError();
 }
 
 cudaError_t launch_splitk_reduce(const void* partials, void* D, int64_t M, int64_t N,

@@ -44,6 +44,15 @@ struct GemmArgs {
 cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream);
 
+// Skinny GEMM (2 <= M <= 64) as a swapped split-K problem: rows = N (weights),
+// columns = Mp = M rounded up to 16/32/64, same K.  Partials go to an FP32
+// workspace [splits][N][Mp]; launch_small_m_reduce transposes and sums them.
+GemmPlan plan_small_m(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits);
+cudaError_t launch_small_m(const GemmPlan& plan, const CUtensorMap& tmW, const CUtensorMap& tmX,
+                           const CUtensorMap& tmP, const GemmArgs& args, cudaStream_t stream);
+cudaError_t launch_small_m_reduce(const void* partials, void* D, int64_t M, int64_t N, int64_t Mp,
+                                  int64_t splits, cudaStream_t stream);
+
 // Enqueue the GEMV kernel: y[n] = sum_k x[k] * W[n][k]; one warp per row;
 // fp16 or bf16 operands and output.
 cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y, bool bf16,
