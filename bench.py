@@ -542,6 +542,33 @@ def measure_extras(tg, dev, stream, l2):
         by = 2.0 * (GEMV_N * GEMV_K + Ms * GEMV_K + Ms * GEMV_N)
         out[f"small_m{Ms}_4096x14336"] = {"us": t_s, "gbs": by / t_s / 1e3,
                                           "tflops": 2.0 * Ms * GEMV_N * GEMV_K / t_s / 1e6}
+
+    # Grouped GEMM: 8 experts, 8192 routed tokens (skewed counts), N=4096, K=2048,
+    # against one dense GEMM over the same 8192 rows.
+    G, T, Ng, Kg = 8, 8192, 4096, 2048
+    rng = torch.Generator().manual_seed(11)
+    w = torch.distributions.Dirichlet(torch.full((G,), 0.7)).sample()
+    counts = torch.floor(w * T).long()
+    counts[0] += T - int(counts.sum())
+    offs = [0] + torch.cumsum(counts, 0).tolist()
+    Ag = (torch.rand((T, Kg), generator=rng) * 2 - 1).half().to(dev)
+    Bg = (torch.rand((G, Ng, Kg), generator=rng) * 2 - 1).half().to(dev)
+    Dg = torch.empty((T, Ng), dtype=torch.float16, device=dev)
+
+    def grouped(i):
+        assert tg.gemm_f16_grouped(G, offs, Ng, Kg, Ag.data_ptr(), Bg.data_ptr(), Dg.data_ptr(),
+                                   sh) == 0
+
+    def dense(i):
+        assert tg.gemm_f16(T, Ng, Kg, Ag.data_ptr(), Bg.data_ptr(), Dg.data_ptr(), sh) == 0
+
+    t_g = _time_launches(grouped, 50, stream)
+    t_d = _time_launches(dense, 50, stream)
+    tg.check(stream)
+    fl = 2.0 * T * Ng * Kg
+    out["grouped_8x(8192_tokens)x4096x2048"] = {
+        "us": t_g, "tflops": fl / t_g / 1e6, "dense_same_rows_us": t_d,
+        "dense_tflops": fl / t_d / 1e6, "group_rows": [int(c) for c in counts]}
     return out
 
 

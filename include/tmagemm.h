@@ -143,6 +143,26 @@ int64_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int64_t 
 int gemv_f16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream);
 
 /*
+ * Grouped GEMM: G independent TN GEMMs that share N and K, with run-time row
+ * counts (e.g. the tokens routed to each of G experts):
+ *   D[r][n] = fp16( sum_k A[r][k] * B[g][n][k] )  for m_offsets[g] <= r < m_offsets[g+1].
+ * The same persistent kernel and pipeline run over the tiles of all groups;
+ * each group only moves the origin of its A/D window ("高级数据搬运：TMA、
+ * Swizzle 与不规则访问", section "任意偏移窗口：view 与 from", the MoE case).
+ *   G         : 1 <= G <= 64 groups.
+ *   m_offsets : HOST array of G + 1 row offsets, m_offsets[0] = 0,
+ *               non-decreasing; group g owns rows [m_offsets[g], m_offsets[g+1])
+ *               (empty groups allowed).  Read during the call only.
+ *   A         : device pointer, m_offsets[G] x K fp16 row-major.
+ *   B         : device pointer, G x N x K fp16 (G stacked row-major N x K).
+ *   D         : device pointer, m_offsets[G] x N fp16 row-major.
+ * Requirements as gemm_f16 (16-byte alignment, K % 8 == 0, N % 8 == 0).
+ * Status codes as gemm_f16; G > 64 returns TMAGEMM_ERR_UNSUPPORTED.
+ */
+int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, const void* A,
+                     const void* B, void* D, void* stream);
+
+/*
  * Skinny GEMM for a few rows of activations, D = fp16(X * W^T) with
  * 2 <= M <= 64: the decode step of "Learning TileLang with GEMV" (§01 GEMV:
  * every linear layer is a GEMV when tokens are decoded one by one) for a

@@ -211,3 +211,28 @@ def bf16_bits_to_float64(a) -> np.ndarray:
     a = _bits16(a)
     lut = np.array([bf16_to_double(h) for h in range(65536)])
     return lut[a]
+
+
+def gemm_f16_grouped(A, B, m_offsets, *, threads: int = 0):
+    """Grouped GEMM: for each group g, rows [m_offsets[g], m_offsets[g+1]) of
+    D are fp16_rne(A[rows] @ B[g].T) with FP64 accumulation.  A: (R, K),
+    B: (G, N, K), m_offsets: G + 1 non-decreasing ints from 0 to R.  Each group
+    is the plain GEMM definition on its window of A ("高级数据搬运：TMA、Swizzle
+    与不规则访问", section "任意偏移窗口：view 与 from": the same computation at
+    a run-time origin)."""
+    A = _bits(A)
+    B = np.ascontiguousarray(B)
+    if B.dtype == np.float16:
+        B = B.view(np.uint16)
+    G, N, K = B.shape
+    offs = [int(v) for v in m_offsets]
+    if len(offs) != G + 1 or offs[0] != 0 or offs[-1] != A.shape[0]:
+        raise ValueError("m_offsets must run from 0 to A.shape[0] with G + 1 entries")
+    D = np.empty((A.shape[0], N), dtype=np.float16)
+    for g in range(G):
+        lo, hi = offs[g], offs[g + 1]
+        if hi < lo:
+            raise ValueError("m_offsets must be non-decreasing")
+        if hi > lo:
+            D[lo:hi] = gemm_f16(A[lo:hi], B[g], threads=threads)
+    return D

@@ -1,0 +1,83 @@
+"""GPU parity of the grouped GEMM (gemm_f16_grouped, through the C ABI) against
+the oracle's grouped definition: per group, the plain GEMM on its row window."""
+import numpy as np
+import pytest
+
+import oracle
+from tma_pipelined_tensor_tn_gb300 import inputs
+from tests.parity_util import assert_bitexact, compare
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tg():
+    import tma_pipelined_tensor_tn_gb300 as m
+    m.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return m
+
+
+def moe_offsets(G, tokens, seed):
+    """Routed token counts per expert (a skewed draw), as row offsets."""
+    rng = np.random.default_rng(seed)
+    w = rng.dirichlet(np.full(G, 0.7))
+    counts = np.floor(w * tokens).astype(np.int64)
+    counts[0] += tokens - counts.sum()
+    return np.concatenate([[0], np.cumsum(counts)]).tolist()
+
+
+def run(tg, A, B, offs):
+    D = tg.gemm_grouped(A.cuda(), B.cuda(), offs)
+    tg.check()
+    return D.cpu().numpy()
+
+
+@pytest.mark.parametrize("G,tokens,N,K", [(8, 4096, 2048, 1024), (16, 3000, 1000, 4160),
+                                          (64, 8192, 512, 256), (1, 1000, 1024, 512)])
+def test_grouped_parity(tg, G, tokens, N, K):
+    offs = moe_offsets(G, tokens, seed=G)
+    g = torch.Generator().manual_seed(G + N)
+    A = (torch.rand((tokens, K), generator=g) * 2 - 1).half()
+    B = (torch.rand((G, N, K), generator=g) * 2 - 1).half()
+    compare(run(tg, A, B, offs), oracle.gemm_f16_grouped(A.numpy(), B.numpy(), offs),
+            f"grouped G={G}")
+
+
+def test_grouped_empty_and_tiny_groups_integer_bitexact(tg):
+    offs = [0, 0, 1, 130, 130, 257, 600]      # empty, 1-row, ragged groups
+    G, N, K = 6, 264, 1000
+    A = inputs.integer_f16((offs[-1], K), seed=90)
+    B = inputs.integer_f16((G, N, K), seed=91)
+    assert_bitexact(run(tg, A, B, offs), oracle.gemm_f16_grouped(A.numpy(), B.numpy(), offs),
+                    "grouped integer")
+
+
+@pytest.mark.parametrize("bn", [256, 224, 192])
+def test_grouped_each_tile_width(tg, bn):
+    offs = moe_offsets(5, 1500, seed=bn)
+    g = torch.Generator().manual_seed(bn)
+    A = (torch.rand((1500, 520), generator=g) * 2 - 1).half()
+    B = (torch.rand((5, 1000, 520), generator=g) * 2 - 1).half()
+    try:
+        assert tg.tmagemm_set_tile_n(bn) == tg.TMAGEMM_OK
+        D = run(tg, A, B, offs)
+    finally:
+        tg.tmagemm_set_tile_n(0)
+    compare(D, oracle.gemm_f16_grouped(A.numpy(), B.numpy(), offs), f"grouped BN={bn}")
+
+
+def test_grouped_rows_outside_groups_untouched_and_errors(tg):
+    offs = [0, 100, 300]
+    A = torch.zeros((300, 64), dtype=torch.float16, device="cuda")
+    B = torch.zeros((2, 64, 64), dtype=torch.float16, device="cuda")
+    buf = torch.full((400, 64), 7.0, dtype=torch.float16, device="cuda")
+    D = buf[:300]
+    assert tg.gemm_f16_grouped(2, offs, 64, 64, A.data_ptr(), B.data_ptr(), D.data_ptr(), None) == 0
+    tg.check()
+    assert torch.all(buf[:300] == 0) and torch.all(buf[300:] == 7.0)
+    p = A.data_ptr()
+    assert tg.gemm_f16_grouped(2, [0, 200, 100], 64, 64, p, p, p, None) == tg.TMAGEMM_ERR_INVALID
+    assert tg.gemm_f16_grouped(2, [1, 2, 3], 64, 64, p, p, p, None) == tg.TMAGEMM_ERR_INVALID
+    assert tg.gemm_f16_grouped(65, list(range(66)), 64, 64, p, p, p, None) == tg.TMAGEMM_ERR_UNSUPPORTED

@@ -246,3 +246,35 @@ def test_threads_do_not_change_results():
     B = f16(rng.uniform(-1, 1, (33, 256)))
     assert np.array_equal(bits(oracle.gemm_f16(A, B, threads=1)),
                           bits(oracle.gemm_f16(A, B, threads=4)))
+
+
+# --------------------------------------------------------------------------
+# grouped GEMM definition
+# --------------------------------------------------------------------------
+
+def test_grouped_integer_exact_per_group():
+    rng = np.random.default_rng(30)
+    offs = [0, 5, 5, 37, 40]            # includes an empty group
+    G, N, K = 4, 24, 64
+    Ai = rng.integers(-2, 3, (offs[-1], K))
+    Bi = rng.integers(-2, 3, (G, N, K))
+    D = oracle.gemm_f16_grouped(f16(Ai), f16(Bi), offs)
+    for g in range(G):
+        lo, hi = offs[g], offs[g + 1]
+        exact = Ai[lo:hi] @ Bi[g].T
+        assert np.array_equal(bits(D[lo:hi]), bits(exact.astype(np.float64).astype(np.float16)))
+
+
+def test_grouped_rows_depend_only_on_their_group():
+    rng = np.random.default_rng(31)
+    offs = [0, 10, 30]
+    A = f16(rng.uniform(-1, 1, (30, 48)))
+    B = f16(rng.uniform(-1, 1, (2, 16, 48)))
+    D1 = oracle.gemm_f16_grouped(A, B, offs)
+    B2 = B.copy()
+    B2[1] = f16(rng.uniform(-1, 1, (16, 48)))
+    D2 = oracle.gemm_f16_grouped(A, B2, offs)
+    assert np.array_equal(bits(D1[:10]), bits(D2[:10]))
+    assert not np.array_equal(bits(D1[10:]), bits(D2[10:]))
+    assert np.array_equal(bits(oracle.gemm_f16_grouped(A, B[:1], [0, 30])),
+                          bits(oracle.gemm_f16(A, B[0])))

@@ -19,11 +19,13 @@ from ._binding import (  # noqa: F401
     gemm,
     gemm_bf16,
     gemm_f16,
+    gemm_f16_grouped,
     gemm_f16_small_m,
     gemm_f16_small_m_workspace_size,
     gemm_f16_splitk,
     gemm_f16_splitk_noalloc,
     gemm_f16_splitk_workspace_size,
+    gemm_grouped,
     gemm_small_m,
     gemm_splitk,
     gemv,

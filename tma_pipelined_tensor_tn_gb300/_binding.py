@@ -29,6 +29,7 @@ SIGNATURES = {
     "gemm_f16": ([_i64, _i64, _i64, _p, _p, _p, _p], _int),
     "gemv_f16": ([_i64, _i64, _p, _p, _p, _p], _int),
     "gemm_bf16": ([_i64, _i64, _i64, _p, _p, _p, _p], _int),
+    "gemm_f16_grouped": ([_i64, _P64, _i64, _i64, _p, _p, _p, _p], _int),
     "gemm_f16_small_m": ([_i64, _i64, _i64, _p, _p, _p, _p, _i64, _p], _int),
     "gemm_f16_small_m_workspace_size": ([_i64, _i64, _i64], _i64),
     "gemv_bf16": ([_i64, _i64, _p, _p, _p, _p], _int),
@@ -82,6 +83,32 @@ def strerror(status: int) -> str:
 
 def gemm_f16(M, N, K, A, B, D, stream=None) -> int:
     return lib().gemm_f16(M, N, K, A, B, D, stream)
+
+
+def gemm_f16_grouped(G, m_offsets, N, K, A, B, D, stream=None) -> int:
+    """m_offsets: a sequence of G + 1 host integers."""
+    offs = (ctypes.c_int64 * (G + 1))(*[int(v) for v in m_offsets])
+    return lib().gemm_f16_grouped(G, offs, N, K, A, B, D, stream)
+
+
+def gemm_grouped(A, B, m_offsets, out=None, stream=None):
+    """Grouped D[rows of g] = A[rows of g] @ B[g].T for CUDA fp16 A (R, K), B (G, N, K)."""
+    import torch
+    _check_f16_cuda("A", A)
+    _check_f16_cuda("B", B)
+    G, N, K = B.shape
+    R, K2 = A.shape
+    if K != K2 or len(m_offsets) != G + 1 or int(m_offsets[-1]) != R:
+        raise ValueError("shapes and m_offsets disagree")
+    if out is None:
+        out = torch.empty((R, N), dtype=torch.float16, device=A.device)
+    _check_f16_cuda("out", out)
+    with torch.cuda.device(A.device):
+        s = gemm_f16_grouped(G, m_offsets, N, K, A.data_ptr(), B.data_ptr(), out.data_ptr(),
+                             _stream_handle(stream, A.device))
+    if s != TMAGEMM_OK:
+        raise TmaGemmError(s, "gemm_f16_grouped")
+    return out
 
 
 def gemm_f16_small_m(M, N, K, X, W, D, workspace, workspace_bytes, stream=None) -> int:

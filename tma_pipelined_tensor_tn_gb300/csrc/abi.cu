@@ -223,6 +223,63 @@ int gemv_f16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* 
     return gemv_impl(N, K, x, W, y, stream);
 }
 
+int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, const void* A,
+                     const void* B, void* D, void* stream) {
+    if (!m_offsets || !A || !B || !D || G <= 0) return TMAGEMM_ERR_INVALID;
+    if (G > kMaxGroupsHost) return TMAGEMM_ERR_UNSUPPORTED;
+    if (m_offsets[0] != 0) return TMAGEMM_ERR_INVALID;
+    for (int64_t g = 0; g < G; ++g)
+        if (m_offsets[g + 1] < m_offsets[g]) return TMAGEMM_ERR_INVALID;
+    const int64_t rows = m_offsets[G];
+    if (rows == 0) return TMAGEMM_OK;                     // nothing to compute
+    if (int s = validate_common(rows, N, K)) return s;
+    if (G * N > (int64_t(1) << 31) - 1) return TMAGEMM_ERR_UNSUPPORTED;
+    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
+        return TMAGEMM_ERR_ALIGN;
+    DeviceState* d = nullptr;
+    if (int s = device_state(&d)) return s;
+    GroupedLaunch g{};
+    g.m_offsets = m_offsets;
+    g.groups = G;
+    g.N = N;
+    g.K = K;
+    g.bn = grouped_tile_n(m_offsets, G, N, d->sms);
+    const int epi_cols = g.bn == 224 ? 32 : 64;
+    if (int s = encode_2d(&g.tmA, A, K, rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+        return s;
+    {
+        cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(G)};
+        cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(N * K) * 2};
+        cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g.bn), 1};
+        cuuint32_t estr[3] = {1, 1, 1};
+        if (g_encode(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(B), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+            return TMAGEMM_ERR_CUDA;
+    }
+    const CUtensorMapSwizzle dswz =
+        epi_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+    for (int64_t i = 0; i < G; ++i) {
+        const int64_t mg = m_offsets[i + 1] - m_offsets[i];
+        if (mg == 0) continue;   // an empty group has no tiles and no map
+        const void* base = static_cast<const uint16_t*>(D) + m_offsets[i] * N;
+        if (int s = encode_2d(&g.tmD[i], base, N, mg, epi_cols, 128, dswz,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE))
+            return s;
+    }
+    GemmArgs args;
+    args.M = static_cast<int32_t>(rows);
+    args.N = static_cast<int32_t>(N);
+    args.K = static_cast<int32_t>(K);
+    args.wait_limit_ns = wait_limit_ns();
+    args.err_word = d->err_word;
+    cudaError_t e = launch_grouped(g, d->sms, args, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
+}
+
 int64_t gemm_f16_small_m_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (int s = validate_common(M, N, K)) return s;
     if (M < 2 || M > 64) return TMAGEMM_ERR_UNSUPPORTED;

@@ -109,17 +109,120 @@ using CfgS16 = Cfg<16, 16, 10, true, false>;
 using CfgS32 = Cfg<32, 32, 9, true, false>;
 using CfgS64 = Cfg<64, 32, 8, true, false>;
 
-// Work decomposition passed to the kernel.  Unit u covers output tile
-// u % num_tiles and k-blocks [split * kb_per_unit, min(k_blocks, ...)) with
-// split = u / num_tiles.  Without split-K, kb_per_unit = k_blocks.
+// What one work unit needs: operand row coordinates, its k-block range and
+// where its output box goes.
+struct UnitInfo {
+    int32_t a_row, b_row;    // TMA row coordinates of the A and B tiles
+    int32_t kb0, kb1;        // k-blocks [kb0, kb1)
+    int32_t store_y;         // output row coordinate (in the store map)
+    int32_t store_z;         // split index (split-K) or group index (grouped)
+    int32_t n_limit;         // columns >= n_limit are outside the output
+};
+
+// Dense problem: D (or split-K partials) = A * B^T.  Unit u covers output
+// tile u % num_tiles and k-blocks [split * kb_per_unit, min(k_blocks, ...))
+// with split = u / num_tiles.  Without split-K, kb_per_unit = k_blocks.
 struct Work {
     int32_t N, grid_m, grid_n, num_tiles, num_units, k_blocks, kb_per_unit;
 };
 
-template <class C>
+struct DenseProblem {
+    CUtensorMap tmA, tmB, tmD;
+    Work w;
+
+    __device__ __forceinline__ int32_t num_units() const { return w.num_units; }
+    __device__ __forceinline__ void prefetch() const {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+        tma_prefetch_desc(&tmD);
+    }
+    __device__ __forceinline__ UnitInfo unit(int32_t u, int BM, int BN, int group_m) const {
+        const int32_t tile = u % w.num_tiles;
+        const int32_t split = u / w.num_tiles;
+        const TileCoord tc = tile_coord(tile, w.grid_m, w.grid_n, group_m);
+        UnitInfo ui;
+        ui.a_row = tc.m_blk * BM;
+        ui.b_row = tc.n_blk * BN;
+        ui.kb0 = split * w.kb_per_unit;
+        ui.kb1 = min(w.k_blocks, ui.kb0 + w.kb_per_unit);
+        ui.store_y = ui.a_row;
+        ui.store_z = split;
+        ui.n_limit = w.N;
+        return ui;
+    }
+    __device__ __forceinline__ void load_a(uint32_t dst, int32_t k, const UnitInfo& ui,
+                                           uint32_t bar) const {
+        tma_load_2d(dst, &tmA, k, ui.a_row, bar);
+    }
+    __device__ __forceinline__ void load_b(uint32_t dst, int32_t k, const UnitInfo& ui,
+                                           uint32_t bar) const {
+        tma_load_2d(dst, &tmB, k, ui.b_row, bar);
+    }
+    template <bool kOutF32>
+    __device__ __forceinline__ void store(uint32_t buf, int32_t x, const UnitInfo& ui) const {
+        if constexpr (kOutF32)
+            tma_store_3d(&tmD, buf, x, ui.store_y, ui.store_z);
+        else
+            tma_store_2d(&tmD, buf, x, ui.store_y);
+    }
+};
+
+// Grouped problem: G independent GEMMs sharing N and K, with the rows of
+// group g at [m_off[g], m_off[g+1]) of one A and one D, and B holding G
+// stacked N x K matrices — the "window at a run-time origin" of the Croqtile
+// chapter ("任意偏移窗口：view 与 from": the pipeline is unchanged, only the
+// origin moves).  A is one 2-D map over all rows (a tile may read rows of the
+// next group; they only reach output rows that are not stored), B a 3-D map
+// {K, N, G} (clamps N per group), D one 2-D map per group, so a store never
+// crosses the group's last row.
+constexpr int kMaxGroups = 64;
+
+struct GroupedProblem {
+    CUtensorMap tmA, tmB;
+    CUtensorMap tmD[kMaxGroups];
+    int32_t tile_start[kMaxGroups + 1];   // prefix sums of the groups' tile counts
+    int32_t m_off[kMaxGroups + 1];        // row offsets; m_off[groups] = all rows
+    int32_t groups, grid_n, N, k_blocks;
+
+    __device__ __forceinline__ int32_t num_units() const { return tile_start[groups]; }
+    __device__ __forceinline__ void prefetch() const {
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    __device__ __forceinline__ UnitInfo unit(int32_t u, int BM, int BN, int group_m) const {
+        int32_t g = 0;
+        while (g + 1 < groups && tile_start[g + 1] <= u) ++g;
+        const int32_t local = u - tile_start[g];
+        const int32_t rows = m_off[g + 1] - m_off[g];
+        const int32_t gm = (rows + BM - 1) / BM;
+        const TileCoord tc = tile_coord(local, gm, grid_n, group_m);
+        UnitInfo ui;
+        ui.a_row = m_off[g] + tc.m_blk * BM;
+        ui.b_row = tc.n_blk * BN;
+        ui.kb0 = 0;
+        ui.kb1 = k_blocks;
+        ui.store_y = tc.m_blk * BM;
+        ui.store_z = g;
+        ui.n_limit = N;
+        return ui;
+    }
+    __device__ __forceinline__ void load_a(uint32_t dst, int32_t k, const UnitInfo& ui,
+                                           uint32_t bar) const {
+        tma_load_2d(dst, &tmA, k, ui.a_row, bar);
+    }
+    __device__ __forceinline__ void load_b(uint32_t dst, int32_t k, const UnitInfo& ui,
+                                           uint32_t bar) const {
+        tma_load_3d(dst, &tmB, k, ui.b_row, ui.store_z, bar);
+    }
+    template <bool kOutF32>
+    __device__ __forceinline__ void store(uint32_t buf, int32_t x, const UnitInfo& ui) const {
+        tma_store_2d(&tmD[ui.store_z], buf, x, ui.store_y);
+    }
+};
+
+template <class C, class P>
 __global__ void __launch_bounds__(C::kThreads, 1)
-gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmD, const Work w, const uint64_t limit_ns,
+gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                    uint32_t* __restrict__ err) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Dynamic shared memory is only guaranteed 16-byte aligned: round up.
@@ -153,9 +256,7 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
             mbar_init(mma_done_bar, 1);
             *abort_flag = 0;
             fence_mbarrier_init();
-            tma_prefetch_desc(&tmA);
-            tma_prefetch_desc(&tmB);
-            tma_prefetch_desc(&tmD);
+            prob.prefetch();
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -172,14 +273,9 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         if (elect_one()) {
             uint32_t it = 0;
             bool ok = true;
-            for (int32_t u = blockIdx.x; ok && u < w.num_units; u += gridDim.x) {
-                const int32_t tile = u % w.num_tiles;
-                const int32_t kb0 = (u / w.num_tiles) * w.kb_per_unit;
-                const int32_t kb1 = min(w.k_blocks, kb0 + w.kb_per_unit);
-                const TileCoord tc = tile_coord(tile, w.grid_m, w.grid_n, C::kGroupM);
-                const int32_t m0 = tc.m_blk * C::BM;
-                const int32_t n0 = tc.n_blk * C::BN;
-                for (int32_t kb = kb0; kb < kb1; ++kb) {
+            for (int32_t u = blockIdx.x; ok && u < prob.num_units(); u += gridDim.x) {
+                const UnitInfo ui = prob.unit(u, C::BM, C::BN, C::kGroupM);
+                for (int32_t kb = ui.kb0; kb < ui.kb1; ++kb) {
                     const uint32_t s = ring_stage(it, C::STAGES);
                     const uint32_t ph = ring_phase(it, C::STAGES);
                     if (!wait_or_abort(empty_bar(s), ph ^ 1u, abort_flag, err, kSiteProducerEmpty,
@@ -188,8 +284,8 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                         break;
                     }
                     mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
-                    tma_load_2d(sbase + C::kOffA + s * C::kABytes, &tmA, kb * C::BK, m0, full_bar(s));
-                    tma_load_2d(sbase + C::kOffB + s * C::kBBytes, &tmB, kb * C::BK, n0, full_bar(s));
+                    prob.load_a(sbase + C::kOffA + s * C::kABytes, kb * C::BK, ui, full_bar(s));
+                    prob.load_b(sbase + C::kOffB + s * C::kBBytes, kb * C::BK, ui, full_bar(s));
                     ++it;
                 }
             }
@@ -206,9 +302,10 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         if (elect_one()) {
             uint32_t it = 0, tcount = 0;
             bool ok = true;
-            for (int32_t u = blockIdx.x; ok && u < w.num_units; u += gridDim.x, ++tcount) {
-                const int32_t kb0 = (u / w.num_tiles) * w.kb_per_unit;
-                const int32_t kb1 = min(w.k_blocks, kb0 + w.kb_per_unit);
+            for (int32_t u = blockIdx.x; ok && u < prob.num_units(); u += gridDim.x, ++tcount) {
+                const UnitInfo ui = prob.unit(u, C::BM, C::BN, C::kGroupM);
+                const int32_t kb0 = ui.kb0;
+                const int32_t kb1 = ui.kb1;
                 const uint32_t acc = tcount & 1u;
                 const uint32_t acc_ph = (tcount >> 1) & 1u;
                 if (!wait_or_abort(acc_empty_bar(acc), acc_ph ^ 1u, abort_flag, err,
@@ -249,12 +346,9 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
         const uint32_t row = quarter * 32u + static_cast<uint32_t>(lane);  // row in tile
         const bool leader = threadIdx.x == 64;
         uint32_t tcount = 0, box = 0;
-        for (int32_t u = blockIdx.x; u < w.num_units; u += gridDim.x, ++tcount) {
-            const int32_t tile = u % w.num_tiles;
-            const int32_t split = u / w.num_tiles;
-            const TileCoord tc = tile_coord(tile, w.grid_m, w.grid_n, C::kGroupM);
-            const int32_t m0 = tc.m_blk * C::BM;
-            const int32_t n0 = tc.n_blk * C::BN;
+        for (int32_t u = blockIdx.x; u < prob.num_units(); u += gridDim.x, ++tcount) {
+            const UnitInfo ui = prob.unit(u, C::BM, C::BN, C::kGroupM);
+            const int32_t n0 = ui.b_row;
             const uint32_t acc = tcount & 1u;
             const uint32_t acc_ph = (tcount >> 1) & 1u;
             bool ok = wait_or_abort(acc_full_bar(acc), acc_ph, abort_flag, err, kSiteEpiAccFull,
@@ -309,12 +403,7 @@ gemm_tn_f16_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constan
                 named_bar_sync(1, C::kEpiThreads);
                 if (leader) {
                     const int32_t x = n0 + c * C::kEpiCols;
-                    if (x < w.N) {
-                        if constexpr (C::kOutF32)
-                            tma_store_3d(&tmD, buf, x, m0, split);
-                        else
-                            tma_store_2d(&tmD, buf, x, m0);
-                    }
+                    if (x < ui.n_limit) prob.template store<C::kOutF32>(buf, x, ui);
                     bulk_commit_group();
                 }
             }
@@ -396,35 +485,103 @@ int64_t plan_cost(const GemmPlan& p) {
     return rounds * p.kb_per_unit * (p.bn + 32);
 }
 
-template <class C>
-cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
-                       const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream) {
-    auto kernel = gemm_tn_f16_kernel<C>;
-    // Per-device opt-in to > 48 KB dynamic shared memory, once per device.
-    static std::atomic<bool> attr_done[64];
+// Per-device opt-in to > 48 KB dynamic shared memory for `kernel`, once per device.
+template <class K>
+cudaError_t smem_opt_in(K kernel, int bytes, std::atomic<bool> (&done)[64]) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64 || !attr_done[dev].load(std::memory_order_acquire)) {
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(C::kSmemBytes));
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 64) attr_done[dev].store(true, std::memory_order_release);
-    }
-    Work w;
-    w.N = args.N;
-    w.grid_m = static_cast<int32_t>(plan.grid_m);
-    w.grid_n = static_cast<int32_t>(plan.grid_n);
-    w.num_tiles = static_cast<int32_t>(plan.tiles);
-    w.num_units = static_cast<int32_t>(plan.units);
-    w.k_blocks = static_cast<int32_t>(plan.k_blocks);
-    w.kb_per_unit = static_cast<int32_t>(plan.kb_per_unit);
-    kernel<<<plan.grid, C::kThreads, C::kSmemBytes, stream>>>(tmA, tmB, tmD, w, args.wait_limit_ns,
+    if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
+    return e;
+}
+
+template <class C>
+cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
+                       const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream) {
+    auto kernel = gemm_tn_f16_kernel<C, DenseProblem>;
+    static std::atomic<bool> attr_done[64];
+    cudaError_t e = smem_opt_in(kernel, static_cast<int>(C::kSmemBytes), attr_done);
+    if (e != cudaSuccess) return e;
+    DenseProblem prob;
+    prob.tmA = tmA;
+    prob.tmB = tmB;
+    prob.tmD = tmD;
+    prob.w.N = args.N;
+    prob.w.grid_m = static_cast<int32_t>(plan.grid_m);
+    prob.w.grid_n = static_cast<int32_t>(plan.grid_n);
+    prob.w.num_tiles = static_cast<int32_t>(plan.tiles);
+    prob.w.num_units = static_cast<int32_t>(plan.units);
+    prob.w.k_blocks = static_cast<int32_t>(plan.k_blocks);
+    prob.w.kb_per_unit = static_cast<int32_t>(plan.kb_per_unit);
+    kernel<<<plan.grid, C::kThreads, C::kSmemBytes, stream>>>(prob, args.wait_limit_ns,
                                                              args.err_word);
     return cudaGetLastError();
 }
 
+template <class C>
+cudaError_t launch_grouped_cfg(const GroupedLaunch& g, int num_sms, const GemmArgs& args,
+                               cudaStream_t stream) {
+    auto kernel = gemm_tn_f16_kernel<C, GroupedProblem>;
+    static std::atomic<bool> attr_done[64];
+    cudaError_t e = smem_opt_in(kernel, static_cast<int>(C::kSmemBytes), attr_done);
+    if (e != cudaSuccess) return e;
+    GroupedProblem prob;
+    prob.tmA = g.tmA;
+    prob.tmB = g.tmB;
+    prob.groups = static_cast<int32_t>(g.groups);
+    prob.grid_n = static_cast<int32_t>(ceil_div(g.N, C::BN));
+    prob.N = static_cast<int32_t>(g.N);
+    prob.k_blocks = static_cast<int32_t>(ceil_div(g.K, C::BK));
+    int32_t t = 0;
+    for (int64_t i = 0; i <= g.groups; ++i) {
+        prob.m_off[i] = static_cast<int32_t>(g.m_offsets[i]);
+        prob.tile_start[i] = t;
+        if (i < g.groups) {
+            prob.tmD[i] = g.tmD[i];
+            const int64_t rows = g.m_offsets[i + 1] - g.m_offsets[i];
+            t += static_cast<int32_t>(ceil_div(rows, C::BM) * prob.grid_n);
+        }
+    }
+    if (t == 0) return cudaSuccess;   // every group is empty
+    const int grid = t < num_sms ? t : num_sms;
+    kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(prob, args.wait_limit_ns, args.err_word);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+int grouped_tile_n(const int64_t* m_offsets, int64_t groups, int64_t N, int num_sms) {
+    // The width that minimises rounds x (BN + 32) over all groups' tiles.
+    const int widths[3] = {256, 224, 192};
+    const int forced = __atomic_load_n(&g_force_tile_n, __ATOMIC_ACQUIRE);
+    if (forced != 0) return forced;
+    int best = 256;
+    int64_t best_cost = -1;
+    for (int bn : widths) {
+        int64_t tiles = 0;
+        for (int64_t i = 0; i < groups; ++i)
+            tiles += ceil_div(m_offsets[i + 1] - m_offsets[i], 128) * ceil_div(N, bn);
+        const int64_t sms = num_sms > 0 ? num_sms : 1;
+        const int64_t cost = ceil_div(tiles, tiles < sms ? (tiles > 0 ? tiles : 1) : sms) * (bn + 32);
+        if (best_cost < 0 || cost < best_cost) {
+            best = bn;
+            best_cost = cost;
+        }
+    }
+    return best;
+}
+
+cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, const GemmArgs& args,
+                           cudaStream_t stream) {
+    switch (g.bn) {
+        case 256: return launch_grouped_cfg<Cfg256<false>>(g, num_sms, args, stream);
+        case 224: return launch_grouped_cfg<Cfg224<false>>(g, num_sms, args, stream);
+        case 192: return launch_grouped_cfg<Cfg192<false>>(g, num_sms, args, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
 
 int g_force_tile_n = 0;
 

@@ -53,6 +53,22 @@ cudaError_t launch_small_m(const GemmPlan& plan, const CUtensorMap& tmW, const C
 cudaError_t launch_small_m_reduce(const void* partials, void* D, int64_t M, int64_t N, int64_t Mp,
                                   int64_t splits, cudaStream_t stream);
 
+// Grouped GEMM: groups g < G with rows [m_offsets[g], m_offsets[g+1]) of A
+// and D and weights B[g] (N x K).  Maps: A {K, rows} box {64, 128}; B
+// {K, N, G} box {64, bn, 1}; tmD[g] = D rows of group g, {N, M_g} box
+// {epi_cols(bn), 128} (unused for empty groups).
+constexpr int kMaxGroupsHost = 64;
+struct GroupedLaunch {
+    CUtensorMap tmA, tmB;
+    CUtensorMap tmD[kMaxGroupsHost];
+    const int64_t* m_offsets;   // host, groups + 1 entries
+    int64_t groups, N, K;
+    int bn;
+};
+int grouped_tile_n(const int64_t* m_offsets, int64_t groups, int64_t N, int num_sms);
+cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, const GemmArgs& args,
+                           cudaStream_t stream);
+
 // Enqueue the GEMV kernel: y[n] = sum_k x[k] * W[n][k]; one warp per row;
 // fp16 or bf16 operands and output.
 cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y, bool bf16,

@@ -206,6 +206,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
+// 3-D tiled load (x inner, then y, then z), completion counted on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int32_t x, int32_t y,
+                                            int32_t z, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];"
+        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z), "r"(bar)
+        : "memory");
+}
+
 // 2-D tiled store of a shared-memory box to global memory (bulk group).
 // Elements outside the tensor are not written.
 __device__ __forceinline__ void tma_store_2d(const void* tmap, uint32_t src, int32_t x, int32_t y) {
