@@ -572,6 +572,92 @@ def measure_extras(tg, dev, stream, l2):
     return out
 
 
+CASES = ("gemm4096", "gemv", "splitk", "small_m8", "small_m16", "grouped", "bf16_gemm", "bf16_gemv",
+         "gemm8192")
+
+
+def run_case(args, name):
+    """One workload alone (for profilers): `warmup` launches, then `steps`
+    launches between one pair of CUDA events; prints a short JSON line."""
+    import torch
+    import tma_pipelined_tensor_tn_gb300 as tg
+    from tma_pipelined_tensor_tn_gb300 import inputs
+    tg.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    if name in ("gemm4096", "bf16_gemm", "gemm8192", "splitk"):
+        M, N, K = {"gemm4096": (4096,) * 3, "bf16_gemm": (4096,) * 3, "gemm8192": (8192,) * 3,
+                   "splitk": (1024, 1024, 16384)}[name]
+        A, B = inputs.gemm_inputs(M, N, K, seed=0)
+        if name == "bf16_gemm":
+            A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
+        a, b = A.to(dev), B.to(dev)
+        d = torch.empty((M, N), dtype=a.dtype, device=dev)
+        need = tg.gemm_f16_splitk_workspace_size(M, N, K, 0) if name == "splitk" else 0
+        ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+        fl = 2.0 * M * N * K
+        if name == "splitk":
+            fn = lambda: tg.gemm_f16_splitk(M, N, K, a.data_ptr(), b.data_ptr(), d.data_ptr(), 0,
+                                            ws.data_ptr(), need, sh)
+        elif name == "bf16_gemm":
+            fn = lambda: tg.gemm_bf16(M, N, K, a.data_ptr(), b.data_ptr(), d.data_ptr(), sh)
+        else:
+            fn = lambda: tg.gemm_f16(M, N, K, a.data_ptr(), b.data_ptr(), d.data_ptr(), sh)
+        unit = ("TFLOP/s", fl / 1e12)
+    elif name in ("gemv", "bf16_gemv", "small_m8", "small_m16"):
+        x, W = inputs.gemv_inputs(GEMV_N, GEMV_K, seed=0)
+        if name == "bf16_gemv":
+            x, W = x.to(torch.bfloat16), W.to(torch.bfloat16)
+        w = W.to(dev)
+        if name.startswith("small_m"):
+            Ms = int(name[7:])
+            X = (torch.randn((Ms, GEMV_K), generator=torch.Generator().manual_seed(1)) * 0.02).half()
+            xv = X.to(dev)
+            y = torch.empty((Ms, GEMV_N), dtype=torch.float16, device=dev)
+            need = tg.gemm_f16_small_m_workspace_size(Ms, GEMV_N, GEMV_K)
+            ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
+            fn = lambda: tg.gemm_f16_small_m(Ms, GEMV_N, GEMV_K, xv.data_ptr(), w.data_ptr(),
+                                             y.data_ptr(), ws.data_ptr(), need, sh)
+            by = 2.0 * (GEMV_N * GEMV_K + Ms * GEMV_K + Ms * GEMV_N)
+        else:
+            xv = x.to(dev)
+            y = torch.empty((GEMV_N,), dtype=w.dtype, device=dev)
+            g = tg.gemv_bf16 if name == "bf16_gemv" else tg.gemv_f16
+            fn = lambda: g(GEMV_N, GEMV_K, xv.data_ptr(), w.data_ptr(), y.data_ptr(), sh)
+            by = gemv_bytes()
+        unit = ("GB/s", by / 1e9)
+    elif name == "grouped":
+        G, T, Ng, Kg = 8, 8192, 4096, 2048
+        counts = [1697, 2233, 321, 376, 105, 1822, 706, 932]
+        offs = [0]
+        for c in counts:
+            offs.append(offs[-1] + c)
+        rng = torch.Generator().manual_seed(11)
+        a = (torch.rand((T, Kg), generator=rng) * 2 - 1).half().to(dev)
+        b = (torch.rand((G, Ng, Kg), generator=rng) * 2 - 1).half().to(dev)
+        d = torch.empty((T, Ng), dtype=torch.float16, device=dev)
+        fn = lambda: tg.gemm_f16_grouped(G, offs, Ng, Kg, a.data_ptr(), b.data_ptr(), d.data_ptr(), sh)
+        unit = ("TFLOP/s", 2.0 * T * Ng * Kg / 1e12)
+    else:
+        raise SystemExit(f"unknown case {name}")
+    for _ in range(args.warmup):
+        assert fn() == 0
+    tg.check(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        assert fn() == 0
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    tg.check(stream)
+    us = e0.elapsed_time(e1) * 1e3 / args.steps
+    print(json.dumps({"case": name, "us_per_launch": us, "value": unit[1] / (us * 1e-6),
+                      "unit": unit[0], "steps": args.steps, "warmup": args.warmup}), flush=True)
+    return 0
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__)
     ap.add_argument("--gpus", type=int, default=1)
@@ -579,6 +665,8 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", choices=CASES, default=None,
+                    help="time one workload alone (for profiling); prints a short line")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -587,6 +675,8 @@ def main(argv=None):
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if args.impl == "reference":
         return run_reference(args, rank, world)
+    if args.case:
+        return run_case(args, args.case)
     if world > 1:
         import torch
         torch.cuda.set_device(local_rank)

@@ -51,7 +51,8 @@ namespace tmagemm {
 
 namespace {
 
-template <int BN_, int EPI_COLS_, int STAGES_, bool OUT_F32_, bool BF16_>
+template <int BN_, int EPI_COLS_, int STAGES_, bool OUT_F32_, bool BF16_, int TMEM_COLS_ = 512,
+          int CTAS_PER_SM_ = 1>
 struct Cfg {
     static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_;
     static constexpr bool kOutF32 = OUT_F32_;
@@ -70,8 +71,11 @@ struct Cfg {
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kEpiBufBytes = BM * kEpiRowBytes;
     static constexpr int kEpiBufs = 2;
-    static constexpr uint32_t kTmemCols = 512;      // two accumulators, 256 columns apart
-    static constexpr uint32_t kAccStride = 256;
+    // Two accumulators, kAccStride columns apart, in kTmemCols allocated
+    // columns (a power of two >= 32; CTAS_PER_SM CTAs must fit in 512).
+    static constexpr uint32_t kTmemCols = TMEM_COLS_;
+    static constexpr uint32_t kAccStride = TMEM_COLS_ / 2;
+    static constexpr int kCtasPerSm = CTAS_PER_SM_;
     static constexpr uint32_t kOffA = 0;
     static constexpr uint32_t kOffB = kOffA + STAGES * kABytes;
     static constexpr uint32_t kOffD = kOffB + STAGES * kBBytes;
@@ -89,6 +93,9 @@ struct Cfg {
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "stages stay 1024-B aligned");
     static_assert(kEpiBufBytes % 1024 == 0, "epilogue boxes stay 1024-B aligned");
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in shared memory");
+    static_assert(kTmemCols * CTAS_PER_SM_ <= 512, "resident CTAs share the SM's 512 TMEM columns");
+    static_assert(CTAS_PER_SM_ == 1 || kSmemBytes * CTAS_PER_SM_ <= 232448,
+                  "resident CTAs share the SM's shared memory");
 };
 
 // Tile shapes the host plan chooses from (all 128 rows x BN columns x 64 K),
@@ -105,9 +112,11 @@ template <bool T> using Cfg192F = Cfg<192, 32, 4, true, T>;
 // matrix is the 128-row "A" operand, the activations the narrow "B" operand,
 // so the MMA is 128 x Mp x 16 with Mp in {16, 32, 64}.  Stages are small, so
 // the ring is deeper to keep more of the weight stream in flight.
-using CfgS16 = Cfg<16, 16, 10, true, false>;
-using CfgS32 = Cfg<32, 32, 9, true, false>;
-using CfgS64 = Cfg<64, 32, 8, true, false>;
+// Two CTAs per SM (each with half the ring and 128 TMEM columns) keep two
+// independent weight streams per SM in flight.
+using CfgS16 = Cfg<16, 16, 5, true, false, 128, 2>;
+using CfgS32 = Cfg<32, 32, 4, true, false, 128, 2>;
+using CfgS64 = Cfg<64, 32, 3, true, false, 128, 2>;
 
 // What one work unit needs: operand row coordinates, its k-block range and
 // where its output box goes.
@@ -221,7 +230,7 @@ struct GroupedProblem {
 };
 
 template <class C, class P>
-__global__ void __launch_bounds__(C::kThreads, 1)
+__global__ void __launch_bounds__(C::kThreads, C::kCtasPerSm)
 gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                    uint32_t* __restrict__ err) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -457,9 +466,10 @@ GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) 
     p.grid_n = ceil_div(N, C::BN);
     p.k_blocks = ceil_div(K, C::BK);
     p.tiles = p.grid_m * p.grid_n;
+    const int64_t slots = sms * C::kCtasPerSm;   // resident CTAs
     if (splits <= 0) {
         // Automatic: enough units to cover the SMs, at least 4 k-blocks each.
-        splits = sms / p.tiles;
+        splits = slots / p.tiles;
         const int64_t max_by_k = p.k_blocks / 4 > 0 ? p.k_blocks / 4 : 1;
         if (splits > max_by_k) splits = max_by_k;
         if (splits > 16) splits = 16;
@@ -469,7 +479,7 @@ GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) 
     p.kb_per_unit = ceil_div(p.k_blocks, splits);
     p.splits = ceil_div(p.k_blocks, p.kb_per_unit);   // no empty split
     p.units = p.tiles * p.splits;
-    p.grid = static_cast<int>(p.units < sms ? p.units : sms);
+    p.grid = static_cast<int>(p.units < slots ? p.units : slots);
     p.threads = C::kThreads;
     p.smem_bytes = static_cast<int>(C::kSmemBytes);
     p.out_f32 = C::kOutF32;
@@ -493,6 +503,11 @@ cudaError_t smem_opt_in(K kernel, int bytes, std::atomic<bool> (&done)[64]) {
     if (e != cudaSuccess) return e;
     if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    // The whole configurable L1/shared split goes to shared memory, so CTAs
+    // that ask for half of it can sit two to an SM.
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 static_cast<int>(cudaSharedmemCarveoutMaxShared));
     if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
     return e;
 }
@@ -665,28 +680,44 @@ namespace {
 
 // D[m][n] = fp16( sum_{s < S} P[s][n][m] ) for m < M: the partials of the
 // swapped problem are N x Mp (weights' rows by padded activation rows).  A
-// thread owns one n and reads its Mp contiguous partials per split; for a
-// fixed m, consecutive threads write consecutive n (coalesced).
+// thread owns one n and 16 consecutive m: per split it reads 64 contiguous
+// bytes (four 16-byte loads), adds in split order, and writes its (up to) 16
+// outputs; for a fixed m, consecutive threads write consecutive n (coalesced).
 __global__ void __launch_bounds__(256)
-small_m_reduce_kernel(const float* __restrict__ P, __half* __restrict__ D, int32_t M, int32_t N,
+small_m_reduce_kernel(const float4* __restrict__ P, __half* __restrict__ D, int32_t M, int32_t N,
                       int32_t Mp, int32_t splits) {
-    const int32_t n = blockIdx.x * blockDim.x + threadIdx.x;
-    if (n >= N) return;
-    const int64_t part = static_cast<int64_t>(N) * Mp;
-    for (int32_t m = 0; m < M; ++m) {
-        float acc = P[static_cast<int64_t>(n) * Mp + m];
-        for (int32_t s = 1; s < splits; ++s) acc += P[s * part + static_cast<int64_t>(n) * Mp + m];
-        D[static_cast<int64_t>(m) * N + n] = __float2half_rn(acc);
+    const int32_t groups16 = Mp / 16;
+    const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+    if (t >= static_cast<int64_t>(N) * groups16) return;
+    const int32_t n = static_cast<int32_t>(t % N);
+    const int32_t m0 = static_cast<int32_t>(t / N) * 16;
+    if (m0 >= M) return;
+    const int64_t part4 = static_cast<int64_t>(N) * Mp / 4;          // float4s per split
+    const float4* p = P + (static_cast<int64_t>(n) * Mp + m0) / 4;
+    float4 a0 = p[0], a1 = p[1], a2 = p[2], a3 = p[3];
+    for (int32_t s = 1; s < splits; ++s) {
+        const float4* q = p + s * part4;
+        const float4 b0 = q[0], b1 = q[1], b2 = q[2], b3 = q[3];
+        a0.x += b0.x; a0.y += b0.y; a0.z += b0.z; a0.w += b0.w;
+        a1.x += b1.x; a1.y += b1.y; a1.z += b1.z; a1.w += b1.w;
+        a2.x += b2.x; a2.y += b2.y; a2.z += b2.z; a2.w += b2.w;
+        a3.x += b3.x; a3.y += b3.y; a3.z += b3.z; a3.w += b3.w;
     }
+    const float v[16] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w,
+                         a2.x, a2.y, a2.z, a2.w, a3.x, a3.y, a3.z, a3.w};
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        if (m0 + i < M) D[static_cast<int64_t>(m0 + i) * N + n] = __float2half_rn(v[i]);
 }
 
 }  // namespace
 
 cudaError_t launch_small_m_reduce(const void* partials, void* D, int64_t M, int64_t N, int64_t Mp,
                                   int64_t splits, cudaStream_t stream) {
-    const int64_t blocks = (N + 255) / 256;
+    const int64_t threads = N * (Mp / 16);
+    const int64_t blocks = (threads + 255) / 256;
     small_m_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const float*>(partials), static_cast<__half*>(D), static_cast<int32_t>(M),
+        static_cast<const float4*>(partials), static_cast<__half*>(D), static_cast<int32_t>(M),
         static_cast<int32_t>(N), static_cast<int32_t>(Mp), static_cast<int32_t>(splits));
     return cudaGetLastError();
 }
