@@ -52,6 +52,25 @@ def gemv_bytes(N=GEMV_N, K=GEMV_K):
     return 2.0 * (N * K + K + N)
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise max of `values` over all ranks of the default process group
+    (the values unchanged when there is none).  Used for the timed region:
+    the job takes as long as its slowest rank."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_value(units_per_step, steps, world, total_seconds):
+    """Throughput of the whole job: the units every rank processed over the
+    slowest rank's time (replicas: each rank runs the full workload)."""
+    return world * steps * units_per_step / total_seconds
+
+
 def sources_hash():
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
@@ -352,11 +371,7 @@ def run_ours(args, rank, world, local_rank):
     tg.check(stream)
 
     times = [evs[0].elapsed_time(evs[1]), evs[1].elapsed_time(evs[2]), wall]
-    if world > 1:
-        t = torch.tensor(times, dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        times = t.tolist()
-    gemm_total_ms, gemv_total_ms, wall = times
+    gemm_total_ms, gemv_total_ms, wall = max_over_ranks(times, device=dev)
 
     # ---- end to end through the C ABI: host buffers, copies inside the region ----
     e2e_steps = max(3, min(args.steps, 10))
@@ -391,7 +406,7 @@ def run_ours(args, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     gemm_avg_s = gemm_total_ms / 1e3 / args.steps
     gemv_avg_s = gemv_total_ms / 1e3 / args.steps
-    value = world * args.steps * gemm_flops() / (gemm_total_ms / 1e3) / 1e12
+    value = whole_job_value(gemm_flops(), args.steps, world, gemm_total_ms / 1e3) / 1e12
     achieved = gemm_flops() / gemm_avg_s / 1e12
     peak_t = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     gemv_gbs = gemv_bytes() / gemv_avg_s / 1e9
