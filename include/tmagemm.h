@@ -230,6 +230,16 @@ int tmagemm_version(void);
 int tmagemm_selftest_wait_timeout(int64_t limit_ms, void* stream);
 
 /*
+ * Tuning/test override of the CTA-pair tiles of gemm_f16 / gemm_bf16: 0 =
+ * automatic (a pair of CTAs on two SMs runs one 256 x N tile with cta_group::2
+ * MMAs when the plan's cost model prefers it), 1 = never use pairs, 2 = use
+ * pairs whenever the device can co-schedule them.  Process-wide; results are
+ * the same up to FP32 accumulation order.  Returns TMAGEMM_ERR_INVALID for
+ * other values.
+ */
+int tmagemm_set_cta_pair(int mode);
+
+/*
  * Tuning/test override of the GEMM's tile width N: 256, 224 or 192 forces that
  * tile shape for every later gemm_f16 call in the process; 0 restores the
  * automatic choice (the width that minimises the number of tile rounds on
@@ -259,13 +269,15 @@ int tmagemm_tile_coord(int64_t tile, int64_t grid_m, int64_t grid_n, int64_t gro
 int tmagemm_ring_position(int64_t it, int64_t stages, int64_t* stage, int64_t* phase);
 
 /*
- * The GEMM launch configuration for (M, N, K) on a device with `num_sms` SMs
- * and a split request (1 = gemm_f16, 0 = automatic split-K, > 1 = that many
- * parts): written to out[0..10] in the order BM, BN, BK, STAGES, tiles, grid,
- * threads, smem bytes, parts, k-blocks per part, work units.  No GPU needed.
+ * The GEMM launch configuration for (M, N, K) on a device with `num_sms` SMs,
+ * of which `num_pairs` two-CTA clusters can be co-resident (0 = no pairs), and
+ * a split request (1 = gemm_f16, 0 = automatic split-K, > 1 = that many
+ * parts): written to out[0..11] in the order BM, BN, BK, STAGES, tiles, grid
+ * (CTAs), threads, smem bytes, parts, k-blocks per part, work units, pair
+ * (1 if CTA pairs; then tiles are 256 rows high).  No GPU needed.
  */
-int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t splits,
-                      int64_t* out);
+int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t num_pairs,
+                      int64_t splits, int64_t* out);
 
 #ifdef __cplusplus
 }

@@ -129,11 +129,14 @@ def test_gemm_edge_shapes(tg, M, N, K):
     compare(D, oracle.gemm_f16(A.numpy(), B.numpy()), f"edge {M}x{N}x{K}")
 
 
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("bn", [256, 224, 192])
 @pytest.mark.parametrize("M,N,K", [(1031, 1000, 1032), (300, 2056, 4160)])
-def test_gemm_each_tile_width(tg, bn, M, N, K):
-    """Every tile shape the plan can pick, on ragged shapes, real and integer inputs."""
+def test_gemm_each_tile_width(tg, bn, M, N, K, pair):
+    """Every tile shape the plan can pick — single-CTA (pair=1) and CTA-pair
+    (pair=2) tiles — on ragged shapes, real and integer inputs."""
     try:
+        assert tg.tmagemm_set_cta_pair(pair) == tg.TMAGEMM_OK
         assert tg.tmagemm_set_tile_n(bn) == tg.TMAGEMM_OK
         A, B = inputs.gemm_inputs(M, N, K, seed=bn)
         compare(run_gemm(tg, A, B), oracle.gemm_f16(A.numpy(), B.numpy()), f"BN={bn} {M}x{N}x{K}")
@@ -142,6 +145,32 @@ def test_gemm_each_tile_width(tg, bn, M, N, K):
         assert_bitexact(run_gemm(tg, Ai, Bi), oracle.gemm_f16(Ai.numpy(), Bi.numpy()), f"BN={bn} int")
     finally:
         tg.tmagemm_set_tile_n(0)
+        tg.tmagemm_set_cta_pair(0)
+
+
+@pytest.mark.parametrize("M,N,K", [(100, 520, 264), (129, 264, 64), (300, 136, 1000)])
+def test_gemm_pair_with_half_tile_outside_m(tg, M, N, K):
+    """CTA-pair tiles are 256 rows: for M <= 128 (or a last tile reaching
+    less than 128 rows into the pair) the second CTA's rows are all outside D
+    and its stores are skipped."""
+    try:
+        assert tg.tmagemm_set_cta_pair(2) == tg.TMAGEMM_OK
+        A, B = inputs.gemm_inputs(M, N, K, seed=M)
+        compare(run_gemm(tg, A, B), oracle.gemm_f16(A.numpy(), B.numpy()), f"pair {M}x{N}x{K}")
+    finally:
+        tg.tmagemm_set_cta_pair(0)
+
+
+def test_gemm_pair_and_single_agree_on_4096(tg):
+    A, B = inputs.gemm_inputs(4096, 4096, 4096, seed=2)
+    out = {}
+    try:
+        for mode in (1, 2):
+            assert tg.tmagemm_set_cta_pair(mode) == tg.TMAGEMM_OK
+            out[mode] = run_gemm(tg, A, B)
+    finally:
+        tg.tmagemm_set_cta_pair(0)
+    compare(out[2], out[1], "pair vs single 4096^3")
 
 
 def test_gemm_out_of_bounds_guard(tg):

@@ -182,6 +182,28 @@ def test_plan_balances_waves_on_gb300():
     assert tg.tmagemm_gemm_plan(8192, 8192, 8192, 152)["BN"] == 256
 
 
+def test_plan_with_cta_pairs_balances_waves():
+    # With 76 co-resident CTA pairs, 256 x 224 pair tiles give 16 x 19 = 304 =
+    # 4 x 76 tiles at 4096^3; 8192^3 takes 256 x 256 pair tiles.
+    p = tg.tmagemm_gemm_plan(4096, 4096, 4096, 152, 1, 76)
+    assert p["pair"] == 1 and p["BN"] == 224 and p["tiles"] == 4 * 76 and p["grid"] == 152
+    q = tg.tmagemm_gemm_plan(8192, 8192, 8192, 152, 1, 76)
+    assert q["pair"] == 1 and q["BN"] == 256
+    # split-K plans never use pairs
+    assert tg.tmagemm_gemm_plan(1024, 1024, 16384, 152, 0, 76)["pair"] == 0
+
+
+def test_cta_pair_override():
+    try:
+        assert tg.tmagemm_set_cta_pair(1) == tg.TMAGEMM_OK
+        assert tg.tmagemm_gemm_plan(4096, 4096, 4096, 152, 1, 76)["pair"] == 0
+        assert tg.tmagemm_set_cta_pair(2) == tg.TMAGEMM_OK
+        assert tg.tmagemm_gemm_plan(256, 256, 256, 152, 1, 76)["pair"] == 1
+        assert tg.tmagemm_set_cta_pair(3) == tg.TMAGEMM_ERR_INVALID
+    finally:
+        assert tg.tmagemm_set_cta_pair(0) == tg.TMAGEMM_OK
+
+
 def test_tile_width_override():
     try:
         assert tg.tmagemm_set_tile_n(256) == tg.TMAGEMM_OK

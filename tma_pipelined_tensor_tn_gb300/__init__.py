@@ -38,6 +38,7 @@ from ._binding import (  # noqa: F401
     tmagemm_last_error_detail,
     tmagemm_ring_position,
     tmagemm_selftest_wait_timeout,
+    tmagemm_set_cta_pair,
     tmagemm_set_tile_n,
     tmagemm_tile_coord,
     tmagemm_version,

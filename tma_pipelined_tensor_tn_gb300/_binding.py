@@ -43,7 +43,8 @@ SIGNATURES = {
     "tmagemm_selftest_wait_timeout": ([_i64, _p], _int),
     "tmagemm_tile_coord": ([_i64, _i64, _i64, _i64, _P64, _P64], _int),
     "tmagemm_ring_position": ([_i64, _i64, _P64, _P64], _int),
-    "tmagemm_gemm_plan": ([_i64, _i64, _i64, _i64, _i64, _P64], _int),
+    "tmagemm_gemm_plan": ([_i64, _i64, _i64, _i64, _i64, _i64, _P64], _int),
+    "tmagemm_set_cta_pair": ([_int], _int),
     "tmagemm_set_tile_n": ([_int], _int),
 }
 
@@ -206,14 +207,18 @@ def tmagemm_ring_position(it, stages):
     return st.value, ph.value
 
 
-def tmagemm_gemm_plan(M, N, K, num_sms, splits=1):
-    out = (ctypes.c_int64 * 11)()
-    s = lib().tmagemm_gemm_plan(M, N, K, num_sms, splits, out)
+def tmagemm_gemm_plan(M, N, K, num_sms, splits=1, num_pairs=0):
+    out = (ctypes.c_int64 * 12)()
+    s = lib().tmagemm_gemm_plan(M, N, K, num_sms, num_pairs, splits, out)
     if s != TMAGEMM_OK:
         raise TmaGemmError(s, "tmagemm_gemm_plan")
     keys = ("BM", "BN", "BK", "STAGES", "tiles", "grid", "threads", "smem", "splits",
-            "kb_per_unit", "units")
+            "kb_per_unit", "units", "pair")
     return dict(zip(keys, list(out)))
+
+
+def tmagemm_set_cta_pair(mode) -> int:
+    return lib().tmagemm_set_cta_pair(mode)
 
 
 # ---- torch-tensor conveniences (marshalling only) ----------------------------

@@ -33,6 +33,7 @@ constexpr int kMaxDevices = 64;
 struct DeviceState {
     bool ready = false;
     int sms = 0;
+    int pairs = 0;          // co-resident two-CTA clusters of the pair kernel
     int cc_major = 0;
     uint32_t* err_word = nullptr;
 };
@@ -77,6 +78,7 @@ int device_state(DeviceState** out) {
                 return TMAGEMM_ERR_CUDA;
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
         }
+        if (d.cc_major == 10) d.pairs = max_resident_pairs();
         d.ready = true;
     }
     if (d.cc_major != 10) return TMAGEMM_ERR_UNSUPPORTED;   // sm_100 family only
@@ -145,7 +147,7 @@ int run_gemm(const GemmPlan& plan, DeviceState* d, int64_t M, int64_t N, int64_t
     if (int s = encode_2d(&tmA, A, K, M, plan.bk, plan.bm, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, plan.bf16))
         return s;
-    if (int s = encode_2d(&tmB, B, K, N, plan.bk, plan.bn, CU_TENSOR_MAP_SWIZZLE_128B,
+    if (int s = encode_2d(&tmB, B, K, N, plan.bk, plan.b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, plan.bf16))
         return s;
     if (plan.out_f32) {
@@ -187,7 +189,8 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void
         return TMAGEMM_ERR_ALIGN;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    return run_gemm(plan_gemm(M, N, K, d->sms, 1), d, M, N, K, A, B, D, nullptr, stream);
+    return run_gemm(plan_gemm(M, N, K, d->sms, 1, false, d->pairs), d, M, N, K, A, B, D, nullptr,
+                    stream);
 }
 
 int64_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int64_t splits) {
@@ -213,7 +216,8 @@ int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void* A, const void* 
     if (int s = device_state(&d)) return s;
     const GemmPlan p = plan_gemm(M, N, K, d->sms, splits == 0 ? 0 : splits);
     if (p.splits <= 1)   // nothing to split: the plain kernel, no workspace needed
-        return run_gemm(plan_gemm(M, N, K, d->sms, 1), d, M, N, K, A, B, D, nullptr, stream);
+        return run_gemm(plan_gemm(M, N, K, d->sms, 1, false, d->pairs), d, M, N, K, A, B, D,
+                        nullptr, stream);
     if (!workspace || !aligned16(workspace) || workspace_bytes < p.splits * M * N * 4)
         return TMAGEMM_ERR_WORKSPACE;
     return run_gemm(p, d, M, N, K, A, B, D, workspace, stream);
@@ -332,7 +336,8 @@ int gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, voi
         return TMAGEMM_ERR_ALIGN;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    return run_gemm(plan_gemm(M, N, K, d->sms, 1, true), d, M, N, K, A, B, D, nullptr, stream);
+    return run_gemm(plan_gemm(M, N, K, d->sms, 1, true, d->pairs), d, M, N, K, A, B, D, nullptr,
+                    stream);
 }
 
 int gemv_bf16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream) {
@@ -377,6 +382,12 @@ const char* tmagemm_strerror(int status) {
 
 int tmagemm_version(void) { return (0 << 16) | (1 << 8) | 0; }
 
+int tmagemm_set_cta_pair(int mode) {
+    if (mode < 0 || mode > 2) return TMAGEMM_ERR_INVALID;
+    __atomic_store_n(&g_pair_mode, mode, __ATOMIC_RELEASE);
+    return TMAGEMM_OK;
+}
+
 int tmagemm_set_tile_n(int bn) {
     if (bn != 0 && bn != 256 && bn != 224 && bn != 192) return TMAGEMM_ERR_INVALID;
     __atomic_store_n(&g_force_tile_n, bn, __ATOMIC_RELEASE);
@@ -402,11 +413,14 @@ int tmagemm_ring_position(int64_t it, int64_t stages, int64_t* stage, int64_t* p
     return TMAGEMM_OK;
 }
 
-int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t splits,
-                      int64_t* out) {
-    if (!out || num_sms <= 0 || splits < 0 || splits > 4096) return TMAGEMM_ERR_INVALID;
+int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t num_pairs,
+                      int64_t splits, int64_t* out) {
+    if (!out || num_sms <= 0 || num_pairs < 0 || num_pairs > num_sms / 2 || splits < 0 ||
+        splits > 4096)
+        return TMAGEMM_ERR_INVALID;
     if (int s = validate_common(M, N, K)) return s;
-    const GemmPlan p = plan_gemm(M, N, K, static_cast<int>(num_sms), splits);
+    const GemmPlan p = plan_gemm(M, N, K, static_cast<int>(num_sms), splits, false,
+                                 static_cast<int>(num_pairs));
     out[0] = p.bm;
     out[1] = p.bn;
     out[2] = p.bk;
@@ -418,6 +432,7 @@ int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t 
     out[8] = p.splits;
     out[9] = p.kb_per_unit;
     out[10] = p.units;
+    out[11] = p.pair ? 1 : 0;
     return TMAGEMM_OK;
 }
 

@@ -52,9 +52,14 @@ namespace tmagemm {
 namespace {
 
 template <int BN_, int EPI_COLS_, int STAGES_, bool OUT_F32_, bool BF16_, int TMEM_COLS_ = 512,
-          int CTAS_PER_SM_ = 1>
+          int CTAS_PER_SM_ = 1, bool PAIR_ = false>
 struct Cfg {
     static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_;
+    // PAIR: a cluster of two CTAs runs one 256 x BN tile with cta_group::2
+    // MMAs; each CTA holds its 128 rows of A and BN/2 rows of B.
+    static constexpr bool kPair = PAIR_;
+    static constexpr int kTileM = PAIR_ ? 256 : 128;       // rows of one work tile
+    static constexpr int kBRows = PAIR_ ? BN_ / 2 : BN_;  // rows of B in this CTA
     static constexpr bool kOutF32 = OUT_F32_;
     static constexpr bool kBF16 = BF16_;           // operands (and D) bf16 instead of fp16
     static constexpr int kThreads = 192;            // 6 warps
@@ -67,7 +72,7 @@ struct Cfg {
     static constexpr uint32_t kEpiChunks = kEpiRowBytes / 16;    // 16-byte chunks per box row
     static constexpr int kGroupM = 8;               // L2 group height in tiles
     static constexpr uint32_t kABytes = BM * BK * 2;
-    static constexpr uint32_t kBBytes = BN * BK * 2;
+    static constexpr uint32_t kBBytes = kBRows * BK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kEpiBufBytes = BM * kEpiRowBytes;
     static constexpr int kEpiBufs = 2;
@@ -83,7 +88,7 @@ struct Cfg {
     static constexpr uint32_t kNumBars = 2 * STAGES + 5;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + base alignment slack
-    static constexpr uint32_t kIdesc = umma_idesc_16bit_f32(BM, BN, BF16_);
+    static constexpr uint32_t kIdesc = umma_idesc_16bit_f32(kTileM, BN, BF16_);
 
     static_assert(BK * 2 == 128, "a K-major row of one k-block is one 128-byte swizzle atom");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
@@ -94,6 +99,8 @@ struct Cfg {
     static_assert(kEpiBufBytes % 1024 == 0, "epilogue boxes stay 1024-B aligned");
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in shared memory");
     static_assert(kTmemCols * CTAS_PER_SM_ <= 512, "resident CTAs share the SM's 512 TMEM columns");
+    static_assert(!PAIR_ || (CTAS_PER_SM_ == 1 && !OUT_F32_ && kBRows % 8 == 0),
+                  "pairs: one CTA per SM, plain output, whole 8-row swizzle atoms of B");
     static_assert(CTAS_PER_SM_ == 1 || kSmemBytes * CTAS_PER_SM_ <= 232448,
                   "resident CTAs share the SM's shared memory");
 };
@@ -112,6 +119,11 @@ template <bool T> using Cfg192F = Cfg<192, 32, 4, true, T>;
 // matrix is the 128-row "A" operand, the activations the narrow "B" operand,
 // so the MMA is 128 x Mp x 16 with Mp in {16, 32, 64}.  Stages are small, so
 // the ring is deeper to keep more of the weight stream in flight.
+// CTA-pair tiles (256 x BN) for the plain fp16/bf16 GEMM.
+template <bool T> using CfgP256 = Cfg<256, 64, 6, false, T, 512, 1, true>;
+template <bool T> using CfgP224 = Cfg<224, 32, 6, false, T, 512, 1, true>;
+template <bool T> using CfgP192 = Cfg<192, 64, 6, false, T, 512, 1, true>;
+
 // Two CTAs per SM (each with half the ring and 128 TMEM columns) keep two
 // independent weight streams per SM in flight.
 using CfgS16 = Cfg<16, 16, 5, true, false, 128, 2>;
@@ -126,13 +138,14 @@ struct UnitInfo {
     int32_t store_y;         // output row coordinate (in the store map)
     int32_t store_z;         // split index (split-K) or group index (grouped)
     int32_t n_limit;         // columns >= n_limit are outside the output
+    int32_t m_limit;         // rows >= m_limit are outside the output (store map rows)
 };
 
 // Dense problem: D (or split-K partials) = A * B^T.  Unit u covers output
 // tile u % num_tiles and k-blocks [split * kb_per_unit, min(k_blocks, ...))
 // with split = u / num_tiles.  Without split-K, kb_per_unit = k_blocks.
 struct Work {
-    int32_t N, grid_m, grid_n, num_tiles, num_units, k_blocks, kb_per_unit;
+    int32_t M, N, grid_m, grid_n, num_tiles, num_units, k_blocks, kb_per_unit;
 };
 
 struct DenseProblem {
@@ -157,6 +170,7 @@ struct DenseProblem {
         ui.store_y = ui.a_row;
         ui.store_z = split;
         ui.n_limit = w.N;
+        ui.m_limit = w.M;
         return ui;
     }
     __device__ __forceinline__ void load_a(uint32_t dst, int32_t k, const UnitInfo& ui,
@@ -166,6 +180,15 @@ struct DenseProblem {
     __device__ __forceinline__ void load_b(uint32_t dst, int32_t k, const UnitInfo& ui,
                                            uint32_t bar) const {
         tma_load_2d(dst, &tmB, k, ui.b_row, bar);
+    }
+    // Pair forms: rows given explicitly, bytes counted on the leader's barrier.
+    __device__ __forceinline__ void load_a_pair(uint32_t dst, int32_t k, int32_t row,
+                                                uint32_t bar_cluster) const {
+        tma_load_2d_pair(dst, &tmA, k, row, bar_cluster);
+    }
+    __device__ __forceinline__ void load_b_pair(uint32_t dst, int32_t k, int32_t row,
+                                                uint32_t bar_cluster) const {
+        tma_load_2d_pair(dst, &tmB, k, row, bar_cluster);
     }
     template <bool kOutF32>
     __device__ __forceinline__ void store(uint32_t buf, int32_t x, const UnitInfo& ui) const {
@@ -213,6 +236,7 @@ struct GroupedProblem {
         ui.store_y = tc.m_blk * BM;
         ui.store_z = g;
         ui.n_limit = N;
+        ui.m_limit = rows;
         return ui;
     }
     __device__ __forceinline__ void load_a(uint32_t dst, int32_t k, const UnitInfo& ui,
@@ -260,7 +284,8 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
             }
             for (uint32_t a = 0; a < 2; ++a) {
                 mbar_init(acc_full_bar(a), 1);
-                mbar_init(acc_empty_bar(a), C::kEpiThreads / 32);
+                // The leader's acc_empty collects the epilogue warps of both CTAs.
+                mbar_init(acc_empty_bar(a), (C::kPair ? 2 : 1) * C::kEpiThreads / 32);
             }
             mbar_init(mma_done_bar, 1);
             *abort_flag = 0;
@@ -269,21 +294,35 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
         }
         __syncwarp();
     } else if (warp == 1) {
-        tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
-        tmem_relinquish();
+        if constexpr (C::kPair) {
+            tmem_alloc_pair(smem_u32(tmem_holder), C::kTmemCols);
+            tmem_relinquish_pair();
+        } else {
+            tmem_alloc(smem_u32(tmem_holder), C::kTmemCols);
+            tmem_relinquish();
+        }
     }
     tc_fence_before();
     __syncthreads();
+    // A pair's barriers must be initialised before the peer's TMA or MMA
+    // commits can reach them.
+    if constexpr (C::kPair) cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // Work distribution: single CTAs step by the grid; pairs by the pair count.
+    const uint32_t rank = C::kPair ? cluster_ctarank() : 0u;
+    const int32_t unit0 =
+        C::kPair ? static_cast<int32_t>(blockIdx.x / 2) : static_cast<int32_t>(blockIdx.x);
+    const int32_t unit_step =
+        C::kPair ? static_cast<int32_t>(gridDim.x / 2) : static_cast<int32_t>(gridDim.x);
 
     if (warp == 0) {
         // ================= TMA producer =================
         if (elect_one()) {
             uint32_t it = 0;
             bool ok = true;
-            for (int32_t u = blockIdx.x; ok && u < prob.num_units(); u += gridDim.x) {
-                const UnitInfo ui = prob.unit(u, C::BM, C::BN, C::kGroupM);
+            for (int32_t u = unit0; ok && u < prob.num_units(); u += unit_step) {
+                const UnitInfo ui = prob.unit(u, C::kTileM, C::BN, C::kGroupM);
                 for (int32_t kb = ui.kb0; kb < ui.kb1; ++kb) {
                     const uint32_t s = ring_stage(it, C::STAGES);
                     const uint32_t ph = ring_phase(it, C::STAGES);
@@ -292,27 +331,44 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                         ok = false;
                         break;
                     }
-                    mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
-                    prob.load_a(sbase + C::kOffA + s * C::kABytes, kb * C::BK, ui, full_bar(s));
-                    prob.load_b(sbase + C::kOffB + s * C::kBBytes, kb * C::BK, ui, full_bar(s));
+                    if constexpr (C::kPair) {
+                        // Both CTAs' bytes land on the leader's full[s]; only the
+                        // leader registers them (its single arrival completes
+                        // the phase once all bytes of both CTAs are in).
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * C::kStageBytes);
+                        const uint32_t leader_full = map_to_rank(full_bar(s), 0);
+                        prob.load_a_pair(sbase + C::kOffA + s * C::kABytes, kb * C::BK,
+                                         ui.a_row + static_cast<int32_t>(rank) * C::BM, leader_full);
+                        prob.load_b_pair(sbase + C::kOffB + s * C::kBBytes, kb * C::BK,
+                                         ui.b_row + static_cast<int32_t>(rank) * C::kBRows,
+                                         leader_full);
+                    } else {
+                        mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
+                        prob.load_a(sbase + C::kOffA + s * C::kABytes, kb * C::BK, ui, full_bar(s));
+                        prob.load_b(sbase + C::kOffB + s * C::kBBytes, kb * C::BK, ui, full_bar(s));
+                    }
                     ++it;
                 }
             }
             // Drain: the last (up to) STAGES issued stages must have landed
-            // before shared memory is released.
-            const uint32_t first = it > (uint32_t)C::STAGES ? it - C::STAGES : 0u;
-            for (uint32_t j = first; j < it; ++j)
-                wait_bounded(full_bar(ring_stage(j, C::STAGES)), ring_phase(j, C::STAGES), err,
-                             kSiteDrainFull, limit_ns);
+            // before shared memory is released.  In a pair the leader's full
+            // barriers count both CTAs' loads; the peer stays until the final
+            // cluster barrier.
+            if (rank == 0) {
+                const uint32_t first = it > (uint32_t)C::STAGES ? it - C::STAGES : 0u;
+                for (uint32_t j = first; j < it; ++j)
+                    wait_bounded(full_bar(ring_stage(j, C::STAGES)), ring_phase(j, C::STAGES), err,
+                                 kSiteDrainFull, limit_ns);
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
-        // ================= MMA issuer =================
-        if (elect_one()) {
+        // ================= MMA issuer (the leader's, for a pair) =================
+        if (rank == 0 && elect_one()) {
             uint32_t it = 0, tcount = 0;
             bool ok = true;
-            for (int32_t u = blockIdx.x; ok && u < prob.num_units(); u += gridDim.x, ++tcount) {
-                const UnitInfo ui = prob.unit(u, C::BM, C::BN, C::kGroupM);
+            for (int32_t u = unit0; ok && u < prob.num_units(); u += unit_step, ++tcount) {
+                const UnitInfo ui = prob.unit(u, C::kTileM, C::BN, C::kGroupM);
                 const int32_t kb0 = ui.kb0;
                 const int32_t kb1 = ui.kb1;
                 const uint32_t acc = tcount & 1u;
@@ -334,18 +390,33 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                     const uint32_t b_addr = sbase + C::kOffB + s * C::kBBytes;
 #pragma unroll
                     for (int j = 0; j < C::BK / 16; ++j) {
-                        mma_f16_ss(d_tmem, umma_desc_sw128_kmajor(a_addr + 32u * j),
-                                   umma_desc_sw128_kmajor(b_addr + 32u * j), C::kIdesc,
-                                   (kb != kb0 || j != 0) ? 1u : 0u);
+                        const uint64_t ad = umma_desc_sw128_kmajor(a_addr + 32u * j);
+                        const uint64_t bd = umma_desc_sw128_kmajor(b_addr + 32u * j);
+                        const uint32_t accum = (kb != kb0 || j != 0) ? 1u : 0u;
+                        if constexpr (C::kPair)
+                            mma_f16_ss_pair(d_tmem, ad, bd, C::kIdesc, accum);
+                        else
+                            mma_f16_ss(d_tmem, ad, bd, C::kIdesc, accum);
                     }
-                    mma_commit(empty_bar(s));   // stage s free once these MMAs finish
+                    // stage s free (in both CTAs of a pair) once these MMAs finish
+                    if constexpr (C::kPair)
+                        mma_commit_pair(empty_bar(s), 0x3);
+                    else
+                        mma_commit(empty_bar(s));
                     ++it;
                 }
                 if (!ok) break;
-                mma_commit(acc_full_bar(acc));  // accumulator ready for the epilogue
+                // accumulator ready for the epilogue (of both CTAs of a pair)
+                if constexpr (C::kPair)
+                    mma_commit_pair(acc_full_bar(acc), 0x3);
+                else
+                    mma_commit(acc_full_bar(acc));
             }
             // All issued MMAs must finish before TMEM is released.
-            mma_commit(mma_done_bar);
+            if constexpr (C::kPair)
+                mma_commit_pair(mma_done_bar, 0x1);
+            else
+                mma_commit(mma_done_bar);
             wait_bounded(mma_done_bar, 0, err, kSiteDrainMma, limit_ns);
         }
         __syncwarp();
@@ -355,8 +426,9 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
         const uint32_t row = quarter * 32u + static_cast<uint32_t>(lane);  // row in tile
         const bool leader = threadIdx.x == 64;
         uint32_t tcount = 0, box = 0;
-        for (int32_t u = blockIdx.x; u < prob.num_units(); u += gridDim.x, ++tcount) {
-            const UnitInfo ui = prob.unit(u, C::BM, C::BN, C::kGroupM);
+        for (int32_t u = unit0; u < prob.num_units(); u += unit_step, ++tcount) {
+            UnitInfo ui = prob.unit(u, C::kTileM, C::BN, C::kGroupM);
+            ui.store_y += static_cast<int32_t>(rank) * C::BM;   // this CTA's 128 rows
             const int32_t n0 = ui.b_row;
             const uint32_t acc = tcount & 1u;
             const uint32_t acc_ph = (tcount >> 1) & 1u;
@@ -383,7 +455,12 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                     // Whole accumulator read: give it back to the MMA warp.
                     tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(acc_empty_bar(acc));
+                    if (lane == 0) {
+                        if constexpr (C::kPair)
+                            mbar_arrive_cluster(map_to_rank(acc_empty_bar(acc), 0));
+                        else
+                            mbar_arrive(acc_empty_bar(acc));
+                    }
                 }
                 const uint32_t buf = sbase + C::kOffD + (box & 1u) * C::kEpiBufBytes;
                 // The store that last read this buffer (two boxes ago) must be done.
@@ -412,7 +489,8 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 named_bar_sync(1, C::kEpiThreads);
                 if (leader) {
                     const int32_t x = n0 + c * C::kEpiCols;
-                    if (x < ui.n_limit) prob.template store<C::kOutF32>(buf, x, ui);
+                    if (x < ui.n_limit && ui.store_y < ui.m_limit)
+                        prob.template store<C::kOutF32>(buf, x, ui);
                     bulk_commit_group();
                 }
             }
@@ -423,9 +501,15 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
     // ---- teardown ----
     tc_fence_before();
     __syncthreads();
+    // A pair stays alive until both CTAs are done with each other's shared
+    // memory and barriers.
+    if constexpr (C::kPair) cluster_sync();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem_base, C::kTmemCols);
+        if constexpr (C::kPair)
+            tmem_dealloc_pair(tmem_base, C::kTmemCols);
+        else
+            tmem_dealloc(tmem_base, C::kTmemCols);
     }
 }
 
@@ -462,11 +546,13 @@ GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) 
     p.bk = C::BK;
     p.stages = C::STAGES;
     p.epi_cols = C::kEpiCols;
-    p.grid_m = ceil_div(M, C::BM);
+    p.grid_m = ceil_div(M, C::kTileM);
     p.grid_n = ceil_div(N, C::BN);
     p.k_blocks = ceil_div(K, C::BK);
     p.tiles = p.grid_m * p.grid_n;
-    const int64_t slots = sms * C::kCtasPerSm;   // resident CTAs
+    // Resident work slots: CTAs, or CTA pairs (sms = the device's co-resident
+    // pair count for pair configurations).
+    const int64_t slots = sms * C::kCtasPerSm;
     if (splits <= 0) {
         // Automatic: enough units to cover the SMs, at least 4 k-blocks each.
         splits = slots / p.tiles;
@@ -479,11 +565,13 @@ GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) 
     p.kb_per_unit = ceil_div(p.k_blocks, splits);
     p.splits = ceil_div(p.k_blocks, p.kb_per_unit);   // no empty split
     p.units = p.tiles * p.splits;
-    p.grid = static_cast<int>(p.units < slots ? p.units : slots);
+    p.grid = static_cast<int>(p.units < slots ? p.units : slots) * (C::kPair ? 2 : 1);
     p.threads = C::kThreads;
     p.smem_bytes = static_cast<int>(C::kSmemBytes);
     p.out_f32 = C::kOutF32;
     p.bf16 = C::kBF16;
+    p.pair = C::kPair;
+    p.b_box_rows = C::kBRows;
     return p;
 }
 
@@ -491,8 +579,10 @@ GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) 
 // kb_per_unit k-blocks, and a k-block costs about BN + 32 units of time (MMA
 // time grows with BN, the A operand traffic per k-block does not).
 int64_t plan_cost(const GemmPlan& p) {
-    const int64_t rounds = ceil_div(p.units, p.grid);
-    return rounds * p.kb_per_unit * (p.bn + 32);
+    const int64_t slots = p.pair ? p.grid / 2 : p.grid;
+    const int64_t rounds = ceil_div(p.units, slots);
+    // A pair streams half of B per SM: less operand traffic per k-block.
+    return rounds * p.kb_per_unit * (p.bn + (p.pair ? 16 : 32));
 }
 
 // Per-device opt-in to > 48 KB dynamic shared memory for `kernel`, once per device.
@@ -523,6 +613,7 @@ cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUten
     prob.tmA = tmA;
     prob.tmB = tmB;
     prob.tmD = tmD;
+    prob.w.M = args.M;
     prob.w.N = args.N;
     prob.w.grid_m = static_cast<int32_t>(plan.grid_m);
     prob.w.grid_n = static_cast<int32_t>(plan.grid_n);
@@ -530,8 +621,25 @@ cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUten
     prob.w.num_units = static_cast<int32_t>(plan.units);
     prob.w.k_blocks = static_cast<int32_t>(plan.k_blocks);
     prob.w.kb_per_unit = static_cast<int32_t>(plan.kb_per_unit);
-    kernel<<<plan.grid, C::kThreads, C::kSmemBytes, stream>>>(prob, args.wait_limit_ns,
-                                                             args.err_word);
+    if constexpr (C::kPair) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
+        cfg.blockDim = dim3(C::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kernel, prob, args.wait_limit_ns, args.err_word);
+        if (e != cudaSuccess) return e;
+    } else {
+        kernel<<<plan.grid, C::kThreads, C::kSmemBytes, stream>>>(prob, args.wait_limit_ns,
+                                                                 args.err_word);
+    }
     return cudaGetLastError();
 }
 
@@ -599,29 +707,43 @@ cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, const GemmArgs& 
 }
 
 int g_force_tile_n = 0;
+int g_pair_mode = 0;
 
 namespace {
 
 template <bool T>
-GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) {
-    GemmPlan cands[3];
+GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs, int64_t splits) {
+    GemmPlan cands[6];
+    int n = 0;
+    const int pair_mode = __atomic_load_n(&g_pair_mode, __ATOMIC_ACQUIRE);
+    const bool pairs_ok = splits == 1 && pairs > 0 && pair_mode != 1;
+    const bool singles_ok = !(pairs_ok && pair_mode == 2);
     if (splits == 1) {
-        cands[0] = plan_for<Cfg256<T>>(M, N, K, sms, 1);
-        cands[1] = plan_for<Cfg224<T>>(M, N, K, sms, 1);
-        cands[2] = plan_for<Cfg192<T>>(M, N, K, sms, 1);
+        if (singles_ok) {
+            cands[n++] = plan_for<Cfg256<T>>(M, N, K, sms, 1);
+            cands[n++] = plan_for<Cfg224<T>>(M, N, K, sms, 1);
+            cands[n++] = plan_for<Cfg192<T>>(M, N, K, sms, 1);
+        }
+        if (pairs_ok) {
+            cands[n++] = plan_for<CfgP256<T>>(M, N, K, pairs, 1);
+            cands[n++] = plan_for<CfgP224<T>>(M, N, K, pairs, 1);
+            cands[n++] = plan_for<CfgP192<T>>(M, N, K, pairs, 1);
+        }
     } else {
-        cands[0] = plan_for<Cfg256F<T>>(M, N, K, sms, splits);
-        cands[1] = plan_for<Cfg224F<T>>(M, N, K, sms, splits);
-        cands[2] = plan_for<Cfg192F<T>>(M, N, K, sms, splits);
+        cands[n++] = plan_for<Cfg256F<T>>(M, N, K, sms, splits);
+        cands[n++] = plan_for<Cfg224F<T>>(M, N, K, sms, splits);
+        cands[n++] = plan_for<Cfg192F<T>>(M, N, K, sms, splits);
     }
     const int forced = __atomic_load_n(&g_force_tile_n, __ATOMIC_ACQUIRE);
     GemmPlan best = cands[0];
-    for (const GemmPlan& c : cands) {
-        if (forced != 0) {
-            if (c.bn == forced) return c;
-            continue;
+    bool have = false;
+    for (int i = 0; i < n; ++i) {
+        const GemmPlan& c = cands[i];
+        if (forced != 0 && c.bn != forced) continue;
+        if (!have || plan_cost(c) < plan_cost(best)) {
+            best = c;
+            have = true;
         }
-        if (plan_cost(c) < plan_cost(best)) best = c;
     }
     return best;
 }
@@ -629,6 +751,14 @@ GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits
 template <bool T>
 cudaError_t launch_typed(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream) {
+    if (plan.pair) {
+        switch (plan.bn) {
+            case 256: return launch_cfg<CfgP256<T>>(plan, tmA, tmB, tmD, args, stream);
+            case 224: return launch_cfg<CfgP224<T>>(plan, tmA, tmB, tmD, args, stream);
+            case 192: return launch_cfg<CfgP192<T>>(plan, tmA, tmB, tmD, args, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     if (!plan.out_f32) {
         switch (plan.bn) {
             case 256: return launch_cfg<Cfg256<T>>(plan, tmA, tmB, tmD, args, stream);
@@ -647,9 +777,33 @@ cudaError_t launch_typed(const GemmPlan& plan, const CUtensorMap& tmA, const CUt
 
 }  // namespace
 
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits, bool bf16) {
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits, bool bf16,
+                   int num_pairs) {
     const int64_t sms = num_sms > 0 ? num_sms : 1;
-    return bf16 ? plan_typed<true>(M, N, K, sms, splits) : plan_typed<false>(M, N, K, sms, splits);
+    return bf16 ? plan_typed<true>(M, N, K, sms, num_pairs, splits)
+                : plan_typed<false>(M, N, K, sms, num_pairs, splits);
+}
+
+int max_resident_pairs() {
+    // How many two-CTA clusters of the pair kernel can be resident at once.
+    auto kernel = gemm_tn_f16_kernel<CfgP256<false>, DenseProblem>;
+    static std::atomic<bool> attr_done[64];
+    if (smem_opt_in(kernel, static_cast<int>(CfgP256<false>::kSmemBytes), attr_done) != cudaSuccess)
+        return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2, 1, 1);
+    cfg.blockDim = dim3(CfgP256<false>::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = CfgP256<false>::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) return 0;
+    return clusters;
 }
 
 cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,

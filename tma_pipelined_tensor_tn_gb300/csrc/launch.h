@@ -20,13 +20,22 @@ struct GemmPlan {
     int epi_cols;          // columns per epilogue TMA store box
     bool out_f32;          // split-K partials (FP32 workspace) instead of fp16 D
     bool bf16;             // bf16 operands and output instead of fp16
+    bool pair;             // CTA-pair (cta_group::2) tiles of 256 x bn
+    int b_box_rows;        // rows of B per CTA (bn, or bn / 2 for a pair)
 };
 
 // Pure function of the problem shape and the SM count (no CUDA calls).
 // splits == 1: the plain GEMM; splits == 0: choose the split count; else that
 // many splits (clamped so that no split is empty).
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits = 1,
-                   bool bf16 = false);
+                   bool bf16 = false, int num_pairs = 0);
+
+// Co-resident two-CTA clusters of the pair kernel on the current device
+// (0 if clusters cannot be launched).
+int max_resident_pairs();
+
+// Pair-mode override for the plan: 0 automatic, 1 never pairs, 2 pairs only.
+extern int g_pair_mode;
 
 // D = fp16/bf16(sum of `splits` FP32 partial M x N matrices laid out back to back).
 cudaError_t launch_splitk_reduce(const void* partials, void* D, int64_t M, int64_t N,
