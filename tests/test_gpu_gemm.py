@@ -241,3 +241,30 @@ def test_wait_timeout_is_reported_and_context_survives(tg):
     assert tg.tmagemm_check(None) == tg.TMAGEMM_OK          # cleared
     A, B = inputs.gemm_inputs(256, 256, 256, seed=9)
     compare(run_gemm(tg, A, B), oracle.gemm_f16(A.numpy(), B.numpy()), "after timeout")
+
+
+def random_shapes(seed, count):
+    """Seeded random shapes across the supported space: M any size >= 2,
+    N and K multiples of 8, spanning one tile to several waves."""
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(count):
+        M = int(rng.integers(2, 2600))
+        N = 8 * int(rng.integers(1, 330))
+        K = 8 * int(rng.integers(1, 600))
+        out.append((M, N, K))
+    return out
+
+
+@pytest.mark.parametrize("M,N,K", random_shapes(2024, 12))
+def test_gemm_random_shapes(tg, M, N, K):
+    A, B = inputs.gemm_inputs(M, N, K, seed=M * 7 + N)
+    compare(run_gemm(tg, A, B), oracle.gemm_f16(A.numpy(), B.numpy()), f"random {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("M,N,K", random_shapes(77, 6))
+def test_splitk_random_shapes(tg, M, N, K):
+    A, B = inputs.gemm_inputs(M, N, K, seed=M + 3 * N)
+    D = tg.gemm_splitk(A.cuda(), B.cuda(), splits=0)
+    tg.check()
+    compare(D.cpu().numpy(), oracle.gemm_f16(A.numpy(), B.numpy()), f"split-K random {M}x{N}x{K}")
