@@ -45,27 +45,37 @@ def test_grouped_parity(tg, G, tokens, N, K):
             f"grouped G={G}")
 
 
-def test_grouped_empty_and_tiny_groups_integer_bitexact(tg):
+@pytest.mark.parametrize("pair", [1, 2])
+def test_grouped_empty_and_tiny_groups_integer_bitexact(tg, pair):
     offs = [0, 0, 1, 130, 130, 257, 600]      # empty, 1-row, ragged groups
     G, N, K = 6, 264, 1000
     A = inputs.integer_f16((offs[-1], K), seed=90)
     B = inputs.integer_f16((G, N, K), seed=91)
-    assert_bitexact(run(tg, A, B, offs), oracle.gemm_f16_grouped(A.numpy(), B.numpy(), offs),
-                    "grouped integer")
+    try:
+        assert tg.tmagemm_set_cta_pair(pair) == tg.TMAGEMM_OK
+        D = run(tg, A, B, offs)
+    finally:
+        tg.tmagemm_set_cta_pair(0)
+    assert_bitexact(D, oracle.gemm_f16_grouped(A.numpy(), B.numpy(), offs), "grouped integer")
 
 
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("bn", [256, 224, 192])
-def test_grouped_each_tile_width(tg, bn):
+def test_grouped_each_tile_width(tg, bn, pair):
+    """Every tile width, single-CTA (pair=1) and CTA-pair (pair=2) tiles; a
+    pair tile's second half often lies past its group's last row."""
     offs = moe_offsets(5, 1500, seed=bn)
     g = torch.Generator().manual_seed(bn)
     A = (torch.rand((1500, 520), generator=g) * 2 - 1).half()
     B = (torch.rand((5, 1000, 520), generator=g) * 2 - 1).half()
     try:
         assert tg.tmagemm_set_tile_n(bn) == tg.TMAGEMM_OK
+        assert tg.tmagemm_set_cta_pair(pair) == tg.TMAGEMM_OK
         D = run(tg, A, B, offs)
     finally:
         tg.tmagemm_set_tile_n(0)
-    compare(D, oracle.gemm_f16_grouped(A.numpy(), B.numpy(), offs), f"grouped BN={bn}")
+        tg.tmagemm_set_cta_pair(0)
+    compare(D, oracle.gemm_f16_grouped(A.numpy(), B.numpy(), offs), f"grouped BN={bn} pair={pair}")
 
 
 def test_grouped_rows_outside_groups_untouched_and_errors(tg):

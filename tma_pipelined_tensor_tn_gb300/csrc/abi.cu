@@ -247,7 +247,7 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
     g.groups = G;
     g.N = N;
     g.K = K;
-    g.bn = grouped_tile_n(m_offsets, G, N, d->sms);
+    g.bn = grouped_tile_n(m_offsets, G, N, d->sms, d->pairs, &g.pair);
     const int epi_cols = g.bn == 224 ? 32 : 64;
     if (int s = encode_2d(&g.tmA, A, K, rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
@@ -256,7 +256,7 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
         cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(G)};
         cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(N * K) * 2};
-        cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g.bn), 1};
+        cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g.pair ? g.bn / 2 : g.bn), 1};
         cuuint32_t estr[3] = {1, 1, 1};
         if (g_encode(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(B), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -280,7 +280,7 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
     args.K = static_cast<int32_t>(K);
     args.wait_limit_ns = wait_limit_ns();
     args.err_word = d->err_word;
-    cudaError_t e = launch_grouped(g, d->sms, args, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_grouped(g, d->sms, d->pairs, args, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 

@@ -181,14 +181,15 @@ struct DenseProblem {
                                            uint32_t bar) const {
         tma_load_2d(dst, &tmB, k, ui.b_row, bar);
     }
-    // Pair forms: rows given explicitly, bytes counted on the leader's barrier.
-    __device__ __forceinline__ void load_a_pair(uint32_t dst, int32_t k, int32_t row,
-                                                uint32_t bar_cluster) const {
-        tma_load_2d_pair(dst, &tmA, k, row, bar_cluster);
+    // Pair forms: this CTA's rows (unit row + offset), bytes counted on the
+    // leader's barrier (cluster address).
+    __device__ __forceinline__ void load_a_pair(uint32_t dst, int32_t k, const UnitInfo& ui,
+                                                int32_t row_off, uint32_t bar_cluster) const {
+        tma_load_2d_pair(dst, &tmA, k, ui.a_row + row_off, bar_cluster);
     }
-    __device__ __forceinline__ void load_b_pair(uint32_t dst, int32_t k, int32_t row,
-                                                uint32_t bar_cluster) const {
-        tma_load_2d_pair(dst, &tmB, k, row, bar_cluster);
+    __device__ __forceinline__ void load_b_pair(uint32_t dst, int32_t k, const UnitInfo& ui,
+                                                int32_t row_off, uint32_t bar_cluster) const {
+        tma_load_2d_pair(dst, &tmB, k, ui.b_row + row_off, bar_cluster);
     }
     template <bool kOutF32>
     __device__ __forceinline__ void store(uint32_t buf, int32_t x, const UnitInfo& ui) const {
@@ -246,6 +247,14 @@ struct GroupedProblem {
     __device__ __forceinline__ void load_b(uint32_t dst, int32_t k, const UnitInfo& ui,
                                            uint32_t bar) const {
         tma_load_3d(dst, &tmB, k, ui.b_row, ui.store_z, bar);
+    }
+    __device__ __forceinline__ void load_a_pair(uint32_t dst, int32_t k, const UnitInfo& ui,
+                                                int32_t row_off, uint32_t bar_cluster) const {
+        tma_load_2d_pair(dst, &tmA, k, ui.a_row + row_off, bar_cluster);
+    }
+    __device__ __forceinline__ void load_b_pair(uint32_t dst, int32_t k, const UnitInfo& ui,
+                                                int32_t row_off, uint32_t bar_cluster) const {
+        tma_load_3d_pair(dst, &tmB, k, ui.b_row + row_off, ui.store_z, bar_cluster);
     }
     template <bool kOutF32>
     __device__ __forceinline__ void store(uint32_t buf, int32_t x, const UnitInfo& ui) const {
@@ -337,11 +346,10 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                         // the phase once all bytes of both CTAs are in).
                         if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * C::kStageBytes);
                         const uint32_t leader_full = map_to_rank(full_bar(s), 0);
-                        prob.load_a_pair(sbase + C::kOffA + s * C::kABytes, kb * C::BK,
-                                         ui.a_row + static_cast<int32_t>(rank) * C::BM, leader_full);
-                        prob.load_b_pair(sbase + C::kOffB + s * C::kBBytes, kb * C::BK,
-                                         ui.b_row + static_cast<int32_t>(rank) * C::kBRows,
-                                         leader_full);
+                        prob.load_a_pair(sbase + C::kOffA + s * C::kABytes, kb * C::BK, ui,
+                                         static_cast<int32_t>(rank) * C::BM, leader_full);
+                        prob.load_b_pair(sbase + C::kOffB + s * C::kBBytes, kb * C::BK, ui,
+                                         static_cast<int32_t>(rank) * C::kBRows, leader_full);
                     } else {
                         mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
                         prob.load_a(sbase + C::kOffA + s * C::kABytes, kb * C::BK, ui, full_bar(s));
@@ -644,8 +652,8 @@ cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUten
 }
 
 template <class C>
-cudaError_t launch_grouped_cfg(const GroupedLaunch& g, int num_sms, const GemmArgs& args,
-                               cudaStream_t stream) {
+cudaError_t launch_grouped_cfg(const GroupedLaunch& g, int num_sms, int num_pairs,
+                               const GemmArgs& args, cudaStream_t stream) {
     auto kernel = gemm_tn_f16_kernel<C, GroupedProblem>;
     static std::atomic<bool> attr_done[64];
     cudaError_t e = smem_opt_in(kernel, static_cast<int>(C::kSmemBytes), attr_done);
@@ -664,44 +672,83 @@ cudaError_t launch_grouped_cfg(const GroupedLaunch& g, int num_sms, const GemmAr
         if (i < g.groups) {
             prob.tmD[i] = g.tmD[i];
             const int64_t rows = g.m_offsets[i + 1] - g.m_offsets[i];
-            t += static_cast<int32_t>(ceil_div(rows, C::BM) * prob.grid_n);
+            t += static_cast<int32_t>(ceil_div(rows, C::kTileM) * prob.grid_n);
         }
     }
     if (t == 0) return cudaSuccess;   // every group is empty
-    const int grid = t < num_sms ? t : num_sms;
-    kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(prob, args.wait_limit_ns, args.err_word);
+    if constexpr (C::kPair) {
+        const int pairs = t < num_pairs ? t : num_pairs;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
+        cfg.blockDim = dim3(C::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = C::kSmemBytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, kernel, prob, args.wait_limit_ns, args.err_word);
+        if (e != cudaSuccess) return e;
+    } else {
+        const int grid = t < num_sms ? t : num_sms;
+        kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(prob, args.wait_limit_ns,
+                                                             args.err_word);
+    }
     return cudaGetLastError();
 }
 
 }  // namespace
 
-int grouped_tile_n(const int64_t* m_offsets, int64_t groups, int64_t N, int num_sms) {
-    // The width that minimises rounds x (BN + 32) over all groups' tiles.
+int grouped_tile_n(const int64_t* m_offsets, int64_t groups, int64_t N, int num_sms, int num_pairs,
+                   bool* pair) {
+    // The width (and single CTAs or pairs) that minimises rounds x (BN + c)
+    // over all groups' tiles, as for the dense plan.
     const int widths[3] = {256, 224, 192};
     const int forced = __atomic_load_n(&g_force_tile_n, __ATOMIC_ACQUIRE);
-    if (forced != 0) return forced;
+    const int pair_mode = __atomic_load_n(&g_pair_mode, __ATOMIC_ACQUIRE);
     int best = 256;
+    bool best_pair = false;
     int64_t best_cost = -1;
-    for (int bn : widths) {
-        int64_t tiles = 0;
-        for (int64_t i = 0; i < groups; ++i)
-            tiles += ceil_div(m_offsets[i + 1] - m_offsets[i], 128) * ceil_div(N, bn);
-        const int64_t sms = num_sms > 0 ? num_sms : 1;
-        const int64_t cost = ceil_div(tiles, tiles < sms ? (tiles > 0 ? tiles : 1) : sms) * (bn + 32);
-        if (best_cost < 0 || cost < best_cost) {
-            best = bn;
-            best_cost = cost;
+    for (int use_pair = 0; use_pair < 2; ++use_pair) {
+        if (use_pair && (num_pairs <= 0 || pair_mode == 1)) continue;
+        if (!use_pair && num_pairs > 0 && pair_mode == 2) continue;
+        const int64_t tile_m = use_pair ? 256 : 128;
+        const int64_t slots = use_pair ? num_pairs : (num_sms > 0 ? num_sms : 1);
+        for (int bn : widths) {
+            if (forced != 0 && bn != forced) continue;
+            int64_t tiles = 0;
+            for (int64_t i = 0; i < groups; ++i)
+                tiles += ceil_div(m_offsets[i + 1] - m_offsets[i], tile_m) * ceil_div(N, bn);
+            const int64_t used = tiles < slots ? (tiles > 0 ? tiles : 1) : slots;
+            const int64_t cost = ceil_div(tiles, used) * (bn + (use_pair ? 16 : 32));
+            if (best_cost < 0 || cost < best_cost) {
+                best = bn;
+                best_pair = use_pair != 0;
+                best_cost = cost;
+            }
         }
     }
+    *pair = best_pair;
     return best;
 }
 
-cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, const GemmArgs& args,
+cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, int num_pairs, const GemmArgs& args,
                            cudaStream_t stream) {
+    if (g.pair) {
+        switch (g.bn) {
+            case 256: return launch_grouped_cfg<CfgP256<false>>(g, num_sms, num_pairs, args, stream);
+            case 224: return launch_grouped_cfg<CfgP224<false>>(g, num_sms, num_pairs, args, stream);
+            case 192: return launch_grouped_cfg<CfgP192<false>>(g, num_sms, num_pairs, args, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (g.bn) {
-        case 256: return launch_grouped_cfg<Cfg256<false>>(g, num_sms, args, stream);
-        case 224: return launch_grouped_cfg<Cfg224<false>>(g, num_sms, args, stream);
-        case 192: return launch_grouped_cfg<Cfg192<false>>(g, num_sms, args, stream);
+        case 256: return launch_grouped_cfg<Cfg256<false>>(g, num_sms, num_pairs, args, stream);
+        case 224: return launch_grouped_cfg<Cfg224<false>>(g, num_sms, num_pairs, args, stream);
+        case 192: return launch_grouped_cfg<Cfg192<false>>(g, num_sms, num_pairs, args, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -73,9 +73,11 @@ struct GroupedLaunch {
     const int64_t* m_offsets;   // host, groups + 1 entries
     int64_t groups, N, K;
     int bn;
+    bool pair;                  // CTA-pair tiles (256 rows; B box bn / 2 rows)
 };
-int grouped_tile_n(const int64_t* m_offsets, int64_t groups, int64_t N, int num_sms);
-cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, const GemmArgs& args,
+int grouped_tile_n(const int64_t* m_offsets, int64_t groups, int64_t N, int num_sms, int num_pairs,
+                   bool* pair);
+cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, int num_pairs, const GemmArgs& args,
                            cudaStream_t stream);
 
 // Enqueue the GEMV kernel: y[n] = sum_k x[k] * W[n][k]; one warp per row;
