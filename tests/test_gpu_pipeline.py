@@ -1,0 +1,40 @@
+"""The host-buffer executor (HostGemmPipeline): overlapping the copies of
+neighbouring steps must not change any step's result."""
+import numpy as np
+import pytest
+
+from tma_pipelined_tensor_tn_gb300 import inputs
+from tests.parity_util import assert_bitexact
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def tg():
+    import tma_pipelined_tensor_tn_gb300 as m
+    m.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return m
+
+
+@pytest.mark.parametrize("depth", [1, 2, 3])
+def test_pipeline_matches_direct_calls(tg, depth):
+    from tma_pipelined_tensor_tn_gb300.pipeline import HostGemmPipeline
+    M, N, K, steps = 640, 520, 1032, 7
+    As, Bs = [], []
+    for i in range(steps):
+        a, b = inputs.gemm_inputs(M, N, K, seed=100 + i)
+        As.append(a.pin_memory())
+        Bs.append(b.pin_memory())
+    Ds = [torch.empty((M, N), dtype=torch.float16).pin_memory() for _ in range(steps)]
+    pipe = HostGemmPipeline(M, N, K, depth=depth)
+    pipe.run(As, Bs, Ds)
+    pipe.synchronize()
+    tg.check()
+    for i in range(steps):
+        ref = tg.gemm(As[i].cuda(), Bs[i].cuda())
+        tg.check()
+        assert_bitexact(Ds[i].numpy(), ref.cpu().numpy(), f"step {i}")
+    assert pipe.h2d_bytes_per_step() == 2 * (M * K + N * K)
+    assert pipe.d2h_bytes_per_step() == 2 * M * N
