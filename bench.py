@@ -579,6 +579,40 @@ def measure_extras(tg, dev, stream, l2):
     t_d = _time_launches(dense, 50, stream)
     tg.check(stream)
     fl = 2.0 * T * Ng * Kg
+    # The parity workloads beyond the headline, for their TFLOP/s: 256^3
+    # (launch-bound: direct calls and 100 calls replayed from one CUDA graph),
+    # the ragged 4000x3000x4160 shape, and 8192^3 (5 launches).
+    for name, (Mw, Nw, Kw, reps) in {"gemm_ragged_4000x3000x4160": (4000, 3000, 4160, 50),
+                                     "gemm_8192": (8192, 8192, 8192, 5),
+                                     "gemm_256": (256, 256, 256, 200)}.items():
+        Aw, Bw = inputs.gemm_inputs(Mw, Nw, Kw, seed=12)
+        aw, bw = Aw.to(dev), Bw.to(dev)
+        dw = torch.empty((Mw, Nw), dtype=torch.float16, device=dev)
+        fn = (lambda i, aw=aw, bw=bw, dw=dw, Mw=Mw, Nw=Nw, Kw=Kw:
+              tg.gemm_f16(Mw, Nw, Kw, aw.data_ptr(), bw.data_ptr(), dw.data_ptr(), sh))
+        t_w = _time_launches(lambda i: fn(i) == 0 or None, reps, stream)
+        entry = {"us": t_w, "tflops": gemm_flops(Mw, Nw, Kw) / t_w / 1e6}
+        if name == "gemm_256":
+            gs = torch.cuda.Stream(dev)
+            gs.wait_stream(stream)
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph, stream=gs):
+                for _ in range(100):
+                    tg.gemm_f16(Mw, Nw, Kw, aw.data_ptr(), bw.data_ptr(), dw.data_ptr(),
+                                gs.cuda_stream)
+            graph.replay()
+            torch.cuda.synchronize(dev)
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            g0.record(stream)
+            for _ in range(5):
+                graph.replay()
+            g1.record(stream)
+            torch.cuda.synchronize(dev)
+            t_g = g0.elapsed_time(g1) * 1e3 / 500
+            entry.update({"us_in_graph": t_g, "tflops_in_graph": gemm_flops(Mw, Nw, Kw) / t_g / 1e6})
+        tg.check(stream)
+        out[name] = entry
+
     out["grouped_8x(8192_tokens)x4096x2048"] = {
         "us": t_g, "tflops": fl / t_g / 1e6, "dense_same_rows_us": t_d,
         "dense_tflops": fl / t_d / 1e6, "group_rows": [int(c) for c in counts]}
@@ -586,7 +620,7 @@ def measure_extras(tg, dev, stream, l2):
 
 
 CASES = ("gemm4096", "gemv", "splitk", "small_m8", "small_m16", "grouped", "bf16_gemm", "bf16_gemv",
-         "gemm8192")
+         "gemm8192", "gemm_ragged", "gemm256")
 
 
 def run_case(args, name):
@@ -600,9 +634,10 @@ def run_case(args, name):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    if name in ("gemm4096", "bf16_gemm", "gemm8192", "splitk"):
+    if name in ("gemm4096", "bf16_gemm", "gemm8192", "splitk", "gemm_ragged", "gemm256"):
         M, N, K = {"gemm4096": (4096,) * 3, "bf16_gemm": (4096,) * 3, "gemm8192": (8192,) * 3,
-                   "splitk": (1024, 1024, 16384)}[name]
+                   "splitk": (1024, 1024, 16384), "gemm_ragged": (4000, 3000, 4160),
+                   "gemm256": (256,) * 3}[name]
         A, B = inputs.gemm_inputs(M, N, K, seed=0)
         if name == "bf16_gemm":
             A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
