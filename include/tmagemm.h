@@ -249,6 +249,18 @@ int tmagemm_set_cta_pair(int mode);
  */
 int tmagemm_set_tile_n(int bn);
 
+/*
+ * Programmatic dependent launch of the library's kernels: 1 (the default)
+ * launches each kernel with CUDA's programmatic-stream-serialization
+ * attribute, so a kernel queued behind another on the same stream is
+ * scheduled while that one finishes and prepares its barriers meanwhile; it
+ * still waits for the earlier kernel to complete (and its writes to become
+ * visible) before it reads or writes any argument buffer, so results and
+ * stream order are the same either way.  0 launches the kernels plainly.
+ * Process-wide.  Returns TMAGEMM_ERR_INVALID for other values.
+ */
+int tmagemm_set_pdl(int on);
+
 /* ---- host-side introspection of the kernels' schedule (no GPU needed) ---- */
 
 /*

@@ -204,6 +204,15 @@ def test_cta_pair_override():
         assert tg.tmagemm_set_cta_pair(0) == tg.TMAGEMM_OK
 
 
+def test_pdl_switch():
+    try:
+        assert tg.tmagemm_set_pdl(0) == tg.TMAGEMM_OK
+        assert tg.tmagemm_set_pdl(2) == tg.TMAGEMM_ERR_INVALID
+        assert tg.tmagemm_set_pdl(-1) == tg.TMAGEMM_ERR_INVALID
+    finally:
+        assert tg.tmagemm_set_pdl(1) == tg.TMAGEMM_OK
+
+
 def test_tile_width_override():
     try:
         assert tg.tmagemm_set_tile_n(256) == tg.TMAGEMM_OK

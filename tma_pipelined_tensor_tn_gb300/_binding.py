@@ -46,6 +46,7 @@ SIGNATURES = {
     "tmagemm_gemm_plan": ([_i64, _i64, _i64, _i64, _i64, _i64, _P64], _int),
     "tmagemm_set_cta_pair": ([_int], _int),
     "tmagemm_set_tile_n": ([_int], _int),
+    "tmagemm_set_pdl": ([_int], _int),
 }
 
 _lock = threading.Lock()
@@ -219,6 +220,10 @@ def tmagemm_gemm_plan(M, N, K, num_sms, splits=1, num_pairs=0):
 
 def tmagemm_set_cta_pair(mode) -> int:
     return lib().tmagemm_set_cta_pair(mode)
+
+
+def tmagemm_set_pdl(on) -> int:
+    return lib().tmagemm_set_pdl(on)
 
 
 # ---- torch-tensor conveniences (marshalling only) ----------------------------

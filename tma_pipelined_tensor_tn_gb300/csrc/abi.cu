@@ -394,6 +394,12 @@ int tmagemm_set_tile_n(int bn) {
     return TMAGEMM_OK;
 }
 
+int tmagemm_set_pdl(int on) {
+    if (on != 0 && on != 1) return TMAGEMM_ERR_INVALID;
+    __atomic_store_n(&g_pdl, on, __ATOMIC_RELEASE);
+    return TMAGEMM_OK;
+}
+
 int tmagemm_tile_coord(int64_t tile, int64_t grid_m, int64_t grid_n, int64_t group_m,
                        int64_t* m_blk, int64_t* n_blk) {
     if (!m_blk || !n_blk || grid_m <= 0 || grid_n <= 0 || group_m <= 0 || tile < 0 ||

@@ -284,6 +284,11 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
     const int lane = static_cast<int>(threadIdx.x) % 32;
 
+    // The next grid on the stream may be scheduled as soon as every CTA of
+    // this one is running: it cannot share an SM with this grid's CTAs (shared
+    // memory), and it waits (below) before touching global memory.
+    grid_launch_dependents();
+
     // ---- one-time setup: barriers (warp 0), TMEM (warp 1) ----
     if (warp == 0) {
         if (elect_one()) {
@@ -302,7 +307,11 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
             prob.prefetch();
         }
         __syncwarp();
-    } else if (warp == 1) {
+    }
+    // A, B and D (and the previous grid's TMEM) are only touched once the
+    // grid before this one on the stream has completed.
+    grid_dependency_wait();
+    if (warp == 1) {
         if constexpr (C::kPair) {
             tmem_alloc_pair(smem_u32(tmem_holder), C::kTmemCols);
             tmem_relinquish_pair();
@@ -528,6 +537,8 @@ template <bool BF16>
 __global__ void __launch_bounds__(256)
 splitk_reduce_kernel(const float4* __restrict__ P, uint4* __restrict__ D, int64_t groups8,
                      int64_t mn4, int32_t splits) {
+    grid_launch_dependents();
+    grid_dependency_wait();   // the partials come from the grid before this one
     for (int64_t g = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; g < groups8;
          g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         float4 a = P[2 * g], b = P[2 * g + 1];
@@ -629,26 +640,9 @@ cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUten
     prob.w.num_units = static_cast<int32_t>(plan.units);
     prob.w.k_blocks = static_cast<int32_t>(plan.k_blocks);
     prob.w.kb_per_unit = static_cast<int32_t>(plan.kb_per_unit);
-    if constexpr (C::kPair) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
-        cfg.blockDim = dim3(C::kThreads, 1, 1);
-        cfg.dynamicSmemBytes = C::kSmemBytes;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kernel, prob, args.wait_limit_ns, args.err_word);
-        if (e != cudaSuccess) return e;
-    } else {
-        kernel<<<plan.grid, C::kThreads, C::kSmemBytes, stream>>>(prob, args.wait_limit_ns,
-                                                                 args.err_word);
-    }
-    return cudaGetLastError();
+    return launch_kernel(kernel, dim3(static_cast<unsigned>(plan.grid)), dim3(C::kThreads),
+                         C::kSmemBytes, stream, C::kPair ? 2u : 1u, prob, args.wait_limit_ns,
+                         args.err_word);
 }
 
 template <class C>
@@ -676,28 +670,10 @@ cudaError_t launch_grouped_cfg(const GroupedLaunch& g, int num_sms, int num_pair
         }
     }
     if (t == 0) return cudaSuccess;   // every group is empty
-    if constexpr (C::kPair) {
-        const int pairs = t < num_pairs ? t : num_pairs;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(static_cast<unsigned>(2 * pairs), 1, 1);
-        cfg.blockDim = dim3(C::kThreads, 1, 1);
-        cfg.dynamicSmemBytes = C::kSmemBytes;
-        cfg.stream = stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = 2;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, kernel, prob, args.wait_limit_ns, args.err_word);
-        if (e != cudaSuccess) return e;
-    } else {
-        const int grid = t < num_sms ? t : num_sms;
-        kernel<<<grid, C::kThreads, C::kSmemBytes, stream>>>(prob, args.wait_limit_ns,
-                                                             args.err_word);
-    }
-    return cudaGetLastError();
+    const int grid = C::kPair ? 2 * (t < num_pairs ? t : num_pairs) : (t < num_sms ? t : num_sms);
+    return launch_kernel(kernel, dim3(static_cast<unsigned>(grid)), dim3(C::kThreads),
+                         C::kSmemBytes, stream, C::kPair ? 2u : 1u, prob, args.wait_limit_ns,
+                         args.err_word);
 }
 
 }  // namespace
@@ -755,6 +731,7 @@ cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, int num_pairs, c
 
 int g_force_tile_n = 0;
 int g_pair_mode = 0;
+int g_pdl = 1;
 
 namespace {
 
@@ -887,6 +864,8 @@ namespace {
 __global__ void __launch_bounds__(256)
 small_m_reduce_kernel(const float4* __restrict__ P, __half* __restrict__ D, int32_t M, int32_t N,
                       int32_t Mp, int32_t splits) {
+    grid_launch_dependents();
+    grid_dependency_wait();   // the partials come from the grid before this one
     const int32_t groups16 = Mp / 16;
     const int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
     if (t >= static_cast<int64_t>(N) * groups16) return;
@@ -917,10 +896,10 @@ cudaError_t launch_small_m_reduce(const void* partials, void* D, int64_t M, int6
                                   int64_t splits, cudaStream_t stream) {
     const int64_t threads = N * (Mp / 16);
     const int64_t blocks = (threads + 255) / 256;
-    small_m_reduce_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const float4*>(partials), static_cast<__half*>(D), static_cast<int32_t>(M),
-        static_cast<int32_t>(N), static_cast<int32_t>(Mp), static_cast<int32_t>(splits));
-    return cudaGetLastError();
+    return launch_kernel(small_m_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
+                         stream, 1u, static_cast<const float4*>(partials), static_cast<__half*>(D),
+                         static_cast<int32_t>(M), static_cast<int32_t>(N),
+                         static_cast<int32_t>(Mp), static_cast<int32_t>(splits));
 }
 
 cudaError_t launch_splitk_reduce(const void* partials, void* D, int64_t M, int64_t N,
@@ -931,10 +910,9 @@ cudaError_t launch_splitk_reduce(const void* partials, void* D, int64_t M, int64
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     auto kernel = bf16 ? splitk_reduce_kernel<true> : splitk_reduce_kernel<false>;
-    kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
-        static_cast<const float4*>(partials), static_cast<uint4*>(D), groups8, M * N / 4,
-        static_cast<int32_t>(splits));
-    return cudaGetLastError();
+    return launch_kernel(kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1u,
+                         static_cast<const float4*>(partials), static_cast<uint4*>(D), groups8,
+                         M * N / 4, static_cast<int32_t>(splits));
 }
 
 }  // namespace tmagemm

@@ -26,6 +26,7 @@
 #include <cstdint>
 
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace tmagemm {
 
@@ -82,9 +83,13 @@ template <bool BF16>
 __global__ void __launch_bounds__(kGvWarps * 32)
 gemv_f16_kernel(const uint4* __restrict__ x, const uint4* __restrict__ W, uint16_t* __restrict__ y,
                 int32_t N, int32_t K8) {
+    // Every block of this grid is resident by the time all have issued this,
+    // so the next grid may be scheduled; it waits for this one to finish.
+    grid_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int32_t n = blockIdx.x * kGvWarps + (threadIdx.x >> 5);
     if (n >= N) return;
+    grid_dependency_wait();   // x and W may come from the grid before this one
     const uint4* wrow = W + static_cast<int64_t>(n) * K8;
     float acc[kGvGroup] = {};
     // Whole groups: group g covers this lane's chunks lane + 32*(g*GROUP + u).
@@ -123,10 +128,9 @@ cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void
     const int32_t K8 = static_cast<int32_t>(K / 8);
     const int64_t blocks = (N + kGvWarps - 1) / kGvWarps;
     auto kernel = bf16 ? gemv_f16_kernel<true> : gemv_f16_kernel<false>;
-    kernel<<<static_cast<unsigned>(blocks), kGvWarps * 32, 0, stream>>>(
-        static_cast<const uint4*>(x), static_cast<const uint4*>(W), static_cast<uint16_t*>(y),
-        static_cast<int32_t>(N), K8);
-    return cudaGetLastError();
+    return launch_kernel(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kGvWarps * 32), 0,
+                         stream, 1u, static_cast<const uint4*>(x), static_cast<const uint4*>(W),
+                         static_cast<uint16_t*>(y), static_cast<int32_t>(N), K8);
 }
 
 }  // namespace tmagemm

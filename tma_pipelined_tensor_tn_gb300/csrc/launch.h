@@ -88,6 +88,45 @@ cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void
 // Tile-N override for the GEMM plan (0 = automatic); a tuning/test knob.
 extern int g_force_tile_n;
 
+// Programmatic dependent launch: 1 (the default) launches every kernel with
+// the programmatic-stream-serialization attribute, so the next kernel on the
+// stream is scheduled while the previous one finishes and runs its set-up
+// (barrier initialisation, descriptor prefetch) meanwhile.  Every kernel of the
+// library executes griddepcontrol.wait before its first global memory access,
+// so stream order of results is unchanged.  0 launches them plainly.
+extern int g_pdl;
+
+// cudaLaunchKernelEx with a cluster of `cluster_x` CTAs along x (1 = none)
+// and, when g_pdl is set, the programmatic-stream-serialization attribute.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem_bytes,
+                          cudaStream_t stream, unsigned cluster_x, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem_bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    unsigned n = 0;
+    if (cluster_x > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster_x;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (__atomic_load_n(&g_pdl, __ATOMIC_ACQUIRE)) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
 // Enqueue a one-block kernel that waits on an mbarrier nobody arrives on, with
 // the given limit; it must end by recording kSiteTest in the error word.
 cudaError_t launch_wait_timeout_probe(uint64_t limit_ns, uint32_t* err_word, cudaStream_t stream);

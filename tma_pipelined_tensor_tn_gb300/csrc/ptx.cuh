@@ -350,6 +350,19 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t addr, uint32_t rank) {
     return out;
 }
 
+// Programmatic dependent launch (PTX griddepcontrol).  grid_dependency_wait
+// returns once the grids this one depends on have completed and their memory
+// writes are visible to it; for a launch without the programmatic-serialization
+// attribute it returns at once.  grid_launch_dependents allows the next grid
+// on the stream to be scheduled once every CTA of this grid has issued it or
+// exited (issuing it more than once per CTA has no further effect).
+__device__ __forceinline__ void grid_dependency_wait() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void grid_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // All threads of all CTAs of the cluster.
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
