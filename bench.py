@@ -537,7 +537,7 @@ def measure_extras(tg, dev, stream, l2):
     out["bf16_gemv_4096x14336"] = {"us": t_vb, "gbs": gemv_bytes() / t_vb / 1e3}
 
     # Skinny decode GEMMs at the GEMV's weight shape: M tokens x (4096 x 14336).
-    for Ms in (8, 16):
+    for Ms in (8, 16, 32, 64):
         Xs = (torch.randn((Ms, GEMV_K), generator=torch.Generator().manual_seed(Ms)) * 0.02).half()
         xsets = [Xs.to(dev)] * rv
         Ds = torch.empty((Ms, GEMV_N), dtype=torch.float16, device=dev)
@@ -554,7 +554,9 @@ def measure_extras(tg, dev, stream, l2):
         tg.check(stream)
         by = 2.0 * (GEMV_N * GEMV_K + Ms * GEMV_K + Ms * GEMV_N)
         out[f"small_m{Ms}_4096x14336"] = {"us": t_s, "gbs": by / t_s / 1e3,
-                                          "tflops": 2.0 * Ms * GEMV_N * GEMV_K / t_s / 1e6}
+                                          "tflops": 2.0 * Ms * GEMV_N * GEMV_K / t_s / 1e6,
+                                          "kernel": "mma.sync fragments" if need_s == 0
+                                          else "tcgen05 swap-AB + reduce"}
 
     # Grouped GEMM: 8 experts, 8192 routed tokens (skewed counts), N=4096, K=2048,
     # against one dense GEMM over the same 8192 rows.

@@ -166,11 +166,18 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
  * Skinny GEMM for a few rows of activations, D = fp16(X * W^T) with
  * 2 <= M <= 64: the decode step of "Learning TileLang with GEMV" (§01 GEMV:
  * every linear layer is a GEMV when tokens are decoded one by one) for a
- * batch of M tokens.  Like the GEMV it is bound by reading W once.  The
- * tcgen05 kernel runs with the roles swapped — W is the 128-row MMA operand
- * and X (rows past M read as zero) the 16/32/64-wide one — and with K split
- * so that enough SMs stream W; FP32 partials go to `workspace` and a second
- * kernel adds them in fixed order, transposes and rounds to fp16.
+ * batch of M tokens.  Like the GEMV it is bound by reading W once.  Two
+ * kernels, chosen by M (tmagemm_set_small_m_route overrides):
+ *   - M <= 16: W streams from HBM straight into mma.sync register fragments
+ *     (16-byte loads, no shared-memory staging); the CTAs of a cluster split
+ *     K and add their FP32 partials in fixed order through distributed
+ *     shared memory.  Needs no workspace (its size is 0; `workspace` may be
+ *     NULL).
+ *   - otherwise: the tcgen05 kernel with the roles swapped — W is the 128-row
+ *     MMA operand and X (rows past M read as zero) the 16- or 64-wide one —
+ *     and K split so that enough SMs stream W; FP32 partials go to
+ *     `workspace` and a second kernel adds them in fixed order, transposes
+ *     and rounds to fp16.
  *   X         : device pointer, M x K fp16 row-major (activations).
  *   W         : device pointer, N x K fp16 row-major (weights).
  *   D         : device pointer, M x N fp16 row-major.
@@ -184,8 +191,19 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
 int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void* W, void* D,
                      void* workspace, int64_t workspace_bytes, void* stream);
 
-/* Workspace bytes gemm_f16_small_m needs on the current device (negative = status). */
+/* Workspace bytes gemm_f16_small_m needs on the current device (negative =
+ * status; 0 when the register-fragment kernel takes this M). */
 int64_t gemm_f16_small_m_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
+ * Route of gemm_f16_small_m, process-wide: 0 = automatic (the register-
+ * fragment kernel for M <= 16, the tcgen05 kernel above), 1 = always the
+ * tcgen05 kernel, 2 = the register-fragment kernel for every M <= 16.  Results
+ * agree up to FP32 accumulation order.  The workspace size depends on the
+ * route: query it after setting the route.  Returns TMAGEMM_ERR_INVALID for
+ * other values.
+ */
+int tmagemm_set_small_m_route(int route);
 
 /*
  * bfloat16 forms of gemm_f16 and gemv_f16: A, B, D (x, W, y) hold bf16

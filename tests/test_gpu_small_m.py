@@ -26,6 +26,16 @@ def run(tg, X, W):
     return D.cpu().numpy()
 
 
+# 1 = the tcgen05 swap-AB kernel, 2 = the register-fragment mma.sync kernel
+# (M <= 16; larger M take the tcgen05 kernel on either setting); the
+# automatic route is exercised by every other test file.
+@pytest.fixture(params=[1, 2], ids=["tcgen05", "fragments"])
+def route(tg, request):
+    assert tg.tmagemm_set_small_m_route(request.param) == tg.TMAGEMM_OK
+    yield request.param
+    assert tg.tmagemm_set_small_m_route(0) == tg.TMAGEMM_OK
+
+
 def decode_inputs(M, N, K, seed):
     g = torch.Generator().manual_seed(seed)
     X = (torch.randn((M, K), generator=g) * 0.02).half()
@@ -33,33 +43,77 @@ def decode_inputs(M, N, K, seed):
     return X, W
 
 
-@pytest.mark.parametrize("M", [2, 3, 8, 16, 17, 32, 33, 64])
-def test_small_m_parity_down_projection(tg, M):
+@pytest.mark.parametrize("M", [2, 3, 8, 16, 17, 32])
+def test_small_m_parity_down_projection(tg, route, M):
+    N, K = 4096, 14336
+    X, W = decode_inputs(M, N, K, seed=M)
+    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M M={M} route {route}")
+
+
+@pytest.mark.parametrize("M", [33, 64])
+def test_small_m_parity_down_projection_wide(tg, M):
     N, K = 4096, 14336
     X, W = decode_inputs(M, N, K, seed=M)
     compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M M={M}")
 
 
-@pytest.mark.parametrize("M,N,K", [(5, 1000, 4160), (16, 136, 72), (40, 264, 8), (2, 8, 1000)])
-def test_small_m_edge_shapes(tg, M, N, K):
+# Ragged N (not a multiple of the 64 weight rows of a cluster), K shorter than
+# the 8 slices, K not a multiple of the 32-k step, one row, one 16-byte chunk.
+@pytest.mark.parametrize("M,N,K", [(5, 1000, 4160), (16, 136, 72), (2, 8, 1000), (9, 72, 8),
+                                   (31, 520, 264), (4, 4104, 14344)])
+def test_small_m_edge_shapes(tg, route, M, N, K):
     X, W = inputs.gemm_inputs(M, N, K, seed=M + N)
-    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M {M}x{N}x{K}")
+    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()),
+            f"small-M {M}x{N}x{K} route {route}")
 
 
-def test_small_m_integer_bitexact_and_deterministic(tg):
-    M, N, K = 12, 2056, 4160
+def test_small_m_edge_shape_wide(tg):
+    X, W = inputs.gemm_inputs(40, 264, 8, seed=304)
+    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), "small-M 40x264x8")
+
+
+@pytest.mark.parametrize("M", [12, 32])
+def test_small_m_integer_bitexact_and_deterministic(tg, route, M):
+    N, K = 2056, 4160
     X = inputs.integer_f16((M, K), seed=80)
     W = inputs.integer_f16((N, K), seed=81)
     d1 = run(tg, X, W)
-    assert_bitexact(d1, oracle.gemm_f16(X.numpy(), W.numpy()), "small-M integer")
+    assert_bitexact(d1, oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M integer route {route}")
     assert_bitexact(run(tg, X, W), d1, "repeat")
+
+
+def test_small_m_routes_agree_on_exact_sums(tg):
+    """Integer inputs make every FP32 partial exact, so the two kernels must
+    give the same bits although they add in different orders."""
+    M, N, K = 16, 4096, 14336
+    X = inputs.integer_f16((M, K), seed=82)
+    W = inputs.integer_f16((N, K), seed=83)
+    out = {}
+    try:
+        for r in (1, 2):
+            assert tg.tmagemm_set_small_m_route(r) == tg.TMAGEMM_OK
+            out[r] = run(tg, X, W)
+    finally:
+        tg.tmagemm_set_small_m_route(0)
+    assert_bitexact(out[2], out[1], "fragments vs tcgen05")
 
 
 def test_small_m_rejects_out_of_range_and_bad_workspace(tg):
     p = torch.zeros(1 << 20, dtype=torch.float16, device="cuda").data_ptr()
     assert tg.gemm_f16_small_m(1, 64, 64, p, p, p, p, 1 << 20, None) == tg.TMAGEMM_ERR_UNSUPPORTED
     assert tg.gemm_f16_small_m(65, 64, 64, p, p, p, p, 1 << 20, None) == tg.TMAGEMM_ERR_UNSUPPORTED
-    assert tg.gemm_f16_small_m(8, 64, 64, p, p, p, None, 0, None) == tg.TMAGEMM_ERR_WORKSPACE
-    need = tg.gemm_f16_small_m_workspace_size(8, 4096, 14336)
+    # M > 16 takes the tcgen05 kernel, which needs its workspace.
+    assert tg.gemm_f16_small_m(40, 64, 64, p, p, p, None, 0, None) == tg.TMAGEMM_ERR_WORKSPACE
+    need = tg.gemm_f16_small_m_workspace_size(40, 4096, 14336)
     assert need > 0
-    assert tg.gemm_f16_small_m(8, 4096, 14336, p, p, p, p, need - 16, None) == tg.TMAGEMM_ERR_WORKSPACE
+    assert tg.gemm_f16_small_m(40, 4096, 14336, p, p, p, p, need - 16, None) == tg.TMAGEMM_ERR_WORKSPACE
+    # M <= 16 takes the register-fragment kernel: no workspace.
+    assert tg.gemm_f16_small_m_workspace_size(8, 4096, 14336) == 0
+    assert tg.gemm_f16_small_m(8, 64, 64, p, p, p, None, 0, None) == tg.TMAGEMM_OK
+    try:
+        assert tg.tmagemm_set_small_m_route(1) == tg.TMAGEMM_OK
+        assert tg.gemm_f16_small_m_workspace_size(8, 4096, 14336) > 0
+        assert tg.gemm_f16_small_m(8, 64, 64, p, p, p, None, 0, None) == tg.TMAGEMM_ERR_WORKSPACE
+    finally:
+        assert tg.tmagemm_set_small_m_route(0) == tg.TMAGEMM_OK
+    torch.cuda.synchronize()

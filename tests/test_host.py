@@ -213,6 +213,16 @@ def test_pdl_switch():
         assert tg.tmagemm_set_pdl(1) == tg.TMAGEMM_OK
 
 
+def test_small_m_route_switch():
+    try:
+        assert tg.tmagemm_set_small_m_route(1) == tg.TMAGEMM_OK
+        assert tg.tmagemm_set_small_m_route(2) == tg.TMAGEMM_OK
+        assert tg.tmagemm_set_small_m_route(3) == tg.TMAGEMM_ERR_INVALID
+        assert tg.tmagemm_set_small_m_route(-1) == tg.TMAGEMM_ERR_INVALID
+    finally:
+        assert tg.tmagemm_set_small_m_route(0) == tg.TMAGEMM_OK
+
+
 def test_tile_width_override():
     try:
         assert tg.tmagemm_set_tile_n(256) == tg.TMAGEMM_OK

@@ -47,6 +47,7 @@ SIGNATURES = {
     "tmagemm_set_cta_pair": ([_int], _int),
     "tmagemm_set_tile_n": ([_int], _int),
     "tmagemm_set_pdl": ([_int], _int),
+    "tmagemm_set_small_m_route": ([_int], _int),
 }
 
 _lock = threading.Lock()
@@ -137,11 +138,12 @@ def gemm_small_m(X, W, workspace=None, out=None, stream=None):
         need = lib().gemm_f16_small_m_workspace_size(M, N, K)
         if need < 0:
             raise TmaGemmError(int(need), "gemm_f16_small_m_workspace_size")
-        if workspace is None:
-            workspace = torch.empty((max(int(need), 16),), dtype=torch.uint8, device=X.device)
+        if workspace is None and need > 0:
+            workspace = torch.empty((int(need),), dtype=torch.uint8, device=X.device)
+        ws_ptr = workspace.data_ptr() if workspace is not None else None
+        ws_bytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
         s = lib().gemm_f16_small_m(M, N, K, X.data_ptr(), W.data_ptr(), out.data_ptr(),
-                                   workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-                                   _stream_handle(stream, X.device))
+                                   ws_ptr, ws_bytes, _stream_handle(stream, X.device))
     if s != TMAGEMM_OK:
         raise TmaGemmError(s, "gemm_f16_small_m")
     return out
@@ -224,6 +226,10 @@ def tmagemm_set_cta_pair(mode) -> int:
 
 def tmagemm_set_pdl(on) -> int:
     return lib().tmagemm_set_pdl(on)
+
+
+def tmagemm_set_small_m_route(route) -> int:
+    return lib().tmagemm_set_small_m_route(route)
 
 
 # ---- torch-tensor conveniences (marshalling only) ----------------------------

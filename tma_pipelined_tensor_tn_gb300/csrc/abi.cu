@@ -284,12 +284,29 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
     return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 
+// Largest M that the automatic route sends to the register-fragment kernel.
+constexpr int64_t kSmallMMmaAutoMaxM = 16;
+
+// Whether gemm_f16_small_m takes the register-fragment kernel for this M.
+static bool small_m_uses_mma(int64_t M) {
+    const int route = __atomic_load_n(&g_small_m_route, __ATOMIC_ACQUIRE);
+    if (route == 1 || M > small_m_mma_max_m()) return false;
+    if (route == 2) return true;
+    return M <= kSmallMMmaAutoMaxM;
+}
+
+// Columns of the tcgen05 swap-AB tile for M activation rows: 16, else 64.
+// Rows 17..32 run padded to 64: on GB300 the 64-wide configuration measured
+// 33 us against 37 us for the 32-wide one at N = 4096, K = 14336.
+static int64_t small_m_tile_rows(int64_t M) { return M <= 16 ? M : 64; }
+
 int64_t gemm_f16_small_m_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (int s = validate_common(M, N, K)) return s;
     if (M < 2 || M > 64) return TMAGEMM_ERR_UNSUPPORTED;
+    if (small_m_uses_mma(M)) return 0;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    const GemmPlan p = plan_small_m(M, N, K, d->sms, 0);
+    const GemmPlan p = plan_small_m(small_m_tile_rows(M), N, K, d->sms, 0);
     return p.splits * N * p.bn * 4;
 }
 
@@ -300,9 +317,16 @@ int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void*
     if (M < 2 || M > 64) return TMAGEMM_ERR_UNSUPPORTED;
     if (!aligned16(X) || !aligned16(W) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
         return TMAGEMM_ERR_ALIGN;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (small_m_uses_mma(M)) {
+        DeviceState* dm = nullptr;
+        if (int s = device_state(&dm)) return s;
+        return launch_small_m_mma(M, N, K, X, W, D, st) == cudaSuccess ? TMAGEMM_OK
+                                                                      : TMAGEMM_ERR_CUDA;
+    }
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    const GemmPlan p = plan_small_m(M, N, K, d->sms, 0);
+    const GemmPlan p = plan_small_m(small_m_tile_rows(M), N, K, d->sms, 0);
     const int64_t need = p.splits * N * p.bn * 4;
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return TMAGEMM_ERR_WORKSPACE;
     // Swapped roles: the weights are the 128-row operand, the activations the
@@ -321,7 +345,6 @@ int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void*
     args.K = static_cast<int32_t>(K);
     args.wait_limit_ns = wait_limit_ns();
     args.err_word = d->err_word;
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_small_m(p, tmW, tmX, tmP, args, st);
     if (e == cudaSuccess) e = launch_small_m_reduce(workspace, D, M, N, p.bn, p.splits, st);
     return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
@@ -391,6 +414,12 @@ int tmagemm_set_cta_pair(int mode) {
 int tmagemm_set_tile_n(int bn) {
     if (bn != 0 && bn != 256 && bn != 224 && bn != 192) return TMAGEMM_ERR_INVALID;
     __atomic_store_n(&g_force_tile_n, bn, __ATOMIC_RELEASE);
+    return TMAGEMM_OK;
+}
+
+int tmagemm_set_small_m_route(int route) {
+    if (route < 0 || route > 2) return TMAGEMM_ERR_INVALID;
+    __atomic_store_n(&g_small_m_route, route, __ATOMIC_RELEASE);
     return TMAGEMM_OK;
 }
 

@@ -62,6 +62,18 @@ cudaError_t launch_small_m(const GemmPlan& plan, const CUtensorMap& tmW, const C
 cudaError_t launch_small_m_reduce(const void* partials, void* D, int64_t M, int64_t N, int64_t Mp,
                                   int64_t splits, cudaStream_t stream);
 
+// Skinny GEMM (2 <= M <= small_m_mma_max_m()) on register fragments: the
+// weights stream from HBM straight into mma.sync operands; K is split over
+// the 8 CTAs of a cluster and reduced through distributed shared memory.
+// No workspace; one launch.
+int64_t small_m_mma_max_m();
+cudaError_t launch_small_m_mma(int64_t M, int64_t N, int64_t K, const void* X, const void* W,
+                               void* D, cudaStream_t stream);
+
+// Route of gemm_f16_small_m: 0 automatic, 1 always the tcgen05 swap-AB
+// kernel, 2 the register-fragment kernel wherever it applies.
+extern int g_small_m_route;
+
 // Grouped GEMM: groups g < G with rows [m_offsets[g], m_offsets[g+1]) of A
 // and D and weights B[g] (N x K).  Maps: A {K, rows} box {64, 128}; B
 // {K, N, G} box {64, bn, 1}; tmD[g] = D rows of group g, {N, M_g} box
