@@ -616,6 +616,21 @@ def measure_extras(tg, dev, stream, l2):
         tg.check(stream)
         out[name] = entry
 
+    # Context, not a target: torch.matmul (cuBLAS) on the same shapes and
+    # rotating fp16 inputs, so the GEMM can be compared on this machine.
+    for name, (Mc, Nc, Kc, reps) in {"cublas_fp16_4096": (4096, 4096, 4096, 50),
+                                     "cublas_fp16_8192": (8192, 8192, 8192, 5)}.items():
+        csets = [inputs.gemm_inputs(Mc, Nc, Kc, seed=20 + j) for j in range(3 if Mc < 8192 else 1)]
+        csets = [(a.to(dev), b.to(dev)) for a, b in csets]
+        def cublas(i, csets=csets):
+            a, b = csets[i % len(csets)]
+            torch.matmul(a, b.T)
+
+        t_c = _time_launches(cublas, reps, stream)
+        out[name] = {"us": t_c, "tflops": gemm_flops(Mc, Nc, Kc) / t_c / 1e6,
+                     "what": "torch.matmul(A, B.T), cuBLAS, for comparison only"}
+        del csets
+
     out["grouped_8x(8192_tokens)x4096x2048"] = {
         "us": t_g, "tflops": fl / t_g / 1e6, "dense_same_rows_us": t_d,
         "dense_tflops": fl / t_d / 1e6, "group_rows": [int(c) for c in counts]}
