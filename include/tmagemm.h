@@ -166,13 +166,15 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
  * Skinny GEMM for a few rows of activations, D = fp16(X * W^T) with
  * 2 <= M <= 64: the decode step of "Learning TileLang with GEMV" (§01 GEMV:
  * every linear layer is a GEMV when tokens are decoded one by one) for a
- * batch of M tokens.  Like the GEMV it is bound by reading W once.  Two
+ * batch of M tokens.  Like the GEMV it is bound by reading W once.  Three
  * kernels, chosen by M (tmagemm_set_small_m_route overrides):
  *   - M <= 16: W streams from HBM straight into mma.sync register fragments
  *     (16-byte loads, no shared-memory staging); the CTAs of a cluster split
  *     K and add their FP32 partials in fixed order through distributed
- *     shared memory.  Needs no workspace (its size is 0; `workspace` may be
- *     NULL).
+ *     shared memory.  Needs no workspace.
+ *   - 17 <= M <= 32: tcgen05 with W staged in shared memory by the SMs' own
+ *     16-byte loads (X by TMA); K split over a cluster and reduced the same
+ *     way.  Needs no workspace.
  *   - otherwise: the tcgen05 kernel with the roles swapped — W is the 128-row
  *     MMA operand and X (rows past M read as zero) the 16- or 64-wide one —
  *     and K split so that enough SMs stream W; FP32 partials go to
@@ -192,13 +194,15 @@ int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void*
                      void* workspace, int64_t workspace_bytes, void* stream);
 
 /* Workspace bytes gemm_f16_small_m needs on the current device (negative =
- * status; 0 when the register-fragment kernel takes this M). */
+ * status; 0 unless the swap-AB kernel takes this M). */
 int64_t gemm_f16_small_m_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
- * Route of gemm_f16_small_m, process-wide: 0 = automatic (the register-
- * fragment kernel for M <= 16, the tcgen05 kernel above), 1 = always the
- * tcgen05 kernel, 2 = the register-fragment kernel for every M <= 16.  Results
+ * Route of gemm_f16_small_m, process-wide: 0 = automatic (register
+ * fragments for M <= 16, the LSU-fed tcgen05 kernel for 17..32, the swap-AB
+ * tcgen05 kernel above), 1 = always the swap-AB kernel, 2 = the register-
+ * fragment kernel for every M <= 16 (swap-AB above), 3 = always the LSU-fed
+ * tcgen05 kernel.  Results
  * agree up to FP32 accumulation order.  The workspace size depends on the
  * route: query it after setting the route.  Returns TMAGEMM_ERR_INVALID for
  * other values.

@@ -27,9 +27,10 @@ def run(tg, X, W):
 
 
 # 1 = the tcgen05 swap-AB kernel, 2 = the register-fragment mma.sync kernel
-# (M <= 16; larger M take the tcgen05 kernel on either setting); the
-# automatic route is exercised by every other test file.
-@pytest.fixture(params=[1, 2], ids=["tcgen05", "fragments"])
+# (M <= 16; larger M take the swap-AB kernel on that setting), 3 = the LSU-fed
+# tcgen05 kernel (every M); the automatic route is exercised by every other
+# test file and by test_small_m_auto_route.
+@pytest.fixture(params=[1, 2, 3], ids=["swap_ab", "fragments", "lsu"])
 def route(tg, request):
     assert tg.tmagemm_set_small_m_route(request.param) == tg.TMAGEMM_OK
     yield request.param
@@ -51,10 +52,10 @@ def test_small_m_parity_down_projection(tg, route, M):
 
 
 @pytest.mark.parametrize("M", [33, 64])
-def test_small_m_parity_down_projection_wide(tg, M):
+def test_small_m_parity_down_projection_wide(tg, route, M):
     N, K = 4096, 14336
     X, W = decode_inputs(M, N, K, seed=M)
-    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M M={M}")
+    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M M={M} route {route}")
 
 
 # Ragged N (not a multiple of the 64 weight rows of a cluster), K shorter than
@@ -67,12 +68,13 @@ def test_small_m_edge_shapes(tg, route, M, N, K):
             f"small-M {M}x{N}x{K} route {route}")
 
 
-def test_small_m_edge_shape_wide(tg):
-    X, W = inputs.gemm_inputs(40, 264, 8, seed=304)
-    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), "small-M 40x264x8")
+@pytest.mark.parametrize("M,N,K", [(40, 264, 8), (64, 1000, 4160), (47, 136, 72), (33, 4104, 1000)])
+def test_small_m_edge_shape_wide(tg, route, M, N, K):
+    X, W = inputs.gemm_inputs(M, N, K, seed=M + N + K)
+    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M {M}x{N}x{K} route {route}")
 
 
-@pytest.mark.parametrize("M", [12, 32])
+@pytest.mark.parametrize("M", [12, 32, 64])
 def test_small_m_integer_bitexact_and_deterministic(tg, route, M):
     N, K = 2056, 4160
     X = inputs.integer_f16((M, K), seed=80)
@@ -90,24 +92,35 @@ def test_small_m_routes_agree_on_exact_sums(tg):
     W = inputs.integer_f16((N, K), seed=83)
     out = {}
     try:
-        for r in (1, 2):
+        for r in (1, 2, 3):
             assert tg.tmagemm_set_small_m_route(r) == tg.TMAGEMM_OK
             out[r] = run(tg, X, W)
     finally:
         tg.tmagemm_set_small_m_route(0)
     assert_bitexact(out[2], out[1], "fragments vs tcgen05")
+    assert_bitexact(out[3], out[1], "LSU-fed vs tcgen05")
+
+
+@pytest.mark.parametrize("M", [2, 16, 17, 32, 33, 64])
+def test_small_m_auto_route(tg, M):
+    """The automatic route on each side of its thresholds (16 and 32)."""
+    N, K = 1032, 2056
+    X, W = inputs.gemm_inputs(M, N, K, seed=400 + M)
+    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M auto M={M}")
+    need = tg.gemm_f16_small_m_workspace_size(M, N, K)
+    assert (need == 0) == (M <= 32)
 
 
 def test_small_m_rejects_out_of_range_and_bad_workspace(tg):
     p = torch.zeros(1 << 20, dtype=torch.float16, device="cuda").data_ptr()
     assert tg.gemm_f16_small_m(1, 64, 64, p, p, p, p, 1 << 20, None) == tg.TMAGEMM_ERR_UNSUPPORTED
     assert tg.gemm_f16_small_m(65, 64, 64, p, p, p, p, 1 << 20, None) == tg.TMAGEMM_ERR_UNSUPPORTED
-    # M > 16 takes the tcgen05 kernel, which needs its workspace.
+    # M > 32 takes the swap-AB kernel, which needs its workspace.
     assert tg.gemm_f16_small_m(40, 64, 64, p, p, p, None, 0, None) == tg.TMAGEMM_ERR_WORKSPACE
     need = tg.gemm_f16_small_m_workspace_size(40, 4096, 14336)
     assert need > 0
     assert tg.gemm_f16_small_m(40, 4096, 14336, p, p, p, p, need - 16, None) == tg.TMAGEMM_ERR_WORKSPACE
-    # M <= 16 takes the register-fragment kernel: no workspace.
+    # M <= 32 takes a kernel that needs no workspace.
     assert tg.gemm_f16_small_m_workspace_size(8, 4096, 14336) == 0
     assert tg.gemm_f16_small_m(8, 64, 64, p, p, p, None, 0, None) == tg.TMAGEMM_OK
     try:

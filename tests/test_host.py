@@ -217,7 +217,8 @@ def test_small_m_route_switch():
     try:
         assert tg.tmagemm_set_small_m_route(1) == tg.TMAGEMM_OK
         assert tg.tmagemm_set_small_m_route(2) == tg.TMAGEMM_OK
-        assert tg.tmagemm_set_small_m_route(3) == tg.TMAGEMM_ERR_INVALID
+        assert tg.tmagemm_set_small_m_route(3) == tg.TMAGEMM_OK
+        assert tg.tmagemm_set_small_m_route(4) == tg.TMAGEMM_ERR_INVALID
         assert tg.tmagemm_set_small_m_route(-1) == tg.TMAGEMM_ERR_INVALID
     finally:
         assert tg.tmagemm_set_small_m_route(0) == tg.TMAGEMM_OK

@@ -284,15 +284,21 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
     return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 
-// Largest M that the automatic route sends to the register-fragment kernel.
-constexpr int64_t kSmallMMmaAutoMaxM = 16;
+enum class SmallMKernel { kSwapAB, kFragments, kLsu };
 
-// Whether gemm_f16_small_m takes the register-fragment kernel for this M.
-static bool small_m_uses_mma(int64_t M) {
+// Which kernel gemm_f16_small_m runs for this M (see tmagemm_set_small_m_route).
+// The automatic choice follows GB300 measurements at N = 4096, K = 14336:
+// M <= 16 register fragments (20.4-23.0 us; TMA swap-AB 25.8-26.2, LSU-fed
+// tcgen05 24.3-27.3), 17..32 the LSU-fed tcgen05 kernel (M = 24: 30.6 us
+// against 33.0), above that the TMA swap-AB kernel (M = 40..64: 32.8 us
+// against 41-47).
+static SmallMKernel small_m_kernel(int64_t M) {
     const int route = __atomic_load_n(&g_small_m_route, __ATOMIC_ACQUIRE);
-    if (route == 1 || M > small_m_mma_max_m()) return false;
-    if (route == 2) return true;
-    return M <= kSmallMMmaAutoMaxM;
+    if (route == 1) return SmallMKernel::kSwapAB;
+    if (route == 3) return SmallMKernel::kLsu;
+    if (route == 2) return M <= small_m_mma_max_m() ? SmallMKernel::kFragments : SmallMKernel::kSwapAB;
+    if (M <= small_m_mma_max_m()) return SmallMKernel::kFragments;
+    return M <= 32 ? SmallMKernel::kLsu : SmallMKernel::kSwapAB;
 }
 
 // Columns of the tcgen05 swap-AB tile for M activation rows: 16, else 64.
@@ -303,7 +309,7 @@ static int64_t small_m_tile_rows(int64_t M) { return M <= 16 ? M : 64; }
 int64_t gemm_f16_small_m_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (int s = validate_common(M, N, K)) return s;
     if (M < 2 || M > 64) return TMAGEMM_ERR_UNSUPPORTED;
-    if (small_m_uses_mma(M)) return 0;
+    if (small_m_kernel(M) != SmallMKernel::kSwapAB) return 0;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
     const GemmPlan p = plan_small_m(small_m_tile_rows(M), N, K, d->sms, 0);
@@ -318,14 +324,23 @@ int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void*
     if (!aligned16(X) || !aligned16(W) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
         return TMAGEMM_ERR_ALIGN;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    if (small_m_uses_mma(M)) {
-        DeviceState* dm = nullptr;
-        if (int s = device_state(&dm)) return s;
-        return launch_small_m_mma(M, N, K, X, W, D, st) == cudaSuccess ? TMAGEMM_OK
-                                                                      : TMAGEMM_ERR_CUDA;
-    }
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
+    const SmallMKernel kern = small_m_kernel(M);
+    if (kern == SmallMKernel::kFragments)
+        return launch_small_m_mma(M, N, K, X, W, D, st) == cudaSuccess ? TMAGEMM_OK
+                                                                      : TMAGEMM_ERR_CUDA;
+    if (kern == SmallMKernel::kLsu) {
+        // X {K, M} in boxes of 64 k x Mp token rows (rows past M read as zero).
+        CUtensorMap tmX;
+        if (int s = encode_2d(&tmX, X, K, M, 64, small_m_lsu_cols(M), CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+            return s;
+        return launch_small_m_lsu(tmX, M, N, K, W, D, wait_limit_ns(), d->err_word, st) ==
+                       cudaSuccess
+                   ? TMAGEMM_OK
+                   : TMAGEMM_ERR_CUDA;
+    }
     const GemmPlan p = plan_small_m(small_m_tile_rows(M), N, K, d->sms, 0);
     const int64_t need = p.splits * N * p.bn * 4;
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return TMAGEMM_ERR_WORKSPACE;
@@ -418,7 +433,7 @@ int tmagemm_set_tile_n(int bn) {
 }
 
 int tmagemm_set_small_m_route(int route) {
-    if (route < 0 || route > 2) return TMAGEMM_ERR_INVALID;
+    if (route < 0 || route > 3) return TMAGEMM_ERR_INVALID;
     __atomic_store_n(&g_small_m_route, route, __ATOMIC_RELEASE);
     return TMAGEMM_OK;
 }
