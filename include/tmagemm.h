@@ -62,7 +62,11 @@ typedef enum {
  *   D       : device pointer, M x N fp16, row-major; written, never read.
  *   stream  : cudaStream_t (NULL = legacy default stream).
  * Requirements: A, B, D 16-byte aligned; K % 8 == 0; N % 8 == 0 when M > 1.
- * M == 1 is computed by the GEMV kernel (x = A, W = B, y = D).
+ * M == 1 is computed by the GEMV kernel (x = A, W = B, y = D); 2 <= M <= 64
+ * by the workspace-free kernels of gemm_f16_small_m (register fragments up to
+ * 16 rows, the LSU-fed tcgen05 kernel above: a single 128-row tile row would
+ * leave most SMs idle while B streams); the tcgen05 tile kernel takes every
+ * larger M.  The results agree up to FP32 accumulation order.
  * Kernel: persistent, warp-specialised: a TMA producer warp feeding a
  * multi-stage mbarrier ring of 128B-swizzled tiles, one thread issuing
  * tcgen05.mma into a double-buffered TMEM accumulator, and four epilogue warps

@@ -123,10 +123,17 @@ def test_gemm_rank1_powers_of_two(tg):
     (2, 8, 8), (127, 120, 64), (129, 136, 72), (200, 200, 24), (1000, 264, 296),
     (128, 256, 64), (129, 264, 8), (513, 1032, 1000), (3, 2056, 136),
 ])
-def test_gemm_edge_shapes(tg, M, N, K):
+@pytest.mark.parametrize("route", [0, 1], ids=["auto", "tile_kernel"])
+def test_gemm_edge_shapes(tg, M, N, K, route):
+    """route 1 (small-M swap-AB, which needs a workspace) keeps gemm_f16 on the
+    tile kernel for the M <= 32 shapes too."""
     A, B = inputs.gemm_inputs(M, N, K, seed=M + N + K)
-    D = run_gemm(tg, A, B)
-    compare(D, oracle.gemm_f16(A.numpy(), B.numpy()), f"edge {M}x{N}x{K}")
+    try:
+        assert tg.tmagemm_set_small_m_route(route) == tg.TMAGEMM_OK
+        D = run_gemm(tg, A, B)
+    finally:
+        tg.tmagemm_set_small_m_route(0)
+    compare(D, oracle.gemm_f16(A.numpy(), B.numpy()), f"edge {M}x{N}x{K} route {route}")
 
 
 @pytest.mark.parametrize("pair", [1, 2])
@@ -191,6 +198,21 @@ def test_gemm_out_of_bounds_guard(tg):
     body = host[guard:guard + M * N]
     assert not np.any(body == sentinel), "some D elements were not written"
     compare(body.view(np.float16).reshape(M, N), oracle.gemm_f16(A.numpy(), B.numpy()), "guarded")
+
+
+@pytest.mark.parametrize("M", [2, 8, 16, 17, 32, 33, 64, 65])
+def test_gemm_few_rows_route(tg, M):
+    """gemm_f16 with 2 <= M <= 32 runs the same workspace-free kernels as
+    gemm_f16_small_m (bit-identical); 33..64 the LSU-fed one (gemm_f16_small_m
+    prefers swap-AB there); M = 65 the tile kernel."""
+    N, K = 4104, 4160
+    A, B = inputs.gemm_inputs(M, N, K, seed=500 + M)
+    a, b = A.cuda(), B.cuda()
+    D = tg.gemm(a, b).cpu().numpy()
+    tg.check()
+    compare(D, oracle.gemm_f16(A.numpy(), B.numpy()), f"gemm_f16 M={M}")
+    if M <= 32:
+        assert_bitexact(D, tg.gemm_small_m(a, b).cpu().numpy(), f"gemm_f16 vs small-M M={M}")
 
 
 def test_gemm_m1_routes_to_gemv(tg):

@@ -180,6 +180,42 @@ using namespace tmagemm;
 
 extern "C" {
 
+enum class SmallMKernel { kSwapAB, kFragments, kLsu };
+
+// Which kernel gemm_f16_small_m runs for this M (see tmagemm_set_small_m_route).
+// The automatic choice follows GB300 measurements at N = 4096, K = 14336:
+// M <= 16 register fragments (20.4-23.0 us; TMA swap-AB 25.8-26.2, LSU-fed
+// tcgen05 24.3-27.3), 17..32 the LSU-fed tcgen05 kernel (M = 24: 30.6 us
+// against 33.0), above that the TMA swap-AB kernel (M = 40..64: 32.8 us
+// against 41-47).
+static SmallMKernel small_m_kernel(int64_t M) {
+    const int route = __atomic_load_n(&g_small_m_route, __ATOMIC_ACQUIRE);
+    if (route == 1) return SmallMKernel::kSwapAB;
+    if (route == 3) return SmallMKernel::kLsu;
+    if (route == 2) return M <= small_m_mma_max_m() ? SmallMKernel::kFragments : SmallMKernel::kSwapAB;
+    if (M <= small_m_mma_max_m()) return SmallMKernel::kFragments;
+    return M <= 32 ? SmallMKernel::kLsu : SmallMKernel::kSwapAB;
+}
+
+// The workspace-free small-M kernels (register fragments, LSU-fed tcgen05).
+static int small_m_no_workspace(SmallMKernel k, int64_t M, int64_t N, int64_t K, const void* X,
+                                const void* W, void* D, void* stream) {
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    DeviceState* d = nullptr;
+    if (int s = device_state(&d)) return s;
+    if (k == SmallMKernel::kFragments)
+        return launch_small_m_mma(M, N, K, X, W, D, st) == cudaSuccess ? TMAGEMM_OK
+                                                                      : TMAGEMM_ERR_CUDA;
+    // X {K, M} in boxes of 64 k x Mp token rows (rows past M read as zero).
+    CUtensorMap tmX;
+    if (int s = encode_2d(&tmX, X, K, M, 64, small_m_lsu_cols(M), CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+        return s;
+    return launch_small_m_lsu(tmX, M, N, K, W, D, wait_limit_ns(), d->err_word, st) == cudaSuccess
+               ? TMAGEMM_OK
+               : TMAGEMM_ERR_CUDA;
+}
+
 int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
              void* stream) {
     if (!A || !B || !D) return TMAGEMM_ERR_INVALID;
@@ -187,6 +223,17 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void
     if (M == 1) return gemv_impl(N, K, A, B, D, stream);
     if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
         return TMAGEMM_ERR_ALIGN;
+    // A few rows: one tile row of the GEMM would leave most SMs idle while B
+    // streams; the workspace-free small-M kernels split K instead.  For
+    // 33..64 rows the automatic small-M choice (swap-AB) needs a workspace,
+    // so the LSU-fed kernel runs (GB300, N = 4096, K = 14336: 41-47 us
+    // against 57 us for the tile kernel).
+    if (M <= 64) {
+        SmallMKernel k = small_m_kernel(M);
+        if (k == SmallMKernel::kSwapAB && __atomic_load_n(&g_small_m_route, __ATOMIC_ACQUIRE) == 0)
+            k = SmallMKernel::kLsu;
+        if (k != SmallMKernel::kSwapAB) return small_m_no_workspace(k, M, N, K, A, B, D, stream);
+    }
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
     return run_gemm(plan_gemm(M, N, K, d->sms, 1, false, d->pairs), d, M, N, K, A, B, D, nullptr,
@@ -284,23 +331,6 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
     return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 
-enum class SmallMKernel { kSwapAB, kFragments, kLsu };
-
-// Which kernel gemm_f16_small_m runs for this M (see tmagemm_set_small_m_route).
-// The automatic choice follows GB300 measurements at N = 4096, K = 14336:
-// M <= 16 register fragments (20.4-23.0 us; TMA swap-AB 25.8-26.2, LSU-fed
-// tcgen05 24.3-27.3), 17..32 the LSU-fed tcgen05 kernel (M = 24: 30.6 us
-// against 33.0), above that the TMA swap-AB kernel (M = 40..64: 32.8 us
-// against 41-47).
-static SmallMKernel small_m_kernel(int64_t M) {
-    const int route = __atomic_load_n(&g_small_m_route, __ATOMIC_ACQUIRE);
-    if (route == 1) return SmallMKernel::kSwapAB;
-    if (route == 3) return SmallMKernel::kLsu;
-    if (route == 2) return M <= small_m_mma_max_m() ? SmallMKernel::kFragments : SmallMKernel::kSwapAB;
-    if (M <= small_m_mma_max_m()) return SmallMKernel::kFragments;
-    return M <= 32 ? SmallMKernel::kLsu : SmallMKernel::kSwapAB;
-}
-
 // Columns of the tcgen05 swap-AB tile for M activation rows: 16, else 64.
 // Rows 17..32 run padded to 64: on GB300 the 64-wide configuration measured
 // 33 us against 37 us for the 32-wide one at N = 4096, K = 14336.
@@ -323,24 +353,11 @@ int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void*
     if (M < 2 || M > 64) return TMAGEMM_ERR_UNSUPPORTED;
     if (!aligned16(X) || !aligned16(W) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
         return TMAGEMM_ERR_ALIGN;
+    const SmallMKernel kern = small_m_kernel(M);
+    if (kern != SmallMKernel::kSwapAB) return small_m_no_workspace(kern, M, N, K, X, W, D, stream);
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    const SmallMKernel kern = small_m_kernel(M);
-    if (kern == SmallMKernel::kFragments)
-        return launch_small_m_mma(M, N, K, X, W, D, st) == cudaSuccess ? TMAGEMM_OK
-                                                                      : TMAGEMM_ERR_CUDA;
-    if (kern == SmallMKernel::kLsu) {
-        // X {K, M} in boxes of 64 k x Mp token rows (rows past M read as zero).
-        CUtensorMap tmX;
-        if (int s = encode_2d(&tmX, X, K, M, 64, small_m_lsu_cols(M), CU_TENSOR_MAP_SWIZZLE_128B,
-                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
-            return s;
-        return launch_small_m_lsu(tmX, M, N, K, W, D, wait_limit_ns(), d->err_word, st) ==
-                       cudaSuccess
-                   ? TMAGEMM_OK
-                   : TMAGEMM_ERR_CUDA;
-    }
     const GemmPlan p = plan_small_m(small_m_tile_rows(M), N, K, d->sms, 0);
     const int64_t need = p.splits * N * p.bn * 4;
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return TMAGEMM_ERR_WORKSPACE;
