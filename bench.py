@@ -494,16 +494,25 @@ def measure_extras(tg, dev, stream, l2):
         assert tg.gemm_f16_splitk(M, N, K, a.data_ptr(), b.data_ptr(), D.data_ptr(), 0,
                                   ws.data_ptr(), need, sh) == 0
 
-    t_plain = _time_launches(plain, 50, stream)
-    t_split = _time_launches(split, 50, stream)
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    auto_plan = tg.tmagemm_gemm_plan(M, N, K, sms, 1, sms // 2)
+    t_auto = _time_launches(plain, 50, stream)          # gemm_f16: cluster split-K
+    t_split = _time_launches(split, 50, stream)         # gemm_f16_splitk: FP32 workspace
+    assert tg.tmagemm_set_cluster_split(1) == 0
+    try:
+        t_plain = _time_launches(plain, 50, stream)     # gemm_f16 on the tile kernel alone
+    finally:
+        tg.tmagemm_set_cluster_split(0)
     tg.check(stream)
     fl = gemm_flops(M, N, K)
     out["splitk_1024x1024x16384"] = {
-        "splits": plan["splits"], "units": plan["units"], "tile_n": plan["BN"],
-        "us_splitk": t_split, "us_plain": t_plain,
-        "tflops_splitk": fl / t_split / 1e6, "tflops_plain": fl / t_plain / 1e6,
-        "speedup": t_plain / t_split, "workspace_bytes": need,
-        "note": "split-K time includes the FP32 partial reduction kernel"}
+        "gemm_f16_us": t_auto, "gemm_f16_tflops": fl / t_auto / 1e6,
+        "gemm_f16_cluster_split": auto_plan["cluster_k"],
+        "splitk_workspace_us": t_split, "splitk_workspace_tflops": fl / t_split / 1e6,
+        "splitk_workspace_parts": plan["splits"], "workspace_bytes": need,
+        "tile_kernel_only_us": t_plain, "tile_kernel_only_tflops": fl / t_plain / 1e6,
+        "note": "gemm_f16 splits K over clusters and reduces in distributed shared memory; "
+                "gemm_f16_splitk writes FP32 partials and reduces in a second kernel"}
 
     # bf16 forms of the two headline kernels, same shapes and rotation rules.
     Mh = Nh = Kh = 4096

@@ -276,6 +276,18 @@ int tmagemm_set_cta_pair(int mode);
 int tmagemm_set_tile_n(int bn);
 
 /*
+ * Cluster split-K of gemm_f16 / gemm_bf16, process-wide: 0 = automatic (for
+ * shapes whose output tiles fill at most half of the SMs, when the plan's cost
+ * model prefers it, the CTAs of a 2-, 4- or 8-CTA cluster compute one
+ * 128 x 256 tile over separate K ranges and add their FP32 accumulators
+ * through distributed shared memory, in fixed order, before writing D: no
+ * workspace, one launch), 1 = never, 2, 4 or 8 = that cluster size whenever
+ * all tiles x that many CTAs fit in one wave.  Results agree up to FP32
+ * accumulation order.  Returns TMAGEMM_ERR_INVALID for other values.
+ */
+int tmagemm_set_cluster_split(int mode);
+
+/*
  * Programmatic dependent launch of the library's kernels: 1 (the default)
  * launches each kernel with CUDA's programmatic-stream-serialization
  * attribute, so a kernel queued behind another on the same stream is
@@ -310,9 +322,13 @@ int tmagemm_ring_position(int64_t it, int64_t stages, int64_t* stage, int64_t* p
  * The GEMM launch configuration for (M, N, K) on a device with `num_sms` SMs,
  * of which `num_pairs` two-CTA clusters can be co-resident (0 = no pairs), and
  * a split request (1 = gemm_f16, 0 = automatic split-K, > 1 = that many
- * parts): written to out[0..11] in the order BM, BN, BK, STAGES, tiles, grid
+ * parts): written to out[0..12] in the order BM, BN, BK, STAGES, tiles, grid
  * (CTAs), threads, smem bytes, parts, k-blocks per part, work units, pair
- * (1 if CTA pairs; then tiles are 256 rows high).  No GPU needed.
+ * (1 if CTA pairs; then tiles are 256 rows high), cluster split (0, or the
+ * number of CTAs (pairs) per cluster that split K for gemm_f16; then parts
+ * == that number).  `out` holds 13 values.  No GPU needed: cluster splits
+ * assume ideal packing of clusters here, while gemm_f16 also checks how many
+ * clusters the device can hold at once.
  */
 int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t num_pairs,
                       int64_t splits, int64_t* out);

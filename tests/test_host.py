@@ -224,6 +224,40 @@ def test_small_m_route_switch():
         assert tg.tmagemm_set_small_m_route(0) == tg.TMAGEMM_OK
 
 
+def test_cluster_split_plan():
+    """Few tiles and a long K: gemm_f16's plan splits K over 4-CTA clusters
+    (32 tiles x 4 = 128 CTAs <= 152); the headline shapes keep the tile plan."""
+    # CTA pairs available: 16 pair tiles of 256 x 256, 4 pairs each (clusters of 8)
+    p = tg.tmagemm_gemm_plan(1024, 1024, 16384, 152, 1, 76)
+    assert (p["cluster_k"], p["splits"], p["grid"], p["BN"], p["pair"]) == (4, 4, 128, 256, 1)
+    assert p["kb_per_unit"] == 64 and p["units"] == 64
+    # without pairs: 32 single-CTA tiles x 4
+    p = tg.tmagemm_gemm_plan(1024, 1024, 16384, 152, 1, 0)
+    assert (p["cluster_k"], p["splits"], p["grid"], p["BN"], p["pair"]) == (4, 4, 128, 256, 0)
+    assert p["kb_per_unit"] == 64 and p["units"] == 128
+    for shape in [(4096, 4096, 4096), (8192, 8192, 8192), (4000, 3000, 4160), (256, 256, 256)]:
+        assert tg.tmagemm_gemm_plan(*shape, 152, 1, 76)["cluster_k"] == 0, shape
+    # explicit split-K requests never use it
+    assert tg.tmagemm_gemm_plan(1024, 1024, 16384, 152, 0, 76)["cluster_k"] == 0
+
+
+def test_cluster_split_override():
+    try:
+        assert tg.tmagemm_set_cluster_split(1) == tg.TMAGEMM_OK
+        assert tg.tmagemm_gemm_plan(1024, 1024, 16384, 152, 1, 76)["cluster_k"] == 0
+        assert tg.tmagemm_set_cluster_split(8) == tg.TMAGEMM_OK
+        p = tg.tmagemm_gemm_plan(512, 1000, 4160, 152, 1, 76)   # 16 tiles x 8 CTAs
+        assert (p["cluster_k"], p["splits"], p["grid"], p["kb_per_unit"], p["pair"]) == (8, 8, 128, 9, 0)
+        # 32 tiles x 8 would not fit one wave: the forced size does not apply
+        assert tg.tmagemm_gemm_plan(1024, 1024, 16384, 152, 1, 76)["cluster_k"] != 8
+        assert tg.tmagemm_set_cluster_split(2) == tg.TMAGEMM_OK
+        assert tg.tmagemm_gemm_plan(1024, 1024, 16384, 152, 1, 76)["cluster_k"] == 2
+        for bad in (3, 5, 16, -1):
+            assert tg.tmagemm_set_cluster_split(bad) == tg.TMAGEMM_ERR_INVALID
+    finally:
+        assert tg.tmagemm_set_cluster_split(0) == tg.TMAGEMM_OK
+
+
 def test_tile_width_override():
     try:
         assert tg.tmagemm_set_tile_n(256) == tg.TMAGEMM_OK

@@ -38,6 +38,7 @@ from ._binding import (  # noqa: F401
     tmagemm_last_error_detail,
     tmagemm_ring_position,
     tmagemm_selftest_wait_timeout,
+    tmagemm_set_cluster_split,
     tmagemm_set_cta_pair,
     tmagemm_set_pdl,
     tmagemm_set_small_m_route,

@@ -48,6 +48,7 @@ SIGNATURES = {
     "tmagemm_set_tile_n": ([_int], _int),
     "tmagemm_set_pdl": ([_int], _int),
     "tmagemm_set_small_m_route": ([_int], _int),
+    "tmagemm_set_cluster_split": ([_int], _int),
 }
 
 _lock = threading.Lock()
@@ -211,12 +212,12 @@ def tmagemm_ring_position(it, stages):
 
 
 def tmagemm_gemm_plan(M, N, K, num_sms, splits=1, num_pairs=0):
-    out = (ctypes.c_int64 * 12)()
+    out = (ctypes.c_int64 * 13)()
     s = lib().tmagemm_gemm_plan(M, N, K, num_sms, num_pairs, splits, out)
     if s != TMAGEMM_OK:
         raise TmaGemmError(s, "tmagemm_gemm_plan")
     keys = ("BM", "BN", "BK", "STAGES", "tiles", "grid", "threads", "smem", "splits",
-            "kb_per_unit", "units", "pair")
+            "kb_per_unit", "units", "pair", "cluster_k")
     return dict(zip(keys, list(out)))
 
 
@@ -230,6 +231,10 @@ def tmagemm_set_pdl(on) -> int:
 
 def tmagemm_set_small_m_route(route) -> int:
     return lib().tmagemm_set_small_m_route(route)
+
+
+def tmagemm_set_cluster_split(mode) -> int:
+    return lib().tmagemm_set_cluster_split(mode)
 
 
 # ---- torch-tensor conveniences (marshalling only) ----------------------------

@@ -34,6 +34,7 @@ struct DeviceState {
     bool ready = false;
     int sms = 0;
     int pairs = 0;          // co-resident two-CTA clusters of the pair kernel
+    ClusterCaps caps;       // co-resident clusters of the cluster-split kernels
     int cc_major = 0;
     uint32_t* err_word = nullptr;
 };
@@ -78,7 +79,10 @@ int device_state(DeviceState** out) {
                 return TMAGEMM_ERR_CUDA;
             g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
         }
-        if (d.cc_major == 10) d.pairs = max_resident_pairs();
+        if (d.cc_major == 10) {
+            d.pairs = max_resident_pairs();
+            d.caps = query_cluster_caps();
+        }
         d.ready = true;
     }
     if (d.cc_major != 10) return TMAGEMM_ERR_UNSUPPORTED;   // sm_100 family only
@@ -166,6 +170,7 @@ int run_gemm(const GemmPlan& plan, DeviceState* d, int64_t M, int64_t N, int64_t
     args.K = static_cast<int32_t>(K);
     args.wait_limit_ns = wait_limit_ns();
     args.err_word = d->err_word;
+    args.d_out = D;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_gemm_tn(plan, tmA, tmB, tmD, args, st);
     if (e == cudaSuccess && plan.out_f32)
@@ -236,8 +241,8 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void
     }
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    return run_gemm(plan_gemm(M, N, K, d->sms, 1, false, d->pairs), d, M, N, K, A, B, D, nullptr,
-                    stream);
+    return run_gemm(plan_gemm(M, N, K, d->sms, 1, false, d->pairs, d->caps), d, M, N, K, A, B, D,
+                    nullptr, stream);
 }
 
 int64_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int64_t splits) {
@@ -247,7 +252,8 @@ int64_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int64_t 
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
     const GemmPlan p = plan_gemm(M, N, K, d->sms, splits == 0 ? 0 : splits);
-    if (p.splits <= 1) return 0;
+    // No FP32 partials (one part, or gemm_f16's own plan): no workspace.
+    if (!p.out_f32 || p.splits <= 1) return 0;
     return p.splits * M * N * 4;
 }
 
@@ -262,9 +268,9 @@ int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void* A, const void* 
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
     const GemmPlan p = plan_gemm(M, N, K, d->sms, splits == 0 ? 0 : splits);
-    if (p.splits <= 1)   // nothing to split: the plain kernel, no workspace needed
-        return run_gemm(plan_gemm(M, N, K, d->sms, 1, false, d->pairs), d, M, N, K, A, B, D,
-                        nullptr, stream);
+    if (!p.out_f32 || p.splits <= 1)   // no FP32 partials: gemm_f16's plan, no workspace
+        return run_gemm(plan_gemm(M, N, K, d->sms, 1, false, d->pairs, d->caps), d, M, N, K, A,
+                        B, D, nullptr, stream);
     if (!workspace || !aligned16(workspace) || workspace_bytes < p.splits * M * N * 4)
         return TMAGEMM_ERR_WORKSPACE;
     return run_gemm(p, d, M, N, K, A, B, D, workspace, stream);
@@ -391,8 +397,8 @@ int gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, voi
         return TMAGEMM_ERR_ALIGN;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    return run_gemm(plan_gemm(M, N, K, d->sms, 1, true, d->pairs), d, M, N, K, A, B, D, nullptr,
-                    stream);
+    return run_gemm(plan_gemm(M, N, K, d->sms, 1, true, d->pairs, d->caps), d, M, N, K, A, B, D,
+                    nullptr, stream);
 }
 
 int gemv_bf16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream) {
@@ -455,6 +461,12 @@ int tmagemm_set_small_m_route(int route) {
     return TMAGEMM_OK;
 }
 
+int tmagemm_set_cluster_split(int mode) {
+    if (mode != 0 && mode != 1 && mode != 2 && mode != 4 && mode != 8) return TMAGEMM_ERR_INVALID;
+    __atomic_store_n(&g_cluster_split, mode, __ATOMIC_RELEASE);
+    return TMAGEMM_OK;
+}
+
 int tmagemm_set_pdl(int on) {
     if (on != 0 && on != 1) return TMAGEMM_ERR_INVALID;
     __atomic_store_n(&g_pdl, on, __ATOMIC_RELEASE);
@@ -500,6 +512,7 @@ int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t 
     out[9] = p.kb_per_unit;
     out[10] = p.units;
     out[11] = p.pair ? 1 : 0;
+    out[12] = p.cluster_k;
     return TMAGEMM_OK;
 }
 

@@ -52,12 +52,16 @@ namespace tmagemm {
 namespace {
 
 template <int BN_, int EPI_COLS_, int STAGES_, bool OUT_F32_, bool BF16_, int TMEM_COLS_ = 512,
-          int CTAS_PER_SM_ = 1, bool PAIR_ = false>
+          int CTAS_PER_SM_ = 1, bool PAIR_ = false, int CK_ = 0>
 struct Cfg {
     static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_;
     // PAIR: a cluster of two CTAs runs one 256 x BN tile with cta_group::2
     // MMAs; each CTA holds its 128 rows of A and BN/2 rows of B.
     static constexpr bool kPair = PAIR_;
+    // CK (2, 4 or 8): the CTAs of a CK-CTA cluster own one output tile and one
+    // K slice each; they add their FP32 accumulators through distributed
+    // shared memory and write D directly (one unit per CTA, no workspace).
+    static constexpr int kClusterK = CK_;
     static constexpr int kTileM = PAIR_ ? 256 : 128;       // rows of one work tile
     static constexpr int kBRows = PAIR_ ? BN_ / 2 : BN_;  // rows of B in this CTA
     static constexpr bool kOutF32 = OUT_F32_;
@@ -75,7 +79,7 @@ struct Cfg {
     static constexpr uint32_t kBBytes = kBRows * BK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kEpiBufBytes = BM * kEpiRowBytes;
-    static constexpr int kEpiBufs = 2;
+    static constexpr int kEpiBufs = CK_ ? 0 : 2;   // cluster splits write D without TMA
     // Two accumulators, kAccStride columns apart, in kTmemCols allocated
     // columns (a power of two >= 32; CTAS_PER_SM CTAs must fit in 512).
     static constexpr uint32_t kTmemCols = TMEM_COLS_;
@@ -88,6 +92,10 @@ struct Cfg {
     static constexpr uint32_t kNumBars = 2 * STAGES + 5;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
     static constexpr uint32_t kSmemBytes = kOffMisc + 16 + 1024;   // + base alignment slack
+    // Cluster split: this CTA's 128 x BN FP32 partial tile, row stride BN + 4
+    // floats (conflict-free 16-byte stores), over the stages once the
+    // mainloop is done.
+    static constexpr uint32_t kPartStride = BN + 4;
     static constexpr uint32_t kIdesc = umma_idesc_16bit_f32(kTileM, BN, BF16_);
 
     static_assert(BK * 2 == 128, "a K-major row of one k-block is one 128-byte swizzle atom");
@@ -103,6 +111,10 @@ struct Cfg {
                   "pairs: one CTA per SM, plain output, whole 8-row swizzle atoms of B");
     static_assert(CTAS_PER_SM_ == 1 || kSmemBytes * CTAS_PER_SM_ <= 232448,
                   "resident CTAs share the SM's shared memory");
+    static_assert(CK_ == 0 || ((CK_ == 2 || CK_ == 4 || (CK_ == 8 && !PAIR_)) && !OUT_F32_ &&
+                               CTAS_PER_SM_ == 1 && BN % 8 == 0 &&
+                               BM * kPartStride * 4 <= STAGES * kStageBytes),
+                  "cluster split: fp16/bf16 D, at most 8 CTAs, partial tile within the stages");
 };
 
 // Tile shapes the host plan chooses from (all 128 rows x BN columns x 64 K),
@@ -123,6 +135,10 @@ template <bool T> using Cfg192F = Cfg<192, 32, 4, true, T>;
 template <bool T> using CfgP256 = Cfg<256, 64, 6, false, T, 512, 1, true>;
 template <bool T> using CfgP224 = Cfg<224, 32, 6, false, T, 512, 1, true>;
 template <bool T> using CfgP192 = Cfg<192, 64, 6, false, T, 512, 1, true>;
+// Cluster split-K tiles: 128 x 256 single CTAs (CK CTAs per tile), or 256 x 256
+// CTA pairs (CK pairs, 2 CK CTAs per cluster; ranks 2p and 2p + 1 form pair p).
+template <bool T, int CK> using CfgCK256 = Cfg<256, 64, 4, false, T, 512, 1, false, CK>;
+template <bool T, int CK> using CfgPCK256 = Cfg<256, 64, 6, false, T, 512, 1, true, CK>;
 
 // Two CTAs per SM (each with half the ring and 128 TMEM columns) keep two
 // independent weight streams per SM in flight.
@@ -151,6 +167,7 @@ struct Work {
 struct DenseProblem {
     CUtensorMap tmA, tmB, tmD;
     Work w;
+    void* d_out;   // D itself (M x N, row-major), for the cluster-split epilogue
 
     __device__ __forceinline__ int32_t num_units() const { return w.num_units; }
     __device__ __forceinline__ void prefetch() const {
@@ -328,11 +345,25 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
     // Work distribution: single CTAs step by the grid; pairs by the pair count.
-    const uint32_t rank = C::kPair ? cluster_ctarank() : 0u;
-    const int32_t unit0 =
+    // Cluster roles: a pair is ranks (2p, 2p + 1) of the cluster; `rank` is
+    // this CTA's half of its pair, `pair_leader` the pair's first rank.
+    const uint32_t cta_rank = (C::kPair || C::kClusterK != 0) ? cluster_ctarank() : 0u;
+    const uint32_t rank = C::kPair ? (cta_rank & 1u) : 0u;
+    const uint32_t pair_leader = C::kPair ? (cta_rank & ~1u) : 0u;
+    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << pair_leader);
+    int32_t unit0 =
         C::kPair ? static_cast<int32_t>(blockIdx.x / 2) : static_cast<int32_t>(blockIdx.x);
-    const int32_t unit_step =
+    int32_t unit_step =
         C::kPair ? static_cast<int32_t>(gridDim.x / 2) : static_cast<int32_t>(gridDim.x);
+    // Cluster split: one unit per CTA (or pair), the tile of the cluster and
+    // the K slice of this CTA's (pair's) index in it (unit = split * tiles + tile).
+    uint32_t ck_rank = 0;
+    if constexpr (C::kClusterK != 0) {
+        ck_rank = C::kPair ? (cta_rank >> 1) : cta_rank;
+        unit0 = static_cast<int32_t>(ck_rank) * prob.w.num_tiles +
+                static_cast<int32_t>(blockIdx.x / (C::kClusterK * (C::kPair ? 2 : 1)));
+        unit_step = prob.num_units();
+    }
 
     if (warp == 0) {
         // ================= TMA producer =================
@@ -354,7 +385,7 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                         // leader registers them (its single arrival completes
                         // the phase once all bytes of both CTAs are in).
                         if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * C::kStageBytes);
-                        const uint32_t leader_full = map_to_rank(full_bar(s), 0);
+                        const uint32_t leader_full = map_to_rank(full_bar(s), pair_leader);
                         prob.load_a_pair(sbase + C::kOffA + s * C::kABytes, kb * C::BK, ui,
                                          static_cast<int32_t>(rank) * C::BM, leader_full);
                         prob.load_b_pair(sbase + C::kOffB + s * C::kBBytes, kb * C::BK, ui,
@@ -417,7 +448,7 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                     }
                     // stage s free (in both CTAs of a pair) once these MMAs finish
                     if constexpr (C::kPair)
-                        mma_commit_pair(empty_bar(s), 0x3);
+                        mma_commit_pair(empty_bar(s), pair_mask);
                     else
                         mma_commit(empty_bar(s));
                     ++it;
@@ -425,23 +456,44 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 if (!ok) break;
                 // accumulator ready for the epilogue (of both CTAs of a pair)
                 if constexpr (C::kPair)
-                    mma_commit_pair(acc_full_bar(acc), 0x3);
+                    mma_commit_pair(acc_full_bar(acc), pair_mask);
                 else
                     mma_commit(acc_full_bar(acc));
             }
             // All issued MMAs must finish before TMEM is released.
             if constexpr (C::kPair)
-                mma_commit_pair(mma_done_bar, 0x1);
+                mma_commit_pair(mma_done_bar, static_cast<uint16_t>(0x1u << pair_leader));
             else
                 mma_commit(mma_done_bar);
             wait_bounded(mma_done_bar, 0, err, kSiteDrainMma, limit_ns);
         }
         __syncwarp();
+    } else if constexpr (C::kClusterK != 0) {
+        // ============ cluster split: accumulator -> this CTA's partial tile ============
+        const uint32_t quarter = static_cast<uint32_t>(warp) & 3u;   // TMEM lane quarter
+        const uint32_t row = quarter * 32u + static_cast<uint32_t>(lane);
+        const bool ok = wait_or_abort(acc_full_bar(0), 0, abort_flag, err, kSiteEpiAccFull,
+                                      limit_ns);
+        if (named_bar_and(1, C::kEpiThreads, ok)) {
+            tc_fence_after();
+            const uint32_t t_row = tmem_base + ((quarter * 32u) << 16);
+            const uint32_t p_row = sbase + C::kOffA + row * C::kPartStride * 4u;
+#pragma unroll 1
+            for (int c = 0; c < C::BN / 32; ++c) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(t_row + 32 * c, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    st_shared_v4(p_row + (32u * c + 4u * j) * 4u, v[4 * j], v[4 * j + 1],
+                                 v[4 * j + 2], v[4 * j + 3]);
+            }
+        }
     } else {
         // ================= epilogue (warps 2..5) =================
         const uint32_t quarter = static_cast<uint32_t>(warp) & 3u;   // TMEM lane quarter
         const uint32_t row = quarter * 32u + static_cast<uint32_t>(lane);  // row in tile
-        const bool leader = threadIdx.x == 64;
+        const bool store_thread = threadIdx.x == 64;   // issues the TMA stores
         uint32_t tcount = 0, box = 0;
         for (int32_t u = unit0; u < prob.num_units(); u += unit_step, ++tcount) {
             UnitInfo ui = prob.unit(u, C::kTileM, C::BN, C::kGroupM);
@@ -474,14 +526,14 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                     __syncwarp();
                     if (lane == 0) {
                         if constexpr (C::kPair)
-                            mbar_arrive_cluster(map_to_rank(acc_empty_bar(acc), 0));
+                            mbar_arrive_cluster(map_to_rank(acc_empty_bar(acc), pair_leader));
                         else
                             mbar_arrive(acc_empty_bar(acc));
                     }
                 }
                 const uint32_t buf = sbase + C::kOffD + (box & 1u) * C::kEpiBufBytes;
                 // The store that last read this buffer (two boxes ago) must be done.
-                if (leader) bulk_wait_group_read<1>();
+                if (store_thread) bulk_wait_group_read<1>();
                 named_bar_sync(1, C::kEpiThreads);
                 // Row `row` of the box holds kEpiChunks 16-byte chunks.  The
                 // TMA swizzle whose span equals the row width (64B or 128B)
@@ -504,7 +556,7 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 }
                 fence_proxy_async_smem();
                 named_bar_sync(1, C::kEpiThreads);
-                if (leader) {
+                if (store_thread) {
                     const int32_t x = n0 + c * C::kEpiCols;
                     if (x < ui.n_limit && ui.store_y < ui.m_limit)
                         prob.template store<C::kOutF32>(buf, x, ui);
@@ -512,7 +564,54 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 }
             }
         }
-        if (leader) bulk_wait_group<0>();
+        if (store_thread) bulk_wait_group<0>();
+    }
+
+    if constexpr (C::kClusterK != 0) {
+        // Every CTA's partial tile is complete and visible cluster-wide; CTA q
+        // finishes rows [q * 128 / CK, (q + 1) * 128 / CK) of the tile: 8
+        // columns per step, the CK partials loaded together and added in
+        // slice order (deterministic), one 16-byte store of D.
+        tc_fence_before();
+        cluster_sync();
+        // A pair's halves reduce separately: CTA (pair p, half h) adds the
+        // partials of ranks 2q + h.
+        constexpr int kRows = C::BM / C::kClusterK;
+        constexpr int kGroups = C::BN / 8;
+        constexpr uint32_t kPeerStride = C::kPair ? 2u : 1u;
+        const UnitInfo ui = prob.unit(unit0, C::kTileM, C::BN, C::kGroupM);
+        uint16_t* dout = static_cast<uint16_t*>(prob.d_out);
+        for (int f = static_cast<int>(threadIdx.x); f < kRows * kGroups; f += C::kThreads) {
+            const int rl = static_cast<int>(ck_rank) * kRows + f / kGroups;
+            const int g = f % kGroups;
+            const int32_t m = ui.a_row + static_cast<int32_t>(rank) * C::BM + rl;
+            const int32_t n = ui.b_row + 8 * g;
+            if (m >= prob.w.M || n >= prob.w.N) continue;
+            const uint32_t local = sbase + C::kOffA + (rl * C::kPartStride + 8u * g) * 4u;
+            float lo[C::kClusterK][4], hi[C::kClusterK][4];
+#pragma unroll
+            for (int q = 0; q < C::kClusterK; ++q) {
+                const uint32_t peer = kPeerStride * static_cast<uint32_t>(q) + rank;
+                ld_shared_cluster_v4(map_to_rank(local, peer), lo[q]);
+                ld_shared_cluster_v4(map_to_rank(local + 16u, peer), hi[q]);
+            }
+            float a[8] = {lo[0][0], lo[0][1], lo[0][2], lo[0][3], hi[0][0], hi[0][1], hi[0][2], hi[0][3]};
+#pragma unroll
+            for (int q = 1; q < C::kClusterK; ++q) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    a[e] += lo[q][e];
+                    a[4 + e] += hi[q][e];
+                }
+            }
+            uint4 o;
+            o.x = pack2_rn<C::kBF16>(__float_as_uint(a[0]), __float_as_uint(a[1]));
+            o.y = pack2_rn<C::kBF16>(__float_as_uint(a[2]), __float_as_uint(a[3]));
+            o.z = pack2_rn<C::kBF16>(__float_as_uint(a[4]), __float_as_uint(a[5]));
+            o.w = pack2_rn<C::kBF16>(__float_as_uint(a[6]), __float_as_uint(a[7]));
+            *reinterpret_cast<uint4*>(dout + static_cast<int64_t>(m) * prob.w.N + n) = o;
+        }
+        cluster_sync();   // peers' shared memory stays alive until every CTA has read it
     }
 
     // ---- teardown ----
@@ -598,6 +697,9 @@ GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) 
 // kb_per_unit k-blocks, and a k-block costs about BN + 32 units of time (MMA
 // time grows with BN, the A operand traffic per k-block does not).
 int64_t plan_cost(const GemmPlan& p) {
+    // A cluster split runs one wave of units and then adds CK partial tiles
+    // through distributed shared memory (about 2 us on GB300, ~2000 units).
+    if (p.cluster_k > 0) return p.kb_per_unit * (p.bn + (p.pair ? 16 : 32)) + 2048;
     const int64_t slots = p.pair ? p.grid / 2 : p.grid;
     const int64_t rounds = ceil_div(p.units, slots);
     // A pair streams half of B per SM: less operand traffic per k-block.
@@ -640,9 +742,10 @@ cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUten
     prob.w.num_units = static_cast<int32_t>(plan.units);
     prob.w.k_blocks = static_cast<int32_t>(plan.k_blocks);
     prob.w.kb_per_unit = static_cast<int32_t>(plan.kb_per_unit);
+    prob.d_out = args.d_out;
+    const unsigned cluster = static_cast<unsigned>((C::kPair ? 2 : 1) * (C::kClusterK ? C::kClusterK : 1));
     return launch_kernel(kernel, dim3(static_cast<unsigned>(plan.grid)), dim3(C::kThreads),
-                         C::kSmemBytes, stream, C::kPair ? 2u : 1u, prob, args.wait_limit_ns,
-                         args.err_word);
+                         C::kSmemBytes, stream, cluster, prob, args.wait_limit_ns, args.err_word);
 }
 
 template <class C>
@@ -731,13 +834,31 @@ cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, int num_pairs, c
 
 int g_force_tile_n = 0;
 int g_pair_mode = 0;
+int g_cluster_split = 0;
 int g_pdl = 1;
 
 namespace {
 
+// A cluster split of CK: valid when all tiles x CK CTAs fit in one wave and K
+// has at least CK k-blocks (otherwise units == 0).
+template <class C>
+GemmPlan plan_cluster_split(int64_t M, int64_t N, int64_t K, int64_t slots, int max_clusters) {
+    GemmPlan p = plan_for<C>(M, N, K, slots, C::kClusterK);
+    // One cluster per tile, all resident at once (a second wave would double
+    // the time).
+    const int64_t clusters_fit = max_clusters != 0 ? max_clusters : slots / C::kClusterK;
+    if (slots <= 0 || p.splits != C::kClusterK || p.tiles * C::kClusterK > slots ||
+        p.tiles > clusters_fit)
+        p.units = 0;
+    p.grid = static_cast<int>(p.units) * (C::kPair ? 2 : 1);
+    p.cluster_k = C::kClusterK;
+    return p;
+}
+
 template <bool T>
-GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs, int64_t splits) {
-    GemmPlan cands[6];
+GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs, int64_t splits,
+                    const ClusterCaps& caps) {
+    GemmPlan cands[11];
     int n = 0;
     const int pair_mode = __atomic_load_n(&g_pair_mode, __ATOMIC_ACQUIRE);
     const bool pairs_ok = splits == 1 && pairs > 0 && pair_mode != 1;
@@ -752,6 +873,30 @@ GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs,
             cands[n++] = plan_for<CfgP256<T>>(M, N, K, pairs, 1);
             cands[n++] = plan_for<CfgP224<T>>(M, N, K, pairs, 1);
             cands[n++] = plan_for<CfgP192<T>>(M, N, K, pairs, 1);
+        }
+        // Few tiles and a long K: split K over clusters (no workspace).
+        const int ck_mode = __atomic_load_n(&g_cluster_split, __ATOMIC_ACQUIRE);
+        if (ck_mode != 1) {
+            const bool pk = pairs > 0 && pair_mode != 1;
+            GemmPlan ck[5] = {
+                plan_cluster_split<CfgCK256<T, 2>>(M, N, K, sms, caps.single_ck[0]),
+                plan_cluster_split<CfgCK256<T, 4>>(M, N, K, sms, caps.single_ck[1]),
+                plan_cluster_split<CfgCK256<T, 8>>(M, N, K, sms, caps.single_ck[2]),
+                plan_cluster_split<CfgPCK256<T, 2>>(M, N, K, pairs, caps.pair_ck[0]),
+                plan_cluster_split<CfgPCK256<T, 4>>(M, N, K, pairs, caps.pair_ck[1])};
+            if (!pk) ck[3].units = ck[4].units = 0;
+            if (pair_mode == 2) ck[0].units = ck[1].units = ck[2].units = 0;
+            bool forced_ck = false;
+            for (const GemmPlan& c : ck)
+                if (c.units > 0 && ck_mode == c.cluster_k &&
+                    (!forced_ck || plan_cost(c) < plan_cost(cands[0]))) {
+                    cands[0] = c;   // a forced split size that applies
+                    n = 1;
+                    forced_ck = true;
+                }
+            if (!forced_ck)
+                for (const GemmPlan& c : ck)
+                    if (c.units > 0) cands[n++] = c;
         }
     } else {
         cands[n++] = plan_for<Cfg256F<T>>(M, N, K, sms, splits);
@@ -775,6 +920,21 @@ GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs,
 template <bool T>
 cudaError_t launch_typed(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
                          const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream) {
+    if (plan.cluster_k > 0 && plan.pair) {
+        switch (plan.cluster_k) {
+            case 2: return launch_cfg<CfgPCK256<T, 2>>(plan, tmA, tmB, tmD, args, stream);
+            case 4: return launch_cfg<CfgPCK256<T, 4>>(plan, tmA, tmB, tmD, args, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+    if (plan.cluster_k > 0) {
+        switch (plan.cluster_k) {
+            case 2: return launch_cfg<CfgCK256<T, 2>>(plan, tmA, tmB, tmD, args, stream);
+            case 4: return launch_cfg<CfgCK256<T, 4>>(plan, tmA, tmB, tmD, args, stream);
+            case 8: return launch_cfg<CfgCK256<T, 8>>(plan, tmA, tmB, tmD, args, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     if (plan.pair) {
         switch (plan.bn) {
             case 256: return launch_cfg<CfgP256<T>>(plan, tmA, tmB, tmD, args, stream);
@@ -802,10 +962,10 @@ cudaError_t launch_typed(const GemmPlan& plan, const CUtensorMap& tmA, const CUt
 }  // namespace
 
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits, bool bf16,
-                   int num_pairs) {
+                   int num_pairs, const ClusterCaps& caps) {
     const int64_t sms = num_sms > 0 ? num_sms : 1;
-    return bf16 ? plan_typed<true>(M, N, K, sms, num_pairs, splits)
-                : plan_typed<false>(M, N, K, sms, num_pairs, splits);
+    return bf16 ? plan_typed<true>(M, N, K, sms, num_pairs, splits, caps)
+                : plan_typed<false>(M, N, K, sms, num_pairs, splits, caps);
 }
 
 int max_resident_pairs() {
@@ -828,6 +988,48 @@ int max_resident_pairs() {
     int clusters = 0;
     if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) return 0;
     return clusters;
+}
+
+namespace {
+
+// Co-resident clusters of CTAS CTAs of configuration C (0 if unknown).
+template <class C>
+int max_active_clusters(int ctas) {
+    auto kernel = gemm_tn_f16_kernel<C, DenseProblem>;
+    static std::atomic<bool> attr_done[64];
+    if (smem_opt_in(kernel, static_cast<int>(C::kSmemBytes), attr_done) != cudaSuccess) return 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
+    cfg.blockDim = dim3(C::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = C::kSmemBytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = static_cast<unsigned>(ctas);
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return clusters;
+}
+
+}  // namespace
+
+ClusterCaps query_cluster_caps() {
+    ClusterCaps c;
+    c.single_ck[0] = max_active_clusters<CfgCK256<false, 2>>(2);
+    c.single_ck[1] = max_active_clusters<CfgCK256<false, 4>>(4);
+    c.single_ck[2] = max_active_clusters<CfgCK256<false, 8>>(8);
+    c.pair_ck[0] = max_active_clusters<CfgPCK256<false, 2>>(4);
+    c.pair_ck[1] = max_active_clusters<CfgPCK256<false, 4>>(8);
+    // A query that failed must not read as "unknown" (ideal packing): forbid.
+    for (int& v : c.single_ck) v = v > 0 ? v : -1;
+    for (int& v : c.pair_ck) v = v > 0 ? v : -1;
+    return c;
 }
 
 cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,

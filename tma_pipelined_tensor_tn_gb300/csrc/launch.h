@@ -22,13 +22,25 @@ struct GemmPlan {
     bool bf16;             // bf16 operands and output instead of fp16
     bool pair;             // CTA-pair (cta_group::2) tiles of 256 x bn
     int b_box_rows;        // rows of B per CTA (bn, or bn / 2 for a pair)
+    int cluster_k;         // > 0: K split over clusters of this many CTAs (one unit per CTA)
+};
+
+// How many clusters of each cluster-split configuration can be co-resident
+// (single CTAs with CK = 2, 4, 8; CTA pairs with CK = 2, 4).  0 = unknown:
+// the plan then assumes ideal packing (slots / CTAs per cluster).
+struct ClusterCaps {
+    int single_ck[3] = {0, 0, 0};
+    int pair_ck[2] = {0, 0};
 };
 
 // Pure function of the problem shape and the SM count (no CUDA calls).
 // splits == 1: the plain GEMM; splits == 0: choose the split count; else that
 // many splits (clamped so that no split is empty).
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits = 1,
-                   bool bf16 = false, int num_pairs = 0);
+                   bool bf16 = false, int num_pairs = 0, const ClusterCaps& caps = ClusterCaps{});
+
+// The co-residency of the cluster-split kernels on the current device.
+ClusterCaps query_cluster_caps();
 
 // Co-resident two-CTA clusters of the pair kernel on the current device
 // (0 if clusters cannot be launched).
@@ -36,6 +48,10 @@ int max_resident_pairs();
 
 // Pair-mode override for the plan: 0 automatic, 1 never pairs, 2 pairs only.
 extern int g_pair_mode;
+
+// Cluster split-K override for the plain GEMM: 0 automatic, 1 never, 2/4/8 that
+// cluster size whenever it applies (every tile x CK CTAs in one wave).
+extern int g_cluster_split;
 
 // D = fp16/bf16(sum of `splits` FP32 partial M x N matrices laid out back to back).
 cudaError_t launch_splitk_reduce(const void* partials, void* D, int64_t M, int64_t N,
@@ -45,6 +61,7 @@ struct GemmArgs {
     int32_t M, N, K;
     uint64_t wait_limit_ns;
     uint32_t* err_word;   // device address of the sticky error word
+    void* d_out = nullptr;   // D itself, for the cluster-split epilogue
 };
 
 // Enqueue the GEMM kernel.  Tensor maps: A {K, M} box {bk, bm}; B {K, N} box

@@ -369,6 +369,15 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Four floats from shared memory at a shared::cluster address (any CTA of
+// the cluster); 16-byte aligned.
+__device__ __forceinline__ void ld_shared_cluster_v4(uint32_t cluster_addr, float (&v)[4]) {
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v[0]), "=f"(v[1]), "=f"(v[2]), "=f"(v[3])
+                 : "r"(cluster_addr)
+                 : "memory");
+}
+
 // One arrival on an mbarrier given by its shared::cluster address (any CTA).
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
