@@ -276,6 +276,16 @@ int tmagemm_set_cta_pair(int mode);
 int tmagemm_set_tile_n(int bn);
 
 /*
+ * Tuning override of the dense GEMM's tile order: tiles are visited in groups
+ * of GROUP_M tile rows (by all tile columns), so that tiles sharing A and B
+ * panels run close together in time.  0 = automatic (about one round of
+ * resident tiles per group), 1..64 = that GROUP_M.  Results are identical
+ * (the order changes which CTA computes a tile, not how).  Returns
+ * TMAGEMM_ERR_INVALID for other values.
+ */
+int tmagemm_set_group_m(int g);
+
+/*
  * Cluster split-K of gemm_f16 / gemm_bf16, process-wide: 0 = automatic (for
  * shapes whose output tiles fill at most half of the SMs, when the plan's cost
  * model prefers it, the CTAs of a 2-, 4- or 8-CTA cluster compute one
@@ -326,7 +336,8 @@ int tmagemm_ring_position(int64_t it, int64_t stages, int64_t* stage, int64_t* p
  * (CTAs), threads, smem bytes, parts, k-blocks per part, work units, pair
  * (1 if CTA pairs; then tiles are 256 rows high), cluster split (0, or the
  * number of CTAs (pairs) per cluster that split K for gemm_f16; then parts
- * == that number).  `out` holds 13 values.  No GPU needed: cluster splits
+ * == that number), GROUP_M (tile rows per L2 group of the tile order).
+ * `out` holds 14 values.  No GPU needed: cluster splits
  * assume ideal packing of clusters here, while gemm_f16 also checks how many
  * clusters the device can hold at once.
  */

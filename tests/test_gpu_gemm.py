@@ -180,6 +180,21 @@ def test_gemm_pair_and_single_agree_on_4096(tg):
     compare(out[2], out[1], "pair vs single 4096^3")
 
 
+@pytest.mark.parametrize("g", [1, 2, 5, 8, 16])
+def test_gemm_group_m_does_not_change_results(tg, g):
+    """The tile order decides which CTA computes a tile, not how: every GROUP_M
+    gives the same bits."""
+    M, N, K = 1000, 3000, 520
+    A, B = inputs.gemm_inputs(M, N, K, seed=70)
+    ref = run_gemm(tg, A, B)
+    try:
+        assert tg.tmagemm_set_group_m(g) == tg.TMAGEMM_OK
+        out = run_gemm(tg, A, B)
+    finally:
+        tg.tmagemm_set_group_m(0)
+    assert_bitexact(out, ref, f"GROUP_M={g}")
+
+
 def test_gemm_out_of_bounds_guard(tg):
     """D sits inside a larger buffer filled with a sentinel: after a ragged run
     the guard regions still hold it and every D element was written."""

@@ -241,6 +241,20 @@ def test_cluster_split_plan():
     assert tg.tmagemm_gemm_plan(1024, 1024, 16384, 152, 0, 76)["cluster_k"] == 0
 
 
+def test_group_m_choice():
+    """Row order when A, B and D fit in L2 together; otherwise the GROUP_M that
+    minimises the A and B panels a round of resident tiles touches."""
+    assert tg.tmagemm_gemm_plan(4096, 4096, 4096, 152, 1, 76)["group_m"] == 1
+    assert tg.tmagemm_gemm_plan(4000, 3000, 4160, 152, 1, 76)["group_m"] == 1
+    assert tg.tmagemm_gemm_plan(8192, 8192, 8192, 152, 1, 76)["group_m"] == 8   # sqrt(76)
+    try:
+        assert tg.tmagemm_set_group_m(3) == tg.TMAGEMM_OK
+        assert tg.tmagemm_gemm_plan(4096, 4096, 4096, 152, 1, 76)["group_m"] == 3
+        assert tg.tmagemm_set_group_m(65) == tg.TMAGEMM_ERR_INVALID
+    finally:
+        assert tg.tmagemm_set_group_m(0) == tg.TMAGEMM_OK
+
+
 def test_cluster_split_override():
     try:
         assert tg.tmagemm_set_cluster_split(1) == tg.TMAGEMM_OK

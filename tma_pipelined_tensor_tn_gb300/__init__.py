@@ -40,6 +40,7 @@ from ._binding import (  # noqa: F401
     tmagemm_selftest_wait_timeout,
     tmagemm_set_cluster_split,
     tmagemm_set_cta_pair,
+    tmagemm_set_group_m,
     tmagemm_set_pdl,
     tmagemm_set_small_m_route,
     tmagemm_set_tile_n,

@@ -49,6 +49,7 @@ SIGNATURES = {
     "tmagemm_set_pdl": ([_int], _int),
     "tmagemm_set_small_m_route": ([_int], _int),
     "tmagemm_set_cluster_split": ([_int], _int),
+    "tmagemm_set_group_m": ([_int], _int),
 }
 
 _lock = threading.Lock()
@@ -212,12 +213,12 @@ def tmagemm_ring_position(it, stages):
 
 
 def tmagemm_gemm_plan(M, N, K, num_sms, splits=1, num_pairs=0):
-    out = (ctypes.c_int64 * 13)()
+    out = (ctypes.c_int64 * 14)()
     s = lib().tmagemm_gemm_plan(M, N, K, num_sms, num_pairs, splits, out)
     if s != TMAGEMM_OK:
         raise TmaGemmError(s, "tmagemm_gemm_plan")
     keys = ("BM", "BN", "BK", "STAGES", "tiles", "grid", "threads", "smem", "splits",
-            "kb_per_unit", "units", "pair", "cluster_k")
+            "kb_per_unit", "units", "pair", "cluster_k", "group_m")
     return dict(zip(keys, list(out)))
 
 
@@ -235,6 +236,10 @@ def tmagemm_set_small_m_route(route) -> int:
 
 def tmagemm_set_cluster_split(mode) -> int:
     return lib().tmagemm_set_cluster_split(mode)
+
+
+def tmagemm_set_group_m(g) -> int:
+    return lib().tmagemm_set_group_m(g)
 
 
 # ---- torch-tensor conveniences (marshalling only) ----------------------------

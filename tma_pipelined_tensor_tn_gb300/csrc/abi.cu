@@ -461,6 +461,12 @@ int tmagemm_set_small_m_route(int route) {
     return TMAGEMM_OK;
 }
 
+int tmagemm_set_group_m(int g) {
+    if (g < 0 || g > 64) return TMAGEMM_ERR_INVALID;
+    __atomic_store_n(&g_force_group_m, g, __ATOMIC_RELEASE);
+    return TMAGEMM_OK;
+}
+
 int tmagemm_set_cluster_split(int mode) {
     if (mode != 0 && mode != 1 && mode != 2 && mode != 4 && mode != 8) return TMAGEMM_ERR_INVALID;
     __atomic_store_n(&g_cluster_split, mode, __ATOMIC_RELEASE);
@@ -513,6 +519,7 @@ int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t 
     out[10] = p.units;
     out[11] = p.pair ? 1 : 0;
     out[12] = p.cluster_k;
+    out[13] = p.group_m;
     return TMAGEMM_OK;
 }
 

@@ -41,6 +41,7 @@
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <atomic>
+#include <cmath>
 #include <cstdint>
 
 #include "launch.h"
@@ -74,7 +75,7 @@ struct Cfg {
     static constexpr uint32_t kEpiElemBytes = OUT_F32_ ? 4 : 2;
     static constexpr uint32_t kEpiRowBytes = kEpiCols * kEpiElemBytes;
     static constexpr uint32_t kEpiChunks = kEpiRowBytes / 16;    // 16-byte chunks per box row
-    static constexpr int kGroupM = 8;               // L2 group height in tiles
+    static constexpr int kGroupM = 8;   // L2 group height in tiles (grouped GEMM; dense: per plan)
     static constexpr uint32_t kABytes = BM * BK * 2;
     static constexpr uint32_t kBBytes = kBRows * BK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
@@ -162,6 +163,7 @@ struct UnitInfo {
 // with split = u / num_tiles.  Without split-K, kb_per_unit = k_blocks.
 struct Work {
     int32_t M, N, grid_m, grid_n, num_tiles, num_units, k_blocks, kb_per_unit;
+    int32_t group_m;   // L2 group height in tiles (chosen by the plan)
 };
 
 struct DenseProblem {
@@ -175,10 +177,10 @@ struct DenseProblem {
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmD);
     }
-    __device__ __forceinline__ UnitInfo unit(int32_t u, int BM, int BN, int group_m) const {
+    __device__ __forceinline__ UnitInfo unit(int32_t u, int BM, int BN, int) const {
         const int32_t tile = u % w.num_tiles;
         const int32_t split = u / w.num_tiles;
-        const TileCoord tc = tile_coord(tile, w.grid_m, w.grid_n, group_m);
+        const TileCoord tc = tile_coord(tile, w.grid_m, w.grid_n, w.group_m);
         UnitInfo ui;
         ui.a_row = tc.m_blk * BM;
         ui.b_row = tc.n_blk * BN;
@@ -656,6 +658,31 @@ splitk_reduce_kernel(const float4* __restrict__ P, uint4* __restrict__ D, int64_
     }
 }
 
+// L2 group height: tiles are visited in groups of GROUP_M tile rows by all
+// grid_n tile columns.  When A, B and D fit in L2 together the order hardly
+// matters and plain row order (GROUP_M = 1) measured best on GB300 (4096^3:
+// 1798 TFLOP/s against 1771 with 8; 4000x3000x4160: 1693 against 1668).
+// Otherwise a round of `slots` resident tiles should touch as few A and B
+// panels as possible: GROUP_M x (tile rows of A) + (slots / GROUP_M) x (BN
+// rows of B) is smallest at GROUP_M = sqrt(slots x BN / tile rows) (8192^3:
+// 8, 1864 TFLOP/s; 4: 1830; 2: 1750).
+constexpr int64_t kL2FitBytes = 96ll << 20;
+
+int choose_group_m(int64_t M, int64_t N, int64_t K, int64_t grid_m, int64_t slots, int tile_m,
+                   int bn) {
+    const int forced = __atomic_load_n(&g_force_group_m, __ATOMIC_ACQUIRE);
+    int64_t g = 1;
+    if (forced > 0) {
+        g = forced;
+    } else if (2 * (M + N) * K + 2 * M * N > kL2FitBytes) {
+        const double best = std::sqrt(static_cast<double>(slots) * bn / tile_m);
+        g = static_cast<int64_t>(best);   // 8.7 at 8192^3 on 76 pairs: 8 measured best
+        if (g > 16) g = 16;
+    }
+    if (g > grid_m) g = grid_m;
+    return static_cast<int>(g < 1 ? 1 : g);
+}
+
 template <class C>
 GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) {
     GemmPlan p{};
@@ -683,6 +710,7 @@ GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) 
     p.kb_per_unit = ceil_div(p.k_blocks, splits);
     p.splits = ceil_div(p.k_blocks, p.kb_per_unit);   // no empty split
     p.units = p.tiles * p.splits;
+    p.group_m = choose_group_m(M, N, K, p.grid_m, slots, C::kTileM, C::BN);
     p.grid = static_cast<int>(p.units < slots ? p.units : slots) * (C::kPair ? 2 : 1);
     p.threads = C::kThreads;
     p.smem_bytes = static_cast<int>(C::kSmemBytes);
@@ -742,6 +770,7 @@ cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUten
     prob.w.num_units = static_cast<int32_t>(plan.units);
     prob.w.k_blocks = static_cast<int32_t>(plan.k_blocks);
     prob.w.kb_per_unit = static_cast<int32_t>(plan.kb_per_unit);
+    prob.w.group_m = static_cast<int32_t>(plan.group_m);
     prob.d_out = args.d_out;
     const unsigned cluster = static_cast<unsigned>((C::kPair ? 2 : 1) * (C::kClusterK ? C::kClusterK : 1));
     return launch_kernel(kernel, dim3(static_cast<unsigned>(plan.grid)), dim3(C::kThreads),
@@ -835,6 +864,7 @@ cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, int num_pairs, c
 int g_force_tile_n = 0;
 int g_pair_mode = 0;
 int g_cluster_split = 0;
+int g_force_group_m = 0;
 int g_pdl = 1;
 
 namespace {

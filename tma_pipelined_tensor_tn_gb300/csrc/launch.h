@@ -23,6 +23,7 @@ struct GemmPlan {
     bool pair;             // CTA-pair (cta_group::2) tiles of 256 x bn
     int b_box_rows;        // rows of B per CTA (bn, or bn / 2 for a pair)
     int cluster_k;         // > 0: K split over clusters of this many CTAs (one unit per CTA)
+    int group_m;           // L2 group height of the tile order, in tiles
 };
 
 // How many clusters of each cluster-split configuration can be co-resident
@@ -126,6 +127,9 @@ cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void
 
 // Tile-N override for the GEMM plan (0 = automatic); a tuning/test knob.
 extern int g_force_tile_n;
+
+// GROUP_M override for the dense tile order (0 = automatic); a tuning knob.
+extern int g_force_group_m;
 
 // Programmatic dependent launch: 1 (the default) launches every kernel with
 // the programmatic-stream-serialization attribute, so the next kernel on the
