@@ -23,6 +23,16 @@
 // The two TMEM accumulators let the epilogue of tile t overlap the mainloop
 // of tile t+1 — the overlap the pages defer to a warp-specialised step 7.
 //
+// CTA pairs (PAIR): the two CTAs of a pair (cluster ranks 2p, 2p + 1) run one
+// 256-row tile with cta_group::2 MMAs issued by the first; each holds its
+// 128 rows of A and half of B, so per SM the B traffic halves.  The tile
+// order visits groups of GROUP_M tile rows; the plan picks GROUP_M per shape
+// (row order when A, B and D fit in L2).
+//
+// Cluster split (CK): for few-tile shapes the CTAs (or pairs) of a cluster
+// compute one tile over separate K ranges and add their FP32 accumulators
+// through distributed shared memory before writing D (no workspace).
+//
 // Ragged M/N/K: TMA zero-fills out-of-range operand elements (the .zfill rule
 // of "高级数据搬运…", 零填充) and clamps out-of-range stores, so interior and
 // edge tiles run the same code.
