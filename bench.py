@@ -565,8 +565,7 @@ def measure_extras(tg, dev, stream, l2):
         out[f"small_m{Ms}_4096x14336"] = {"us": t_s, "gbs": by / t_s / 1e3,
                                           "tflops": 2.0 * Ms * GEMV_N * GEMV_K / t_s / 1e6,
                                           "kernel": ("mma.sync register fragments" if Ms <= 16
-                                                     else "tcgen05, W staged by SM loads" if Ms <= 32
-                                                     else "tcgen05 swap-AB + reduce")}
+                                                     else "tcgen05 tile kernel, cluster split-K")}
 
     # Grouped GEMM: 8 experts, 8192 routed tokens (skewed counts), N=4096, K=2048,
     # against one dense GEMM over the same 8192 rows.

@@ -62,11 +62,11 @@ typedef enum {
  *   D       : device pointer, M x N fp16, row-major; written, never read.
  *   stream  : cudaStream_t (NULL = legacy default stream).
  * Requirements: A, B, D 16-byte aligned; K % 8 == 0; N % 8 == 0 when M > 1.
- * M == 1 is computed by the GEMV kernel (x = A, W = B, y = D); 2 <= M <= 64
- * by the workspace-free kernels of gemm_f16_small_m (register fragments up to
- * 16 rows, the LSU-fed tcgen05 kernel above: a single 128-row tile row would
- * leave most SMs idle while B streams); the tcgen05 tile kernel takes every
- * larger M.  The results agree up to FP32 accumulation order.
+ * M == 1 is computed by the GEMV kernel (x = A, W = B, y = D); 2 <= M <= 16
+ * by the register-fragment kernel of gemm_f16_small_m (B streamed straight
+ * into mma.sync operands); larger M by the tcgen05 tile kernel, which splits
+ * K over clusters when the output has too few tiles to fill the SMs.  The
+ * results agree up to FP32 accumulation order.
  * Kernel: persistent, warp-specialised: a TMA producer warp feeding a
  * multi-stage mbarrier ring of 128B-swizzled tiles, one thread issuing
  * tcgen05.mma into a double-buffered TMEM accumulator, and four epilogue warps
@@ -170,20 +170,19 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
  * Skinny GEMM for a few rows of activations, D = fp16(X * W^T) with
  * 2 <= M <= 64: the decode step of "Learning TileLang with GEMV" (§01 GEMV:
  * every linear layer is a GEMV when tokens are decoded one by one) for a
- * batch of M tokens.  Like the GEMV it is bound by reading W once.  Three
- * kernels, chosen by M (tmagemm_set_small_m_route overrides):
+ * batch of M tokens.  Like the GEMV it is bound by reading W once.  The
+ * automatic choice (tmagemm_set_small_m_route overrides it):
  *   - M <= 16: W streams from HBM straight into mma.sync register fragments
  *     (16-byte loads, no shared-memory staging); the CTAs of a cluster split
  *     K and add their FP32 partials in fixed order through distributed
- *     shared memory.  Needs no workspace.
- *   - 17 <= M <= 32: tcgen05 with W staged in shared memory by the SMs' own
- *     16-byte loads (X by TMA); K split over a cluster and reduced the same
- *     way.  Needs no workspace.
- *   - otherwise: the tcgen05 kernel with the roles swapped — W is the 128-row
- *     MMA operand and X (rows past M read as zero) the 16- or 64-wide one —
- *     and K split so that enough SMs stream W; FP32 partials go to
- *     `workspace` and a second kernel adds them in fixed order, transposes
- *     and rounds to fp16.
+ *     shared memory.
+ *   - otherwise: the tcgen05 tile kernel of gemm_f16, which splits K over
+ *     clusters when the output has too few tiles to fill the SMs.
+ * Neither needs a workspace.  Two more kernels are available by route: the
+ * tcgen05 kernel with the roles swapped (W the 128-row MMA operand, X the
+ * 16- or 64-wide one, rows past M zero; K split, FP32 partials in
+ * `workspace`, a second kernel adds them in fixed order, transposes and
+ * rounds), and tcgen05 with W staged in shared memory by the SMs' own loads.
  *   X         : device pointer, M x K fp16 row-major (activations).
  *   W         : device pointer, N x K fp16 row-major (weights).
  *   D         : device pointer, M x N fp16 row-major.
@@ -198,15 +197,15 @@ int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void*
                      void* workspace, int64_t workspace_bytes, void* stream);
 
 /* Workspace bytes gemm_f16_small_m needs on the current device (negative =
- * status; 0 unless the swap-AB kernel takes this M). */
+ * status; 0 unless route 1 sends this M to the swap-AB kernel). */
 int64_t gemm_f16_small_m_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
- * Route of gemm_f16_small_m, process-wide: 0 = automatic (register
- * fragments for M <= 16, the LSU-fed tcgen05 kernel for 17..32, the swap-AB
- * tcgen05 kernel above), 1 = always the swap-AB kernel, 2 = the register-
- * fragment kernel for every M <= 16 (swap-AB above), 3 = always the LSU-fed
- * tcgen05 kernel.  Results
+ * Route of gemm_f16_small_m, process-wide: 0 and 2 = automatic (register
+ * fragments for M <= 16, the tile kernel above), 1 = always the swap-AB
+ * kernel (needs the workspace), 3 = always the LSU-fed tcgen05 kernel.
+ * gemm_f16 / gemm_bf16 with 2 <= M <= 64 follow routes 0, 2 and 3 and take
+ * the tile kernel under route 1.  Results
  * agree up to FP32 accumulation order.  The workspace size depends on the
  * route: query it after setting the route.  Returns TMAGEMM_ERR_INVALID for
  * other values.
@@ -216,9 +215,9 @@ int tmagemm_set_small_m_route(int route);
 /*
  * bfloat16 forms of gemm_f16 and gemv_f16: A, B, D (x, W, y) hold bf16
  * values; accumulation is FP32 and each output is rounded once to bf16
- * (nearest even).  Same kernels, tiles, requirements and status codes; only
- * the element type of the tensor maps, the MMA operand format and the final
- * conversion change.  "TensorCore_GEMM_with_TMA" runs this TN GEMM in bf16
+ * (nearest even).  Same kernels, tiles, shape routing (M = 1 the GEMV,
+ * 2 <= M <= 16 the register-fragment kernel), requirements and status codes; only the element type of the tensor maps, the MMA operand format and
+ * the final conversion change.  "TensorCore_GEMM_with_TMA" runs this TN GEMM in bf16
  * (§2.1 init tensor map: CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; §2.3: bf16 output
  * rounded to nearest).
  */

@@ -112,3 +112,35 @@ def test_gemv_bf16_integer_bitexact(tg):
     y = tg.gemv(x.cuda(), W.cuda())
     tg.check()
     assert np.array_equal(to_bits(y), oracle.gemv_bf16(to_bits(x), to_bits(W)))
+
+
+@pytest.mark.parametrize("M", [2, 8, 16, 17, 32, 33, 64])
+def test_gemm_bf16_few_rows(tg, M):
+    """gemm_bf16 with a few rows: the bf16 register-fragment kernel up to 16
+    rows, the tile kernel with its cluster split above; route 3 forces the
+    bf16 LSU-fed tcgen05 kernel (checked in test_gemm_bf16_lsu_forced)."""
+    N, K = 4104, 4160
+    A, B = uniform_bf16((M, K), 700 + M), uniform_bf16((N, K), 701 + M)
+    compare_bf16(run(tg, A, B), oracle.gemm_bf16(to_bits(A), to_bits(B)), f"bf16 few rows M={M}")
+
+
+@pytest.mark.parametrize("M", [8, 24, 64])
+def test_gemm_bf16_few_rows_integer_bitexact(tg, M):
+    N, K = 2056, 4160
+    A = inputs.integer_f16((M, K), seed=710 + M).to(torch.bfloat16)
+    B = inputs.integer_f16((N, K), seed=711 + M).to(torch.bfloat16)
+    got = run(tg, A, B)
+    ref = oracle.gemm_bf16(to_bits(A), to_bits(B))
+    assert np.array_equal(np.ascontiguousarray(got).view(np.uint16), ref), f"M={M}"
+
+
+@pytest.mark.parametrize("M", [2, 17, 40, 64])
+def test_gemm_bf16_lsu_forced(tg, M):
+    N, K = 1032, 4160
+    A, B = uniform_bf16((M, K), 720 + M), uniform_bf16((N, K), 721 + M)
+    try:
+        assert tg.tmagemm_set_small_m_route(3) == tg.TMAGEMM_OK
+        got = run(tg, A, B)
+    finally:
+        tg.tmagemm_set_small_m_route(0)
+    compare_bf16(got, oracle.gemm_bf16(to_bits(A), to_bits(B)), f"bf16 LSU-fed M={M}")

@@ -217,16 +217,16 @@ def test_gemm_out_of_bounds_guard(tg):
 
 @pytest.mark.parametrize("M", [2, 8, 16, 17, 32, 33, 64, 65])
 def test_gemm_few_rows_route(tg, M):
-    """gemm_f16 with 2 <= M <= 32 runs the same workspace-free kernels as
-    gemm_f16_small_m (bit-identical); 33..64 the LSU-fed one (gemm_f16_small_m
-    prefers swap-AB there); M = 65 the tile kernel."""
+    """gemm_f16 with 2 <= M <= 16 runs the register-fragment kernel of
+    gemm_f16_small_m (bit-identical); larger M the tile kernel (with its
+    cluster split for these few-tile shapes)."""
     N, K = 4104, 4160
     A, B = inputs.gemm_inputs(M, N, K, seed=500 + M)
     a, b = A.cuda(), B.cuda()
     D = tg.gemm(a, b).cpu().numpy()
     tg.check()
     compare(D, oracle.gemm_f16(A.numpy(), B.numpy()), f"gemm_f16 M={M}")
-    if M <= 32:
+    if M <= 16:
         assert_bitexact(D, tg.gemm_small_m(a, b).cpu().numpy(), f"gemm_f16 vs small-M M={M}")
 
 

@@ -26,11 +26,10 @@ def run(tg, X, W):
     return D.cpu().numpy()
 
 
-# 1 = the tcgen05 swap-AB kernel, 2 = the register-fragment mma.sync kernel
-# (M <= 16; larger M take the swap-AB kernel on that setting), 3 = the LSU-fed
-# tcgen05 kernel (every M); the automatic route is exercised by every other
-# test file and by test_small_m_auto_route.
-@pytest.fixture(params=[1, 2, 3], ids=["swap_ab", "fragments", "lsu"])
+# 1 = the tcgen05 swap-AB kernel, 2 = automatic (the register-fragment
+# mma.sync kernel up to 16 rows, the tile kernel above), 3 = the LSU-fed
+# tcgen05 kernel (every M).
+@pytest.fixture(params=[1, 2, 3], ids=["swap_ab", "auto", "lsu"])
 def route(tg, request):
     assert tg.tmagemm_set_small_m_route(request.param) == tg.TMAGEMM_OK
     yield request.param
@@ -103,28 +102,32 @@ def test_small_m_routes_agree_on_exact_sums(tg):
 
 @pytest.mark.parametrize("M", [2, 16, 17, 32, 33, 64])
 def test_small_m_auto_route(tg, M):
-    """The automatic route on each side of its thresholds (16 and 32)."""
+    """The automatic route on each side of its threshold (16): no workspace,
+    and the same bits as gemm_f16 (which routes the same way)."""
     N, K = 1032, 2056
     X, W = inputs.gemm_inputs(M, N, K, seed=400 + M)
-    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M auto M={M}")
-    need = tg.gemm_f16_small_m_workspace_size(M, N, K)
-    assert (need == 0) == (M <= 32)
+    d = run(tg, X, W)
+    compare(d, oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M auto M={M}")
+    assert tg.gemm_f16_small_m_workspace_size(M, N, K) == 0
+    assert_bitexact(d, tg.gemm(X.cuda(), W.cuda()).cpu().numpy(), f"small-M auto vs gemm_f16 M={M}")
 
 
 def test_small_m_rejects_out_of_range_and_bad_workspace(tg):
     p = torch.zeros(1 << 20, dtype=torch.float16, device="cuda").data_ptr()
     assert tg.gemm_f16_small_m(1, 64, 64, p, p, p, p, 1 << 20, None) == tg.TMAGEMM_ERR_UNSUPPORTED
     assert tg.gemm_f16_small_m(65, 64, 64, p, p, p, p, 1 << 20, None) == tg.TMAGEMM_ERR_UNSUPPORTED
-    # M > 32 takes the swap-AB kernel, which needs its workspace.
-    assert tg.gemm_f16_small_m(40, 64, 64, p, p, p, None, 0, None) == tg.TMAGEMM_ERR_WORKSPACE
-    need = tg.gemm_f16_small_m_workspace_size(40, 4096, 14336)
-    assert need > 0
-    assert tg.gemm_f16_small_m(40, 4096, 14336, p, p, p, p, need - 16, None) == tg.TMAGEMM_ERR_WORKSPACE
-    # M <= 32 takes a kernel that needs no workspace.
-    assert tg.gemm_f16_small_m_workspace_size(8, 4096, 14336) == 0
-    assert tg.gemm_f16_small_m(8, 64, 64, p, p, p, None, 0, None) == tg.TMAGEMM_OK
+    # The automatic choices need no workspace.
+    for M in (8, 40):
+        assert tg.gemm_f16_small_m_workspace_size(M, 4096, 14336) == 0
+        assert tg.gemm_f16_small_m(M, 64, 64, p, p, p, None, 0, None) == tg.TMAGEMM_OK
+    # The swap-AB kernel (route 1) does.
     try:
         assert tg.tmagemm_set_small_m_route(1) == tg.TMAGEMM_OK
+        assert tg.gemm_f16_small_m(40, 64, 64, p, p, p, None, 0, None) == tg.TMAGEMM_ERR_WORKSPACE
+        need = tg.gemm_f16_small_m_workspace_size(40, 4096, 14336)
+        assert need > 0
+        assert tg.gemm_f16_small_m(40, 4096, 14336, p, p, p, p, need - 16, None) == \
+            tg.TMAGEMM_ERR_WORKSPACE
         assert tg.gemm_f16_small_m_workspace_size(8, 4096, 14336) > 0
         assert tg.gemm_f16_small_m(8, 64, 64, p, p, p, None, 0, None) == tg.TMAGEMM_ERR_WORKSPACE
     finally:

@@ -185,40 +185,58 @@ using namespace tmagemm;
 
 extern "C" {
 
-enum class SmallMKernel { kSwapAB, kFragments, kLsu };
+enum class SmallMKernel { kSwapAB, kFragments, kLsu, kTile };
 
 // Which kernel gemm_f16_small_m runs for this M (see tmagemm_set_small_m_route).
-// The automatic choice follows GB300 measurements at N = 4096, K = 14336:
-// M <= 16 register fragments (20.4-23.0 us; TMA swap-AB 25.8-26.2, LSU-fed
-// tcgen05 24.3-27.3), 17..32 the LSU-fed tcgen05 kernel (M = 24: 30.6 us
-// against 33.0), above that the TMA swap-AB kernel (M = 40..64: 32.8 us
-// against 41-47).
+// The automatic choice follows GB300 measurements over N x K in {4096 x
+// 14336, 14336 x 4096, 4096 x 4096}: up to 16 rows the register-fragment
+// kernel is fastest (4096 x 14336, M = 8: 21.4 us; swap-AB 26.1, LSU-fed 25.6,
+// tile kernel 30.0); above that the tile kernel with its cluster split of K is
+// the fastest or within 7 % of it everywhere (14336 x 4096, M = 17..64:
+// 26.0-28.4 us; swap-AB 29.2-30.4, LSU-fed 48.8-88.6).
 static SmallMKernel small_m_kernel(int64_t M) {
     const int route = __atomic_load_n(&g_small_m_route, __ATOMIC_ACQUIRE);
     if (route == 1) return SmallMKernel::kSwapAB;
     if (route == 3) return SmallMKernel::kLsu;
-    if (route == 2) return M <= small_m_mma_max_m() ? SmallMKernel::kFragments : SmallMKernel::kSwapAB;
-    if (M <= small_m_mma_max_m()) return SmallMKernel::kFragments;
-    return M <= 32 ? SmallMKernel::kLsu : SmallMKernel::kSwapAB;
+    return M <= small_m_mma_max_m() ? SmallMKernel::kFragments : SmallMKernel::kTile;
 }
 
-// The workspace-free small-M kernels (register fragments, LSU-fed tcgen05).
+// The workspace-free small-M kernels (register fragments, LSU-fed tcgen05),
+// fp16 or bf16 operands and output.
 static int small_m_no_workspace(SmallMKernel k, int64_t M, int64_t N, int64_t K, const void* X,
-                                const void* W, void* D, void* stream) {
+                                const void* W, void* D, void* stream, bool bf16 = false) {
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
     if (k == SmallMKernel::kFragments)
-        return launch_small_m_mma(M, N, K, X, W, D, st) == cudaSuccess ? TMAGEMM_OK
-                                                                      : TMAGEMM_ERR_CUDA;
+        return launch_small_m_mma(M, N, K, X, W, D, st, bf16, d->sms) == cudaSuccess
+                   ? TMAGEMM_OK
+                   : TMAGEMM_ERR_CUDA;
     // X {K, M} in boxes of 64 k x Mp token rows (rows past M read as zero).
     CUtensorMap tmX;
     if (int s = encode_2d(&tmX, X, K, M, 64, small_m_lsu_cols(M), CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, bf16))
         return s;
-    return launch_small_m_lsu(tmX, M, N, K, W, D, wait_limit_ns(), d->err_word, st) == cudaSuccess
+    return launch_small_m_lsu(tmX, M, N, K, W, D, wait_limit_ns(), d->err_word, st, bf16) ==
+                   cudaSuccess
                ? TMAGEMM_OK
                : TMAGEMM_ERR_CUDA;
+}
+
+// gemm_f16 / gemm_bf16 with a few rows: runs the register-fragment kernel for
+// M <= 16 (or the LSU-fed kernel up to 64 when route 3 forces it) and
+// returns true with its status in *status; false if the tile kernel should
+// run.  Above 16 rows the tile kernel, with its cluster split of K for
+// few-tile shapes, measured faster on GB300 than the workspace-free small-M
+// kernels: N = 4096, K = 14336, M = 33..64: 33-34 us against 39-48 us;
+// N = 14336, K = 4096, M = 17..64: 26-28 us against 49-89 us.
+static bool few_rows(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+                     void* stream, bool bf16, int* status) {
+    if (M > 64) return false;
+    const SmallMKernel k = small_m_kernel(M);
+    if (k != SmallMKernel::kFragments && k != SmallMKernel::kLsu) return false;
+    *status = small_m_no_workspace(k, M, N, K, A, B, D, stream, bf16);
+    return true;
 }
 
 int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
@@ -228,17 +246,11 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void
     if (M == 1) return gemv_impl(N, K, A, B, D, stream);
     if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
         return TMAGEMM_ERR_ALIGN;
-    // A few rows: one tile row of the GEMM would leave most SMs idle while B
-    // streams; the workspace-free small-M kernels split K instead.  For
-    // 33..64 rows the automatic small-M choice (swap-AB) needs a workspace,
-    // so the LSU-fed kernel runs (GB300, N = 4096, K = 14336: 41-47 us
-    // against 57 us for the tile kernel).
-    if (M <= 64) {
-        SmallMKernel k = small_m_kernel(M);
-        if (k == SmallMKernel::kSwapAB && __atomic_load_n(&g_small_m_route, __ATOMIC_ACQUIRE) == 0)
-            k = SmallMKernel::kLsu;
-        if (k != SmallMKernel::kSwapAB) return small_m_no_workspace(k, M, N, K, A, B, D, stream);
-    }
+    // A few rows: the register-fragment kernel streams B fastest up to 16
+    // rows (GB300, N = 4096, K = 14336: 21.5 us against 30 us for the tile
+    // kernel); above that the tile kernel with its cluster split.
+    int fr = TMAGEMM_OK;
+    if (few_rows(M, N, K, A, B, D, stream, false, &fr)) return fr;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
     return run_gemm(plan_gemm(M, N, K, d->sms, 1, false, d->pairs, d->caps), d, M, N, K, A, B, D,
@@ -345,7 +357,7 @@ static int64_t small_m_tile_rows(int64_t M) { return M <= 16 ? M : 64; }
 int64_t gemm_f16_small_m_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (int s = validate_common(M, N, K)) return s;
     if (M < 2 || M > 64) return TMAGEMM_ERR_UNSUPPORTED;
-    if (small_m_kernel(M) != SmallMKernel::kSwapAB) return 0;
+    if (small_m_kernel(M) != SmallMKernel::kSwapAB) return 0;   // only swap-AB needs one
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
     const GemmPlan p = plan_small_m(small_m_tile_rows(M), N, K, d->sms, 0);
@@ -360,6 +372,7 @@ int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void*
     if (!aligned16(X) || !aligned16(W) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
         return TMAGEMM_ERR_ALIGN;
     const SmallMKernel kern = small_m_kernel(M);
+    if (kern == SmallMKernel::kTile) return gemm_f16(M, N, K, X, W, D, stream);
     if (kern != SmallMKernel::kSwapAB) return small_m_no_workspace(kern, M, N, K, X, W, D, stream);
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     DeviceState* d = nullptr;
@@ -395,6 +408,8 @@ int gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, voi
     if (M == 1) return gemv_impl(N, K, A, B, D, stream, true);
     if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
         return TMAGEMM_ERR_ALIGN;
+    int fr = TMAGEMM_OK;
+    if (few_rows(M, N, K, A, B, D, stream, true, &fr)) return fr;   // as in gemm_f16
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
     return run_gemm(plan_gemm(M, N, K, d->sms, 1, true, d->pairs, d->caps), d, M, N, K, A, B, D,

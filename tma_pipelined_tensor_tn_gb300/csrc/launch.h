@@ -86,7 +86,7 @@ cudaError_t launch_small_m_reduce(const void* partials, void* D, int64_t M, int6
 // No workspace; one launch.
 int64_t small_m_mma_max_m();
 cudaError_t launch_small_m_mma(int64_t M, int64_t N, int64_t K, const void* X, const void* W,
-                               void* D, cudaStream_t stream);
+                               void* D, cudaStream_t stream, bool bf16 = false, int num_sms = 0);
 
 // Skinny GEMM (2 <= M <= 64) on tcgen05 with the weights staged in shared
 // memory by the SMs' own 16-byte loads (X by TMA); K split over 8-CTA clusters
@@ -95,7 +95,7 @@ cudaError_t launch_small_m_mma(int64_t M, int64_t N, int64_t K, const void* X, c
 int64_t small_m_lsu_cols(int64_t M);
 cudaError_t launch_small_m_lsu(const CUtensorMap& tmX, int64_t M, int64_t N, int64_t K,
                                const void* W, void* D, uint64_t limit_ns, uint32_t* err,
-                               cudaStream_t stream);
+                               cudaStream_t stream, bool bf16 = false);
 
 // Route of gemm_f16_small_m: 0 automatic, 1 always the tcgen05 swap-AB
 // kernel, 2 the register-fragment kernel wherever it applies, 3 always the

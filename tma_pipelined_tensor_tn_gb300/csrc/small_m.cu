@@ -1,4 +1,5 @@
-// Skinny GEMM for a few tokens, D = fp16(X W^T) with 2 <= M <= 16, streamed
+// Skinny GEMM for a few tokens, D = fp16(X W^T) with 2 <= M <= 16 (and the
+// same with bf16 operands and output), streamed
 // like the GEMV: the weights go from HBM straight into tensor-core register
 // fragments, with no shared-memory staging.
 //
@@ -28,6 +29,7 @@
 // the rows, adding the S partials in slice order through distributed shared
 // memory, rounding once to fp16 and writing D.  No workspace, one launch,
 // deterministic.
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -51,14 +53,22 @@ __device__ __forceinline__ uint4 ld_weights(const uint4* p) {
     return r;
 }
 
-// c += A * B for one m16n8k16 tile (fp16 operands, FP32 accumulators).
+// c += A * B for one m16n8k16 tile (fp16 or bf16 operands, FP32 accumulators).
+template <bool BF16>
 __device__ __forceinline__ void mma_m16n8k16(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
                                              uint32_t a3, uint32_t b0, uint32_t b1) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
-        "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    if constexpr (BF16)
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+    else
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
+            "{%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+            : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+            : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
 __device__ __forceinline__ float ld_shared_cluster_f32(uint32_t addr) {
@@ -97,7 +107,7 @@ __device__ __forceinline__ void load_group(Group<NT, U, XB>& G, const uint4* wro
     }
 }
 
-template <int NT, int U, bool XB>
+template <bool BF16, int NT, int U, bool XB>
 __device__ __forceinline__ void mma_group(const Group<NT, U, XB>& G, const uint4* const (&xrow)[NT],
                                           int32_t chunk0, int32_t c_end, float (&acc)[NT][4]) {
     const uint4 z = make_uint4(0u, 0u, 0u, 0u);
@@ -114,16 +124,16 @@ __device__ __forceinline__ void mma_group(const Group<NT, U, XB>& G, const uint4
                 x = (ok && xrow[j]) ? __ldg(xrow[j] + c) : z;
             // MMA 0: physical k 8t + {0,1} (slots 2t, 2t+1) and 8t + {2,3}
             // (slots 2t+8, 2t+9); MMA 1: 8t + {4,5} and 8t + {6,7}.
-            mma_m16n8k16(acc[j], G.wa[u].x, G.wb[u].x, G.wa[u].y, G.wb[u].y, x.x, x.y);
-            mma_m16n8k16(acc[j], G.wa[u].z, G.wb[u].z, G.wa[u].w, G.wb[u].w, x.z, x.w);
+            mma_m16n8k16<BF16>(acc[j], G.wa[u].x, G.wb[u].x, G.wa[u].y, G.wb[u].y, x.x, x.y);
+            mma_m16n8k16<BF16>(acc[j], G.wa[u].z, G.wb[u].z, G.wa[u].w, G.wb[u].w, x.z, x.w);
         }
     }
 }
 
-template <int NT, int U, bool XB, int MIN_CTAS, int S>
+template <int NT, int U, bool XB, int MIN_CTAS, int S, bool BF16>
 __global__ void __launch_bounds__(kSmWarps * 32, MIN_CTAS)
 small_m_mma_kernel(const uint4* __restrict__ X, const uint4* __restrict__ W,
-                   __half* __restrict__ D, int32_t M, int32_t N, int32_t K8, int32_t slice8) {
+                   uint16_t* __restrict__ D, int32_t M, int32_t N, int32_t K8, int32_t slice8) {
     constexpr int kMp = 8 * NT;
     __shared__ float part[kSmRows][kMp];
 
@@ -158,9 +168,9 @@ small_m_mma_kernel(const uint4* __restrict__ X, const uint4* __restrict__ W,
         const int32_t ca = c_begin + t + i * kGroupChunks;
         const int32_t cb = ca + kGroupChunks;
         if (i + 1 < groups) load_group(gb, wrow_a, wrow_b, xrow, cb, c_end);
-        mma_group(ga, xrow, ca, c_end, acc);
+        mma_group<BF16>(ga, xrow, ca, c_end, acc);
         if (i + 2 < groups) load_group(ga, wrow_a, wrow_b, xrow, cb + kGroupChunks, c_end);
-        if (i + 1 < groups) mma_group(gb, xrow, cb, c_end, acc);
+        if (i + 1 < groups) mma_group<BF16>(gb, xrow, cb, c_end, acc);
     }
 
     // This slice's partial tile: C rows g, g+8 of the warp's 16 weight rows,
@@ -191,7 +201,12 @@ small_m_mma_kernel(const uint4* __restrict__ X, const uint4* __restrict__ W,
 #pragma unroll
         for (int q = 1; q < S; ++q) sum += v[q];
         const int32_t n = row0 + rl;
-        if (m < M && n < N) D[static_cast<int64_t>(m) * N + n] = __float2half_rn(sum);
+        if (m < M && n < N) {
+            if constexpr (BF16)
+                D[static_cast<int64_t>(m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+            else
+                D[static_cast<int64_t>(m) * N + n] = __half_as_ushort(__float2half_rn(sum));
+        }
     }
     cluster_sync();   // peers' shared memory stays alive until every CTA has read it
 }
@@ -206,41 +221,42 @@ namespace {
 
 // Grid of S-CTA clusters over ceil(N / 64) row groups; K is cut into S
 // ranges of whole 4-chunk (32-k) steps.
-template <int NT, int U, bool XB, int MIN_CTAS, int S>
+template <int NT, int U, bool XB, int MIN_CTAS, int S, bool BF16>
 cudaError_t launch_variant(int64_t M, int64_t N, int64_t K, const void* X, const void* W, void* D,
                            cudaStream_t stream) {
     const int32_t K8 = static_cast<int32_t>(K / 8);
     const int32_t per = (K8 + S - 1) / S;
     const int32_t slice8 = (per + 3) / 4 * 4;
     const int64_t clusters = (N + kSmRows - 1) / kSmRows;
-    return launch_kernel(small_m_mma_kernel<NT, U, XB, MIN_CTAS, S>,
+    return launch_kernel(small_m_mma_kernel<NT, U, XB, MIN_CTAS, S, BF16>,
                          dim3(static_cast<unsigned>(clusters * S)), dim3(kSmWarps * 32), 0,
                          stream, static_cast<unsigned>(S), static_cast<const uint4*>(X),
-                         static_cast<const uint4*>(W), static_cast<__half*>(D),
+                         static_cast<const uint4*>(W), static_cast<uint16_t*>(D),
                          static_cast<int32_t>(M), static_cast<int32_t>(N), K8, slice8);
 }
 
-}  // namespace
+// Slices per cluster: 8 when the clusters of 64 weight rows are few enough
+// for one wave of CTAs (4 per SM: 512 CTAs at N = 4096), fewer for more rows
+// so that the grid stays one wave with longer K slices (N = 14336: 2).
+template <int NT, int U, bool BF16>
+cudaError_t launch_sliced(int64_t M, int64_t N, int64_t K, const void* X, const void* W, void* D,
+                          int num_sms, cudaStream_t stream) {
+    const int64_t clusters = (N + kSmRows - 1) / kSmRows;
+    const int64_t wave = 4ll * (num_sms > 0 ? num_sms : 152);
+    if (clusters * 8 <= wave) return launch_variant<NT, U, true, 1, 8, BF16>(M, N, K, X, W, D, stream);
+    if (clusters * 4 <= wave) return launch_variant<NT, U, true, 1, 4, BF16>(M, N, K, X, W, D, stream);
+    return launch_variant<NT, U, true, 1, 2, BF16>(M, N, K, X, W, D, stream);
+}
 
-#ifdef TMAGEMM_SMALL_M_SWEEP
-// Variants (token tiles, unroll, X prefetched, CTAs per SM, slices), for
-// tuning builds only.
-cudaError_t launch_small_m_mma_cfg(int64_t M, int64_t N, int64_t K, const void* X, const void* W,
-                                   void* D, int u, int xb, int slices, int min_ctas,
-                                   cudaStream_t stream) {
-#define TMAGEMM_SM_VARIANT(NT, UU, XX, MC, SS)                                                 \
-    if (M <= 8 * NT && (NT == 1 || M > 4 * NT) && u == UU && xb == XX && min_ctas == MC &&     \
-        slices == SS)                                                                          \
-        return launch_variant<NT, UU, XX, MC, SS>(M, N, K, X, W, D, stream);
-    TMAGEMM_SM_VARIANT(1, 4, 1, 1, 8) TMAGEMM_SM_VARIANT(1, 4, 1, 4, 8) TMAGEMM_SM_VARIANT(1, 4, 1, 1, 7)
-    TMAGEMM_SM_VARIANT(1, 6, 1, 3, 6) TMAGEMM_SM_VARIANT(1, 6, 1, 1, 6) TMAGEMM_SM_VARIANT(1, 4, 0, 1, 8)
-    TMAGEMM_SM_VARIANT(2, 4, 1, 2, 4) TMAGEMM_SM_VARIANT(2, 4, 1, 3, 6) TMAGEMM_SM_VARIANT(2, 4, 1, 1, 6)
-    TMAGEMM_SM_VARIANT(2, 3, 1, 3, 6) TMAGEMM_SM_VARIANT(2, 4, 1, 1, 4) TMAGEMM_SM_VARIANT(2, 4, 1, 1, 8)
-    TMAGEMM_SM_VARIANT(2, 2, 1, 1, 8)
-#undef TMAGEMM_SM_VARIANT
+template <bool BF16>
+cudaError_t launch_typed(int64_t M, int64_t N, int64_t K, const void* X, const void* W, void* D,
+                         int num_sms, cudaStream_t stream) {
+    if (M <= 8) return launch_sliced<1, 4, BF16>(M, N, K, X, W, D, num_sms, stream);
+    if (M <= 16) return launch_sliced<2, 2, BF16>(M, N, K, X, W, D, num_sms, stream);
     return cudaErrorInvalidValue;
 }
-#endif
+
+}  // namespace
 
 // Measured on GB300 at N = 4096, K = 14336 over unroll 2..6, X prefetched or
 // not, 1..4 CTAs per SM and 4..8 slices: the best keep every CTA resident
@@ -249,10 +265,9 @@ cudaError_t launch_small_m_mma_cfg(int64_t M, int64_t N, int64_t K, const void* 
 // 8 slices, 23.1 us.  A slice count read at run time instead of fixed at
 // compile time cost 2 us; above 16 tokens the tcgen05 kernel is faster.
 cudaError_t launch_small_m_mma(int64_t M, int64_t N, int64_t K, const void* X, const void* W,
-                               void* D, cudaStream_t stream) {
-    if (M <= 8) return launch_variant<1, 4, true, 1, 8>(M, N, K, X, W, D, stream);
-    if (M <= 16) return launch_variant<2, 2, true, 1, 8>(M, N, K, X, W, D, stream);
-    return cudaErrorInvalidValue;
+                               void* D, cudaStream_t stream, bool bf16, int num_sms) {
+    return bf16 ? launch_typed<true>(M, N, K, X, W, D, num_sms, stream)
+                : launch_typed<false>(M, N, K, X, W, D, num_sms, stream);
 }
 
 }  // namespace tmagemm

@@ -1,4 +1,5 @@
-// Skinny GEMM for a few tokens, D = fp16(X W^T) with 2 <= M <= 64, on tcgen05
+// Skinny GEMM for a few tokens, D = fp16(X W^T) with 2 <= M <= 64 (and the same
+// with bf16 operands and output), on tcgen05
 // with the weights staged in shared memory by the SMs' own loads.
 //
 // The decode step reads each weight once ("Learning TileLang with GEMV", §01
@@ -30,6 +31,7 @@
 // No workspace, one launch, deterministic.  Every mbarrier wait is bounded
 // (the CTA-wide abort flag and the device error word, as in the GEMM).
 #include <cuda.h>
+#include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <atomic>
@@ -100,10 +102,10 @@ struct TmLayout {
 // Two producer warpgroups, the MMA warp and the X warp; two CTAs per SM.
 constexpr int kTmThreads = 320;
 
-template <int MP>
+template <int MP, bool BF16>
 __global__ void __launch_bounds__(kTmThreads, 2)
 small_m_lsu_kernel(const __grid_constant__ CUtensorMap tmX, const uint4* __restrict__ W,
-                   __half* __restrict__ D, int32_t M, int32_t N, int32_t K8, int32_t kb_total,
+                   uint16_t* __restrict__ D, int32_t M, int32_t N, int32_t K8, int32_t kb_total,
                     int32_t kb_per_slice, uint64_t limit_ns, uint32_t* __restrict__ err) {
     using L = TmLayout<MP>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -220,7 +222,7 @@ small_m_lsu_kernel(const __grid_constant__ CUtensorMap tmX, const uint4* __restr
     } else if (warp == kTmMmaWarp) {
         // ============ MMA issuer ============
         if (lane == 0) {
-            constexpr uint32_t kIdesc = umma_idesc_16bit_f32(kTmRows, MP, false);
+            constexpr uint32_t kIdesc = umma_idesc_16bit_f32(kTmRows, MP, BF16);
             bool ok = true;
             for (int32_t i = 0; i < nkb; ++i) {
                 const uint32_t s = static_cast<uint32_t>(i) % kTmStages;
@@ -286,7 +288,10 @@ small_m_lsu_kernel(const __grid_constant__ CUtensorMap tmX, const uint4* __restr
         float sum = v[0];
 #pragma unroll
         for (int q = 1; q < kTmSlices; ++q) sum += v[q];
-        D[static_cast<int64_t>(m) * N + n] = __float2half_rn(sum);
+        if constexpr (BF16)
+            D[static_cast<int64_t>(m) * N + n] = __bfloat16_as_ushort(__float2bfloat16_rn(sum));
+        else
+            D[static_cast<int64_t>(m) * N + n] = __half_as_ushort(__float2half_rn(sum));
     }
     cluster_sync();   // peers' shared memory stays alive until every CTA has read it
     if (warp == 0) {
@@ -295,10 +300,10 @@ small_m_lsu_kernel(const __grid_constant__ CUtensorMap tmX, const uint4* __restr
     }
 }
 
-template <int MP>
+template <int MP, bool BF16>
 cudaError_t launch_mp(const CUtensorMap& tmX, int64_t M, int64_t N, int64_t K, const void* W,
                       void* D, uint64_t limit_ns, uint32_t* err, cudaStream_t stream) {
-    auto kernel = small_m_lsu_kernel<MP>;
+    auto kernel = small_m_lsu_kernel<MP, BF16>;
     static std::atomic<bool> attr_done{false};
     if (!attr_done.load(std::memory_order_acquire)) {
         cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -311,7 +316,7 @@ cudaError_t launch_mp(const CUtensorMap& tmX, int64_t M, int64_t N, int64_t K, c
     const int64_t clusters = (N + kTmRows - 1) / kTmRows;
     return launch_kernel(kernel, dim3(static_cast<unsigned>(clusters * kTmSlices)), dim3(kTmThreads),
                          TmLayout<MP>::kSmemBytes, stream, static_cast<unsigned>(kTmSlices), tmX,
-                         static_cast<const uint4*>(W), static_cast<__half*>(D),
+                         static_cast<const uint4*>(W), static_cast<uint16_t*>(D),
                          static_cast<int32_t>(M), static_cast<int32_t>(N),
                          static_cast<int32_t>(K / 8), kb_total, kb_per_slice, limit_ns, err);
 }
@@ -322,11 +327,14 @@ int64_t small_m_lsu_cols(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
 
 cudaError_t launch_small_m_lsu(const CUtensorMap& tmX, int64_t M, int64_t N, int64_t K,
                                const void* W, void* D, uint64_t limit_ns, uint32_t* err,
-                               cudaStream_t stream) {
-    switch (small_m_lsu_cols(M)) {
-        case 16: return launch_mp<16>(tmX, M, N, K, W, D, limit_ns, err, stream);
-        case 32: return launch_mp<32>(tmX, M, N, K, W, D, limit_ns, err, stream);
-        default: return launch_mp<64>(tmX, M, N, K, W, D, limit_ns, err, stream);
+                               cudaStream_t stream, bool bf16) {
+    switch (small_m_lsu_cols(M) * (bf16 ? -1 : 1)) {
+        case 16: return launch_mp<16, false>(tmX, M, N, K, W, D, limit_ns, err, stream);
+        case 32: return launch_mp<32, false>(tmX, M, N, K, W, D, limit_ns, err, stream);
+        case 64: return launch_mp<64, false>(tmX, M, N, K, W, D, limit_ns, err, stream);
+        case -16: return launch_mp<16, true>(tmX, M, N, K, W, D, limit_ns, err, stream);
+        case -32: return launch_mp<32, true>(tmX, M, N, K, W, D, limit_ns, err, stream);
+        default: return launch_mp<64, true>(tmX, M, N, K, W, D, limit_ns, err, stream);
     }
 }
 
