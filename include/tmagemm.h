@@ -331,7 +331,7 @@ int tmagemm_ring_position(int64_t it, int64_t stages, int64_t* stage, int64_t* p
  * The GEMM launch configuration for (M, N, K) on a device with `num_sms` SMs,
  * of which `num_pairs` two-CTA clusters can be co-resident (0 = no pairs), and
  * a split request (1 = gemm_f16, 0 = automatic split-K, > 1 = that many
- * parts): written to out[0..12] in the order BM, BN, BK, STAGES, tiles, grid
+ * parts): written to out[0..13] in the order BM, BN, BK, STAGES, tiles, grid
  * (CTAs), threads, smem bytes, parts, k-blocks per part, work units, pair
  * (1 if CTA pairs; then tiles are 256 rows high), cluster split (0, or the
  * number of CTAs (pairs) per cluster that split K for gemm_f16; then parts
@@ -342,6 +342,39 @@ int tmagemm_ring_position(int64_t it, int64_t stages, int64_t* stage, int64_t* p
  */
 int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t num_pairs,
                       int64_t splits, int64_t* out);
+
+/*
+ * Host-buffer executor: GEMMs whose operands and results live in host memory.
+ * The paper pages have no counterpart; it is the end-to-end path of the
+ * library.  A step copies A_i (M x K) and B_i (N x K) host -> device, runs
+ * gemm_f16 (gemm_bf16 when created with bf16 = 1) and copies D_i (M x N)
+ * device -> host.  Three streams carry the three phases and `depth` device
+ * slots rotate, so the input copies of step i+1, the GEMM of step i and the
+ * result copy of step i-1 overlap; events order the phases of one slot.
+ * Every step moves all of its own bytes (one cudaMemcpyAsync per copy).
+ *   create     : allocates `depth` (1..16) slots of device memory for A, B
+ *                and D on the current device (the only device allocation the
+ *                library makes), three non-blocking streams and the events.
+ *                TMAGEMM_ERR_INVALID for bad sizes, TMAGEMM_ERR_CUDA if an
+ *                allocation fails.
+ *   run        : enqueues `steps` steps and returns without waiting; A_host,
+ *                B_host, D_host are arrays of `steps` host pointers (host
+ *                memory should be page-locked for the copies to overlap; the
+ *                caller keeps the buffers alive and unchanged until
+ *                synchronize returns).  Status as gemm_f16.
+ *   synchronize: waits for every enqueued step and reports a device-side
+ *                timeout like tmagemm_check.
+ *   destroy    : waits, then frees everything (NULL is a no-op).
+ * One object per thread at a time; the object is tied to the device that was
+ * current at create.
+ */
+typedef struct tmagemm_host_pipeline tmagemm_host_pipeline;
+int tmagemm_host_pipeline_create(int64_t M, int64_t N, int64_t K, int depth, int bf16,
+                                 tmagemm_host_pipeline** out);
+int tmagemm_host_pipeline_run(tmagemm_host_pipeline* p, int64_t steps, const void* const* A_host,
+                              const void* const* B_host, void* const* D_host);
+int tmagemm_host_pipeline_synchronize(tmagemm_host_pipeline* p);
+void tmagemm_host_pipeline_destroy(tmagemm_host_pipeline* p);
 
 #ifdef __cplusplus
 }

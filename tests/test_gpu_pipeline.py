@@ -38,3 +38,37 @@ def test_pipeline_matches_direct_calls(tg, depth):
         assert_bitexact(Ds[i].numpy(), ref.cpu().numpy(), f"step {i}")
     assert pipe.h2d_bytes_per_step() == 2 * (M * K + N * K)
     assert pipe.d2h_bytes_per_step() == 2 * M * N
+
+
+def test_pipeline_bf16_pageable_and_two_runs(tg):
+    """bf16 steps from pageable host memory, enqueued by two run() calls
+    before one synchronize: every step equals the direct call."""
+    from tma_pipelined_tensor_tn_gb300.pipeline import HostGemmPipeline
+    M, N, K = 256, 264, 520
+    g = torch.Generator().manual_seed(130)
+    As = [(torch.rand((M, K), generator=g) * 2 - 1).to(torch.bfloat16) for _ in range(5)]
+    Bs = [(torch.rand((N, K), generator=g) * 2 - 1).to(torch.bfloat16) for _ in range(5)]
+    Ds = [torch.empty((M, N), dtype=torch.bfloat16) for _ in range(5)]
+    pipe = HostGemmPipeline(M, N, K, dtype=torch.bfloat16, depth=2)
+    pipe.run(As[:2], Bs[:2], Ds[:2])
+    pipe.run(As[2:], Bs[2:], Ds[2:])
+    pipe.run([], [], [])
+    pipe.synchronize()
+    for i in range(5):
+        ref = tg.gemm(As[i].cuda(), Bs[i].cuda())
+        tg.check()
+        assert torch.equal(Ds[i], ref.cpu()), f"step {i}"
+    pipe.close()
+    pipe.close()   # idempotent
+
+
+def test_pipeline_rejects_bad_arguments(tg):
+    from tma_pipelined_tensor_tn_gb300.pipeline import HostGemmPipeline
+    pipe = HostGemmPipeline(64, 64, 64)
+    with pytest.raises(ValueError):
+        pipe.run([torch.zeros((64, 32), dtype=torch.float16)], [torch.zeros((64, 64), dtype=torch.float16)],
+                 [torch.zeros((64, 64), dtype=torch.float16)])
+    with pytest.raises(ValueError):
+        pipe.run([torch.zeros((64, 64), dtype=torch.float16).cuda()],
+                 [torch.zeros((64, 64), dtype=torch.float16)], [torch.zeros((64, 64), dtype=torch.float16)])
+    pipe.close()

@@ -39,6 +39,21 @@ def test_library_exports_every_header_symbol():
         assert n in tg.SIGNATURES, n
 
 
+def test_host_pipeline_argument_checks():
+    """Checked before any CUDA call: bad sizes and NULL handles are refused."""
+    import ctypes
+    L = tg.lib()
+    h = ctypes.c_void_p()
+    for args in [(0, 64, 64, 2, 0), (64, -1, 64, 2, 0), (64, 64, 64, 0, 0), (64, 64, 64, 17, 0),
+                 (64, 64, 64, 2, 2)]:
+        assert L.tmagemm_host_pipeline_create(*args, ctypes.byref(h)) == tg.TMAGEMM_ERR_INVALID
+        assert not h.value
+    assert L.tmagemm_host_pipeline_create(64, 64, 64, 2, 0, None) == tg.TMAGEMM_ERR_INVALID
+    assert L.tmagemm_host_pipeline_run(None, 1, None, None, None) == tg.TMAGEMM_ERR_INVALID
+    assert L.tmagemm_host_pipeline_synchronize(None) == tg.TMAGEMM_ERR_INVALID
+    L.tmagemm_host_pipeline_destroy(None)   # a no-op
+
+
 def test_strerror_covers_all_codes():
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert tg.strerror(code) and tg.strerror(code) != "unknown status"

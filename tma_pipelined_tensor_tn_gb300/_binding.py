@@ -50,6 +50,10 @@ SIGNATURES = {
     "tmagemm_set_small_m_route": ([_int], _int),
     "tmagemm_set_cluster_split": ([_int], _int),
     "tmagemm_set_group_m": ([_int], _int),
+    "tmagemm_host_pipeline_create": ([_i64, _i64, _i64, _int, _int, ctypes.POINTER(_p)], _int),
+    "tmagemm_host_pipeline_run": ([_p, _i64, _p, _p, _p], _int),
+    "tmagemm_host_pipeline_synchronize": ([_p], _int),
+    "tmagemm_host_pipeline_destroy": ([_p], None),
 }
 
 _lock = threading.Lock()

@@ -23,8 +23,8 @@
 // contiguous bytes of each row.
 //
 // Work split.  A CTA of 4 warps owns 64 weight rows (16 per warp, one MMA
-// row tile); the S CTAs of a thread-block cluster (S = 8) own the same
-// rows and split K into S slices.  Each CTA leaves its 64 x 8NT FP32 partial
+// row tile); the S CTAs of a thread-block cluster (S = 8, 4 or 2, so that
+// the grid stays one wave) own the same rows and split K into S slices.  Each CTA leaves its 64 x 8NT FP32 partial
 // tile in shared memory; after a cluster barrier each CTA finishes 64 / S of
 // the rows, adding the S partials in slice order through distributed shared
 // memory, rounding once to fp16 and writing D.  No workspace, one launch,
