@@ -266,11 +266,11 @@ int tmagemm_set_cta_pair(int mode);
 
 /*
  * Tuning/test override of the GEMM's tile width N: 256, 224 or 192 forces that
- * tile shape for every later gemm_f16 call in the process; 0 restores the
- * automatic choice (the width that minimises the number of tile rounds on
- * the device's SMs, weighted by tile cost).  Results are the same for every
- * width up to FP32 accumulation order.  Returns TMAGEMM_ERR_INVALID for other
- * values.
+ * tile shape for every later gemm_f16 call in the process (128 exists only for
+ * cluster splits, so it applies where one does); 0 restores the automatic
+ * choice (the width that minimises the number of tile rounds on the device's
+ * SMs, weighted by tile cost).  Results are the same for every width up to
+ * FP32 accumulation order.  Returns TMAGEMM_ERR_INVALID for other values.
  */
 int tmagemm_set_tile_n(int bn);
 
@@ -288,10 +288,11 @@ int tmagemm_set_group_m(int g);
  * Cluster split-K of gemm_f16 / gemm_bf16, process-wide: 0 = automatic (for
  * shapes whose output tiles fill at most half of the SMs, when the plan's cost
  * model prefers it, the CTAs of a 2-, 4- or 8-CTA cluster compute one
- * 128 x 256 tile over separate K ranges and add their FP32 accumulators
- * through distributed shared memory, in fixed order, before writing D: no
- * workspace, one launch), 1 = never, 2, 4 or 8 = that cluster size whenever
- * all tiles x that many CTAs fit in one wave.  Results agree up to FP32
+ * 128 x 256, 128 x 192 or 128 x 128 tile (or a 256 x 256 tile in CTA pairs)
+ * over separate K ranges and add their FP32 accumulators through distributed
+ * shared memory, in fixed order, before writing D: no workspace, one launch),
+ * 1 = never, 2, 4 or 8 = that cluster size whenever all tiles x that many
+ * CTAs fit in one wave.  Results agree up to FP32
  * accumulation order.  Returns TMAGEMM_ERR_INVALID for other values.
  */
 int tmagemm_set_cluster_split(int mode);
@@ -338,7 +339,9 @@ int tmagemm_ring_position(int64_t it, int64_t stages, int64_t* stage, int64_t* p
  * == that number), GROUP_M (tile rows per L2 group of the tile order).
  * `out` holds 14 values.  No GPU needed: cluster splits
  * assume ideal packing of clusters here, while gemm_f16 also checks how many
- * clusters the device can hold at once.
+ * clusters the device can hold at once.  num_sms == 0 asks instead for the
+ * plan gemm_f16 runs on the current device (its SMs, CTA pairs and cluster
+ * co-residency; num_pairs is then ignored and a CUDA device is required).
  */
 int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t num_pairs,
                       int64_t splits, int64_t* out);

@@ -117,3 +117,59 @@ def test_output_guard(tg):
     body = host[guard:guard + M * N]
     assert not np.any(body == sentinel)
     compare(body.view(np.float16).reshape(M, N), oracle.gemm_f16(A.numpy(), B.numpy()), "guarded")
+
+
+def forced_plan_and_gemm(tg, A, B, bn, ck):
+    """gemm_f16 with the tile width and the cluster split forced; returns the
+    device plan it ran and D."""
+    M, K = A.shape
+    N = B.shape[0]
+    try:
+        assert tg.tmagemm_set_tile_n(bn) == tg.TMAGEMM_OK
+        assert tg.tmagemm_set_cluster_split(ck) == tg.TMAGEMM_OK
+        p = tg.tmagemm_gemm_plan(M, N, K, 0)
+        D = tg.gemm(A.cuda(), B.cuda())
+        tg.check()
+    finally:
+        tg.tmagemm_set_cluster_split(0)
+        tg.tmagemm_set_tile_n(0)
+    return p, D.cpu().numpy()
+
+
+# The narrower cluster-split tiles (128 x 128 and 128 x 192) that a few rows
+# against a wide weight matrix get.  Shapes: ragged N (partial last tile), a
+# row count that is not a multiple of anything (two tile rows at M = 130), K
+# with an odd number of k-blocks or shorter than two k-blocks per CTA.
+@pytest.mark.parametrize("bn,ck", [(128, 4), (128, 8), (192, 2), (192, 4)])
+@pytest.mark.parametrize("M,N,K", [(40, 1032, 4160), (130, 776, 8200), (17, 1672, 1000)])
+def test_narrow_tiles_parity(tg, bn, ck, M, N, K):
+    A, B = inputs.gemm_inputs(M, N, K, seed=M + N + bn + ck)
+    p, D = forced_plan_and_gemm(tg, A, B, bn, ck)
+    assert (p["BN"], p["cluster_k"], p["pair"]) == (bn, ck, 0), p
+    compare(D, oracle.gemm_f16(A.numpy(), B.numpy()), f"cluster split {bn}x{ck} {M}x{N}x{K}")
+
+
+@pytest.mark.parametrize("bn,ck", [(128, 4), (128, 8), (192, 2), (192, 4)])
+def test_narrow_tiles_integer_bitexact(tg, bn, ck):
+    M, N, K = 64, 1032, 4160
+    A = inputs.integer_f16((M, K), seed=65)
+    B = inputs.integer_f16((N, K), seed=66)
+    p, D = forced_plan_and_gemm(tg, A, B, bn, ck)
+    assert (p["BN"], p["cluster_k"]) == (bn, ck), p
+    assert_bitexact(D, oracle.gemm_f16(A.numpy(), B.numpy()), f"cluster split {bn}x{ck} integer")
+
+
+@pytest.mark.parametrize("M,N,K", [(32, 4096, 14336), (64, 14336, 4096)])
+def test_decode_shapes_fill_the_sms(tg, M, N, K):
+    """The automatic plan for a few tokens against a Llama-3-8B-sized weight
+    splits K over clusters and keeps at least 80 % of the SMs streaming the
+    weights; D matches the oracle on sampled rows."""
+    p = tg.tmagemm_gemm_plan(M, N, K, 0)
+    assert p["cluster_k"] in (2, 4, 8) and p["grid"] >= 0.8 * sms(), p
+    g = torch.Generator().manual_seed(M + N)
+    X = (torch.randn((M, K), generator=g) * 0.02).half()
+    W = (torch.randn((N, K), generator=g) * 0.02).half()
+    D = tg.gemm(X.cuda(), W.cuda()).cpu().numpy()
+    tg.check()
+    rows = np.arange(0, N, 97)
+    compare(D[:, rows], oracle.gemm_f16(X.numpy(), W.numpy()[rows]), f"decode {M}x{N}x{K}")

@@ -287,6 +287,34 @@ def test_cluster_split_override():
         assert tg.tmagemm_set_cluster_split(0) == tg.TMAGEMM_OK
 
 
+def test_narrow_cluster_split_plans():
+    """A few rows against a wide weight matrix: the narrower cluster-split
+    tiles put more CTAs on the weight stream (14336 columns: 75 tiles of 192
+    x 2 = 150 CTAs instead of 56 tiles of 256 x 2 = 112)."""
+    p = tg.tmagemm_gemm_plan(32, 14336, 4096, 152, 1, 76)
+    assert (p["cluster_k"], p["BN"], p["pair"], p["tiles"], p["grid"]) == (2, 192, 0, 75, 150)
+    try:
+        assert tg.tmagemm_set_tile_n(128) == tg.TMAGEMM_OK
+        assert tg.tmagemm_set_cluster_split(4) == tg.TMAGEMM_OK
+        p = tg.tmagemm_gemm_plan(32, 4096, 14336, 152, 1, 76)
+        assert (p["cluster_k"], p["BN"], p["tiles"], p["grid"], p["kb_per_unit"]) == (4, 128, 32, 128, 56)
+        # 128 only exists for cluster splits: a plain plan keeps its width
+        assert tg.tmagemm_set_cluster_split(1) == tg.TMAGEMM_OK
+        assert tg.tmagemm_gemm_plan(4096, 4096, 4096, 152)["BN"] != 128
+    finally:
+        assert tg.tmagemm_set_cluster_split(0) == tg.TMAGEMM_OK
+        assert tg.tmagemm_set_tile_n(0) == tg.TMAGEMM_OK
+
+
+def test_device_plan_needs_a_device():
+    """num_sms == 0 asks for the current device's plan: an error without one."""
+    torch = pytest.importorskip("torch")
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    with pytest.raises(tg.TmaGemmError):
+        tg.tmagemm_gemm_plan(32, 4096, 14336, 0)
+
+
 def test_tile_width_override():
     try:
         assert tg.tmagemm_set_tile_n(256) == tg.TMAGEMM_OK
@@ -294,6 +322,7 @@ def test_tile_width_override():
         assert tg.tmagemm_set_tile_n(192) == tg.TMAGEMM_OK
         assert tg.tmagemm_gemm_plan(4096, 4096, 4096, 152)["BN"] == 192
         assert tg.tmagemm_set_tile_n(100) == tg.TMAGEMM_ERR_INVALID
+        assert tg.tmagemm_set_tile_n(64) == tg.TMAGEMM_ERR_INVALID
     finally:
         assert tg.tmagemm_set_tile_n(0) == tg.TMAGEMM_OK
     assert tg.tmagemm_gemm_plan(4096, 4096, 4096, 152)["BN"] == 224

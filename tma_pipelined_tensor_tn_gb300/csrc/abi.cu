@@ -193,7 +193,7 @@ enum class SmallMKernel { kSwapAB, kFragments, kLsu, kTile };
 // kernel is fastest (4096 x 14336, M = 8: 21.4 us; swap-AB 26.1, LSU-fed 25.6,
 // tile kernel 30.0); above that the tile kernel with its cluster split of K is
 // the fastest or within 7 % of it everywhere (14336 x 4096, M = 17..64:
-// 26.0-28.4 us; swap-AB 29.2-30.4, LSU-fed 48.8-88.6).
+// 24.0-25.9 us; swap-AB 29.2-30.4, LSU-fed 48.8-88.6).
 static SmallMKernel small_m_kernel(int64_t M) {
     const int route = __atomic_load_n(&g_small_m_route, __ATOMIC_ACQUIRE);
     if (route == 1) return SmallMKernel::kSwapAB;
@@ -228,8 +228,8 @@ static int small_m_no_workspace(SmallMKernel k, int64_t M, int64_t N, int64_t K,
 // returns true with its status in *status; false if the tile kernel should
 // run.  Above 16 rows the tile kernel, with its cluster split of K for
 // few-tile shapes, measured faster on GB300 than the workspace-free small-M
-// kernels: N = 4096, K = 14336, M = 33..64: 33-34 us against 39-48 us;
-// N = 14336, K = 4096, M = 17..64: 26-28 us against 49-89 us.
+// kernels: N = 4096, K = 14336, M = 17..64: 25.5-26.9 us against 39-48 us;
+// N = 14336, K = 4096, M = 17..64: 24-26 us against 49-89 us.
 static bool few_rows(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
                      void* stream, bool bf16, int* status) {
     if (M > 64) return false;
@@ -465,7 +465,7 @@ int tmagemm_set_cta_pair(int mode) {
 }
 
 int tmagemm_set_tile_n(int bn) {
-    if (bn != 0 && bn != 256 && bn != 224 && bn != 192) return TMAGEMM_ERR_INVALID;
+    if (bn != 0 && bn != 256 && bn != 224 && bn != 192 && bn != 128) return TMAGEMM_ERR_INVALID;
     __atomic_store_n(&g_force_tile_n, bn, __ATOMIC_RELEASE);
     return TMAGEMM_OK;
 }
@@ -515,12 +515,20 @@ int tmagemm_ring_position(int64_t it, int64_t stages, int64_t* stage, int64_t* p
 
 int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t num_pairs,
                       int64_t splits, int64_t* out) {
-    if (!out || num_sms <= 0 || num_pairs < 0 || num_pairs > num_sms / 2 || splits < 0 ||
+    if (!out || num_sms < 0 || num_pairs < 0 || num_pairs > num_sms / 2 || splits < 0 ||
         splits > 4096)
         return TMAGEMM_ERR_INVALID;
     if (int s = validate_common(M, N, K)) return s;
-    const GemmPlan p = plan_gemm(M, N, K, static_cast<int>(num_sms), splits, false,
-                                 static_cast<int>(num_pairs));
+    GemmPlan p;
+    if (num_sms == 0) {
+        // The plan gemm_f16 runs on the current device.
+        DeviceState* d = nullptr;
+        if (int s = device_state(&d)) return s;
+        p = plan_gemm(M, N, K, d->sms, splits, false, d->pairs, d->caps);
+    } else {
+        p = plan_gemm(M, N, K, static_cast<int>(num_sms), splits, false,
+                      static_cast<int>(num_pairs));
+    }
     out[0] = p.bm;
     out[1] = p.bn;
     out[2] = p.bk;

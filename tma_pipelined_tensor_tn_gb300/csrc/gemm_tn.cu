@@ -150,6 +150,12 @@ template <bool T> using CfgP192 = Cfg<192, 64, 6, false, T, 512, 1, true>;
 // CTA pairs (CK pairs, 2 CK CTAs per cluster; ranks 2p and 2p + 1 form pair p).
 template <bool T, int CK> using CfgCK256 = Cfg<256, 64, 4, false, T, 512, 1, false, CK>;
 template <bool T, int CK> using CfgPCK256 = Cfg<256, 64, 6, false, T, 512, 1, true, CK>;
+// Narrower cluster-split tiles for outputs with only a few tile rows (a few
+// tokens against a wide weight matrix): more tiles, so more CTAs stream the
+// weights at once within the device's cluster co-residency (GB300 holds 15
+// clusters of 8 CTAs at ~200 KB each, 36 of 4, 76 of 2), with deeper rings.
+template <bool T, int CK> using CfgCK128 = Cfg<128, 64, 6, false, T, 256, 1, false, CK>;
+template <bool T, int CK> using CfgCK192 = Cfg<192, 64, 5, false, T, 512, 1, false, CK>;
 
 // Two CTAs per SM (each with half the ring and 128 TMEM columns) keep two
 // independent weight streams per SM in flight.
@@ -898,9 +904,10 @@ GemmPlan plan_cluster_split(int64_t M, int64_t N, int64_t K, int64_t slots, int 
 template <bool T>
 GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs, int64_t splits,
                     const ClusterCaps& caps) {
-    GemmPlan cands[11];
+    GemmPlan cands[15];
     int n = 0;
     const int pair_mode = __atomic_load_n(&g_pair_mode, __ATOMIC_ACQUIRE);
+    const int forced = __atomic_load_n(&g_force_tile_n, __ATOMIC_ACQUIRE);
     const bool pairs_ok = splits == 1 && pairs > 0 && pair_mode != 1;
     const bool singles_ok = !(pairs_ok && pair_mode == 2);
     if (splits == 1) {
@@ -918,17 +925,25 @@ GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs,
         const int ck_mode = __atomic_load_n(&g_cluster_split, __ATOMIC_ACQUIRE);
         if (ck_mode != 1) {
             const bool pk = pairs > 0 && pair_mode != 1;
-            GemmPlan ck[5] = {
+            // The narrower single-CTA tiles take the co-residency measured for
+            // the 256-wide ones: all need one CTA per SM, so a cluster of CK
+            // CTAs packs the same way.
+            GemmPlan ck[9] = {
                 plan_cluster_split<CfgCK256<T, 2>>(M, N, K, sms, caps.single_ck[0]),
                 plan_cluster_split<CfgCK256<T, 4>>(M, N, K, sms, caps.single_ck[1]),
                 plan_cluster_split<CfgCK256<T, 8>>(M, N, K, sms, caps.single_ck[2]),
                 plan_cluster_split<CfgPCK256<T, 2>>(M, N, K, pairs, caps.pair_ck[0]),
-                plan_cluster_split<CfgPCK256<T, 4>>(M, N, K, pairs, caps.pair_ck[1])};
+                plan_cluster_split<CfgPCK256<T, 4>>(M, N, K, pairs, caps.pair_ck[1]),
+                plan_cluster_split<CfgCK192<T, 2>>(M, N, K, sms, caps.single_ck[0]),
+                plan_cluster_split<CfgCK192<T, 4>>(M, N, K, sms, caps.single_ck[1]),
+                plan_cluster_split<CfgCK128<T, 4>>(M, N, K, sms, caps.single_ck[1]),
+                plan_cluster_split<CfgCK128<T, 8>>(M, N, K, sms, caps.single_ck[2])};
             if (!pk) ck[3].units = ck[4].units = 0;
-            if (pair_mode == 2) ck[0].units = ck[1].units = ck[2].units = 0;
+            if (pair_mode == 2)
+                for (int i : {0, 1, 2, 5, 6, 7, 8}) ck[i].units = 0;
             bool forced_ck = false;
             for (const GemmPlan& c : ck)
-                if (c.units > 0 && ck_mode == c.cluster_k &&
+                if (c.units > 0 && ck_mode == c.cluster_k && (forced == 0 || c.bn == forced) &&
                     (!forced_ck || plan_cost(c) < plan_cost(cands[0]))) {
                     cands[0] = c;   // a forced split size that applies
                     n = 1;
@@ -943,7 +958,6 @@ GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs,
         cands[n++] = plan_for<Cfg224F<T>>(M, N, K, sms, splits);
         cands[n++] = plan_for<Cfg192F<T>>(M, N, K, sms, splits);
     }
-    const int forced = __atomic_load_n(&g_force_tile_n, __ATOMIC_ACQUIRE);
     GemmPlan best = cands[0];
     bool have = false;
     for (int i = 0; i < n; ++i) {
@@ -968,10 +982,14 @@ cudaError_t launch_typed(const GemmPlan& plan, const CUtensorMap& tmA, const CUt
         }
     }
     if (plan.cluster_k > 0) {
-        switch (plan.cluster_k) {
-            case 2: return launch_cfg<CfgCK256<T, 2>>(plan, tmA, tmB, tmD, args, stream);
-            case 4: return launch_cfg<CfgCK256<T, 4>>(plan, tmA, tmB, tmD, args, stream);
-            case 8: return launch_cfg<CfgCK256<T, 8>>(plan, tmA, tmB, tmD, args, stream);
+        switch (plan.bn * 16 + plan.cluster_k) {
+            case 256 * 16 + 2: return launch_cfg<CfgCK256<T, 2>>(plan, tmA, tmB, tmD, args, stream);
+            case 256 * 16 + 4: return launch_cfg<CfgCK256<T, 4>>(plan, tmA, tmB, tmD, args, stream);
+            case 256 * 16 + 8: return launch_cfg<CfgCK256<T, 8>>(plan, tmA, tmB, tmD, args, stream);
+            case 192 * 16 + 2: return launch_cfg<CfgCK192<T, 2>>(plan, tmA, tmB, tmD, args, stream);
+            case 192 * 16 + 4: return launch_cfg<CfgCK192<T, 4>>(plan, tmA, tmB, tmD, args, stream);
+            case 128 * 16 + 4: return launch_cfg<CfgCK128<T, 4>>(plan, tmA, tmB, tmD, args, stream);
+            case 128 * 16 + 8: return launch_cfg<CfgCK128<T, 8>>(plan, tmA, tmB, tmD, args, stream);
             default: return cudaErrorInvalidValue;
         }
     }
