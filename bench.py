@@ -649,7 +649,8 @@ def measure_extras(tg, dev, stream, l2):
 # (one draw of a Dirichlet(0.7) routing, stored so every run times the same shapes).
 GROUPED_COUNTS = [1697, 2233, 321, 376, 105, 1822, 706, 932]
 
-CASES = ("gemm4096", "gemv", "splitk", "small_m8", "small_m16", "grouped", "bf16_gemm", "bf16_gemv",
+CASES = ("gemm4096", "gemv", "splitk", "small_m8", "small_m16", "small_m32", "small_m64", "grouped",
+         "bf16_gemm", "bf16_gemv",
          "gemm8192", "gemm_ragged", "gemm256")
 
 
@@ -684,7 +685,7 @@ def run_case(args, name):
         else:
             fn = lambda: tg.gemm_f16(M, N, K, a.data_ptr(), b.data_ptr(), d.data_ptr(), sh)
         unit = ("TFLOP/s", fl / 1e12)
-    elif name in ("gemv", "bf16_gemv", "small_m8", "small_m16"):
+    elif name in ("gemv", "bf16_gemv", "small_m8", "small_m16", "small_m32", "small_m64"):
         x, W = inputs.gemv_inputs(GEMV_N, GEMV_K, seed=0)
         if name == "bf16_gemv":
             x, W = x.to(torch.bfloat16), W.to(torch.bfloat16)
