@@ -904,6 +904,7 @@ GemmPlan plan_cluster_split(int64_t M, int64_t N, int64_t K, int64_t slots, int 
 template <bool T>
 GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs, int64_t splits,
                     const ClusterCaps& caps) {
+    // 3 single-CTA and 3 pair tile plans, up to 9 cluster splits.
     GemmPlan cands[15];
     int n = 0;
     const int pair_mode = __atomic_load_n(&g_pair_mode, __ATOMIC_ACQUIRE);
@@ -938,6 +939,8 @@ GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs,
                 plan_cluster_split<CfgCK192<T, 4>>(M, N, K, sms, caps.single_ck[1]),
                 plan_cluster_split<CfgCK128<T, 4>>(M, N, K, sms, caps.single_ck[1]),
                 plan_cluster_split<CfgCK128<T, 8>>(M, N, K, sms, caps.single_ck[2])};
+            static_assert(sizeof(ck) / sizeof(ck[0]) + 6 <= sizeof(cands) / sizeof(cands[0]),
+                          "every candidate fits");
             if (!pk) ck[3].units = ck[4].units = 0;
             if (pair_mode == 2)
                 for (int i : {0, 1, 2, 5, 6, 7, 8}) ck[i].units = 0;
