@@ -144,3 +144,25 @@ def test_gemm_bf16_lsu_forced(tg, M):
     finally:
         tg.tmagemm_set_small_m_route(0)
     compare_bf16(got, oracle.gemm_bf16(to_bits(A), to_bits(B)), f"bf16 LSU-fed M={M}")
+
+
+@pytest.mark.parametrize("bn,ck", [(128, 4), (128, 8), (192, 2), (192, 4)])
+def test_gemm_bf16_narrow_cluster_split(tg, bn, ck):
+    """The bf16 forms of the 128- and 192-wide cluster-split tiles (forced):
+    integer inputs bit for bit, uniform inputs within the bf16 rule."""
+    M, N, K = 40, 1032, 4160
+    Ai = inputs.integer_f16((M, K), seed=730 + bn + ck).to(torch.bfloat16)
+    Bi = inputs.integer_f16((N, K), seed=731 + bn + ck).to(torch.bfloat16)
+    Au, Bu = uniform_bf16((M, K), 732 + bn + ck), uniform_bf16((N, K), 733 + bn + ck)
+    try:
+        assert tg.tmagemm_set_tile_n(bn) == tg.TMAGEMM_OK
+        assert tg.tmagemm_set_cluster_split(ck) == tg.TMAGEMM_OK
+        p = tg.tmagemm_gemm_plan(M, N, K, 0)
+        got_i, got_u = run(tg, Ai, Bi), run(tg, Au, Bu)
+    finally:
+        tg.tmagemm_set_cluster_split(0)
+        tg.tmagemm_set_tile_n(0)
+    assert (p["BN"], p["cluster_k"]) == (bn, ck), p
+    ref_i = oracle.gemm_bf16(to_bits(Ai), to_bits(Bi))
+    assert np.array_equal(np.ascontiguousarray(got_i).view(np.uint16), ref_i), (bn, ck)
+    compare_bf16(got_u, oracle.gemm_bf16(to_bits(Au), to_bits(Bu)), f"bf16 split {bn}x{ck}")
