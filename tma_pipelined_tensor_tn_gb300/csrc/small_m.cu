@@ -6,10 +6,11 @@
 // The decode step reads each weight once ("Learning TileLang with GEMV", §01
 // GEMV, §02 Bandwidth Bound), so the weight stream sets the time.  Per-thread
 // 16-byte loads with enough of them in flight keep HBM busier on this part
-// than a TMA-fed shared-memory ring (the tcgen05 swap-AB kernel levels off
-// near 4 TB/s).  The arithmetic, 2 M flops per weight byte, still wants
-// tensor cores: mma.sync m16n8k16 (FP16 in, FP32 accumulate) takes its
-// operands from registers, which is what lets the weights skip shared memory.
+// than the TMA-fed tcgen05 kernels do at these sizes (the swap-AB kernel
+// streams at about 4 TB/s).  The arithmetic, 2 M flops per weight byte,
+// still wants tensor cores: mma.sync m16n8k16 (FP16 in, FP32 accumulate)
+// takes its operands from registers, which is what lets the weights skip
+// shared memory.
 //
 // Fragment layout.  In m16n8k16 a thread with groupID g = lane / 4 and
 // t = lane % 4 holds A(row g and g + 8; k slots 2t, 2t+1, 2t+8, 2t+9) and

@@ -5,7 +5,7 @@
 // The decode step reads each weight once ("Learning TileLang with GEMV", §01
 // GEMV, §02 Bandwidth Bound), so the weight stream sets the time.  On GB300
 // per-thread 16-byte loads with enough of them in flight stream HBM faster
-// than a TMA-fed shared-memory ring, which levels off near 4 TB/s.  This
+// than the TMA-fed swap-AB kernel does (about 4 TB/s).  This
 // kernel keeps the tensor-core path (tcgen05.mma from shared-memory
 // descriptors, FP32 accumulator in TMEM) and moves only the weight operand
 // off TMA.
