@@ -379,8 +379,10 @@ def run_ours(args, rank, world, local_rank):
     # back to pinned host memory; the three phases run on their own streams so
     # step i+1's inputs travel while step i computes.  Timed on the host clock
     # from the call to the return of synchronize (what a caller waits).
+    # Up to 32 steps: the first step's upload and the last one's download do
+    # not overlap anything, so short runs understate the steady state.
     from tma_pipelined_tensor_tn_gb300.pipeline import HostGemmPipeline
-    e2e_steps = max(4, min(args.steps, 12))
+    e2e_steps = max(4, min(args.steps, 32))
     pipe = HostGemmPipeline(GEMM_M, GEMM_N, GEMM_K, torch.float16, depth=2, device=dev)
     hA = A.pin_memory()
     hB = B.pin_memory()
@@ -388,11 +390,14 @@ def run_ours(args, rank, world, local_rank):
     pipe.run([hA] * 2, [hB] * 2, hDs)        # warm-up of the copy path
     pipe.synchronize()
     torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
     t0 = time.perf_counter()
     pipe.run([hA] * e2e_steps, [hB] * e2e_steps, [hDs[i % 2] for i in range(e2e_steps)])
     pipe.synchronize()
     e2e_ms = (time.perf_counter() - t0) * 1e3
     pipe.close()
+    e2e_ms = max_over_ranks([e2e_ms], device=dev)[0]
     tg.check(stream)
 
     extras = measure_extras(tg, dev, stream, l2)
