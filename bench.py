@@ -565,11 +565,18 @@ def measure_extras(tg, dev, stream, l2):
 
         t_s = _time_launches(small, 100, stream)
         tg.check(stream)
+        Dc = torch.empty_like(Ds)
+
+        def small_cublas(i, Dc=Dc):   # context only: cuBLAS on the same inputs
+            torch.matmul(xsets[i % rv], wsets[i % rv].T, out=Dc)
+
+        t_c = _time_launches(small_cublas, 100, stream)
         by = 2.0 * (GEMV_N * GEMV_K + Ms * GEMV_K + Ms * GEMV_N)
         out[f"small_m{Ms}_4096x14336"] = {"us": t_s, "gbs": by / t_s / 1e3,
                                           "tflops": 2.0 * Ms * GEMV_N * GEMV_K / t_s / 1e6,
                                           "kernel": ("mma.sync register fragments" if Ms <= 16
-                                                     else "tcgen05 tile kernel, cluster split-K")}
+                                                     else "tcgen05 tile kernel, cluster split-K"),
+                                          "cublas_us": t_c}
 
     # Grouped GEMM: 8 experts, 8192 routed tokens (skewed counts), N=4096, K=2048,
     # against one dense GEMM over the same 8192 rows.
@@ -635,13 +642,15 @@ def measure_extras(tg, dev, stream, l2):
                                      "cublas_fp16_8192": (8192, 8192, 8192, 5)}.items():
         csets = [inputs.gemm_inputs(Mc, Nc, Kc, seed=20 + j) for j in range(3 if Mc < 8192 else 1)]
         csets = [(a.to(dev), b.to(dev)) for a, b in csets]
-        def cublas(i, csets=csets):
+        dc = torch.empty((Mc, Nc), dtype=torch.float16, device=dev)
+
+        def cublas(i, csets=csets, dc=dc):
             a, b = csets[i % len(csets)]
-            torch.matmul(a, b.T)
+            torch.matmul(a, b.T, out=dc)
 
         t_c = _time_launches(cublas, reps, stream)
         out[name] = {"us": t_c, "tflops": gemm_flops(Mc, Nc, Kc) / t_c / 1e6,
-                     "what": "torch.matmul(A, B.T), cuBLAS, for comparison only"}
+                     "what": "torch.matmul(A, B.T, out=D), cuBLAS, for comparison only"}
         del csets
 
     out["grouped_8x(8192_tokens)x4096x2048"] = {

@@ -586,48 +586,67 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
     }
 
     if constexpr (C::kClusterK != 0) {
-        // Every CTA's partial tile is complete and visible cluster-wide; CTA q
-        // finishes rows [q * 128 / CK, (q + 1) * 128 / CK) of the tile: 8
-        // columns per step, the CK partials loaded together and added in
-        // slice order (deterministic), one 16-byte store of D.
+        // Every CTA's partial tile is complete and visible cluster-wide.  The
+        // outputs of the tile that exist (rows below M, 8-column groups left of
+        // N) are dealt out evenly over the CK CTAs (a pair's halves reduce
+        // separately: CTA (pair p, half h) adds the partials of ranks 2q + h),
+        // so with a few rows every CTA of the cluster still takes a share.
+        // Each 8-column group: the CK partials loaded together and added in
+        // slice order (deterministic), one 16-byte store of D; kItems groups
+        // per thread have their loads in flight at once.
         tc_fence_before();
         cluster_sync();
-        // A pair's halves reduce separately: CTA (pair p, half h) adds the
-        // partials of ranks 2q + h.
-        constexpr int kRows = C::BM / C::kClusterK;
         constexpr int kGroups = C::BN / 8;
+        constexpr int kItems = C::kClusterK <= 4 ? 2 : 1;
         constexpr uint32_t kPeerStride = C::kPair ? 2u : 1u;
         const UnitInfo ui = prob.unit(unit0, C::kTileM, C::BN, C::kGroupM);
         uint16_t* dout = static_cast<uint16_t*>(prob.d_out);
-        for (int f = static_cast<int>(threadIdx.x); f < kRows * kGroups; f += C::kThreads) {
-            const int rl = static_cast<int>(ck_rank) * kRows + f / kGroups;
-            const int g = f % kGroups;
-            const int32_t m = ui.a_row + static_cast<int32_t>(rank) * C::BM + rl;
-            const int32_t n = ui.b_row + 8 * g;
-            if (m >= prob.w.M || n >= prob.w.N) continue;
-            const uint32_t local = sbase + C::kOffA + (rl * C::kPartStride + 8u * g) * 4u;
-            float lo[C::kClusterK][4], hi[C::kClusterK][4];
+        const int32_t m0 = ui.a_row + static_cast<int32_t>(rank) * C::BM;
+        const int rows = max(0, min(C::BM, prob.w.M - m0));
+        // (N is a multiple of 8, so a group is either whole or outside.)
+        const int groups = max(0, min(kGroups, (prob.w.N - ui.b_row + 7) / 8));
+        const int total = rows * groups;
+        const int f_begin = static_cast<int>(ck_rank) * total / C::kClusterK;
+        const int f_end = (static_cast<int>(ck_rank) + 1) * total / C::kClusterK;
+        for (int f0 = f_begin + static_cast<int>(threadIdx.x); f0 < f_end;
+             f0 += kItems * C::kThreads) {
+            float lo[kItems][C::kClusterK][4], hi[kItems][C::kClusterK][4];
 #pragma unroll
-            for (int q = 0; q < C::kClusterK; ++q) {
-                const uint32_t peer = kPeerStride * static_cast<uint32_t>(q) + rank;
-                ld_shared_cluster_v4(map_to_rank(local, peer), lo[q]);
-                ld_shared_cluster_v4(map_to_rank(local + 16u, peer), hi[q]);
-            }
-            float a[8] = {lo[0][0], lo[0][1], lo[0][2], lo[0][3], hi[0][0], hi[0][1], hi[0][2], hi[0][3]};
+            for (int it = 0; it < kItems; ++it) {
+                const int f = f0 + it * C::kThreads;
+                if (f >= f_end) break;
+                const int rl = f / groups, g = f % groups;
+                const uint32_t local = sbase + C::kOffA + (rl * C::kPartStride + 8u * g) * 4u;
 #pragma unroll
-            for (int q = 1; q < C::kClusterK; ++q) {
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    a[e] += lo[q][e];
-                    a[4 + e] += hi[q][e];
+                for (int q = 0; q < C::kClusterK; ++q) {
+                    const uint32_t peer = kPeerStride * static_cast<uint32_t>(q) + rank;
+                    ld_shared_cluster_v4(map_to_rank(local, peer), lo[it][q]);
+                    ld_shared_cluster_v4(map_to_rank(local + 16u, peer), hi[it][q]);
                 }
             }
-            uint4 o;
-            o.x = pack2_rn<C::kBF16>(__float_as_uint(a[0]), __float_as_uint(a[1]));
-            o.y = pack2_rn<C::kBF16>(__float_as_uint(a[2]), __float_as_uint(a[3]));
-            o.z = pack2_rn<C::kBF16>(__float_as_uint(a[4]), __float_as_uint(a[5]));
-            o.w = pack2_rn<C::kBF16>(__float_as_uint(a[6]), __float_as_uint(a[7]));
-            *reinterpret_cast<uint4*>(dout + static_cast<int64_t>(m) * prob.w.N + n) = o;
+#pragma unroll
+            for (int it = 0; it < kItems; ++it) {
+                const int f = f0 + it * C::kThreads;
+                if (f >= f_end) break;
+                const int rl = f / groups, g = f % groups;
+                float a[8] = {lo[it][0][0], lo[it][0][1], lo[it][0][2], lo[it][0][3],
+                              hi[it][0][0], hi[it][0][1], hi[it][0][2], hi[it][0][3]};
+#pragma unroll
+                for (int q = 1; q < C::kClusterK; ++q) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        a[e] += lo[it][q][e];
+                        a[4 + e] += hi[it][q][e];
+                    }
+                }
+                uint4 o;
+                o.x = pack2_rn<C::kBF16>(__float_as_uint(a[0]), __float_as_uint(a[1]));
+                o.y = pack2_rn<C::kBF16>(__float_as_uint(a[2]), __float_as_uint(a[3]));
+                o.z = pack2_rn<C::kBF16>(__float_as_uint(a[4]), __float_as_uint(a[5]));
+                o.w = pack2_rn<C::kBF16>(__float_as_uint(a[6]), __float_as_uint(a[7]));
+                const int32_t m = m0 + rl, n = ui.b_row + 8 * g;
+                *reinterpret_cast<uint4*>(dout + static_cast<int64_t>(m) * prob.w.N + n) = o;
+            }
         }
         cluster_sync();   // peers' shared memory stays alive until every CTA has read it
     }
