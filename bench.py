@@ -401,6 +401,7 @@ def run_ours(args, rank, world, local_rank):
     tg.check(stream)
 
     extras = measure_extras(tg, dev, stream, l2)
+    extras.update(measure_distributions(tg, dev, stream, l2))
 
     peaks, peak_src = load_peaks()
     gemm_avg_s = gemm_total_ms / 1e3 / args.steps
@@ -469,6 +470,70 @@ def _time_launches(fn, reps, stream):
     e1.record(stream)
     torch.cuda.synchronize()
     return e0.elapsed_time(e1) * 1e3 / reps
+
+
+def _launch_distribution(fn, reps, stream):
+    """Per-launch device times of `fn` (an event pair around every launch,
+    which also keeps consecutive launches from overlapping): min, median and
+    90th percentile in microseconds."""
+    import torch
+    for _ in range(3):
+        fn(0)
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(reps)]
+    torch.cuda.synchronize()
+    for i, (e0, e1) in enumerate(evs):
+        e0.record(stream)
+        fn(i)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    t = sorted(e0.elapsed_time(e1) * 1e3 for e0, e1 in evs)
+    return {"min_us": t[0], "median_us": statistics.median(t),
+            "p90_us": t[min(len(t) - 1, int(0.9 * len(t)))], "launches": reps}
+
+
+def measure_distributions(tg, dev, stream, l2):
+    """Per-launch statistics of the two headline kernels over 100 launches
+    each: the 4096^3 GEMM and the GEMV on inputs rotated past L2 (cold), and
+    the GEMV once more on one weight set that stays in L2 between launches
+    (warm, labelled as such)."""
+    import torch
+    from tma_pipelined_tensor_tn_gb300 import inputs
+    sh = stream.cuda_stream
+    out = {}
+    A, B = inputs.gemm_inputs(GEMM_M, GEMM_N, GEMM_K, seed=0)
+    n_g = inputs.l2_rotation_count(2 * (GEMM_M * GEMM_K + GEMM_N * GEMM_K), l2)
+    gsets = [(A.to(dev), B.to(dev))]
+    gsets += [(gsets[0][0].clone(), gsets[0][1].clone()) for _ in range(n_g - 1)]
+    D = torch.empty((GEMM_M, GEMM_N), dtype=torch.float16, device=dev)
+
+    def gemm(i):
+        a, b = gsets[i % n_g]
+        assert tg.gemm_f16(GEMM_M, GEMM_N, GEMM_K, a.data_ptr(), b.data_ptr(), D.data_ptr(), sh) == 0
+
+    dist = _launch_distribution(gemm, 100, stream)
+    dist["tflops_at_median"] = gemm_flops() / dist["median_us"] / 1e6
+    out["gemm_4096_per_launch"] = dist
+    del gsets
+    x, W = inputs.gemv_inputs(GEMV_N, GEMV_K, seed=0)
+    n_v = inputs.l2_rotation_count(gemv_bytes(), l2)
+    vsets = [(x.to(dev), W.to(dev))]
+    vsets += [(vsets[0][0].clone(), vsets[0][1].clone()) for _ in range(n_v - 1)]
+    y = torch.empty((GEMV_N,), dtype=torch.float16, device=dev)
+
+    def gemv(i, sets=vsets):
+        xv, wv = sets[i % len(sets)]
+        assert tg.gemv_f16(GEMV_N, GEMV_K, xv.data_ptr(), wv.data_ptr(), y.data_ptr(), sh) == 0
+
+    dist = _launch_distribution(gemv, 100, stream)
+    dist["gbs_at_median"] = gemv_bytes() / dist["median_us"] / 1e3
+    out["gemv_4096x14336_per_launch_cold"] = dist
+    dist = _launch_distribution(lambda i: gemv(i, vsets[:1]), 100, stream)
+    dist["gbs_at_median"] = gemv_bytes() / dist["median_us"] / 1e3
+    dist["note"] = "warm L2: the same 117 MB weight set every launch"
+    out["gemv_4096x14336_per_launch_warm_l2"] = dist
+    tg.check(stream)
+    return out
 
 
 def measure_extras(tg, dev, stream, l2):
