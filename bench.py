@@ -245,6 +245,57 @@ def cpu_baseline(target_s=12.0):
                       f"({rows}x4096x4096 FP64 MACs, {dt:.1f} s)"}
 
 
+def cpu_model():
+    """The host CPU's model name, from /proc/cpuinfo or lscpu (empty if neither)."""
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return ""
+
+
+def oracle_per_config():
+    """The oracle's wall time on each workload configuration: 256^3 and the
+    GEMV in full on one core and on all cores, the ragged 4000x3000x4160 GEMM
+    in full on all cores, and 8192^3 on its first 256 rows (scaled to the
+    whole GEMM), with the core count and CPU model."""
+    import oracle
+    from tma_pipelined_tensor_tn_gb300 import inputs
+    oracle.build()
+    out = {"cores": oracle.max_threads(), "cpu_model": cpu_model()}
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        fn()
+        return time.perf_counter() - t0
+
+    A, B = inputs.gemm_inputs(256, 256, 256, seed=0)
+    a, b = A.numpy(), B.numpy()
+    for th, key in ((1, "gemm_256_1core_s"), (0, "gemm_256_all_cores_s")):
+        out[key] = timed(lambda: oracle.gemm_f16(a, b, threads=th))
+    x, W = inputs.gemv_inputs(GEMV_N, GEMV_K, seed=0)
+    xv, wv = x.numpy(), W.numpy()
+    for th, key in ((1, "gemv_1core_s"), (0, "gemv_all_cores_s")):
+        out[key] = timed(lambda: oracle.gemv_f16(xv, wv, threads=th))
+    A, B = inputs.gemm_inputs(4000, 3000, 4160, seed=0)
+    a, b = A.numpy(), B.numpy()
+    out["gemm_ragged_all_cores_s"] = timed(lambda: oracle.gemm_f16(a, b))
+    A, B = inputs.gemm_inputs(8192, 8192, 8192, seed=0)
+    a, b = A.numpy()[:256], B.numpy()
+    out["gemm_8192_all_cores_s_scaled"] = timed(lambda: oracle.gemm_f16(a, b)) * 8192 / 256
+    return out
+
+
 def run_reference(args, rank, world):
     """The reference arm: the CPU oracle, as it stands, on a bounded sample."""
     if rank != 0:
@@ -452,6 +503,7 @@ def run_ours(args, rank, world, local_rank):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline()
+        line["cpu_baseline"]["per_config"] = oracle_per_config()
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
