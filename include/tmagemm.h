@@ -50,8 +50,10 @@ typedef enum {
     TMAGEMM_ERR_TIMEOUT = -5,      /* a device-side pipeline wait timed out      */
     TMAGEMM_ERR_WORKSPACE = -6,    /* split-K workspace missing, misaligned or
                                       smaller than required                      */
-    TMAGEMM_ERR_SCRATCH_LIMIT = -7 /* gemm_f16_splitk_noalloc: the problem needs
+    TMAGEMM_ERR_SCRATCH_LIMIT = -7, /* gemm_f16_splitk_noalloc: the problem needs
                                       more than its fixed 32 MiB scratch         */
+    TMAGEMM_ERR_CHECK = -8         /* checked build only: a kernel self-check
+                                      failed (site in tmagemm_last_error_detail) */
 } tmagemm_status;
 
 /*
@@ -237,6 +239,22 @@ int tmagemm_check(void* stream);
  * bits 0..7 the wait site, bits 8..31 the block index.  Does not clear it.
  */
 int tmagemm_last_error_detail(void);
+
+/*
+ * Checked build (libtmagemm_checked.so, compiled with -DTMAGEMM_CHECKED): the
+ * kernels check their own invariants in place of a sanitizer.  A TMA
+ * coordinate that breaks the 16-byte rule or is negative, an epilogue index
+ * outside its tile or D, or producer and MMA issuer that consumed different
+ * numbers of k-blocks record a site (11..13) in the error word, skip the
+ * access, and make tmagemm_check return TMAGEMM_ERR_CHECK.  Every work unit
+ * that completes (an output tile, or one K part of it) increments a counter.
+ * tmagemm_checked_unit_counts waits for `stream`, copies the first n counters
+ * of the tile kernel (unit u at index u mod 65536; units are numbered as in
+ * tmagemm_gemm_plan: K part * tiles + tile; the grouped GEMM numbers the
+ * groups' tiles one after the other) to host memory `counts` and zeroes all
+ * of them.  In the normal build it returns TMAGEMM_ERR_UNSUPPORTED.
+ */
+int tmagemm_checked_unit_counts(uint32_t* counts, int64_t n, void* stream);
 
 /* Static text for a status code (never NULL). */
 const char* tmagemm_strerror(int status);

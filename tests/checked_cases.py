@@ -1,0 +1,101 @@
+"""Runs the library's work-split paths under the checked build
+(libtmagemm_checked.so, loaded because TMAGEMM_CHECKED=1 is set by the test
+that starts this script) and verifies, after each call, that no self-check
+fired and that every work unit completed exactly once.  Prints one JSON line
+per case and exits non-zero on the first failure."""
+import json
+import os
+import sys
+
+import torch
+
+assert os.environ.get("TMAGEMM_CHECKED") == "1"
+import tma_pipelined_tensor_tn_gb300 as tg  # noqa: E402
+
+tg.build()
+assert tg.CHECKED and tg.LIB_PATH.endswith("libtmagemm_checked.so")
+dev = torch.device("cuda")
+
+
+def ceil_div(a, b):
+    return -(-a // b)
+
+
+def rnd(shape, dtype=torch.float16, seed=0):
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    return (torch.rand(shape, device=dev, generator=g) * 2 - 1).to(dtype)
+
+
+def verify(name, counts, expected_units=None, ref=None, got=None):
+    st = tg.lib().tmagemm_check(None)
+    assert st == tg.TMAGEMM_OK, (name, tg.strerror(st), tg.tmagemm_last_error_detail())
+    assert all(c <= 1 for c in counts), (name, "a unit ran twice", max(counts))
+    done = sum(counts)
+    assert all(c == 1 for c in counts[:done]), (name, "units done are not 0..U-1")
+    if expected_units is not None:
+        exp = expected_units if isinstance(expected_units, (list, tuple)) else [expected_units]
+        assert done in exp, (name, "units done", done, "expected", exp)
+    if ref is not None:
+        err = (got.float() - ref.float()).abs().max().item()
+        scale = ref.float().abs().max().item()
+        assert err <= 1e-2 + 4e-3 * scale, (name, err)
+    print(json.dumps({"case": name, "units": done}), flush=True)
+
+
+def plain(name, M, N, K, dtype=torch.float16, knobs=()):
+    for setter, value in knobs:
+        assert setter(value) == tg.TMAGEMM_OK
+    try:
+        p = tg.tmagemm_gemm_plan(M, N, K, 0)
+        a, b = rnd((M, K), dtype, 1), rnd((N, K), dtype, 2)
+        d = tg.gemm(a, b)
+        counts = tg.checked_unit_counts(min(p["units"] + 64, 65536))
+        verify(name, counts, p["units"], torch.matmul(a, b.T), d)
+    finally:
+        for setter, _ in knobs:
+            setter(0)
+
+
+plain("pairs_4096", 4096, 4096, 4096)
+plain("ragged", 4000, 3000, 4160)
+plain("bf16_4096", 4096, 4096, 4096, torch.bfloat16)
+for bn in (256, 224, 192):
+    plain(f"single_{bn}", 1000, 1000, 1000, knobs=((tg.tmagemm_set_cta_pair, 1), (tg.tmagemm_set_tile_n, bn)))
+    plain(f"pair_{bn}", 1000, 1000, 1000, knobs=((tg.tmagemm_set_cta_pair, 2), (tg.tmagemm_set_tile_n, bn)))
+plain("cluster_auto", 1024, 1024, 16384)
+for ck in (2, 4, 8):
+    plain(f"cluster_{ck}", 512, 1000, 4160, knobs=((tg.tmagemm_set_cluster_split, ck),))
+plain("decode_32x4096x14336", 32, 4096, 14336)
+plain("decode_64x14336x4096", 64, 14336, 4096)
+plain("group_m_8", 8192, 8192, 1024)
+
+# Split-K with a caller workspace: units are tiles x parts.
+M, N, K, S = 1000, 1000, 4160, 3
+p = tg.tmagemm_gemm_plan(M, N, K, 0, S)
+a, b = rnd((M, K), seed=3), rnd((N, K), seed=4)
+d = tg.gemm_splitk(a, b, splits=S)
+verify("splitk_3", tg.checked_unit_counts(p["units"] + 64), p["units"], torch.matmul(a, b.T), d)
+
+# Grouped: the groups' tiles, numbered one after the other.
+counts_g = [1697, 2233, 321, 376, 105, 1822, 706, 932]
+Ng, Kg = 4096, 2048
+A = rnd((sum(counts_g), Kg), seed=5)
+B = rnd((len(counts_g), Ng, Kg), seed=6)
+offsets = [0]
+for c in counts_g:
+    offsets.append(offsets[-1] + c)
+D = tg.gemm_grouped(A, B, offsets)
+ref = torch.cat([torch.matmul(A[offsets[g]:offsets[g + 1]], B[g].T) for g in range(len(counts_g))])
+exp = [sum(ceil_div(c, tm) for c in counts_g) * ceil_div(Ng, bn)
+       for tm in (128, 256) for bn in (256, 224, 192)]
+verify("grouped", tg.checked_unit_counts(4000), exp, ref, D)
+
+# Swap-AB small-M (route 1): tile kernel units with FP32 partials.
+assert tg.tmagemm_set_small_m_route(1) == tg.TMAGEMM_OK
+try:
+    X, W = rnd((24, 14336), seed=7), rnd((4096, 14336), seed=8)
+    Y = tg.gemm_small_m(X, W)
+    verify("swap_ab", tg.checked_unit_counts(4096), None, torch.matmul(X, W.T), Y)
+finally:
+    tg.tmagemm_set_small_m_route(0)
+print("CHECKED OK", flush=True)

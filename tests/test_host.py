@@ -54,8 +54,16 @@ def test_host_pipeline_argument_checks():
     L.tmagemm_host_pipeline_destroy(None)   # a no-op
 
 
+def test_checked_api_in_the_normal_build():
+    """The normal build exports the checked-build query and refuses it before
+    any CUDA call; the check status has its own message."""
+    assert not tg.CHECKED and tg.LIB_PATH.endswith("libtmagemm.so")
+    assert tg.lib().tmagemm_checked_unit_counts(None, 0, None) == tg.TMAGEMM_ERR_UNSUPPORTED
+    assert "self-check" in tg.strerror(tg.TMAGEMM_ERR_CHECK)
+
+
 def test_strerror_covers_all_codes():
-    for code in (0, -1, -2, -3, -4, -5, -6):
+    for code in (0, -1, -2, -3, -4, -5, -6, -7, -8):
         assert tg.strerror(code) and tg.strerror(code) != "unknown status"
     assert tg.strerror(12345) == "unknown status"
 

@@ -4,9 +4,12 @@ The compute path is the CUDA library ``libtmagemm.so`` built from ``csrc/``;
 this package only marshals arguments to its C ABI (``include/tmagemm.h``).
 """
 from ._binding import (  # noqa: F401
+    CHECKED,
     LIB_PATH,
+    checked_unit_counts,
     SIGNATURES,
     TMAGEMM_ERR_ALIGN,
+    TMAGEMM_ERR_CHECK,
     TMAGEMM_ERR_CUDA,
     TMAGEMM_ERR_INVALID,
     TMAGEMM_ERR_TIMEOUT,
@@ -50,6 +53,8 @@ from ._binding import (  # noqa: F401
 
 
 def build(force: bool = False) -> str:
-    """Compile libtmagemm.so in-tree (nvcc, sm_103a)."""
+    """Compile libtmagemm.so in-tree (nvcc, sm_103a); with TMAGEMM_CHECKED=1 in
+    the environment, the checked build libtmagemm_checked.so instead."""
     from ._build import build as _b
-    return _b(force=force)
+    from ._binding import CHECKED
+    return _b(force=force, checked=CHECKED)

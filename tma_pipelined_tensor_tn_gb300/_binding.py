@@ -11,7 +11,10 @@ import os
 import threading
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_PKG, "libtmagemm.so")
+# TMAGEMM_CHECKED=1 selects the checked build (kernels that check their own
+# invariants and count their work units; see tmagemm_checked_unit_counts).
+CHECKED = os.environ.get("TMAGEMM_CHECKED", "") == "1"
+LIB_PATH = os.path.join(_PKG, "libtmagemm_checked.so" if CHECKED else "libtmagemm.so")
 
 TMAGEMM_OK = 0
 TMAGEMM_ERR_INVALID = -1
@@ -21,6 +24,7 @@ TMAGEMM_ERR_CUDA = -4
 TMAGEMM_ERR_TIMEOUT = -5
 TMAGEMM_ERR_WORKSPACE = -6
 TMAGEMM_ERR_SCRATCH_LIMIT = -7
+TMAGEMM_ERR_CHECK = -8
 
 # Every symbol include/tmagemm.h declares, with (argtypes, restype).
 _i64, _p, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
@@ -38,6 +42,7 @@ SIGNATURES = {
     "gemm_f16_splitk_noalloc": ([_i64, _i64, _i64, _p, _p, _p, _i64, _p], _int),
     "tmagemm_check": ([_p], _int),
     "tmagemm_last_error_detail": ([], _int),
+    "tmagemm_checked_unit_counts": ([ctypes.POINTER(ctypes.c_uint32), _i64, _p], _int),
     "tmagemm_strerror": ([_int], ctypes.c_char_p),
     "tmagemm_version": ([], _int),
     "tmagemm_selftest_wait_timeout": ([_i64, _p], _int),
@@ -344,3 +349,14 @@ def check(stream=None, device=None):
         s = lib().tmagemm_check(_stream_handle(stream, dev))
     if s != TMAGEMM_OK:
         raise TmaGemmError(s, f"tmagemm_check (detail 0x{tmagemm_last_error_detail():x})")
+
+
+def checked_unit_counts(n, stream=None):
+    """Checked build: the first n work-unit counters (then zeroed), as a list."""
+    import torch
+    buf = (ctypes.c_uint32 * max(int(n), 1))()
+    dev = torch.cuda.current_device()
+    s = lib().tmagemm_checked_unit_counts(buf, int(n), _stream_handle(stream, torch.device("cuda", dev)))
+    if s != TMAGEMM_OK:
+        raise TmaGemmError(s, "tmagemm_checked_unit_counts")
+    return list(buf)[: int(n)]

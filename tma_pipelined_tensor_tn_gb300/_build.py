@@ -18,6 +18,10 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libtmagemm.so")
+# The checked build (-DTMAGEMM_CHECKED): kernels that check their own
+# invariants and count the work units they complete.
+BUILD_CHECKED = os.path.join(PKG, "_build_checked")
+LIB_CHECKED = os.path.join(PKG, "libtmagemm_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE,
@@ -40,24 +44,28 @@ def _deps():
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(d) <= t for d in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    """Compile every CUDA source and link libtmagemm.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=None,
+          checked: bool = False) -> str:
+    """Compile every CUDA source and link libtmagemm.so (or, with checked=True,
+    libtmagemm_checked.so); returns its path."""
+    lib_path = LIB_CHECKED if checked else LIB
+    build_dir = BUILD_CHECKED if checked else BUILD
+    if not force and up_to_date(lib_path):
+        return lib_path
+    os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
-    flags = ARCH + NVCC_FLAGS + list(extra_flags or [])
+    flags = ARCH + NVCC_FLAGS + (["-DTMAGEMM_CHECKED"] if checked else []) + list(extra_flags or [])
     procs = []
     objs = []
     for src in _sources():
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src) + ".o")
         objs.append(obj)
         cmd = [cc, *flags, "-c", src, "-o", obj]
         procs.append((cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT)))
@@ -72,14 +80,14 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
     if failed:
         msg = "\n".join(" ".join(c) + "\n" + t for c, t in failed)
         raise RuntimeError("nvcc failed:\n" + msg)
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     link = [cc, *ARCH, "-shared", "-Xcompiler", "-fPIC", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + " ".join(link) + "\n" + r.stdout + r.stderr)
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, checked="--checked" in sys.argv))

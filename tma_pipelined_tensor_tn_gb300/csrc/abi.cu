@@ -23,8 +23,14 @@
 
 namespace tmagemm {
 
-// Sticky per-device error word written by the kernels' bounded waits.
-__device__ uint32_t g_err_word = 0;
+// Sticky per-device error word written by the kernels' bounded waits (and, in
+// the checked build, their self-checks), followed there by the work-unit
+// counters.
+#ifdef TMAGEMM_CHECKED
+__device__ uint32_t g_err_word[1 + kCheckUnits];
+#else
+__device__ uint32_t g_err_word[1];
+#endif
 
 namespace {
 
@@ -433,7 +439,25 @@ int tmagemm_check(void* stream) {
     const uint32_t zero = 0;
     if (cudaMemcpy(d->err_word, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
         return TMAGEMM_ERR_CUDA;
-    return TMAGEMM_ERR_TIMEOUT;
+    const uint32_t site = v & 0xffu;
+    return site >= kSiteCheckRing && site <= kSiteCheckBounds ? TMAGEMM_ERR_CHECK
+                                                             : TMAGEMM_ERR_TIMEOUT;
+}
+
+int tmagemm_checked_unit_counts(uint32_t* counts, int64_t n, void* stream) {
+    if (!kChecked) return TMAGEMM_ERR_UNSUPPORTED;
+    if (n < 0 || n > static_cast<int64_t>(kCheckUnits) || (n > 0 && !counts))
+        return TMAGEMM_ERR_INVALID;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TMAGEMM_ERR_CUDA;
+    DeviceState* d = nullptr;
+    if (int s = device_state(&d)) return s;
+    if (n > 0 && cudaMemcpy(counts, d->err_word + 1, static_cast<size_t>(n) * sizeof(uint32_t),
+                            cudaMemcpyDeviceToHost) != cudaSuccess)
+        return TMAGEMM_ERR_CUDA;
+    if (cudaMemset(d->err_word + 1, 0, kCheckUnits * sizeof(uint32_t)) != cudaSuccess)
+        return TMAGEMM_ERR_CUDA;
+    return TMAGEMM_OK;
 }
 
 int tmagemm_last_error_detail(void) { return g_last_detail.load(); }
@@ -447,6 +471,8 @@ const char* tmagemm_strerror(int status) {
         case TMAGEMM_ERR_UNSUPPORTED: return "unsupported size or device";
         case TMAGEMM_ERR_CUDA: return "CUDA runtime or driver call failed";
         case TMAGEMM_ERR_TIMEOUT: return "device-side pipeline wait timed out";
+        case TMAGEMM_ERR_CHECK:
+            return "a self-check of the checked build failed (site in tmagemm_last_error_detail)";
         case TMAGEMM_ERR_WORKSPACE:
             return "split-K workspace missing, not 16-byte aligned, or smaller than required";
         case TMAGEMM_ERR_SCRATCH_LIMIT:

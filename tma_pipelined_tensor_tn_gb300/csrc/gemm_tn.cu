@@ -315,6 +315,8 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
     const uint32_t mma_done_bar = bar0 + 8u * (2 * C::STAGES + 4);
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 4);
+    // Checked build: the k-blocks the producer issued and the MMA issuer consumed.
+    volatile uint32_t* ring_count = reinterpret_cast<volatile uint32_t*>(smem + C::kOffMisc + 8);
 
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
     const int lane = static_cast<int>(threadIdx.x) % 32;
@@ -338,6 +340,10 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
             }
             mbar_init(mma_done_bar, 1);
             *abort_flag = 0;
+            if constexpr (kChecked) {
+                ring_count[0] = 0;
+                ring_count[1] = 0;
+            }
             fence_mbarrier_init();
             prob.prefetch();
         }
@@ -398,6 +404,12 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                         ok = false;
                         break;
                     }
+                    if (!check_ok(((kb * C::BK) & 7) == 0 && ui.a_row >= 0 && ui.b_row >= 0, err,
+                                  kSiteCheckTma)) {
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
                     if constexpr (C::kPair) {
                         // Both CTAs' bytes land on the leader's full[s]; only the
                         // leader registers them (its single arrival completes
@@ -416,6 +428,7 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                     ++it;
                 }
             }
+            if constexpr (kChecked) ring_count[0] = it;
             // Drain: the last (up to) STAGES issued stages must have landed
             // before shared memory is released.  In a pair the leader's full
             // barriers count both CTAs' loads; the peer stays until the final
@@ -478,6 +491,7 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 else
                     mma_commit(acc_full_bar(acc));
             }
+            if constexpr (kChecked) ring_count[1] = it;
             // All issued MMAs must finish before TMEM is released.
             if constexpr (C::kPair)
                 mma_commit_pair(mma_done_bar, static_cast<uint16_t>(0x1u << pair_leader));
@@ -576,11 +590,13 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 named_bar_sync(1, C::kEpiThreads);
                 if (store_thread) {
                     const int32_t x = n0 + c * C::kEpiCols;
-                    if (x < ui.n_limit && ui.store_y < ui.m_limit)
+                    if (x < ui.n_limit && ui.store_y < ui.m_limit &&
+                        check_ok((x & 7) == 0 && x >= 0 && ui.store_y >= 0, err, kSiteCheckTma))
                         prob.template store<C::kOutF32>(buf, x, ui);
                     bulk_commit_group();
                 }
             }
+            if (store_thread && rank == 0) check_count_unit(err, u);
         }
         if (store_thread) bulk_wait_group<0>();
     }
@@ -645,15 +661,22 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 o.z = pack2_rn<C::kBF16>(__float_as_uint(a[4]), __float_as_uint(a[5]));
                 o.w = pack2_rn<C::kBF16>(__float_as_uint(a[6]), __float_as_uint(a[7]));
                 const int32_t m = m0 + rl, n = ui.b_row + 8 * g;
-                *reinterpret_cast<uint4*>(dout + static_cast<int64_t>(m) * prob.w.N + n) = o;
+                if (check_ok(rl < C::BM && g < kGroups && m < prob.w.M && n + 8 <= prob.w.N, err,
+                             kSiteCheckBounds))
+                    *reinterpret_cast<uint4*>(dout + static_cast<int64_t>(m) * prob.w.N + n) = o;
             }
         }
+        if (threadIdx.x == 0 && rank == 0 && !*abort_flag) check_count_unit(err, unit0);
         cluster_sync();   // peers' shared memory stays alive until every CTA has read it
     }
 
     // ---- teardown ----
     tc_fence_before();
     __syncthreads();
+    if constexpr (kChecked) {
+        if (threadIdx.x == 0 && rank == 0 && !*abort_flag)
+            check_ok(ring_count[0] == ring_count[1], err, kSiteCheckRing);
+    }
     // A pair stays alive until both CTAs are done with each other's shared
     // memory and barriers.
     if constexpr (C::kPair) cluster_sync();

@@ -119,12 +119,46 @@ enum WaitSite : uint32_t {
     kSiteTest = 7,
     kSiteGemvFull = 8,
     kSiteGemvX = 9,
+    // Checked build only (TMAGEMM_CHECKED): a self-check failed.
+    kSiteCheckRing = 11,     // producer and MMA issuer saw different k-block counts
+    kSiteCheckTma = 12,      // a TMA coordinate broke the 16-byte rule or was negative
+    kSiteCheckBounds = 13,   // an epilogue index left its tile or D
 };
 
 // Sticky per-device error word: 0 = fine, otherwise site | (block << 8).
 __device__ __forceinline__ void record_error(uint32_t* err_word, uint32_t site) {
     uint32_t code = (site & 0xffu) | ((blockIdx.x & 0xffffffu) << 8);
     atomicCAS(err_word, 0u, code == 0u ? 1u : code);
+}
+
+// ----------------------------------------------------------- checked build ----
+// Built with -DTMAGEMM_CHECKED, the kernels check their own invariants in place
+// of a sanitizer: a failed check records its site in the error word and the
+// kernel skips the access (no trap, no assert), and every work unit that
+// completes increments its counter in the words after the error word
+// (err_word[1 + unit % kCheckUnits]), so the host can see that each unit ran
+// exactly once.  In the normal build the checks compile away.
+#ifdef TMAGEMM_CHECKED
+constexpr bool kChecked = true;
+#else
+constexpr bool kChecked = false;
+#endif
+constexpr uint32_t kCheckUnits = 1u << 16;   // unit counters after the error word
+
+__device__ __forceinline__ void check_count_unit(uint32_t* err_word, int32_t unit) {
+    if constexpr (kChecked)
+        atomicAdd(err_word + 1 + (static_cast<uint32_t>(unit) % kCheckUnits), 1u);
+}
+
+// True if `cond` holds (always, in the normal build); otherwise records `site`.
+__device__ __forceinline__ bool check_ok(bool cond, uint32_t* err_word, uint32_t site) {
+    if constexpr (kChecked) {
+        if (!cond) {
+            record_error(err_word, site);
+            return false;
+        }
+    }
+    return true;
 }
 
 // Waits are timed with the SM cycle counter (cheap to read, unlike the global
