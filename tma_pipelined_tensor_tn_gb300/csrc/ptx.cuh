@@ -93,19 +93,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Non-blocking probe: true once the phase with parity `parity` has completed.
-__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred P;\n\t"
-        "mbarrier.test_wait.parity.acquire.cta.shared::cta.b64 P, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, P;\n\t}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
 // ----------------------------------------------------------- error word ----
 
 // Wait-site ids recorded in the error word (bits 0..7).
@@ -180,26 +167,6 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
         if (mbar_try_wait(bar, parity)) return true;
         if (*abort_flag) return false;
         if ((spin & 15u) == 15u && static_cast<uint64_t>(clock64()) - t0 > lim) {
-            *abort_flag = 1;
-            record_error(err_word, site);
-            return false;
-        }
-    }
-}
-
-// Like wait_or_abort, but polls with the non-blocking test_wait instead of
-// letting try_wait suspend the thread: for waits on the critical path of a
-// latency-bound loop, where the wake-up delay of a suspended thread shows.
-__device__ __forceinline__ bool poll_or_abort(uint32_t bar, uint32_t parity,
-                                              volatile int* abort_flag, uint32_t* err_word,
-                                              uint32_t site, uint64_t limit_ns) {
-    if (mbar_test_wait(bar, parity)) return true;
-    const uint64_t t0 = clock64();
-    const uint64_t lim = limit_cycles(limit_ns);
-    for (uint32_t spin = 0;; ++spin) {
-        if (mbar_test_wait(bar, parity)) return true;
-        if (*abort_flag) return false;
-        if ((spin & 63u) == 63u && static_cast<uint64_t>(clock64()) - t0 > lim) {
             *abort_flag = 1;
             record_error(err_word, site);
             return false;
