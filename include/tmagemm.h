@@ -249,10 +249,11 @@ int tmagemm_last_error_detail(void);
  * access, and make tmagemm_check return TMAGEMM_ERR_CHECK.  Every work unit
  * that completes (an output tile, or one K part of it) increments a counter.
  * tmagemm_checked_unit_counts waits for `stream`, copies the first n counters
- * of the tile kernel (unit u at index u mod 65536; units are numbered as in
- * tmagemm_gemm_plan: K part * tiles + tile; the grouped GEMM numbers the
- * groups' tiles one after the other) to host memory `counts` and zeroes all
- * of them.  In the normal build it returns TMAGEMM_ERR_UNSUPPORTED.
+ * (unit u at index u mod 65536; the tile kernel numbers its units as
+ * tmagemm_gemm_plan does: K part * tiles + tile, the grouped GEMM the groups'
+ * tiles one after the other; the small-M kernels count one unit per CTA and
+ * the GEMV one per output row) to host memory `counts` and zeroes all of
+ * them.  In the normal build it returns TMAGEMM_ERR_UNSUPPORTED.
  */
 int tmagemm_checked_unit_counts(uint32_t* counts, int64_t n, void* stream);
 

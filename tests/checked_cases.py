@@ -98,4 +98,29 @@ try:
     verify("swap_ab", tg.checked_unit_counts(4096), None, torch.matmul(X, W.T), Y)
 finally:
     tg.tmagemm_set_small_m_route(0)
+# Register-fragment small-M kernel: one unit per CTA, clusters of S CTAs over
+# 64-row groups (S = 8 at N = 4096, 2 at N = 14336 on 152 SMs).
+sms = torch.cuda.get_device_properties(0).multi_processor_count
+for Mx, Nw, Kw, dt in ((8, 4096, 14336, torch.float16), (16, 14336, 4096, torch.float16),
+                       (8, 4096, 14336, torch.bfloat16)):
+    X, W = rnd((Mx, Kw), dt, 9), rnd((Nw, Kw), dt, 10)
+    Y = tg.gemm(X, W)
+    groups = ceil_div(Nw, 64)
+    S = 8 if groups * 8 <= 4 * sms else 4 if groups * 4 <= 4 * sms else 2
+    verify(f"fragments_{Mx}x{Nw}x{Kw}_{dt}", tg.checked_unit_counts(groups * S + 64), groups * S,
+           torch.matmul(X, W.T), Y)
+
+# SM-load-fed tcgen05 small-M kernel (route 3): 128-row CTAs, 8 K slices.
+assert tg.tmagemm_set_small_m_route(3) == tg.TMAGEMM_OK
+try:
+    X, W = rnd((40, 14336), seed=11), rnd((4096, 14336), seed=12)
+    Y = tg.gemm_small_m(X, W)
+    verify("lsu_40", tg.checked_unit_counts(256 + 64), 32 * 8, torch.matmul(X, W.T), Y)
+finally:
+    tg.tmagemm_set_small_m_route(0)
+
+# GEMV: one unit per output row.
+x, W = rnd((14336,), seed=13), rnd((4096, 14336), seed=14)
+y = tg.gemv(x, W)
+verify("gemv", tg.checked_unit_counts(4096 + 64), 4096, torch.matmul(W, x), y)
 print("CHECKED OK", flush=True)

@@ -145,7 +145,7 @@ int gemv_impl(int64_t N, int64_t K, const void* x, const void* W, void* y, void*
     if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (K % 8) != 0) return TMAGEMM_ERR_ALIGN;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    cudaError_t e = launch_gemv(N, K, x, W, y, bf16, static_cast<cudaStream_t>(stream));
+    cudaError_t e = launch_gemv(N, K, x, W, y, bf16, static_cast<cudaStream_t>(stream), d->err_word);
     return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 
@@ -215,7 +215,7 @@ static int small_m_no_workspace(SmallMKernel k, int64_t M, int64_t N, int64_t K,
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
     if (k == SmallMKernel::kFragments)
-        return launch_small_m_mma(M, N, K, X, W, D, st, bf16, d->sms) == cudaSuccess
+        return launch_small_m_mma(M, N, K, X, W, D, st, bf16, d->sms, d->err_word) == cudaSuccess
                    ? TMAGEMM_OK
                    : TMAGEMM_ERR_CUDA;
     // X {K, M} in boxes of 64 k x Mp token rows (rows past M read as zero).

@@ -82,7 +82,7 @@ __device__ __forceinline__ void consume_group(const uint4* __restrict__ x, int32
 template <bool BF16>
 __global__ void __launch_bounds__(kGvWarps * 32)
 gemv_f16_kernel(const uint4* __restrict__ x, const uint4* __restrict__ W, uint16_t* __restrict__ y,
-                int32_t N, int32_t K8) {
+                int32_t N, int32_t K8, uint32_t* __restrict__ err) {
     // Every block of this grid is resident by the time all have issued this,
     // so the next grid may be scheduled; it waits for this one to finish.
     grid_launch_dependents();
@@ -118,19 +118,20 @@ gemv_f16_kernel(const uint4* __restrict__ x, const uint4* __restrict__ W, uint16
             y[n] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
         else
             y[n] = __half_as_ushort(__float2half_rn(s));
+        check_count_unit(err, n);   // checked build: output rows written
     }
 }
 
 }  // namespace
 
 cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y, bool bf16,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, uint32_t* err) {
     const int32_t K8 = static_cast<int32_t>(K / 8);
     const int64_t blocks = (N + kGvWarps - 1) / kGvWarps;
     auto kernel = bf16 ? gemv_f16_kernel<true> : gemv_f16_kernel<false>;
     return launch_kernel(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kGvWarps * 32), 0,
                          stream, 1u, static_cast<const uint4*>(x), static_cast<const uint4*>(W),
-                         static_cast<uint16_t*>(y), static_cast<int32_t>(N), K8);
+                         static_cast<uint16_t*>(y), static_cast<int32_t>(N), K8, err);
 }
 
 }  // namespace tmagemm

@@ -86,7 +86,8 @@ cudaError_t launch_small_m_reduce(const void* partials, void* D, int64_t M, int6
 // No workspace; one launch.
 int64_t small_m_mma_max_m();
 cudaError_t launch_small_m_mma(int64_t M, int64_t N, int64_t K, const void* X, const void* W,
-                               void* D, cudaStream_t stream, bool bf16 = false, int num_sms = 0);
+                               void* D, cudaStream_t stream, bool bf16, int num_sms,
+                               uint32_t* err);
 
 // Skinny GEMM (2 <= M <= 64) on tcgen05 with the weights staged in shared
 // memory by the SMs' own 16-byte loads (X by TMA); K split over 8-CTA clusters
@@ -123,7 +124,7 @@ cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, int num_pairs, c
 // Enqueue the GEMV kernel: y[n] = sum_k x[k] * W[n][k]; one warp per row;
 // fp16 or bf16 operands and output.
 cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y, bool bf16,
-                        cudaStream_t stream);
+                        cudaStream_t stream, uint32_t* err);
 
 // Tile-N override for the GEMM plan (0 = automatic); a tuning/test knob.
 extern int g_force_tile_n;

@@ -134,7 +134,8 @@ __device__ __forceinline__ void mma_group(const Group<NT, U, XB>& G, const uint4
 template <int NT, int U, bool XB, int MIN_CTAS, int S, bool BF16>
 __global__ void __launch_bounds__(kSmWarps * 32, MIN_CTAS)
 small_m_mma_kernel(const uint4* __restrict__ X, const uint4* __restrict__ W,
-                   uint16_t* __restrict__ D, int32_t M, int32_t N, int32_t K8, int32_t slice8) {
+                   uint16_t* __restrict__ D, int32_t M, int32_t N, int32_t K8, int32_t slice8,
+                   uint32_t* __restrict__ err) {
     constexpr int kMp = 8 * NT;
     __shared__ float part[kSmRows][kMp];
 
@@ -210,6 +211,7 @@ small_m_mma_kernel(const uint4* __restrict__ X, const uint4* __restrict__ W,
         }
     }
     cluster_sync();   // peers' shared memory stays alive until every CTA has read it
+    if (threadIdx.x == 0) check_count_unit(err, static_cast<int32_t>(blockIdx.x));
 }
 
 }  // namespace
@@ -224,7 +226,7 @@ namespace {
 // ranges of whole 4-chunk (32-k) steps.
 template <int NT, int U, bool XB, int MIN_CTAS, int S, bool BF16>
 cudaError_t launch_variant(int64_t M, int64_t N, int64_t K, const void* X, const void* W, void* D,
-                           cudaStream_t stream) {
+                           cudaStream_t stream, uint32_t* err) {
     const int32_t K8 = static_cast<int32_t>(K / 8);
     const int32_t per = (K8 + S - 1) / S;
     const int32_t slice8 = (per + 3) / 4 * 4;
@@ -233,7 +235,7 @@ cudaError_t launch_variant(int64_t M, int64_t N, int64_t K, const void* X, const
                          dim3(static_cast<unsigned>(clusters * S)), dim3(kSmWarps * 32), 0,
                          stream, static_cast<unsigned>(S), static_cast<const uint4*>(X),
                          static_cast<const uint4*>(W), static_cast<uint16_t*>(D),
-                         static_cast<int32_t>(M), static_cast<int32_t>(N), K8, slice8);
+                         static_cast<int32_t>(M), static_cast<int32_t>(N), K8, slice8, err);
 }
 
 // Slices per cluster: 8 when the clusters of 64 weight rows are few enough
@@ -241,19 +243,21 @@ cudaError_t launch_variant(int64_t M, int64_t N, int64_t K, const void* X, const
 // so that the grid stays one wave with longer K slices (N = 14336: 2).
 template <int NT, int U, bool BF16>
 cudaError_t launch_sliced(int64_t M, int64_t N, int64_t K, const void* X, const void* W, void* D,
-                          int num_sms, cudaStream_t stream) {
+                          int num_sms, cudaStream_t stream, uint32_t* err) {
     const int64_t clusters = (N + kSmRows - 1) / kSmRows;
     const int64_t wave = 4ll * (num_sms > 0 ? num_sms : 152);
-    if (clusters * 8 <= wave) return launch_variant<NT, U, true, 1, 8, BF16>(M, N, K, X, W, D, stream);
-    if (clusters * 4 <= wave) return launch_variant<NT, U, true, 1, 4, BF16>(M, N, K, X, W, D, stream);
-    return launch_variant<NT, U, true, 1, 2, BF16>(M, N, K, X, W, D, stream);
+    if (clusters * 8 <= wave)
+        return launch_variant<NT, U, true, 1, 8, BF16>(M, N, K, X, W, D, stream, err);
+    if (clusters * 4 <= wave)
+        return launch_variant<NT, U, true, 1, 4, BF16>(M, N, K, X, W, D, stream, err);
+    return launch_variant<NT, U, true, 1, 2, BF16>(M, N, K, X, W, D, stream, err);
 }
 
 template <bool BF16>
 cudaError_t launch_typed(int64_t M, int64_t N, int64_t K, const void* X, const void* W, void* D,
-                         int num_sms, cudaStream_t stream) {
-    if (M <= 8) return launch_sliced<1, 4, BF16>(M, N, K, X, W, D, num_sms, stream);
-    if (M <= 16) return launch_sliced<2, 2, BF16>(M, N, K, X, W, D, num_sms, stream);
+                         int num_sms, cudaStream_t stream, uint32_t* err) {
+    if (M <= 8) return launch_sliced<1, 4, BF16>(M, N, K, X, W, D, num_sms, stream, err);
+    if (M <= 16) return launch_sliced<2, 2, BF16>(M, N, K, X, W, D, num_sms, stream, err);
     return cudaErrorInvalidValue;
 }
 
@@ -266,9 +270,10 @@ cudaError_t launch_typed(int64_t M, int64_t N, int64_t K, const void* X, const v
 // 8 slices, 23.1 us.  A slice count read at run time instead of fixed at
 // compile time cost 2 us; above 16 tokens the tcgen05 kernel is faster.
 cudaError_t launch_small_m_mma(int64_t M, int64_t N, int64_t K, const void* X, const void* W,
-                               void* D, cudaStream_t stream, bool bf16, int num_sms) {
-    return bf16 ? launch_typed<true>(M, N, K, X, W, D, num_sms, stream)
-                : launch_typed<false>(M, N, K, X, W, D, num_sms, stream);
+                               void* D, cudaStream_t stream, bool bf16, int num_sms,
+                               uint32_t* err) {
+    return bf16 ? launch_typed<true>(M, N, K, X, W, D, num_sms, stream, err)
+                : launch_typed<false>(M, N, K, X, W, D, num_sms, stream, err);
 }
 
 }  // namespace tmagemm

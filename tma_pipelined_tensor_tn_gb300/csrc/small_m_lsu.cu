@@ -298,6 +298,7 @@ small_m_lsu_kernel(const __grid_constant__ CUtensorMap tmX, const uint4* __restr
         tc_fence_after();
         tmem_dealloc(tmem_base, L::kTmemCols);
     }
+    if (threadIdx.x == 0 && !*abort_flag) check_count_unit(err, static_cast<int32_t>(blockIdx.x));
 }
 
 template <int MP, bool BF16>
