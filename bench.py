@@ -453,6 +453,7 @@ def run_ours(args, rank, world, local_rank):
 
     extras = measure_extras(tg, dev, stream, l2)
     extras.update(measure_distributions(tg, dev, stream, l2))
+    extras["gemm_4096_plan"] = tg.tmagemm_gemm_plan(GEMM_M, GEMM_N, GEMM_K, 0)
 
     peaks, peak_src = load_peaks()
     gemm_avg_s = gemm_total_ms / 1e3 / args.steps
