@@ -133,3 +133,16 @@ def test_small_m_rejects_out_of_range_and_bad_workspace(tg):
     finally:
         assert tg.tmagemm_set_small_m_route(0) == tg.TMAGEMM_OK
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("M", [8, 16])
+def test_fragments_wide_n_without_k_split(tg, M):
+    """N = 28672: 448 groups of 64 weight rows; even two K slices per group
+    would not fit in one wave of CTAs, so each CTA takes its 64 rows over the
+    whole K (clusters of one CTA).  Parity, and integer inputs bit for bit."""
+    N, K = 28672, 1032
+    X, W = decode_inputs(M, N, K, seed=500 + M)
+    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"wide N M={M}")
+    Xi = inputs.integer_f16((M, K), seed=502 + M)
+    Wi = inputs.integer_f16((N, K), seed=503 + M)
+    assert_bitexact(run(tg, Xi, Wi), oracle.gemm_f16(Xi.numpy(), Wi.numpy()), f"wide N integer M={M}")

@@ -24,7 +24,7 @@
 // contiguous bytes of each row.
 //
 // Work split.  A CTA of 4 warps owns 64 weight rows (16 per warp, one MMA
-// row tile); the S CTAs of a thread-block cluster (S = 8, 4 or 2, so that
+// row tile); the S CTAs of a thread-block cluster (S = 8, 4, 2 or 1, so that
 // the grid stays one wave) own the same rows and split K into S slices.  Each CTA leaves its 64 x 8NT FP32 partial
 // tile in shared memory; after a cluster barrier each CTA finishes 64 / S of
 // the rows, adding the S partials in slice order through distributed shared
@@ -240,7 +240,9 @@ cudaError_t launch_variant(int64_t M, int64_t N, int64_t K, const void* X, const
 
 // Slices per cluster: 8 when the clusters of 64 weight rows are few enough
 // for one wave of CTAs (4 per SM: 512 CTAs at N = 4096), fewer for more rows
-// so that the grid stays one wave with longer K slices (N = 14336: 2).
+// so that the grid stays one wave with longer K slices (N = 14336: 2), and
+// none (one CTA per 64 rows, whole K) when even 2 slices would not fit in one
+// wave (N = 28672: 448 CTAs).
 template <int NT, int U, bool BF16>
 cudaError_t launch_sliced(int64_t M, int64_t N, int64_t K, const void* X, const void* W, void* D,
                           int num_sms, cudaStream_t stream, uint32_t* err) {
@@ -250,7 +252,9 @@ cudaError_t launch_sliced(int64_t M, int64_t N, int64_t K, const void* X, const 
         return launch_variant<NT, U, true, 1, 8, BF16>(M, N, K, X, W, D, stream, err);
     if (clusters * 4 <= wave)
         return launch_variant<NT, U, true, 1, 4, BF16>(M, N, K, X, W, D, stream, err);
-    return launch_variant<NT, U, true, 1, 2, BF16>(M, N, K, X, W, D, stream, err);
+    if (clusters * 2 <= wave)
+        return launch_variant<NT, U, true, 1, 2, BF16>(M, N, K, X, W, D, stream, err);
+    return launch_variant<NT, U, true, 1, 1, BF16>(M, N, K, X, W, D, stream, err);
 }
 
 template <bool BF16>
