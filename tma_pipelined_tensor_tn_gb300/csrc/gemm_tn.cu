@@ -506,7 +506,12 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
         const uint32_t row = quarter * 32u + static_cast<uint32_t>(lane);
         const bool ok = wait_or_abort(acc_full_bar(0), 0, abort_flag, err, kSiteEpiAccFull,
                                       limit_ns);
-        if (named_bar_and(1, C::kEpiThreads, ok)) {
+        // A warp whose 32 rows all lie past the last row of D (index >= M)
+        // holds nothing the reduction reads: it skips the copy.
+        const UnitInfo ui0 = prob.unit(unit0, C::kTileM, C::BN, C::kGroupM);
+        const bool rows_exist = ui0.a_row + static_cast<int32_t>(rank) * C::BM +
+                                    static_cast<int32_t>(quarter) * 32 < prob.w.M;
+        if (named_bar_and(1, C::kEpiThreads, ok) && rows_exist) {
             tc_fence_after();
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16);
             const uint32_t p_row = sbase + C::kOffA + row * C::kPartStride * 4u;
