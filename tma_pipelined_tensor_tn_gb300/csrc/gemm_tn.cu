@@ -193,6 +193,13 @@ struct DenseProblem {
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmD);
     }
+    // L2 warm-up of one k-block of this CTA's A and B rows (row offsets
+    // row_a and row_b into the unit's tiles).
+    __device__ __forceinline__ void prefetch_l2(int32_t k, const UnitInfo& ui, int32_t row_a,
+                                                int32_t row_b) const {
+        tma_prefetch_l2_2d(&tmA, k, ui.a_row + row_a);
+        tma_prefetch_l2_2d(&tmB, k, ui.b_row + row_b);
+    }
     __device__ __forceinline__ UnitInfo unit(int32_t u, int BM, int BN, int) const {
         const int32_t tile = u % w.num_tiles;
         const int32_t split = u / w.num_tiles;
@@ -257,6 +264,7 @@ struct GroupedProblem {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
+    __device__ __forceinline__ void prefetch_l2(int32_t, const UnitInfo&, int32_t, int32_t) const {}
     __device__ __forceinline__ UnitInfo unit(int32_t u, int BM, int BN, int group_m) const {
         int32_t g = 0;
         while (g + 1 < groups && tile_start[g + 1] <= u) ++g;
@@ -321,6 +329,27 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
     const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x) / 32, 0);
     const int lane = static_cast<int>(threadIdx.x) % 32;
 
+    // Work distribution: single CTAs step by the grid; pairs by the pair count.
+    // Cluster roles: a pair is ranks (2p, 2p + 1) of the cluster; `rank` is
+    // this CTA's half of its pair, `pair_leader` the pair's first rank.
+    const uint32_t cta_rank = (C::kPair || C::kClusterK != 0) ? cluster_ctarank() : 0u;
+    const uint32_t rank = C::kPair ? (cta_rank & 1u) : 0u;
+    const uint32_t pair_leader = C::kPair ? (cta_rank & ~1u) : 0u;
+    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << pair_leader);
+    int32_t unit0 =
+        C::kPair ? static_cast<int32_t>(blockIdx.x / 2) : static_cast<int32_t>(blockIdx.x);
+    int32_t unit_step =
+        C::kPair ? static_cast<int32_t>(gridDim.x / 2) : static_cast<int32_t>(gridDim.x);
+    // Cluster split: one unit per CTA (or pair), the tile of the cluster and
+    // the K slice of this CTA's (pair's) index in it (unit = split * tiles + tile).
+    uint32_t ck_rank = 0;
+    if constexpr (C::kClusterK != 0) {
+        ck_rank = C::kPair ? (cta_rank >> 1) : cta_rank;
+        unit0 = static_cast<int32_t>(ck_rank) * prob.w.num_tiles +
+                static_cast<int32_t>(blockIdx.x / (C::kClusterK * (C::kPair ? 2 : 1)));
+        unit_step = prob.num_units();
+    }
+
     // The next grid on the stream may be scheduled as soon as every CTA of
     // this one is running: it cannot share an SM with this grid's CTAs (shared
     // memory), and it waits (below) before touching global memory.
@@ -346,6 +375,16 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
             }
             fence_mbarrier_init();
             prob.prefetch();
+            // While the previous grid finishes, warm L2 with this CTA's first
+            // k-blocks (a prefetch cannot see stale data: L2 is where global
+            // memory is coherent), so the first loads after the wait hit L2.
+            if (unit0 < prob.num_units()) {
+                const UnitInfo ui = prob.unit(unit0, C::kTileM, C::BN, C::kGroupM);
+                const int32_t kb_end = min(ui.kb1, ui.kb0 + C::STAGES);
+                for (int32_t kb = ui.kb0; kb < kb_end; ++kb)
+                    prob.prefetch_l2(kb * C::BK, ui, static_cast<int32_t>(rank) * C::BM,
+                                     static_cast<int32_t>(rank) * C::kBRows);
+            }
         }
         __syncwarp();
     }
@@ -368,26 +407,6 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
     if constexpr (C::kPair) cluster_sync();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
-    // Work distribution: single CTAs step by the grid; pairs by the pair count.
-    // Cluster roles: a pair is ranks (2p, 2p + 1) of the cluster; `rank` is
-    // this CTA's half of its pair, `pair_leader` the pair's first rank.
-    const uint32_t cta_rank = (C::kPair || C::kClusterK != 0) ? cluster_ctarank() : 0u;
-    const uint32_t rank = C::kPair ? (cta_rank & 1u) : 0u;
-    const uint32_t pair_leader = C::kPair ? (cta_rank & ~1u) : 0u;
-    const uint16_t pair_mask = static_cast<uint16_t>(0x3u << pair_leader);
-    int32_t unit0 =
-        C::kPair ? static_cast<int32_t>(blockIdx.x / 2) : static_cast<int32_t>(blockIdx.x);
-    int32_t unit_step =
-        C::kPair ? static_cast<int32_t>(gridDim.x / 2) : static_cast<int32_t>(gridDim.x);
-    // Cluster split: one unit per CTA (or pair), the tile of the cluster and
-    // the K slice of this CTA's (pair's) index in it (unit = split * tiles + tile).
-    uint32_t ck_rank = 0;
-    if constexpr (C::kClusterK != 0) {
-        ck_rank = C::kPair ? (cta_rank >> 1) : cta_rank;
-        unit0 = static_cast<int32_t>(ck_rank) * prob.w.num_tiles +
-                static_cast<int32_t>(blockIdx.x / (C::kClusterK * (C::kPair ? 2 : 1)));
-        unit_step = prob.num_units();
-    }
 
     if (warp == 0) {
         // ================= TMA producer =================

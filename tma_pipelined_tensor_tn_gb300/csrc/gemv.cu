@@ -34,6 +34,11 @@ namespace {
 
 constexpr int kGvWarps = 8;      // rows per block
 constexpr int kGvGroup = 4;      // 16-byte loads per lane per group
+#ifndef TMAGEMM_GV_PREFETCH_CHUNKS
+#define TMAGEMM_GV_PREFETCH_CHUNKS 256
+#endif
+// 16-byte chunks at the head of each row warmed in L2 before the wait (4 KB).
+constexpr int32_t kGvPrefetchChunks = TMAGEMM_GV_PREFETCH_CHUNKS;
 
 __device__ __forceinline__ uint4 ld_stream_v4(const uint4* p) {
     uint4 r;
@@ -89,8 +94,13 @@ gemv_f16_kernel(const uint4* __restrict__ x, const uint4* __restrict__ W, uint16
     const int lane = threadIdx.x & 31;
     const int32_t n = blockIdx.x * kGvWarps + (threadIdx.x >> 5);
     if (n >= N) return;
-    grid_dependency_wait();   // x and W may come from the grid before this one
     const uint4* wrow = W + static_cast<int64_t>(n) * K8;
+    // While the previous grid finishes, pull the head of this row into L2 (a
+    // prefetch cannot see stale data: L2 is where global memory is coherent),
+    // so the first loads after the wait hit L2 instead of HBM.
+    if (kGvPrefetchChunks > 0 && lane == 0)
+        prefetch_l2_bytes(wrow, static_cast<uint32_t>(min(K8, kGvPrefetchChunks)) * 16u);
+    grid_dependency_wait();   // x and W may come from the grid before this one
     float acc[kGvGroup] = {};
     // Whole groups: group g covers this lane's chunks lane + 32*(g*GROUP + u).
     constexpr int32_t kStep = 32 * kGvGroup;

@@ -207,6 +207,23 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
+// Prefetch of a 2-D box into L2 only (no shared memory, no completion to
+// wait for).  L2 is where global memory is kept coherent, so a prefetched line
+// is never stale: a kernel may issue this for its inputs even before the grid
+// that writes them has finished.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y)
+                 : "memory");
+}
+
+// Prefetch of `bytes` contiguous bytes (16-byte aligned start and size) into L2.
+__device__ __forceinline__ void prefetch_l2_bytes(const void* p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
+                 ::"l"(reinterpret_cast<uint64_t>(p)), "r"(bytes)
+                 : "memory");
+}
+
 // 3-D tiled load (x inner, then y, then z), completion counted on `bar`.
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void* tmap, int32_t x, int32_t y,
                                             int32_t z, uint32_t bar) {

@@ -158,6 +158,15 @@ small_m_mma_kernel(const uint4* __restrict__ X, const uint4* __restrict__ W,
         xrow[j] = g + 8 * j < M ? X + static_cast<int64_t>(g + 8 * j) * K8 : nullptr;
 
     float acc[NT][4] = {};
+    // While the previous grid finishes, pull the first eighth of this CTA's K
+    // slice of its weight rows into L2 (a prefetch cannot see stale data: L2
+    // is where global memory is coherent), so the first loads after the wait
+    // hit L2 instead of HBM.
+    if (t == 0 && c_end > c_begin) {
+        const uint32_t bytes = static_cast<uint32_t>(max(1, (c_end - c_begin) / 8)) * 16u;
+        if (wrow_a) prefetch_l2_bytes(wrow_a + c_begin, bytes);
+        if (wrow_b) prefetch_l2_bytes(wrow_b + c_begin, bytes);
+    }
     grid_dependency_wait();   // X and W may come from the grid before this one
 
     // Groups of kSmUnroll steps (4 chunks each); group i+1's loads are issued
