@@ -62,6 +62,12 @@ namespace tmagemm {
 
 namespace {
 
+#ifndef TMAGEMM_L2_WARMUP
+#define TMAGEMM_L2_WARMUP 1
+#endif
+// Prefetch of each CTA's first k-blocks into L2 before the dependency wait.
+constexpr bool kL2WarmUp = TMAGEMM_L2_WARMUP != 0;
+
 template <int BN_, int EPI_COLS_, int STAGES_, bool OUT_F32_, bool BF16_, int TMEM_COLS_ = 512,
           int CTAS_PER_SM_ = 1, bool PAIR_ = false, int CK_ = 0>
 struct Cfg {
@@ -378,7 +384,7 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
             // While the previous grid finishes, warm L2 with this CTA's first
             // k-blocks (a prefetch cannot see stale data: L2 is where global
             // memory is coherent), so the first loads after the wait hit L2.
-            if (unit0 < prob.num_units()) {
+            if (kL2WarmUp && unit0 < prob.num_units()) {
                 const UnitInfo ui = prob.unit(unit0, C::kTileM, C::BN, C::kGroupM);
                 const int32_t kb_end = min(ui.kb1, ui.kb0 + C::STAGES);
                 for (int32_t kb = ui.kb0; kb < kb_end; ++kb)
