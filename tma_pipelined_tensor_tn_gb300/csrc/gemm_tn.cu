@@ -270,7 +270,11 @@ struct GroupedProblem {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
     }
-    __device__ __forceinline__ void prefetch_l2(int32_t, const UnitInfo&, int32_t, int32_t) const {}
+    __device__ __forceinline__ void prefetch_l2(int32_t k, const UnitInfo& ui, int32_t row_a,
+                                                int32_t row_b) const {
+        tma_prefetch_l2_2d(&tmA, k, ui.a_row + row_a);
+        tma_prefetch_l2_3d(&tmB, k, ui.b_row + row_b, ui.store_z);
+    }
     __device__ __forceinline__ UnitInfo unit(int32_t u, int BM, int BN, int group_m) const {
         int32_t g = 0;
         while (g + 1 < groups && tile_start[g + 1] <= u) ++g;

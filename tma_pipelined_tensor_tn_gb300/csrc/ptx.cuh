@@ -217,6 +217,14 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, 
                  : "memory");
 }
 
+// 3-D form of tma_prefetch_l2_2d (x inner, then y, then z).
+__device__ __forceinline__ void tma_prefetch_l2_3d(const void* tmap, int32_t x, int32_t y,
+                                                   int32_t z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];"
+                 ::"l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // Prefetch of `bytes` contiguous bytes (16-byte aligned start and size) into L2.
 __device__ __forceinline__ void prefetch_l2_bytes(const void* p, uint32_t bytes) {
     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;"
