@@ -64,10 +64,11 @@ typedef enum {
  *   D       : device pointer, M x N fp16, row-major; written, never read.
  *   stream  : cudaStream_t (NULL = legacy default stream).
  * Requirements: A, B, D 16-byte aligned; K % 8 == 0; N % 8 == 0 when M > 1.
- * M == 1 is computed by the GEMV kernel (x = A, W = B, y = D); 2 <= M <= 16
- * by the register-fragment kernel of gemm_f16_small_m (B streamed straight
- * into mma.sync operands); larger M by the tcgen05 tile kernel, which splits
- * K over clusters when the output has too few tiles to fill the SMs.  The
+ * M == 1 is computed by the GEMV kernel (x = A, W = B, y = D); 2 <= M <= 8,
+ * and 9 <= M <= 16 where its grid fills at least 80 % of a wave, by the
+ * register-fragment kernel of gemm_f16_small_m (B streamed straight into
+ * mma.sync operands); other M by the tcgen05 tile kernel, which splits K
+ * over clusters when the output has too few tiles to fill the SMs.  The
  * results agree up to FP32 accumulation order.
  * Kernel: persistent, warp-specialised: a TMA producer warp feeding a
  * multi-stage mbarrier ring of 128B-swizzled tiles, one thread issuing
@@ -174,10 +175,11 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
  * every linear layer is a GEMV when tokens are decoded one by one) for a
  * batch of M tokens.  Like the GEMV it is bound by reading W once.  The
  * automatic choice (tmagemm_set_small_m_route overrides it):
- *   - M <= 16: W streams from HBM straight into mma.sync register fragments
- *     (16-byte loads, no shared-memory staging); the CTAs of a cluster split
- *     K and add their FP32 partials in fixed order through distributed
- *     shared memory.
+ *   - M <= 8, and M <= 16 when N is such that this kernel's grid fills at
+ *     least 80 % of a wave (4 CTAs per SM; e.g. N = 4096 or 8192): W streams
+ *     from HBM straight into mma.sync register fragments (16-byte loads, no
+ *     shared-memory staging); the CTAs of a cluster split K and add their
+ *     FP32 partials in fixed order through distributed shared memory.
  *   - otherwise: the tcgen05 tile kernel of gemm_f16, which splits K over
  *     clusters when the output has too few tiles to fill the SMs.
  * Neither needs a workspace.  Two more kernels are available by route: the
@@ -203,9 +205,10 @@ int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void*
 int64_t gemm_f16_small_m_workspace_size(int64_t M, int64_t N, int64_t K);
 
 /*
- * Route of gemm_f16_small_m, process-wide: 0 and 2 = automatic (register
- * fragments for M <= 16, the tile kernel above), 1 = always the swap-AB
- * kernel (needs the workspace), 3 = always the LSU-fed tcgen05 kernel.
+ * Route of gemm_f16_small_m, process-wide: 0 = automatic (above), 2 = the
+ * register fragments wherever they apply (M <= 16) and the tile kernel
+ * above, 1 = always the swap-AB kernel (needs the workspace), 3 = always the
+ * LSU-fed tcgen05 kernel.
  * gemm_f16 / gemm_bf16 with 2 <= M <= 64 follow routes 0, 2 and 3 and take
  * the tile kernel under route 1.  Results
  * agree up to FP32 accumulation order.  The workspace size depends on the
@@ -217,8 +220,9 @@ int tmagemm_set_small_m_route(int route);
 /*
  * bfloat16 forms of gemm_f16 and gemv_f16: A, B, D (x, W, y) hold bf16
  * values; accumulation is FP32 and each output is rounded once to bf16
- * (nearest even).  Same kernels, tiles, shape routing (M = 1 the GEMV,
- * 2 <= M <= 16 the register-fragment kernel), requirements and status codes; only the element type of the tensor maps, the MMA operand format and
+ * (nearest even).  Same kernels, tiles, shape routing (M = 1 the GEMV, a
+ * few rows the register-fragment kernel, as for gemm_f16), requirements and
+ * status codes; only the element type of the tensor maps, the MMA operand format and
  * the final conversion change.  "TensorCore_GEMM_with_TMA" runs this TN GEMM in bf16
  * (§2.1 init tensor map: CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; §2.3: bf16 output
  * rounded to nearest).

@@ -154,7 +154,7 @@ int gemv_impl(int64_t N, int64_t K, const void* x, const void* W, void* y, void*
 int run_gemm(const GemmPlan& plan, DeviceState* d, int64_t M, int64_t N, int64_t K, const void* A,
              const void* B, void* D, void* workspace, void* stream) {
     CUtensorMap tmA, tmB, tmD;
-    if (int s = encode_2d(&tmA, A, K, M, plan.bk, plan.bm, CU_TENSOR_MAP_SWIZZLE_128B,
+    if (int s = encode_2d(&tmA, A, K, M, plan.bk, plan.a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, plan.bf16))
         return s;
     if (int s = encode_2d(&tmB, B, K, N, plan.bk, plan.b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -193,18 +193,29 @@ extern "C" {
 
 enum class SmallMKernel { kSwapAB, kFragments, kLsu, kTile };
 
-// Which kernel gemm_f16_small_m runs for this M (see tmagemm_set_small_m_route).
-// The automatic choice follows GB300 measurements over N x K in {4096 x
-// 14336, 14336 x 4096, 4096 x 4096}: up to 16 rows the register-fragment
-// kernel is fastest (4096 x 14336, M = 8: 21.4 us; swap-AB 26.1, LSU-fed 25.6,
-// tile kernel 30.0); above that the tile kernel with its cluster split of K is
-// the fastest or within 7 % of it everywhere (14336 x 4096, M = 17..64:
-// 24.0-25.9 us; swap-AB 29.2-30.4, LSU-fed 48.8-88.6).
-static SmallMKernel small_m_kernel(int64_t M) {
+// Which kernel gemm_f16_small_m runs for M rows against N weight rows (see
+// tmagemm_set_small_m_route).  The automatic choice follows GB300
+// measurements:
+// - up to 8 rows the register-fragment kernel, fastest everywhere measured
+//   (4096 x 14336, M = 8: 19.6 us against 22-23 us for the tile kernel);
+// - 9..16 rows the fragments only when their grid fills at least 80 % of its
+//   wave (512 of 608 CTAs at N = 4096 or 8192), otherwise the tile kernel's
+//   cluster split (M = 16: 14336 x 4096 22.4 against 24.9 us, 11008 x 4096
+//   18.9 against 23.8, 6144 x 4096 12.6 against 14.9, where the fragment
+//   grid fills 57-74 %);
+// - above 16 rows the tile kernel, the fastest or within 7 % of it
+//   everywhere (14336 x 4096, M = 17..64: 23-26 us; swap-AB 29-30, LSU-fed
+//   49-89).
+// Route 2 forces the fragments wherever they apply (M <= 16).
+static SmallMKernel small_m_kernel(int64_t M, int64_t N, int num_sms) {
     const int route = __atomic_load_n(&g_small_m_route, __ATOMIC_ACQUIRE);
     if (route == 1) return SmallMKernel::kSwapAB;
     if (route == 3) return SmallMKernel::kLsu;
-    return M <= small_m_mma_max_m() ? SmallMKernel::kFragments : SmallMKernel::kTile;
+    if (M > small_m_mma_max_m()) return SmallMKernel::kTile;
+    if (route == 2 || M <= 8) return SmallMKernel::kFragments;
+    return 5 * small_m_mma_ctas(N, num_sms) >= 4 * small_m_mma_wave(num_sms)
+               ? SmallMKernel::kFragments
+               : SmallMKernel::kTile;
 }
 
 // The workspace-free small-M kernels (register fragments, LSU-fed tcgen05),
@@ -229,17 +240,19 @@ static int small_m_no_workspace(SmallMKernel k, int64_t M, int64_t N, int64_t K,
                : TMAGEMM_ERR_CUDA;
 }
 
-// gemm_f16 / gemm_bf16 with a few rows: runs the register-fragment kernel for
-// M <= 16 (or the LSU-fed kernel up to 64 when route 3 forces it) and
-// returns true with its status in *status; false if the tile kernel should
-// run.  Above 16 rows the tile kernel, with its cluster split of K for
-// few-tile shapes, measured faster on GB300 than the workspace-free small-M
-// kernels: N = 4096, K = 14336, M = 17..64: 25.5-26.9 us against 39-48 us;
-// N = 14336, K = 4096, M = 17..64: 24-26 us against 49-89 us.
+// gemm_f16 / gemm_bf16 with a few rows: runs the register-fragment kernel
+// where small_m_kernel picks it (or the LSU-fed kernel up to 64 rows when
+// route 3 forces it) and returns true with its status in *status; false if
+// the tile kernel should run.
 static bool few_rows(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
                      void* stream, bool bf16, int* status) {
     if (M > 64) return false;
-    const SmallMKernel k = small_m_kernel(M);
+    DeviceState* d = nullptr;
+    if (int s = device_state(&d)) {
+        *status = s;
+        return true;
+    }
+    const SmallMKernel k = small_m_kernel(M, N, d->sms);
     if (k != SmallMKernel::kFragments && k != SmallMKernel::kLsu) return false;
     *status = small_m_no_workspace(k, M, N, K, A, B, D, stream, bf16);
     return true;
@@ -363,7 +376,8 @@ static int64_t small_m_tile_rows(int64_t M) { return M <= 16 ? M : 64; }
 int64_t gemm_f16_small_m_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (int s = validate_common(M, N, K)) return s;
     if (M < 2 || M > 64) return TMAGEMM_ERR_UNSUPPORTED;
-    if (small_m_kernel(M) != SmallMKernel::kSwapAB) return 0;   // only swap-AB needs one
+    // Only swap-AB needs one (route 1, which does not depend on the shape).
+    if (small_m_kernel(M, N, 0) != SmallMKernel::kSwapAB) return 0;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
     const GemmPlan p = plan_small_m(small_m_tile_rows(M), N, K, d->sms, 0);
@@ -377,7 +391,9 @@ int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void*
     if (M < 2 || M > 64) return TMAGEMM_ERR_UNSUPPORTED;
     if (!aligned16(X) || !aligned16(W) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
         return TMAGEMM_ERR_ALIGN;
-    const SmallMKernel kern = small_m_kernel(M);
+    DeviceState* dev = nullptr;
+    if (int s = device_state(&dev)) return s;
+    const SmallMKernel kern = small_m_kernel(M, N, dev->sms);
     if (kern == SmallMKernel::kTile) return gemm_f16(M, N, K, X, W, D, stream);
     if (kern != SmallMKernel::kSwapAB) return small_m_no_workspace(kern, M, N, K, X, W, D, stream);
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -389,7 +405,7 @@ int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void*
     // Swapped roles: the weights are the 128-row operand, the activations the
     // narrow one (rows past M read as zero), partials [splits][N][Mp].
     CUtensorMap tmW, tmX, tmP;
-    if (int s = encode_2d(&tmW, W, K, N, p.bk, p.bm, CU_TENSOR_MAP_SWIZZLE_128B,
+    if (int s = encode_2d(&tmW, W, K, N, p.bk, p.a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
         return s;
     if (int s = encode_2d(&tmX, X, K, M, p.bk, p.bn, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -186,6 +186,7 @@ struct UnitInfo {
 struct Work {
     int32_t M, N, grid_m, grid_n, num_tiles, num_units, k_blocks, kb_per_unit;
     int32_t group_m;   // L2 group height in tiles (chosen by the plan)
+    int32_t a_box_rows;   // rows of each A box (the A part of a stage's bytes)
 };
 
 struct DenseProblem {
@@ -194,6 +195,10 @@ struct DenseProblem {
     void* d_out;   // D itself (M x N, row-major), for the cluster-split epilogue
 
     __device__ __forceinline__ int32_t num_units() const { return w.num_units; }
+    // Bytes one stage's A box brings (the rest of the A stage is not written).
+    __device__ __forceinline__ uint32_t a_box_bytes(int BK) const {
+        return static_cast<uint32_t>(w.a_box_rows) * static_cast<uint32_t>(BK) * 2u;
+    }
     __device__ __forceinline__ void prefetch() const {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
@@ -266,6 +271,9 @@ struct GroupedProblem {
     int32_t groups, grid_n, N, k_blocks;
 
     __device__ __forceinline__ int32_t num_units() const { return tile_start[groups]; }
+    __device__ __forceinline__ uint32_t a_box_bytes(int BK) const {
+        return 128u * static_cast<uint32_t>(BK) * 2u;
+    }
     __device__ __forceinline__ void prefetch() const {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
@@ -443,14 +451,16 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                         // Both CTAs' bytes land on the leader's full[s]; only the
                         // leader registers them (its single arrival completes
                         // the phase once all bytes of both CTAs are in).
-                        if (rank == 0) mbar_arrive_expect_tx(full_bar(s), 2 * C::kStageBytes);
+                        if (rank == 0)
+                            mbar_arrive_expect_tx(full_bar(s),
+                                                  2 * (prob.a_box_bytes(C::BK) + C::kBBytes));
                         const uint32_t leader_full = map_to_rank(full_bar(s), pair_leader);
                         prob.load_a_pair(sbase + C::kOffA + s * C::kABytes, kb * C::BK, ui,
                                          static_cast<int32_t>(rank) * C::BM, leader_full);
                         prob.load_b_pair(sbase + C::kOffB + s * C::kBBytes, kb * C::BK, ui,
                                          static_cast<int32_t>(rank) * C::kBRows, leader_full);
                     } else {
-                        mbar_arrive_expect_tx(full_bar(s), C::kStageBytes);
+                        mbar_arrive_expect_tx(full_bar(s), prob.a_box_bytes(C::BK) + C::kBBytes);
                         prob.load_a(sbase + C::kOffA + s * C::kABytes, kb * C::BK, ui, full_bar(s));
                         prob.load_b(sbase + C::kOffB + s * C::kBBytes, kb * C::BK, ui, full_bar(s));
                     }
@@ -810,6 +820,11 @@ GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) 
     p.bf16 = C::kBF16;
     p.pair = C::kPair;
     p.b_box_rows = C::kBRows;
+    // With fewer than 128 rows, a box only as tall as the rows that exist
+    // (16-row multiples: whole 8-row swizzle atoms) spares the TMA unit the
+    // zero fill of the rest; the stage rows above it keep stale data, which
+    // reaches only accumulator rows >= M, never stored or reduced.
+    p.a_box_rows = M < C::BM ? static_cast<int>((M + 15) / 16 * 16) : C::BM;
     return p;
 }
 
@@ -863,6 +878,7 @@ cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUten
     prob.w.k_blocks = static_cast<int32_t>(plan.k_blocks);
     prob.w.kb_per_unit = static_cast<int32_t>(plan.kb_per_unit);
     prob.w.group_m = static_cast<int32_t>(plan.group_m);
+    prob.w.a_box_rows = plan.a_box_rows;
     prob.d_out = args.d_out;
     const unsigned cluster = static_cast<unsigned>((C::kPair ? 2 : 1) * (C::kClusterK ? C::kClusterK : 1));
     return launch_kernel(kernel, dim3(static_cast<unsigned>(plan.grid)), dim3(C::kThreads),

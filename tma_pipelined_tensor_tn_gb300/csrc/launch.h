@@ -22,6 +22,7 @@ struct GemmPlan {
     bool bf16;             // bf16 operands and output instead of fp16
     bool pair;             // CTA-pair (cta_group::2) tiles of 256 x bn
     int b_box_rows;        // rows of B per CTA (bn, or bn / 2 for a pair)
+    int a_box_rows;        // rows of A per TMA box: 128, or M rounded up to 16 when M < 128
     int cluster_k;         // > 0: K split over clusters of this many CTAs (one unit per CTA)
     int group_m;           // L2 group height of the tile order, in tiles
 };
@@ -85,6 +86,8 @@ cudaError_t launch_small_m_reduce(const void* partials, void* D, int64_t M, int6
 // the 8 CTAs of a cluster and reduced through distributed shared memory.
 // No workspace; one launch.
 int64_t small_m_mma_max_m();
+int64_t small_m_mma_ctas(int64_t N, int num_sms);
+int64_t small_m_mma_wave(int num_sms);
 cudaError_t launch_small_m_mma(int64_t M, int64_t N, int64_t K, const void* X, const void* W,
                                void* D, cudaStream_t stream, bool bf16, int num_sms,
                                uint32_t* err);

@@ -229,6 +229,18 @@ int g_small_m_route = 0;
 
 int64_t small_m_mma_max_m() { return 16; }
 
+// CTAs the register-fragment kernel launches for N weight rows, and the wave
+// it sizes them against (4 per SM): the same slice choice as launch_sliced.
+int64_t small_m_mma_ctas(int64_t N, int num_sms) {
+    const int64_t groups = (N + kSmRows - 1) / kSmRows;
+    const int64_t wave = small_m_mma_wave(num_sms);
+    for (int64_t s : {8, 4, 2})
+        if (groups * s <= wave) return groups * s;
+    return groups;
+}
+
+int64_t small_m_mma_wave(int num_sms) { return 4ll * (num_sms > 0 ? num_sms : 152); }
+
 namespace {
 
 // Grid of S-CTA clusters over ceil(N / 64) row groups; K is cut into S
