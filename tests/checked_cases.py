@@ -98,17 +98,22 @@ try:
     verify("swap_ab", tg.checked_unit_counts(4096), None, torch.matmul(X, W.T), Y)
 finally:
     tg.tmagemm_set_small_m_route(0)
-# Register-fragment small-M kernel: one unit per CTA, clusters of S CTAs over
-# 64-row groups (S = 8 at N = 4096, 2 at N = 14336 on 152 SMs).
+# Register-fragment small-M kernel (route 2: wherever it applies): one unit
+# per CTA, clusters of S CTAs over 64-row groups (S = 8 at N = 4096, 2 at
+# N = 14336, 1 at N = 28672 on 152 SMs).
 sms = torch.cuda.get_device_properties(0).multi_processor_count
-for Mx, Nw, Kw, dt in ((8, 4096, 14336, torch.float16), (16, 14336, 4096, torch.float16),
-                       (8, 4096, 14336, torch.bfloat16)):
-    X, W = rnd((Mx, Kw), dt, 9), rnd((Nw, Kw), dt, 10)
-    Y = tg.gemm(X, W)
-    groups = ceil_div(Nw, 64)
-    S = 8 if groups * 8 <= 4 * sms else 4 if groups * 4 <= 4 * sms else 2
-    verify(f"fragments_{Mx}x{Nw}x{Kw}_{dt}", tg.checked_unit_counts(groups * S + 64), groups * S,
-           torch.matmul(X, W.T), Y)
+assert tg.tmagemm_set_small_m_route(2) == tg.TMAGEMM_OK
+try:
+    for Mx, Nw, Kw, dt in ((8, 4096, 14336, torch.float16), (16, 14336, 4096, torch.float16),
+                           (8, 4096, 14336, torch.bfloat16), (12, 28672, 1024, torch.float16)):
+        X, W = rnd((Mx, Kw), dt, 9), rnd((Nw, Kw), dt, 10)
+        Y = tg.gemm(X, W)
+        groups = ceil_div(Nw, 64)
+        S = next((s for s in (8, 4, 2) if groups * s <= 4 * sms), 1)
+        verify(f"fragments_{Mx}x{Nw}x{Kw}_{dt}", tg.checked_unit_counts(groups * S + 64),
+               groups * S, torch.matmul(X, W.T), Y)
+finally:
+    tg.tmagemm_set_small_m_route(0)
 
 # SM-load-fed tcgen05 small-M kernel (route 3): 128-row CTAs, 8 K slices.
 assert tg.tmagemm_set_small_m_route(3) == tg.TMAGEMM_OK
