@@ -732,6 +732,10 @@ def measure_extras(tg, dev, stream, l2):
               tg.gemm_f16(Mw, Nw, Kw, aw.data_ptr(), bw.data_ptr(), dw.data_ptr(), sh))
         t_w = _time_launches(lambda i: fn(i) == 0 or None, reps, stream)
         entry = {"us": t_w, "tflops": gemm_flops(Mw, Nw, Kw) / t_w / 1e6}
+        pw = tg.tmagemm_gemm_plan(Mw, Nw, Kw, 0)
+        entry["plan"] = {"BN": pw["BN"], "pair": pw["pair"], "tiles": pw["tiles"],
+                         "units": pw["units"], "cluster_k": pw["cluster_k"],
+                         **tg.tmagemm_gemm_tail_plan(Mw, Nw, Kw, 0)}
         if name == "gemm_256":
             gs = torch.cuda.Stream(dev)
             gs.wait_stream(stream)

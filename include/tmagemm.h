@@ -321,6 +321,19 @@ int tmagemm_set_group_m(int g);
 int tmagemm_set_cluster_split(int mode);
 
 /*
+ * Tail split of gemm_f16 / gemm_bf16, process-wide: 0 = automatic, 1 = never.
+ * A persistent schedule whose last round of output tiles fills at most half
+ * of the resident CTAs (or CTA pairs) runs each tile of that round as two
+ * work units of its column range — 128 columns and the rest of the tile
+ * (128, 96 or 64 for tiles 256, 224 or 192 wide) — so the round takes about
+ * half as long; the plan's cost model weighs it against the other tile
+ * widths.  Every output is still summed over all of K by one unit, in the
+ * same k order as in an unsplit tile.  Returns TMAGEMM_ERR_INVALID for other
+ * values.
+ */
+int tmagemm_set_tail_split(int mode);
+
+/*
  * Programmatic dependent launch of the library's kernels: 1 (the default)
  * launches each kernel with CUDA's programmatic-stream-serialization
  * attribute, so a kernel queued behind another on the same stream is
@@ -368,6 +381,17 @@ int tmagemm_ring_position(int64_t it, int64_t stages, int64_t* stage, int64_t* p
  */
 int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t num_pairs,
                       int64_t splits, int64_t* out);
+
+/*
+ * The tail split of the gemm_f16 plan for (M, N, K) on `num_sms` SMs with
+ * `num_pairs` co-resident CTA pairs (num_sms == 0: the current device, as for
+ * tmagemm_gemm_plan): out[0] = work units that are whole tiles, out[1] = tiles
+ * of the last round split in two (each two units; tmagemm_gemm_plan's unit
+ * count includes both), out[2] = columns of each split tile's first part
+ * (0 when nothing is split).  `out` holds 3 values.
+ */
+int tmagemm_gemm_tail_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t num_pairs,
+                           int64_t* out);
 
 /*
  * Host-buffer executor: GEMMs whose operands and results live in host memory.

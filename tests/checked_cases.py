@@ -62,6 +62,11 @@ plain("bf16_4096", 4096, 4096, 4096, torch.bfloat16)
 for bn in (256, 224, 192):
     plain(f"single_{bn}", 1000, 1000, 1000, knobs=((tg.tmagemm_set_cta_pair, 1), (tg.tmagemm_set_tile_n, bn)))
     plain(f"pair_{bn}", 1000, 1000, 1000, knobs=((tg.tmagemm_set_cta_pair, 2), (tg.tmagemm_set_tile_n, bn)))
+# Tail split: 80 pair tiles (156 single-CTA tiles) on 76 pairs (152 SMs),
+# the last round's 4 tiles in two column parts each.
+plain("tail_split_pairs", 5070, 984, 520, knobs=((tg.tmagemm_set_cta_pair, 2), (tg.tmagemm_set_tile_n, 256)))
+plain("tail_split_single_224", 4942, 856, 520, knobs=((tg.tmagemm_set_cta_pair, 1), (tg.tmagemm_set_tile_n, 224)))
+plain("tail_split_8192", 8192, 8192, 512)
 plain("cluster_auto", 1024, 1024, 16384)
 for ck in (2, 4, 8):
     plain(f"cluster_{ck}", 512, 1000, 4160, knobs=((tg.tmagemm_set_cluster_split, ck),))

@@ -194,7 +194,9 @@ def test_plan_for_the_workloads():
     r = tg.tmagemm_gemm_plan(4000, 3000, 4160, 152)
     assert r["tiles"] == -(-4000 // r["BM"]) * -(-3000 // r["BN"])
     s = tg.tmagemm_gemm_plan(256, 256, 256, 152)
-    assert s["grid"] == s["tiles"] <= 4
+    assert s["tiles"] <= 4
+    # One short round: every tile runs as its two column parts.
+    assert s["grid"] == s["units"] == 2 * s["tiles"]
 
 
 def test_plan_balances_waves_on_gb300():
@@ -214,6 +216,62 @@ def test_plan_with_cta_pairs_balances_waves():
     assert q["pair"] == 1 and q["BN"] == 256
     # split-K plans never use pairs
     assert tg.tmagemm_gemm_plan(1024, 1024, 16384, 152, 0, 76)["pair"] == 0
+
+
+def test_tail_split_plan():
+    """A last round at most half full runs its tiles as two column parts: the
+    whole rounds keep whole tiles, the parts fill the last round once."""
+    t = tg.tmagemm_gemm_tail_plan(8192, 8192, 8192, 152, 76)
+    p = tg.tmagemm_gemm_plan(8192, 8192, 8192, 152, 1, 76)
+    # 32 x 32 = 1024 pair tiles = 13 rounds of 76 + 36
+    assert (p["BN"], p["pair"], p["tiles"]) == (256, 1, 1024)
+    assert t == {"full_units": 13 * 76, "split_tiles": 36, "narrow_cols": 128}
+    assert p["units"] == 13 * 76 + 72 and p["grid"] == 152
+    # 4096^3 fills four whole rounds of 256 x 224 pair tiles: nothing to split.
+    assert tg.tmagemm_gemm_tail_plan(4096, 4096, 4096, 152, 76)["split_tiles"] == 0
+    assert tg.tmagemm_gemm_plan(4096, 4096, 4096, 152, 1, 76)["BN"] == 224
+    try:
+        assert tg.tmagemm_set_tail_split(1) == tg.TMAGEMM_OK
+        off = tg.tmagemm_gemm_tail_plan(8192, 8192, 8192, 152, 76)
+        assert off == {"full_units": 1024, "split_tiles": 0, "narrow_cols": 0}
+        assert tg.tmagemm_gemm_plan(8192, 8192, 8192, 152, 1, 76)["units"] == 1024
+        assert tg.tmagemm_set_tail_split(2) == tg.TMAGEMM_ERR_INVALID
+        assert tg.tmagemm_set_tail_split(-1) == tg.TMAGEMM_ERR_INVALID
+    finally:
+        assert tg.tmagemm_set_tail_split(0) == tg.TMAGEMM_OK
+    with pytest.raises(tg.TmaGemmError):
+        tg.tmagemm_gemm_tail_plan(0, 8, 8, 152, 76)
+
+
+@pytest.mark.parametrize("sms,pairs", [(152, 76), (152, 0), (132, 66), (148, 0)])
+def test_tail_split_plan_invariants(sms, pairs):
+    """Over many shapes: units = whole tiles + 2 x split tiles; a split happens
+    only after whole rounds, on a last round at most half full, and each
+    split tile's two parts are 128 columns and the rest of the tile."""
+    import random
+    rng = random.Random(sms + pairs)
+    seen = 0
+    for _ in range(400):
+        M = rng.choice([rng.randint(1, 512), rng.randint(17, 9000)])
+        N = 8 * rng.randint(1, 1200)
+        K = 8 * rng.randint(1, 1200)
+        p = tg.tmagemm_gemm_plan(M, N, K, sms, 1, pairs)
+        t = tg.tmagemm_gemm_tail_plan(M, N, K, sms, pairs)
+        assert p["units"] == t["full_units"] + 2 * t["split_tiles"], (M, N, K, p, t)
+        if t["split_tiles"] == 0:
+            assert t["narrow_cols"] == 0
+            continue
+        seen += 1
+        slots = p["grid"] // (2 if p["pair"] else 1) if t["full_units"] else None
+        assert p["cluster_k"] == 0 and p["splits"] == 1
+        assert p["BN"] in (256, 224, 192) and t["narrow_cols"] == 128
+        assert t["full_units"] + t["split_tiles"] == p["tiles"]
+        s = pairs if p["pair"] else sms
+        assert t["full_units"] % s == 0 and 2 * t["split_tiles"] <= s
+        assert p["grid"] == min(p["units"], s) * (2 if p["pair"] else 1)
+        if slots is not None:
+            assert slots == s
+    assert seen > 10
 
 
 def test_cta_pair_override():

@@ -38,6 +38,7 @@ from ._binding import (  # noqa: F401
     strerror,
     tmagemm_check,
     tmagemm_gemm_plan,
+    tmagemm_gemm_tail_plan,
     tmagemm_last_error_detail,
     tmagemm_ring_position,
     tmagemm_selftest_wait_timeout,
@@ -46,6 +47,7 @@ from ._binding import (  # noqa: F401
     tmagemm_set_group_m,
     tmagemm_set_pdl,
     tmagemm_set_small_m_route,
+    tmagemm_set_tail_split,
     tmagemm_set_tile_n,
     tmagemm_tile_coord,
     tmagemm_version,

@@ -49,11 +49,13 @@ SIGNATURES = {
     "tmagemm_tile_coord": ([_i64, _i64, _i64, _i64, _P64, _P64], _int),
     "tmagemm_ring_position": ([_i64, _i64, _P64, _P64], _int),
     "tmagemm_gemm_plan": ([_i64, _i64, _i64, _i64, _i64, _i64, _P64], _int),
+    "tmagemm_gemm_tail_plan": ([_i64, _i64, _i64, _i64, _i64, _P64], _int),
     "tmagemm_set_cta_pair": ([_int], _int),
     "tmagemm_set_tile_n": ([_int], _int),
     "tmagemm_set_pdl": ([_int], _int),
     "tmagemm_set_small_m_route": ([_int], _int),
     "tmagemm_set_cluster_split": ([_int], _int),
+    "tmagemm_set_tail_split": ([_int], _int),
     "tmagemm_set_group_m": ([_int], _int),
     "tmagemm_host_pipeline_create": ([_i64, _i64, _i64, _int, _int, ctypes.POINTER(_p)], _int),
     "tmagemm_host_pipeline_run": ([_p, _i64, _p, _p, _p], _int),
@@ -231,6 +233,14 @@ def tmagemm_gemm_plan(M, N, K, num_sms, splits=1, num_pairs=0):
     return dict(zip(keys, list(out)))
 
 
+def tmagemm_gemm_tail_plan(M, N, K, num_sms, num_pairs=0):
+    out = (ctypes.c_int64 * 3)()
+    s = lib().tmagemm_gemm_tail_plan(M, N, K, num_sms, num_pairs, out)
+    if s != TMAGEMM_OK:
+        raise TmaGemmError(s, "tmagemm_gemm_tail_plan")
+    return dict(zip(("full_units", "split_tiles", "narrow_cols"), list(out)))
+
+
 def tmagemm_set_cta_pair(mode) -> int:
     return lib().tmagemm_set_cta_pair(mode)
 
@@ -245,6 +255,10 @@ def tmagemm_set_small_m_route(route) -> int:
 
 def tmagemm_set_cluster_split(mode) -> int:
     return lib().tmagemm_set_cluster_split(mode)
+
+
+def tmagemm_set_tail_split(mode) -> int:
+    return lib().tmagemm_set_tail_split(mode)
 
 
 def tmagemm_set_group_m(g) -> int:

@@ -177,6 +177,15 @@ int run_gemm(const GemmPlan& plan, DeviceState* d, int64_t M, int64_t N, int64_t
     args.wait_limit_ns = wait_limit_ns();
     args.err_word = d->err_word;
     args.d_out = D;
+    // Tail-split parts read B through a box of narrow_b_rows rows.
+    CUtensorMap tmBn;
+    if (plan.narrow_cols > 0) {
+        if (int s = encode_2d(&tmBn, B, K, N, plan.bk, plan.narrow_b_rows,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              plan.bf16))
+            return s;
+        args.tmBn = &tmBn;
+    }
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_gemm_tn(plan, tmA, tmB, tmD, args, st);
     if (e == cudaSuccess && plan.out_f32)
@@ -530,6 +539,12 @@ int tmagemm_set_cluster_split(int mode) {
     return TMAGEMM_OK;
 }
 
+int tmagemm_set_tail_split(int mode) {
+    if (mode != 0 && mode != 1) return TMAGEMM_ERR_INVALID;
+    __atomic_store_n(&g_tail_split, mode, __ATOMIC_RELEASE);
+    return TMAGEMM_OK;
+}
+
 int tmagemm_set_pdl(int on) {
     if (on != 0 && on != 1) return TMAGEMM_ERR_INVALID;
     __atomic_store_n(&g_pdl, on, __ATOMIC_RELEASE);
@@ -555,22 +570,47 @@ int tmagemm_ring_position(int64_t it, int64_t stages, int64_t* stage, int64_t* p
     return TMAGEMM_OK;
 }
 
-int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t num_pairs,
-                      int64_t splits, int64_t* out) {
-    if (!out || num_sms < 0 || num_pairs < 0 || num_pairs > num_sms / 2 || splits < 0 ||
-        splits > 4096)
+}  // extern "C"
+
+namespace {
+
+int plan_query(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t num_pairs, int64_t splits,
+               GemmPlan* p) {
+    if (num_sms < 0 || num_pairs < 0 || num_pairs > num_sms / 2 || splits < 0 || splits > 4096)
         return TMAGEMM_ERR_INVALID;
     if (int s = validate_common(M, N, K)) return s;
-    GemmPlan p;
     if (num_sms == 0) {
         // The plan gemm_f16 runs on the current device.
         DeviceState* d = nullptr;
         if (int s = device_state(&d)) return s;
-        p = plan_gemm(M, N, K, d->sms, splits, false, d->pairs, d->caps);
+        *p = plan_gemm(M, N, K, d->sms, splits, false, d->pairs, d->caps);
     } else {
-        p = plan_gemm(M, N, K, static_cast<int>(num_sms), splits, false,
-                      static_cast<int>(num_pairs));
+        *p = plan_gemm(M, N, K, static_cast<int>(num_sms), splits, false,
+                       static_cast<int>(num_pairs));
     }
+    return TMAGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int tmagemm_gemm_tail_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t num_pairs,
+                           int64_t* out) {
+    if (!out) return TMAGEMM_ERR_INVALID;
+    GemmPlan p;
+    if (int s = plan_query(M, N, K, num_sms, num_pairs, 1, &p)) return s;
+    out[0] = p.full_units;
+    out[1] = (p.units - p.full_units) / 2;
+    out[2] = p.narrow_cols;
+    return TMAGEMM_OK;
+}
+
+int tmagemm_gemm_plan(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t num_pairs,
+                      int64_t splits, int64_t* out) {
+    if (!out) return TMAGEMM_ERR_INVALID;
+    GemmPlan p;
+    if (int s = plan_query(M, N, K, num_sms, num_pairs, splits, &p)) return s;
     out[0] = p.bm;
     out[1] = p.bn;
     out[2] = p.bk;

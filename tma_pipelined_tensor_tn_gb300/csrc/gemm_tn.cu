@@ -114,6 +114,17 @@ struct Cfg {
     // mainloop is done.
     static constexpr uint32_t kPartStride = BN + 4;
     static constexpr uint32_t kIdesc = umma_idesc_16bit_f32(kTileM, BN, BF16_);
+    // Tail split: a tile of the last, partly filled round of the schedule may
+    // run as two units of kNarrowCols and BN - kNarrowCols columns (whole
+    // store boxes; MMA N a multiple of 16), so that round takes about half as
+    // long.  A narrow unit's B box has kNarrowBRows rows in this CTA.
+    static constexpr int kNarrowStep = kEpiCols > 16 ? kEpiCols : 16;
+    static constexpr int kNarrowCols = (BN_ / 2 + kNarrowStep - 1) / kNarrowStep * kNarrowStep;
+    static constexpr int kNarrowBRows = PAIR_ ? kNarrowCols / 2 : kNarrowCols;
+    static constexpr uint32_t kNarrowBBytes = kNarrowBRows * BK * 2;
+    static constexpr bool kTailSplit = !OUT_F32_ && CK_ == 0 && kNarrowCols < BN_ &&
+                                       kNarrowBRows % 8 == 0 &&
+                                       ((BN_ - kNarrowCols) / (PAIR_ ? 2 : 1)) % 8 == 0;
 
     static_assert(BK * 2 == 128, "a K-major row of one k-block is one 128-byte swizzle atom");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
@@ -178,6 +189,8 @@ struct UnitInfo {
     int32_t store_z;         // split index (split-K) or group index (grouped)
     int32_t n_limit;         // columns >= n_limit are outside the output
     int32_t m_limit;         // rows >= m_limit are outside the output (store map rows)
+    int32_t cols;            // output columns of this unit (BN, or a tail-split part)
+    int32_t narrow;          // 1: a tail-split part (B through the narrow box)
 };
 
 // Dense problem: D (or split-K partials) = A * B^T.  Unit u covers output
@@ -187,10 +200,16 @@ struct Work {
     int32_t M, N, grid_m, grid_n, num_tiles, num_units, k_blocks, kb_per_unit;
     int32_t group_m;   // L2 group height in tiles (chosen by the plan)
     int32_t a_box_rows;   // rows of each A box (the A part of a stage's bytes)
+    // Tail split: units < full_units are whole tiles; unit full_units + 2 t + p
+    // is part p of tile full_units + t, columns [0, narrow_cols) for p = 0 and
+    // [narrow_cols, BN) for p = 1.  narrow_cols = 0 (and full_units =
+    // num_units): no tail split.
+    int32_t full_units, narrow_cols;
 };
 
 struct DenseProblem {
     CUtensorMap tmA, tmB, tmD;
+    CUtensorMap tmBn;   // B with the narrow box of tail-split parts
     Work w;
     void* d_out;   // D itself (M x N, row-major), for the cluster-split epilogue
 
@@ -203,21 +222,30 @@ struct DenseProblem {
         tma_prefetch_desc(&tmA);
         tma_prefetch_desc(&tmB);
         tma_prefetch_desc(&tmD);
+        if (w.narrow_cols > 0) tma_prefetch_desc(&tmBn);
     }
     // L2 warm-up of one k-block of this CTA's A and B rows (row offsets
     // row_a and row_b into the unit's tiles).
     __device__ __forceinline__ void prefetch_l2(int32_t k, const UnitInfo& ui, int32_t row_a,
                                                 int32_t row_b) const {
         tma_prefetch_l2_2d(&tmA, k, ui.a_row + row_a);
-        tma_prefetch_l2_2d(&tmB, k, ui.b_row + row_b);
+        tma_prefetch_l2_2d(ui.narrow ? &tmBn : &tmB, k, ui.b_row + row_b);
     }
     __device__ __forceinline__ UnitInfo unit(int32_t u, int BM, int BN, int) const {
-        const int32_t tile = u % w.num_tiles;
-        const int32_t split = u / w.num_tiles;
+        int32_t tile, split = 0, part = -1;
+        if (u < w.full_units) {
+            tile = u % w.num_tiles;
+            split = u / w.num_tiles;
+        } else {
+            tile = w.full_units + ((u - w.full_units) >> 1);
+            part = (u - w.full_units) & 1;
+        }
         const TileCoord tc = tile_coord(tile, w.grid_m, w.grid_n, w.group_m);
         UnitInfo ui;
         ui.a_row = tc.m_blk * BM;
-        ui.b_row = tc.n_blk * BN;
+        ui.b_row = tc.n_blk * BN + (part == 1 ? w.narrow_cols : 0);
+        ui.cols = part < 0 ? BN : (part == 0 ? w.narrow_cols : BN - w.narrow_cols);
+        ui.narrow = part >= 0 ? 1 : 0;
         ui.kb0 = split * w.kb_per_unit;
         ui.kb1 = min(w.k_blocks, ui.kb0 + w.kb_per_unit);
         ui.store_y = ui.a_row;
@@ -232,7 +260,7 @@ struct DenseProblem {
     }
     __device__ __forceinline__ void load_b(uint32_t dst, int32_t k, const UnitInfo& ui,
                                            uint32_t bar) const {
-        tma_load_2d(dst, &tmB, k, ui.b_row, bar);
+        tma_load_2d(dst, ui.narrow ? &tmBn : &tmB, k, ui.b_row, bar);
     }
     // Pair forms: this CTA's rows (unit row + offset), bytes counted on the
     // leader's barrier (cluster address).
@@ -242,7 +270,7 @@ struct DenseProblem {
     }
     __device__ __forceinline__ void load_b_pair(uint32_t dst, int32_t k, const UnitInfo& ui,
                                                 int32_t row_off, uint32_t bar_cluster) const {
-        tma_load_2d_pair(dst, &tmB, k, ui.b_row + row_off, bar_cluster);
+        tma_load_2d_pair(dst, ui.narrow ? &tmBn : &tmB, k, ui.b_row + row_off, bar_cluster);
     }
     template <bool kOutF32>
     __device__ __forceinline__ void store(uint32_t buf, int32_t x, const UnitInfo& ui) const {
@@ -299,6 +327,8 @@ struct GroupedProblem {
         ui.store_z = g;
         ui.n_limit = N;
         ui.m_limit = rows;
+        ui.cols = BN;
+        ui.narrow = 0;
         return ui;
     }
     __device__ __forceinline__ void load_a(uint32_t dst, int32_t k, const UnitInfo& ui,
@@ -401,7 +431,7 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 const int32_t kb_end = min(ui.kb1, ui.kb0 + C::STAGES);
                 for (int32_t kb = ui.kb0; kb < kb_end; ++kb)
                     prob.prefetch_l2(kb * C::BK, ui, static_cast<int32_t>(rank) * C::BM,
-                                     static_cast<int32_t>(rank) * C::kBRows);
+                                     static_cast<int32_t>(rank) * (ui.cols / 2));
             }
         }
         __syncwarp();
@@ -433,6 +463,10 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
             bool ok = true;
             for (int32_t u = unit0; ok && u < prob.num_units(); u += unit_step) {
                 const UnitInfo ui = prob.unit(u, C::kTileM, C::BN, C::kGroupM);
+                // A pair's B rows: this CTA's half of the unit's columns.
+                const bool narrow = C::kTailSplit && ui.narrow != 0;
+                const uint32_t b_bytes = narrow ? C::kNarrowBBytes : C::kBBytes;
+                const int32_t b_off = static_cast<int32_t>(rank) * (ui.cols / 2);
                 for (int32_t kb = ui.kb0; kb < ui.kb1; ++kb) {
                     const uint32_t s = ring_stage(it, C::STAGES);
                     const uint32_t ph = ring_phase(it, C::STAGES);
@@ -453,14 +487,14 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                         // the phase once all bytes of both CTAs are in).
                         if (rank == 0)
                             mbar_arrive_expect_tx(full_bar(s),
-                                                  2 * (prob.a_box_bytes(C::BK) + C::kBBytes));
+                                                  2 * (prob.a_box_bytes(C::BK) + b_bytes));
                         const uint32_t leader_full = map_to_rank(full_bar(s), pair_leader);
                         prob.load_a_pair(sbase + C::kOffA + s * C::kABytes, kb * C::BK, ui,
                                          static_cast<int32_t>(rank) * C::BM, leader_full);
-                        prob.load_b_pair(sbase + C::kOffB + s * C::kBBytes, kb * C::BK, ui,
-                                         static_cast<int32_t>(rank) * C::kBRows, leader_full);
+                        prob.load_b_pair(sbase + C::kOffB + s * C::kBBytes, kb * C::BK, ui, b_off,
+                                         leader_full);
                     } else {
-                        mbar_arrive_expect_tx(full_bar(s), prob.a_box_bytes(C::BK) + C::kBBytes);
+                        mbar_arrive_expect_tx(full_bar(s), prob.a_box_bytes(C::BK) + b_bytes);
                         prob.load_a(sbase + C::kOffA + s * C::kABytes, kb * C::BK, ui, full_bar(s));
                         prob.load_b(sbase + C::kOffB + s * C::kBBytes, kb * C::BK, ui, full_bar(s));
                     }
@@ -489,6 +523,11 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 const UnitInfo ui = prob.unit(u, C::kTileM, C::BN, C::kGroupM);
                 const int32_t kb0 = ui.kb0;
                 const int32_t kb1 = ui.kb1;
+                // A tail-split part is an MMA of its own width (N = its columns).
+                const uint32_t idesc =
+                    C::kTailSplit && ui.narrow
+                        ? umma_idesc_16bit_f32(C::kTileM, static_cast<uint32_t>(ui.cols), C::kBF16)
+                        : C::kIdesc;
                 const uint32_t acc = tcount & 1u;
                 const uint32_t acc_ph = (tcount >> 1) & 1u;
                 if (!wait_or_abort(acc_empty_bar(acc), acc_ph ^ 1u, abort_flag, err,
@@ -512,9 +551,9 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                         const uint64_t bd = umma_desc_sw128_kmajor(b_addr + 32u * j);
                         const uint32_t accum = (kb != kb0 || j != 0) ? 1u : 0u;
                         if constexpr (C::kPair)
-                            mma_f16_ss_pair(d_tmem, ad, bd, C::kIdesc, accum);
+                            mma_f16_ss_pair(d_tmem, ad, bd, idesc, accum);
                         else
-                            mma_f16_ss(d_tmem, ad, bd, C::kIdesc, accum);
+                            mma_f16_ss(d_tmem, ad, bd, idesc, accum);
                     }
                     // stage s free (in both CTAs of a pair) once these MMAs finish
                     if constexpr (C::kPair)
@@ -583,8 +622,9 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
             if (!named_bar_and(1, C::kEpiThreads, ok)) break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + acc * C::kAccStride;
+            const int chunks = (C::kTailSplit && ui.narrow ? ui.cols : C::BN) / C::kEpiCols;
 #pragma unroll 1
-            for (int c = 0; c < C::BN / C::kEpiCols; ++c, ++box) {
+            for (int c = 0; c < chunks; ++c, ++box) {
                 uint32_t v[C::kEpiCols];
                 if constexpr (C::kEpiCols == 16) {
                     tmem_ld_32x32b_x16(t_row + c * C::kEpiCols,
@@ -596,7 +636,7 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                                            *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
                 }
                 tmem_ld_wait();
-                if (c == C::BN / C::kEpiCols - 1) {
+                if (c == chunks - 1) {
                     // Whole accumulator read: give it back to the MMA warp.
                     tc_fence_before();
                     __syncwarp();
@@ -812,6 +852,23 @@ GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) 
     p.kb_per_unit = ceil_div(p.k_blocks, splits);
     p.splits = ceil_div(p.k_blocks, p.kb_per_unit);   // no empty split
     p.units = p.tiles * p.splits;
+    p.full_units = p.units;
+    p.narrow_cols = 0;
+    p.narrow_b_rows = 0;
+    if constexpr (C::kTailSplit) {
+        // The last round holds tiles % slots tiles: at most half the slots,
+        // its tiles run as two parts each and that round takes about half
+        // the time.  (A fuller last round would still need one whole round.)
+        const int64_t full = p.tiles / slots * slots;
+        const int64_t tail = p.tiles - full;
+        if (p.splits == 1 && tail > 0 && 2 * tail <= slots &&
+            __atomic_load_n(&g_tail_split, __ATOMIC_ACQUIRE) != 1) {
+            p.full_units = full;
+            p.units = full + 2 * tail;
+            p.narrow_cols = C::kNarrowCols;
+            p.narrow_b_rows = C::kNarrowBRows;
+        }
+    }
     p.group_m = choose_group_m(M, N, K, p.grid_m, slots, C::kTileM, C::BN);
     p.grid = static_cast<int>(p.units < slots ? p.units : slots) * (C::kPair ? 2 : 1);
     p.threads = C::kThreads;
@@ -836,9 +893,29 @@ int64_t plan_cost(const GemmPlan& p) {
     // through distributed shared memory (about 2 us on GB300, ~2000 units).
     if (p.cluster_k > 0) return p.kb_per_unit * (p.bn + (p.pair ? 16 : 32)) + 2048;
     const int64_t slots = p.pair ? p.grid / 2 : p.grid;
-    const int64_t rounds = ceil_div(p.units, slots);
     // A pair streams half of B per SM: less operand traffic per k-block.
-    return rounds * p.kb_per_unit * (p.bn + (p.pair ? 16 : 32));
+    const int64_t c = p.pair ? 16 : 32;
+    if (p.narrow_cols > 0) {
+        // Whole rounds, then one round of the wider tail part.  A part moves
+        // more operand bytes per output than a whole tile: charge it 8 more.
+        // After whole rounds, a last round full of parts is slower still (on
+        // GB300, 8192^3: 72 parts on 76 pairs took 0.86 of a whole round,
+        // 8 parts at 4096 x 11008 x 4096 about 0.6): charge it 60 % more
+        // when every slot holds a part, in proportion below that.
+        const int64_t full_rounds = p.full_units / slots;
+        const int64_t parts = p.units - p.full_units;
+        int64_t narrow = p.kb_per_unit * (p.narrow_cols + c + 8);
+        if (full_rounds > 0) narrow += narrow * 3 * parts / (5 * slots);
+        // A single tile row: every B row streams from HBM once, and a part's
+        // B stages hold half the bytes of a tile's, too few in flight to hide
+        // the latency (256 x 8192 x 8192: 36.9 us in parts, 34.5 us for a
+        // 2-pair cluster split; 512 x 4096 x 4096, two tile rows: 24.3
+        // against 28.4 us).
+        if (full_rounds == 0 && p.grid_m == 1) narrow += narrow / 2;
+        return full_rounds * p.kb_per_unit * (p.bn + c) + narrow;
+    }
+    const int64_t rounds = ceil_div(p.units, slots);
+    return rounds * p.kb_per_unit * (p.bn + c);
 }
 
 // Per-device opt-in to > 48 KB dynamic shared memory for `kernel`, once per device.
@@ -879,6 +956,18 @@ cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUten
     prob.w.kb_per_unit = static_cast<int32_t>(plan.kb_per_unit);
     prob.w.group_m = static_cast<int32_t>(plan.group_m);
     prob.w.a_box_rows = plan.a_box_rows;
+    prob.w.full_units = static_cast<int32_t>(plan.full_units);
+    prob.w.narrow_cols = plan.narrow_cols;
+    if (plan.narrow_cols > 0) {
+        // The parts' B box must be the one the kernel counts bytes for.
+        if (!C::kTailSplit || args.tmBn == nullptr || plan.narrow_cols != C::kNarrowCols ||
+            plan.narrow_b_rows != C::kNarrowBRows || plan.full_units > plan.units)
+            return cudaErrorInvalidValue;
+        prob.tmBn = *args.tmBn;
+    } else {
+        if (plan.full_units != plan.units) return cudaErrorInvalidValue;
+        prob.tmBn = tmB;
+    }
     prob.d_out = args.d_out;
     const unsigned cluster = static_cast<unsigned>((C::kPair ? 2 : 1) * (C::kClusterK ? C::kClusterK : 1));
     return launch_kernel(kernel, dim3(static_cast<unsigned>(plan.grid)), dim3(C::kThreads),
@@ -972,6 +1061,7 @@ cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, int num_pairs, c
 int g_force_tile_n = 0;
 int g_pair_mode = 0;
 int g_cluster_split = 0;
+int g_tail_split = 0;
 int g_force_group_m = 0;
 int g_pdl = 1;
 
@@ -988,6 +1078,7 @@ GemmPlan plan_cluster_split(int64_t M, int64_t N, int64_t K, int64_t slots, int 
     if (slots <= 0 || p.splits != C::kClusterK || p.tiles * C::kClusterK > slots ||
         p.tiles > clusters_fit)
         p.units = 0;
+    p.full_units = p.units;
     p.grid = static_cast<int>(p.units) * (C::kPair ? 2 : 1);
     p.cluster_k = C::kClusterK;
     return p;

@@ -25,6 +25,13 @@ struct GemmPlan {
     int a_box_rows;        // rows of A per TMA box: 128, or M rounded up to 16 when M < 128
     int cluster_k;         // > 0: K split over clusters of this many CTAs (one unit per CTA)
     int group_m;           // L2 group height of the tile order, in tiles
+    // Tail split: the tiles of the last, partly filled round run as two units
+    // each (narrow_cols and bn - narrow_cols columns), when that round is at
+    // most half full.  Units < full_units are whole tiles; narrow_cols = 0
+    // (full_units = units) without a tail split.
+    int64_t full_units;
+    int narrow_cols;
+    int narrow_b_rows;     // rows of B per CTA in a part's box (narrow_cols, or half for a pair)
 };
 
 // How many clusters of each cluster-split configuration can be co-resident
@@ -55,6 +62,9 @@ extern int g_pair_mode;
 // cluster size whenever it applies (every tile x CK CTAs in one wave).
 extern int g_cluster_split;
 
+// Tail split of the plain GEMM: 0 automatic (wherever it applies), 1 never.
+extern int g_tail_split;
+
 // D = fp16/bf16(sum of `splits` FP32 partial M x N matrices laid out back to back).
 cudaError_t launch_splitk_reduce(const void* partials, void* D, int64_t M, int64_t N,
                                  int64_t splits, bool bf16, int num_sms, cudaStream_t stream);
@@ -64,6 +74,7 @@ struct GemmArgs {
     uint64_t wait_limit_ns;
     uint32_t* err_word;   // device address of the sticky error word
     void* d_out = nullptr;   // D itself, for the cluster-split epilogue
+    const CUtensorMap* tmBn = nullptr;   // B with box {bk, narrow_b_rows} (tail split only)
 };
 
 // Enqueue the GEMM kernel.  Tensor maps: A {K, M} box {bk, bm}; B {K, N} box
