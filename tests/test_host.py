@@ -218,6 +218,23 @@ def test_plan_with_cta_pairs_balances_waves():
     assert tg.tmagemm_gemm_plan(1024, 1024, 16384, 152, 0, 76)["pair"] == 0
 
 
+def test_cluster_split_ranking():
+    """Among cluster splits the plan weighs each CTA's B stream, the HBM
+    floor and the distributed-shared-memory reduction, not k-blocks alone:
+    a full 128-row tile makes a 4-way reduction of 256-wide tiles cost more
+    than the 2-way reduction of 192-wide ones (measured on GB300: 31.5-32.1
+    against 32.7-33.3 us at 128 x 8192 x 8192), and few tiles of a small
+    problem favour 4-way 128-wide over 8-way 256-wide splits (11.9 against
+    16.4 us at 128 x 3072 x 3072)."""
+    p = tg.tmagemm_gemm_plan(128, 8192, 8192, 152, 1, 76)
+    assert (p["cluster_k"], p["BN"], p["pair"], p["grid"]) == (2, 192, 0, 86), p
+    q = tg.tmagemm_gemm_plan(128, 3072, 3072, 152, 1, 76)
+    assert (q["cluster_k"], q["BN"], q["pair"]) == (4, 128, 0), q
+    # A few tokens keep the 4-way 256-wide split: its reduction covers one warp of rows.
+    r = tg.tmagemm_gemm_plan(32, 8192, 8192, 152, 1, 76)
+    assert (r["cluster_k"], r["BN"], r["pair"]) == (4, 256, 0), r
+
+
 def test_tail_split_plan():
     """A last round at most half full runs its tiles as two column parts: the
     whole rounds keep whole tiles, the parts fill the last round once."""

@@ -50,6 +50,7 @@
 // MMAs are drained, TMEM is freed, and the error word records the site.
 #include <cuda.h>
 #include <cuda_runtime.h>
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -193,9 +194,11 @@ struct UnitInfo {
     int32_t narrow;          // 1: a tail-split part (B through the narrow box)
 };
 
-// Dense problem: D (or split-K partials) = A * B^T.  Unit u covers output
-// tile u % num_tiles and k-blocks [split * kb_per_unit, min(k_blocks, ...))
-// with split = u / num_tiles.  Without split-K, kb_per_unit = k_blocks.
+// Dense problem: D (or split-K partials) = A * B^T.  Unit u < full_units
+// covers output tile u % num_tiles and k-blocks [split * kb_per_unit,
+// min(k_blocks, ...)) with split = u / num_tiles (without split-K,
+// kb_per_unit = k_blocks); the units after full_units are the column parts
+// of the tail-split tiles, over all of K.
 struct Work {
     int32_t M, N, grid_m, grid_n, num_tiles, num_units, k_blocks, kb_per_unit;
     int32_t group_m;   // L2 group height in tiles (chosen by the plan)
@@ -828,6 +831,9 @@ int choose_group_m(int64_t M, int64_t N, int64_t K, int64_t grid_m, int64_t slot
 template <class C>
 GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) {
     GemmPlan p{};
+    p.m = M;
+    p.n = N;
+    p.k = K;
     p.bm = C::BM;
     p.bn = C::BN;
     p.bk = C::BK;
@@ -888,9 +894,10 @@ GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) 
 // Modelled time of a plan: the busiest CTA runs ceil(units / grid) units of
 // kb_per_unit k-blocks, and a k-block costs about BN + 32 units of time (MMA
 // time grows with BN, the A operand traffic per k-block does not).
+// Cluster splits against the other plans: each split runs one wave of
+// units and then adds CK partial tiles through distributed shared memory
+// (about 2 us on GB300, ~2000 units).
 int64_t plan_cost(const GemmPlan& p) {
-    // A cluster split runs one wave of units and then adds CK partial tiles
-    // through distributed shared memory (about 2 us on GB300, ~2000 units).
     if (p.cluster_k > 0) return p.kb_per_unit * (p.bn + (p.pair ? 16 : 32)) + 2048;
     const int64_t slots = p.pair ? p.grid / 2 : p.grid;
     // A pair streams half of B per SM: less operand traffic per k-block.
@@ -916,6 +923,26 @@ int64_t plan_cost(const GemmPlan& p) {
     }
     const int64_t rounds = ceil_div(p.units, slots);
     return rounds * p.kb_per_unit * (p.bn + c);
+}
+
+// Cluster splits among themselves (in ns): the mainloop takes the slowest
+// of the MMAs, this CTA's own B stream (about 68 GB/s per SM; tile rows that
+// share B rows gain little from L2 in one wave) and all unique operand bytes
+// at about 6.5 TB/s; then the partial tiles are added through distributed shared memory:
+// about 2 us, plus 0.34 ns per remote float, (CK - 1) / CK of the tile's
+// existing rows (whole warps of 32) x BN; a CTA pair's coupled loads and
+// 256-row MMAs cost about 4.5 us more.  Fitted to GB300 timings of the 2-,
+// 4- and 8-CTA splits of 32..256 x 4096..14336 x 4096..14336 (each within
+// ~2.5 us; 8-CTA splits measured slower than it says).  Against the k-block
+// ranking it replaced it was faster on 10 of 11 shapes checked (up to 27 %,
+// 128 x 3072 x 3072) and 3.7 % slower on 384 x 4096 x 14336.
+int64_t cluster_split_cost(const GemmPlan& p) {
+    const int64_t compute = p.kb_per_unit * (p.bn + (p.pair ? 16 : 32));
+    const int64_t stream = p.b_box_rows * p.kb_per_unit * p.bk * 2 / 68;
+    const int64_t hbm = (p.m + p.n) * p.k * 2 / 6500;
+    const int64_t rows = (p.a_box_rows + 31) / 32 * 32;
+    const int64_t reduce = 2048 + rows * p.bn * (p.cluster_k - 1) * 34 / (100 * p.cluster_k);
+    return std::max(compute, std::max(stream, hbm)) + reduce + (p.pair ? 4500 : 0);
 }
 
 // Per-device opt-in to > 48 KB dynamic shared memory for `kernel`, once per device.
@@ -1094,6 +1121,7 @@ GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs,
     const int forced = __atomic_load_n(&g_force_tile_n, __ATOMIC_ACQUIRE);
     const bool pairs_ok = splits == 1 && pairs > 0 && pair_mode != 1;
     const bool singles_ok = !(pairs_ok && pair_mode == 2);
+    bool forced_ck = false;   // a forced cluster split size applies (the only candidate)
     if (splits == 1) {
         if (singles_ok) {
             cands[n++] = plan_for<Cfg256<T>>(M, N, K, sms, 1);
@@ -1127,7 +1155,6 @@ GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs,
             if (!pk) ck[3].units = ck[4].units = 0;
             if (pair_mode == 2)
                 for (int i : {0, 1, 2, 5, 6, 7, 8}) ck[i].units = 0;
-            bool forced_ck = false;
             for (const GemmPlan& c : ck)
                 if (c.units > 0 && ck_mode == c.cluster_k && (forced == 0 || c.bn == forced) &&
                     (!forced_ck || plan_cost(c) < plan_cost(cands[0]))) {
@@ -1152,6 +1179,18 @@ GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs,
         if (!have || plan_cost(c) < plan_cost(best)) {
             best = c;
             have = true;
+        }
+    }
+    // Where a cluster split wins, which one: its stream, HBM and reduction
+    // terms rank the splits better than k-blocks alone (128 x 8192 x 8192:
+    // 2-way 192-wide 31.5 us against 4-way 256-wide 32.7 us; 256 x 4096 x
+    // 4096: 18.4 against 20.0 us).
+    if (have && best.cluster_k > 0 && !forced_ck) {
+        for (int i = 0; i < n; ++i) {
+            const GemmPlan& c = cands[i];
+            if (c.cluster_k > 0 && (forced == 0 || c.bn == forced) &&
+                cluster_split_cost(c) < cluster_split_cost(best))
+                best = c;
         }
     }
     return best;

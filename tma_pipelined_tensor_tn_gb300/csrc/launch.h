@@ -32,6 +32,7 @@ struct GemmPlan {
     int64_t full_units;
     int narrow_cols;
     int narrow_b_rows;     // rows of B per CTA in a part's box (narrow_cols, or half for a pair)
+    int64_t m, n, k;       // the problem the plan is for
 };
 
 // How many clusters of each cluster-split configuration can be co-resident
