@@ -787,7 +787,7 @@ GROUPED_COUNTS = [1697, 2233, 321, 376, 105, 1822, 706, 932]
 
 CASES = ("gemm4096", "gemv", "splitk", "small_m8", "small_m16", "small_m32", "small_m64", "grouped",
          "bf16_gemm", "bf16_gemv",
-         "gemm8192", "gemm_ragged", "gemm256")
+         "gemm8192", "gemm_ragged", "gemm256", "decode128_8192")
 
 
 def run_case(args, name):
@@ -801,10 +801,11 @@ def run_case(args, name):
     torch.cuda.set_device(dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    if name in ("gemm4096", "bf16_gemm", "gemm8192", "splitk", "gemm_ragged", "gemm256"):
+    if name in ("gemm4096", "bf16_gemm", "gemm8192", "splitk", "gemm_ragged", "gemm256",
+                "decode128_8192"):
         M, N, K = {"gemm4096": (4096,) * 3, "bf16_gemm": (4096,) * 3, "gemm8192": (8192,) * 3,
                    "splitk": (1024, 1024, 16384), "gemm_ragged": (4000, 3000, 4160),
-                   "gemm256": (256,) * 3}[name]
+                   "gemm256": (256,) * 3, "decode128_8192": (128, 8192, 8192)}[name]
         A, B = inputs.gemm_inputs(M, N, K, seed=0)
         if name == "bf16_gemm":
             A, B = A.to(torch.bfloat16), B.to(torch.bfloat16)
