@@ -908,11 +908,16 @@ int64_t plan_cost(const GemmPlan& p) {
         // After whole rounds, a last round full of parts is slower still (on
         // GB300, 8192^3: 72 parts on 76 pairs took 0.86 of a whole round,
         // 8 parts at 4096 x 11008 x 4096 about 0.6): charge it 60 % more
-        // when every slot holds a part, in proportion below that.
+        // when every slot holds a part, in proportion below that.  Parts of
+        // pair tiles whose operands fit in L2 run near their width instead
+        // (1024 x 6144 x 4096: 72 parts in 0.69 of a 224-wide round); single
+        // CTAs' parts did not (384 x 14336 x 2048: 146 parts after one
+        // round, 26.5 us against 24.8 us for two rounds of pairs).
         const int64_t full_rounds = p.full_units / slots;
         const int64_t parts = p.units - p.full_units;
         int64_t narrow = p.kb_per_unit * (p.narrow_cols + c + 8);
-        if (full_rounds > 0) narrow += narrow * 3 * parts / (5 * slots);
+        const bool in_l2 = 2 * (p.m + p.n) * p.k + 2 * p.m * p.n <= kL2FitBytes;
+        if (full_rounds > 0 && !(in_l2 && p.pair)) narrow += narrow * 3 * parts / (5 * slots);
         // A single tile row: every B row streams from HBM once, and a part's
         // B stages hold half the bytes of a tile's, too few in flight to hide
         // the latency (256 x 8192 x 8192: 36.9 us in parts, 34.5 us for a
