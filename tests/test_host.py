@@ -260,6 +260,20 @@ def test_tail_split_plan():
         tg.tmagemm_gemm_tail_plan(0, 8, 8, 152, 76)
 
 
+def test_tail_split_with_operands_in_l2():
+    """Operands that fit in L2 (2(M+N)K + 2MN <= 96 MiB): a pair plan's parts
+    run near their width, so 1024 x 6144 x 4096 takes 112 pair tiles of 224
+    with the last 36 split (measured 36.4 us) over 128 tiles of 192 in two
+    whole rounds (37.7 us).  Single CTAs' parts keep the full-round charge:
+    384 x 14336 x 2048 stays on two rounds of 192-wide pair tiles."""
+    p = tg.tmagemm_gemm_plan(1024, 6144, 4096, 152, 1, 76)
+    t = tg.tmagemm_gemm_tail_plan(1024, 6144, 4096, 152, 76)
+    assert (p["BN"], p["pair"], p["tiles"]) == (224, 1, 112), p
+    assert t == {"full_units": 76, "split_tiles": 36, "narrow_cols": 128}
+    q = tg.tmagemm_gemm_plan(384, 14336, 2048, 152, 1, 76)
+    assert (q["BN"], q["pair"], q["tiles"], q["units"]) == (192, 1, 150, 150), q
+
+
 @pytest.mark.parametrize("sms,pairs", [(152, 76), (152, 0), (132, 66), (148, 0)])
 def test_tail_split_plan_invariants(sms, pairs):
     """Over many shapes: units = whole tiles + 2 x split tiles; a split happens
