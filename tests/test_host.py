@@ -30,6 +30,22 @@ def header_functions():
     return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\**\s+\**(\w+)\s*\(", text, flags=re.M)))
 
 
+def test_header_is_plain_c(tmp_path):
+    """include/tmagemm.h is a C ABI: it compiles as C99 and as C++17 with no
+    warnings, with nothing but the standard headers it includes itself."""
+    import shutil
+    import subprocess
+    src = tmp_path / "use_header.c"
+    src.write_text('#include "tmagemm.h"\nint main(void) { return tmagemm_version() > 0 ? 0 : 1; }\n')
+    inc = os.path.join(ROOT, "include")
+    for cc, args in (("gcc", ["-std=c99"]), ("g++", ["-std=c++17", "-x", "c++"])):
+        if shutil.which(cc) is None:
+            pytest.skip(f"{cc} not available")
+        r = subprocess.run([cc, *args, "-Wall", "-Wextra", "-Werror", "-I", inc, "-fsyntax-only",
+                            str(src)], capture_output=True, text=True)
+        assert r.returncode == 0, (cc, r.stderr)
+
+
 def test_library_exports_every_header_symbol():
     names = header_functions()
     assert "gemm_f16" in names and "gemv_f16" in names
