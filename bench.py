@@ -525,16 +525,26 @@ def _time_launches(fn, reps, stream):
     return e0.elapsed_time(e1) * 1e3 / reps
 
 
+# Spin cycles queued ahead of a per-launch distribution: about 10 ms at GB300
+# clocks, longer than the host needs to enqueue 100 launches and their events.
+HOLD_CYCLES = 20_000_000
+
+
 def _launch_distribution(fn, reps, stream):
     """Per-launch device times of `fn` (an event pair around every launch,
     which also keeps consecutive launches from overlapping): min, median and
-    90th percentile in microseconds."""
+    90th percentile in microseconds.  A spin kernel queued first holds the
+    stream until every launch and event is enqueued, so the time the host
+    takes to issue a launch (Python, ctypes, tensor-map encoding) never falls
+    between an event and its kernel."""
     import torch
     for _ in range(3):
         fn(0)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(reps)]
     torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(HOLD_CYCLES)
     for i, (e0, e1) in enumerate(evs):
         e0.record(stream)
         fn(i)
@@ -581,6 +591,16 @@ def measure_distributions(tg, dev, stream, l2):
     dist = _launch_distribution(gemv, 100, stream)
     dist["gbs_at_median"] = gemv_bytes() / dist["median_us"] / 1e3
     out["gemv_4096x14336_per_launch_cold"] = dist
+    # The same without programmatic dependent launch: each launch waits for
+    # the end of the event before it, with no early scheduling at all.
+    assert tg.tmagemm_set_pdl(0) == 0
+    try:
+        dist = _launch_distribution(gemv, 100, stream)
+    finally:
+        tg.tmagemm_set_pdl(1)
+    dist["gbs_at_median"] = gemv_bytes() / dist["median_us"] / 1e3
+    dist["note"] = "plain launches (no programmatic dependent launch)"
+    out["gemv_4096x14336_per_launch_cold_plain"] = dist
     dist = _launch_distribution(lambda i: gemv(i, vsets[:1]), 100, stream)
     dist["gbs_at_median"] = gemv_bytes() / dist["median_us"] / 1e3
     dist["note"] = "warm L2: the same 117 MB weight set every launch"

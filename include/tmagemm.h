@@ -27,6 +27,15 @@
  * early and record a sticky error; tmagemm_check() reports it.
  *
  * Thread safety: all entry points may be called from several host threads.
+ * The tuning setters (tmagemm_set_*) change process-wide defaults: every call
+ * reads them once, when it starts, so a call in progress is never affected,
+ * but a setter called while other threads use the library changes those
+ * threads' later calls.  Set them before the threads start, or pass per-call
+ * options to gemm_f16_ex / gemm_bf16_ex, which read no process-wide setting.
+ *
+ * Device state: per device and per CUDA context the library looks up its own
+ * device addresses and kernel attributes on first use; after cudaDeviceReset
+ * the next call in the new context looks them up again.
  */
 #ifndef TMAGEMM_H
 #define TMAGEMM_H
@@ -82,6 +91,48 @@ int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void
              void* stream);
 
 /*
+ * Per-call tuning of gemm_f16_ex / gemm_bf16_ex.  Every field 0 = the
+ * automatic choice; the other values mean what they mean for the
+ * process-wide setters further below:
+ *   tile_n        : tmagemm_set_tile_n       (256, 224, 192; 128 cluster splits only)
+ *   cta_pair      : tmagemm_set_cta_pair     (1 never, 2 always where possible)
+ *   cluster_split : tmagemm_set_cluster_split (1 never, 2, 4 or 8 CTAs)
+ *   tail_split    : tmagemm_set_tail_split   (1 never)
+ *   group_m       : tmagemm_set_group_m      (1..64)
+ *   small_m_route : tmagemm_set_small_m_route (1..3; 1 keeps 2 <= M <= 64 on
+ *                   the tile kernel here, since these calls take no workspace)
+ *   plain_launch  : 1 = launch without programmatic dependent launch, as
+ *                   tmagemm_set_pdl(0) does process-wide
+ *   m1_route      : 1 = compute M = 1 with the tcgen05 tile kernel instead of
+ *                   the GEMV (N % 8 == 0 is then required, as for M > 1)
+ * Results agree with the automatic choice up to FP32 accumulation order.
+ */
+typedef struct tmagemm_options {
+    int32_t tile_n;
+    int32_t cta_pair;
+    int32_t cluster_split;
+    int32_t tail_split;
+    int32_t group_m;
+    int32_t small_m_route;
+    int32_t plain_launch;
+    int32_t m1_route;
+} tmagemm_options;
+
+/* Sets every field of *opts to 0 (the automatic choices).  NULL is a no-op. */
+void tmagemm_options_init(tmagemm_options* opts);
+
+/*
+ * gemm_f16 / gemm_bf16 with per-call options instead of the process-wide
+ * settings (opts == NULL: the process-wide settings, i.e. gemm_f16 /
+ * gemm_bf16 themselves).  Same arguments, requirements and results; a field
+ * outside its range returns TMAGEMM_ERR_INVALID and launches nothing.
+ */
+int gemm_f16_ex(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+                const tmagemm_options* opts, void* stream);
+int gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+                 const tmagemm_options* opts, void* stream);
+
+/*
  * Split-K form of gemm_f16 for shapes with too few output tiles to fill the
  * GPU (e.g. small M x N with long K): the K range is cut into `splits` parts,
  * each (tile, part) is one work unit of the same persistent tcgen05 kernel,
@@ -119,7 +170,8 @@ int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void* A, const void* 
  *   32 MiB are rejected with TMAGEMM_ERR_SCRATCH_LIMIT; nothing is launched.
  *   No call allocates: no cudaMalloc, cudaFree or allocating library routine.
  *   The first call on each device looks up the array's device address on
- *   that device; make that first call before any stream capture.
+ *   that device (again after a cudaDeviceReset, in the new context); make
+ *   that first call before any stream capture.
  *   Every call shares the one array.  Calls whose kernels may overlap on the
  *   GPU (different streams, or several host threads) race on it; order them
  *   on one stream.  Its contents between calls do not matter: each call

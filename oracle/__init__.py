@@ -17,7 +17,9 @@ W N x K row-major, FP32 accumulate).
 from __future__ import annotations
 
 import ctypes
+import hashlib
 import os
+import platform
 import subprocess
 import threading
 
@@ -30,11 +32,20 @@ _lock = threading.Lock()
 _lib = None
 
 
+def _stamp() -> str:
+    """This machine's architecture and the bytes of ``oracle.c``."""
+    with open(_SRC, "rb") as f:
+        return hashlib.sha256(platform.machine().encode() + f.read()).hexdigest()
+
+
 def build(force: bool = False) -> str:
-    """Compile ``oracle.c`` into ``liboracle.so`` (gcc, -O2, OpenMP if available)."""
-    if (not force and os.path.exists(_LIB)
-            and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
-        return _LIB
+    """Compile ``oracle.c`` into ``liboracle.so`` (gcc, -O2, OpenMP if available),
+    unless a library built here from the same source exists."""
+    stamp = _LIB + ".stamp"
+    if not force and os.path.exists(_LIB) and os.path.exists(stamp):
+        with open(stamp) as f:
+            if f.read().strip() == _stamp():
+                return _LIB
     base = ["gcc", "-O2", "-std=c11", "-fPIC", "-shared", _SRC, "-o", _LIB + ".tmp", "-lm"]
     # -fno-fast-math keeps IEEE semantics; no -march flags so x86 and Arm agree.
     try:
@@ -44,6 +55,8 @@ def build(force: bool = False) -> str:
         subprocess.run(base[:1] + ["-fno-fast-math"] + base[1:], check=True,
                        capture_output=True)
     os.replace(_LIB + ".tmp", _LIB)
+    with open(stamp, "w") as f:
+        f.write(_stamp() + "\n")
     return _LIB
 
 

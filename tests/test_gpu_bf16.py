@@ -11,12 +11,10 @@ import pytest
 
 import oracle
 from tma_pipelined_tensor_tn_gb300 import inputs
+from tests.parity_util import compare_bf16
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
-
-ATOL, RTOL, SLACK = 1e-2, 8e-3, 2.0 ** -11
-
 
 @pytest.fixture(scope="module")
 def tg():
@@ -28,25 +26,6 @@ def tg():
 
 def to_bits(t):
     return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
-
-
-def bits_value(b):
-    with np.errstate(invalid="ignore"):
-        return (np.asarray(b, dtype=np.uint32) << 16).view(np.float32).astype(np.float64)
-
-
-def bf16_step(v):
-    a = np.abs(v)
-    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
-    return 2.0 ** (e - 7)
-
-
-def compare_bf16(gpu_bits, ref_bits, what):
-    g, r = bits_value(gpu_bits), bits_value(ref_bits)
-    assert np.all(np.isfinite(g)), what
-    err = np.abs(g - r)
-    assert np.all(err <= ATOL + RTOL * np.abs(r)), (what, float(err.max()))
-    assert np.all(err <= bf16_step(r) + SLACK), (what, float((err - bf16_step(r)).max()))
 
 
 def uniform_bf16(shape, seed):

@@ -1,10 +1,13 @@
-"""The host-buffer executor (HostGemmPipeline): overlapping the copies of
-neighbouring steps must not change any step's result."""
+"""The host-buffer executor (HostGemmPipeline, the end-to-end path the bench
+times): every step's D, copied back to host memory, matches the CPU oracle on
+that step's inputs, and overlapping the copies of neighbouring steps changes no
+step's result (each equals the direct device call bit for bit)."""
 import numpy as np
 import pytest
 
+import oracle
 from tma_pipelined_tensor_tn_gb300 import inputs
-from tests.parity_util import assert_bitexact
+from tests.parity_util import assert_bitexact, compare, compare_bf16
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -33,6 +36,8 @@ def test_pipeline_matches_direct_calls(tg, depth):
     pipe.synchronize()
     tg.check()
     for i in range(steps):
+        compare(Ds[i].numpy(), oracle.gemm_f16(As[i].numpy(), Bs[i].numpy()),
+                f"pipeline step {i} vs oracle")
         ref = tg.gemm(As[i].cuda(), Bs[i].cuda())
         tg.check()
         assert_bitexact(Ds[i].numpy(), ref.cpu().numpy(), f"step {i}")
@@ -55,6 +60,10 @@ def test_pipeline_bf16_pageable_and_two_runs(tg):
     pipe.run([], [], [])
     pipe.synchronize()
     for i in range(5):
+        ref_bits = oracle.gemm_bf16(As[i].view(torch.int16).numpy().view(np.uint16),
+                                    Bs[i].view(torch.int16).numpy().view(np.uint16))
+        compare_bf16(Ds[i].view(torch.int16).numpy().view(np.uint16), ref_bits,
+                     f"bf16 pipeline step {i} vs oracle")
         ref = tg.gemm(As[i].cuda(), Bs[i].cuda())
         tg.check()
         assert torch.equal(Ds[i], ref.cpu()), f"step {i}"

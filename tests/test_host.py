@@ -55,6 +55,29 @@ def test_library_exports_every_header_symbol():
         assert n in tg.SIGNATURES, n
 
 
+def test_options_init_and_validation():
+    """tmagemm_options_init zeroes every field; gemm_f16_ex / gemm_bf16_ex refuse
+    a field outside its range before any CUDA call."""
+    import ctypes
+    o = tg.TmagemmOptions()
+    for name, _ in tg.TmagemmOptions._fields_:
+        setattr(o, name, 7)
+    tg.lib().tmagemm_options_init(ctypes.byref(o))
+    assert all(getattr(o, name) == 0 for name, _ in tg.TmagemmOptions._fields_)
+    tg.lib().tmagemm_options_init(None)   # a no-op
+    assert ctypes.sizeof(tg.TmagemmOptions) == 8 * 4
+    bad = [dict(tile_n=100), dict(tile_n=-1), dict(cta_pair=3), dict(cluster_split=3),
+           dict(cluster_split=16), dict(tail_split=2), dict(group_m=65), dict(small_m_route=4),
+           dict(plain_launch=2), dict(m1_route=2), dict(m1_route=-1)]
+    dummy = 1 << 20   # never dereferenced: validation fails first
+    for fields in bad:
+        opts = tg.options(**fields)
+        for fn in (tg.gemm_f16_ex, tg.gemm_bf16_ex):
+            assert fn(256, 256, 256, dummy, dummy, dummy, opts) == tg.TMAGEMM_ERR_INVALID, fields
+    with pytest.raises(TypeError):
+        tg.options(no_such_field=1)
+
+
 def test_host_pipeline_argument_checks():
     """Checked before any CUDA call: bad sizes and NULL handles are refused."""
     import ctypes

@@ -3,13 +3,15 @@
 gemm_f16_splitk_noalloc runs split-K with the library's own fixed 32 MiB
 device array as workspace, for callers that cannot hand the library a buffer
 (no cudaMalloc allowed past their start-up, or all device memory owned by a
-host framework's pool).  This checks it through the C ABI against the
-existing entry point (gemm_f16_splitk with a caller workspace) on two calls in
-a row, and that oversized problems are refused.  The file is collected last
-on purpose and also passes on its own in a fresh process.
+host framework's pool).  This checks it through the C ABI against the CPU
+oracle and against the existing entry point (gemm_f16_splitk with a caller
+workspace) on two calls in a row, that repeated calls leave the device's free
+memory unchanged, and that oversized problems are refused.  The file is
+collected last on purpose and also passes on its own in a fresh process.
 """
 import pytest
 
+import oracle
 from tma_pipelined_tensor_tn_gb300 import inputs
 from tests.parity_util import compare
 
@@ -56,9 +58,35 @@ def test_noalloc_matches_caller_workspace_on_two_calls(tg):
         assert tg.gemm_f16_splitk_workspace_size(M, N, K, splits) <= SCRATCH_BYTES
         D = torch.full((M, N), float("nan"), dtype=torch.float16, device="cuda")
         assert without_allocation(tg, dA, dB, splits, D) == tg.TMAGEMM_OK
+        tg.check()
+        got = D.cpu().numpy()
+        compare(got, oracle.gemm_f16(A.numpy(), B.numpy()), f"no-alloc split-K {M}x{N}x{K} vs oracle")
         ref = with_caller_workspace(tg, dA, dB, splits)
         tg.check()
-        compare(D.cpu().numpy(), ref.cpu().numpy(), f"no-alloc split-K {M}x{N}x{K}")
+        compare(got, ref.cpu().numpy(), f"no-alloc split-K {M}x{N}x{K}")
+
+
+def test_noalloc_calls_leave_free_device_memory_unchanged(tg):
+    # After one call per shape (the first call on the device looks up the
+    # array's address and may load kernels), further calls must not change the
+    # device's free memory: nothing is allocated per call.
+    cases = []
+    for (M, N, K, splits, seed) in ((512, 768, 8192, 0, 62), (1000, 520, 4160, 4, 63)):
+        A, B = inputs.gemm_inputs(M, N, K, seed=seed)
+        D = torch.empty((M, N), dtype=torch.float16, device="cuda")
+        cases.append((A.cuda(), B.cuda(), splits, D))
+    for dA, dB, splits, D in cases:
+        assert without_allocation(tg, dA, dB, splits, D) == tg.TMAGEMM_OK
+    tg.check()
+    torch.cuda.synchronize()
+    free0, _ = torch.cuda.mem_get_info()
+    for _ in range(3):
+        for dA, dB, splits, D in cases:
+            assert without_allocation(tg, dA, dB, splits, D) == tg.TMAGEMM_OK
+    tg.check()
+    torch.cuda.synchronize()
+    free1, _ = torch.cuda.mem_get_info()
+    assert free1 == free0, f"free device memory changed by {free0 - free1} bytes"
 
 
 def test_noalloc_refuses_problems_beyond_its_scratch(tg):

@@ -18,10 +18,13 @@ from ._binding import (  # noqa: F401
     TMAGEMM_ERR_WORKSPACE,
     TMAGEMM_OK,
     TmaGemmError,
+    TmagemmOptions,
     check,
     gemm,
     gemm_bf16,
     gemm_f16,
+    gemm_f16_ex,
+    gemm_bf16_ex,
     gemm_f16_grouped,
     gemm_f16_small_m,
     gemm_f16_small_m_workspace_size,
@@ -35,6 +38,7 @@ from ._binding import (  # noqa: F401
     gemv_f16,
     gemv_bf16,
     lib,
+    options,
     strerror,
     tmagemm_check,
     tmagemm_gemm_plan,

@@ -26,11 +26,25 @@ TMAGEMM_ERR_WORKSPACE = -6
 TMAGEMM_ERR_SCRATCH_LIMIT = -7
 TMAGEMM_ERR_CHECK = -8
 
+
+
+class TmagemmOptions(ctypes.Structure):
+    """struct tmagemm_options: per-call tuning of gemm_f16_ex / gemm_bf16_ex
+    (every field 0 = automatic)."""
+    _fields_ = [(name, ctypes.c_int32) for name in (
+        "tile_n", "cta_pair", "cluster_split", "tail_split", "group_m", "small_m_route",
+        "plain_launch", "m1_route")]
+
+
 # Every symbol include/tmagemm.h declares, with (argtypes, restype).
 _i64, _p, _int = ctypes.c_int64, ctypes.c_void_p, ctypes.c_int
 _P64 = ctypes.POINTER(ctypes.c_int64)
+_POPT = ctypes.POINTER(TmagemmOptions)
 SIGNATURES = {
     "gemm_f16": ([_i64, _i64, _i64, _p, _p, _p, _p], _int),
+    "gemm_f16_ex": ([_i64, _i64, _i64, _p, _p, _p, _POPT, _p], _int),
+    "gemm_bf16_ex": ([_i64, _i64, _i64, _p, _p, _p, _POPT, _p], _int),
+    "tmagemm_options_init": ([_POPT], None),
     "gemv_f16": ([_i64, _i64, _p, _p, _p, _p], _int),
     "gemm_bf16": ([_i64, _i64, _i64, _p, _p, _p, _p], _int),
     "gemm_f16_grouped": ([_i64, _P64, _i64, _i64, _p, _p, _p, _p], _int),
@@ -99,6 +113,27 @@ def strerror(status: int) -> str:
 
 def gemm_f16(M, N, K, A, B, D, stream=None) -> int:
     return lib().gemm_f16(M, N, K, A, B, D, stream)
+
+
+def options(**fields) -> TmagemmOptions:
+    """A tmagemm_options with the named fields set (tmagemm_options_init first)."""
+    o = TmagemmOptions()
+    lib().tmagemm_options_init(ctypes.byref(o))
+    for k, v in fields.items():
+        if k not in dict(TmagemmOptions._fields_):
+            raise TypeError(f"unknown option {k!r}")
+        setattr(o, k, int(v))
+    return o
+
+
+def gemm_f16_ex(M, N, K, A, B, D, opts=None, stream=None) -> int:
+    return lib().gemm_f16_ex(M, N, K, A, B, D, ctypes.byref(opts) if opts is not None else None,
+                             stream)
+
+
+def gemm_bf16_ex(M, N, K, A, B, D, opts=None, stream=None) -> int:
+    return lib().gemm_bf16_ex(M, N, K, A, B, D, ctypes.byref(opts) if opts is not None else None,
+                              stream)
 
 
 def gemm_f16_grouped(G, m_offsets, N, K, A, B, D, stream=None) -> int:
@@ -285,8 +320,9 @@ def _check_f16_cuda(name, t, dtype=None):
         raise ValueError(f"{name} must be contiguous (row-major)")
 
 
-def gemm(A, B, out=None, stream=None):
-    """D = A @ B.T for CUDA fp16 or bf16 tensors A (M, K), B (N, K); returns D (M, N)."""
+def gemm(A, B, out=None, stream=None, opts=None):
+    """D = A @ B.T for CUDA fp16 or bf16 tensors A (M, K), B (N, K); returns D (M, N).
+    `opts` (a TmagemmOptions, see options()) selects gemm_f16_ex / gemm_bf16_ex."""
     import torch
     dt = A.dtype if A.dtype in (torch.float16, torch.bfloat16) else torch.float16
     _check_f16_cuda("A", A, dt)
@@ -300,11 +336,16 @@ def gemm(A, B, out=None, stream=None):
     _check_f16_cuda("out", out, dt)
     if tuple(out.shape) != (M, N):
         raise ValueError("out must be (M, N)")
-    fn = lib().gemm_bf16 if dt == torch.bfloat16 else lib().gemm_f16
+    name = "gemm_bf16" if dt == torch.bfloat16 else "gemm_f16"
     with torch.cuda.device(A.device):
-        s = fn(M, N, K, A.data_ptr(), B.data_ptr(), out.data_ptr(), _stream_handle(stream, A.device))
+        args = (M, N, K, A.data_ptr(), B.data_ptr(), out.data_ptr())
+        if opts is None:
+            s = getattr(lib(), name)(*args, _stream_handle(stream, A.device))
+        else:
+            name += "_ex"
+            s = getattr(lib(), name)(*args, ctypes.byref(opts), _stream_handle(stream, A.device))
     if s != TMAGEMM_OK:
-        raise TmaGemmError(s, "gemm_bf16" if dt == torch.bfloat16 else "gemm_f16")
+        raise TmaGemmError(s, name)
     return out
 
 

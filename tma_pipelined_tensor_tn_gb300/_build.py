@@ -7,7 +7,9 @@ shared library with the CUDA runtime linked statically, so the library loads
 from __future__ import annotations
 
 import glob
+import hashlib
 import os
+import platform
 import shutil
 import subprocess
 import sys
@@ -44,11 +46,29 @@ def _deps():
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)])
 
 
-def up_to_date(lib: str = LIB) -> bool:
-    if not os.path.exists(lib):
+def _stamp(flags) -> str:
+    """What a build depends on: this machine's architecture, the compiler
+    flags and the bytes of every source and header."""
+    h = hashlib.sha256()
+    h.update(platform.machine().encode())
+    h.update(" ".join(flags).encode())
+    for d in sorted(_deps()):
+        h.update(os.path.relpath(d, ROOT).encode())
+        with open(d, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def up_to_date(lib: str = LIB, flags=None) -> bool:
+    """True if `lib` exists and was built here from the current sources with
+    these flags (a library built on another machine or from other sources is
+    rebuilt)."""
+    if flags is None:
+        flags = ARCH + NVCC_FLAGS + (["-DTMAGEMM_CHECKED"] if lib == LIB_CHECKED else [])
+    if not os.path.exists(lib) or not os.path.exists(lib + ".stamp"):
         return False
-    t = os.path.getmtime(lib)
-    return all(os.path.getmtime(d) <= t for d in _deps())
+    with open(lib + ".stamp") as f:
+        return f.read().strip() == _stamp(flags)
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=None,
@@ -57,11 +77,11 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None,
     libtmagemm_checked.so); returns its path."""
     lib_path = LIB_CHECKED if checked else LIB
     build_dir = BUILD_CHECKED if checked else BUILD
-    if not force and up_to_date(lib_path):
+    flags = ARCH + NVCC_FLAGS + (["-DTMAGEMM_CHECKED"] if checked else []) + list(extra_flags or [])
+    if not force and up_to_date(lib_path, flags):
         return lib_path
     os.makedirs(build_dir, exist_ok=True)
     cc = nvcc()
-    flags = ARCH + NVCC_FLAGS + (["-DTMAGEMM_CHECKED"] if checked else []) + list(extra_flags or [])
     procs = []
     objs = []
     for src in _sources():
@@ -86,6 +106,8 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None,
     if r.returncode != 0:
         raise RuntimeError("link failed:\n" + " ".join(link) + "\n" + r.stdout + r.stderr)
     os.replace(tmp, lib_path)
+    with open(lib_path + ".stamp", "w") as f:
+        f.write(_stamp(flags) + "\n")
     return lib_path
 
 

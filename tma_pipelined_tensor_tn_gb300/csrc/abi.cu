@@ -36,8 +36,19 @@ namespace {
 
 constexpr int kMaxDevices = 64;
 
+// Process-wide tuning defaults (tmagemm_set_*); each call reads them once, at
+// its start, into a Tuning of its own.
+int g_force_tile_n = 0;
+int g_pair_mode = 0;
+int g_cluster_split = 0;
+int g_tail_split = 0;
+int g_force_group_m = 0;
+int g_small_m_route = 0;
+int g_pdl = 1;
+
 struct DeviceState {
     bool ready = false;
+    uint64_t ctx_id = 0;    // the context the set-up below belongs to
     int sms = 0;
     int pairs = 0;          // co-resident two-CTA clusters of the pair kernel
     ClusterCaps caps;       // co-resident clusters of the cluster-split kernels
@@ -49,6 +60,9 @@ std::mutex g_mutex;
 DeviceState g_dev[kMaxDevices];
 std::atomic<int> g_last_detail{0};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+PFN_cuCtxGetCurrent_v4000 g_ctx_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_id = nullptr;
+std::once_flag g_ctx_fns_once;
 
 uint64_t wait_limit_ns() {
     static const uint64_t v = [] {
@@ -60,14 +74,63 @@ uint64_t wait_limit_ns() {
     return v;
 }
 
-// Per-device set-up, once, with that device current.
+}  // namespace
+
+Tuning process_tuning() {
+    Tuning t;
+    t.tile_n = __atomic_load_n(&g_force_tile_n, __ATOMIC_ACQUIRE);
+    t.pair_mode = __atomic_load_n(&g_pair_mode, __ATOMIC_ACQUIRE);
+    t.cluster_split = __atomic_load_n(&g_cluster_split, __ATOMIC_ACQUIRE);
+    t.tail_split = __atomic_load_n(&g_tail_split, __ATOMIC_ACQUIRE);
+    t.group_m = __atomic_load_n(&g_force_group_m, __ATOMIC_ACQUIRE);
+    t.small_m_route = __atomic_load_n(&g_small_m_route, __ATOMIC_ACQUIRE);
+    t.plain_launch = __atomic_load_n(&g_pdl, __ATOMIC_ACQUIRE) ? 0 : 1;
+    return t;
+}
+
+uint64_t current_context_id() {
+    std::call_once(g_ctx_fns_once, [] {
+        cudaDriverEntryPointQueryResult q{};
+        void* fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+    if (!g_ctx_current || !g_ctx_id) return 0;
+    CUcontext ctx = nullptr;
+    if (g_ctx_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    unsigned long long id = 0;
+    if (g_ctx_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return static_cast<uint64_t>(id);
+}
+
+namespace {
+
+// Per-device set-up, with that device current: once per context of the
+// device (a cudaDeviceReset ends the context; the next call finds a new one
+// and repeats the set-up, since the error word's address may have moved).
 int device_state(DeviceState** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TMAGEMM_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return TMAGEMM_ERR_UNSUPPORTED;
+    uint64_t ctx = current_context_id();
+    if (ctx == 0) {
+        // No context current yet: the runtime creates the device's primary
+        // context on its first call that needs one, e.g. this look-up.
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_err_word) != cudaSuccess) return TMAGEMM_ERR_CUDA;
+        ctx = current_context_id();
+    }
     std::lock_guard<std::mutex> lock(g_mutex);
     DeviceState& d = g_dev[dev];
-    if (!d.ready) {
+    if (!d.ready || d.ctx_id != ctx) {
+        d.ready = false;
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return TMAGEMM_ERR_CUDA;
         if (cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) !=
@@ -89,6 +152,7 @@ int device_state(DeviceState** out) {
             d.pairs = max_resident_pairs();
             d.caps = query_cluster_caps();
         }
+        d.ctx_id = ctx;
         d.ready = true;
     }
     if (d.cc_major != 10) return TMAGEMM_ERR_UNSUPPORTED;   // sm_100 family only
@@ -138,21 +202,22 @@ int validate_common(int64_t a, int64_t b, int64_t c) {
     return TMAGEMM_OK;
 }
 
-int gemv_impl(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream,
-              bool bf16 = false) {
+int gemv_impl(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream, bool bf16,
+              const Tuning& t) {
     if (!x || !W || !y) return TMAGEMM_ERR_INVALID;
     if (int s = validate_common(N, K, 1)) return s;
     if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (K % 8) != 0) return TMAGEMM_ERR_ALIGN;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    cudaError_t e = launch_gemv(N, K, x, W, y, bf16, static_cast<cudaStream_t>(stream), d->err_word);
+    cudaError_t e = launch_gemv(N, K, x, W, y, bf16, static_cast<cudaStream_t>(stream), d->err_word,
+                                t.pdl());
     return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 
 // Encodes the tensor maps for `plan` and launches it; for a split-K plan also
 // the reduction of the workspace into D.
 int run_gemm(const GemmPlan& plan, DeviceState* d, int64_t M, int64_t N, int64_t K, const void* A,
-             const void* B, void* D, void* workspace, void* stream) {
+             const void* B, void* D, void* workspace, void* stream, const Tuning& t) {
     CUtensorMap tmA, tmB, tmD;
     if (int s = encode_2d(&tmA, A, K, M, plan.bk, plan.a_box_rows, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, plan.bf16))
@@ -177,6 +242,7 @@ int run_gemm(const GemmPlan& plan, DeviceState* d, int64_t M, int64_t N, int64_t
     args.wait_limit_ns = wait_limit_ns();
     args.err_word = d->err_word;
     args.d_out = D;
+    args.pdl = t.pdl();
     // Tail-split parts read B through a box of narrow_b_rows rows.
     CUtensorMap tmBn;
     if (plan.narrow_cols > 0) {
@@ -189,7 +255,7 @@ int run_gemm(const GemmPlan& plan, DeviceState* d, int64_t M, int64_t N, int64_t
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_gemm_tn(plan, tmA, tmB, tmD, args, st);
     if (e == cudaSuccess && plan.out_f32)
-        e = launch_splitk_reduce(workspace, D, M, N, plan.splits, plan.bf16, d->sms, st);
+        e = launch_splitk_reduce(workspace, D, M, N, plan.splits, plan.bf16, d->sms, t.pdl(), st);
     return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 
@@ -198,7 +264,7 @@ int run_gemm(const GemmPlan& plan, DeviceState* d, int64_t M, int64_t N, int64_t
 
 using namespace tmagemm;
 
-extern "C" {
+namespace {
 
 enum class SmallMKernel { kSwapAB, kFragments, kLsu, kTile };
 
@@ -216,8 +282,8 @@ enum class SmallMKernel { kSwapAB, kFragments, kLsu, kTile };
 //   everywhere (14336 x 4096, M = 17..64: 23-26 us; swap-AB 29-30, LSU-fed
 //   49-89).
 // Route 2 forces the fragments wherever they apply (M <= 16).
-static SmallMKernel small_m_kernel(int64_t M, int64_t N, int num_sms) {
-    const int route = __atomic_load_n(&g_small_m_route, __ATOMIC_ACQUIRE);
+SmallMKernel small_m_kernel(int64_t M, int64_t N, int num_sms, const Tuning& t) {
+    const int route = t.small_m_route;
     if (route == 1) return SmallMKernel::kSwapAB;
     if (route == 3) return SmallMKernel::kLsu;
     if (M > small_m_mma_max_m()) return SmallMKernel::kTile;
@@ -229,13 +295,14 @@ static SmallMKernel small_m_kernel(int64_t M, int64_t N, int num_sms) {
 
 // The workspace-free small-M kernels (register fragments, LSU-fed tcgen05),
 // fp16 or bf16 operands and output.
-static int small_m_no_workspace(SmallMKernel k, int64_t M, int64_t N, int64_t K, const void* X,
-                                const void* W, void* D, void* stream, bool bf16 = false) {
+int small_m_no_workspace(SmallMKernel k, int64_t M, int64_t N, int64_t K, const void* X,
+                         const void* W, void* D, void* stream, bool bf16, const Tuning& t) {
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
     if (k == SmallMKernel::kFragments)
-        return launch_small_m_mma(M, N, K, X, W, D, st, bf16, d->sms, d->err_word) == cudaSuccess
+        return launch_small_m_mma(M, N, K, X, W, D, st, bf16, d->sms, d->err_word, t.pdl()) ==
+                       cudaSuccess
                    ? TMAGEMM_OK
                    : TMAGEMM_ERR_CUDA;
     // X {K, M} in boxes of 64 k x Mp token rows (rows past M read as zero).
@@ -243,8 +310,8 @@ static int small_m_no_workspace(SmallMKernel k, int64_t M, int64_t N, int64_t K,
     if (int s = encode_2d(&tmX, X, K, M, 64, small_m_lsu_cols(M), CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, bf16))
         return s;
-    return launch_small_m_lsu(tmX, M, N, K, W, D, wait_limit_ns(), d->err_word, st, bf16) ==
-                   cudaSuccess
+    return launch_small_m_lsu(tmX, M, N, K, W, D, wait_limit_ns(), d->err_word, st, bf16,
+                              t.pdl()) == cudaSuccess
                ? TMAGEMM_OK
                : TMAGEMM_ERR_CUDA;
 }
@@ -253,36 +320,101 @@ static int small_m_no_workspace(SmallMKernel k, int64_t M, int64_t N, int64_t K,
 // where small_m_kernel picks it (or the LSU-fed kernel up to 64 rows when
 // route 3 forces it) and returns true with its status in *status; false if
 // the tile kernel should run.
-static bool few_rows(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
-                     void* stream, bool bf16, int* status) {
-    if (M > 64) return false;
+bool few_rows(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+              void* stream, bool bf16, const Tuning& t, int* status) {
+    if (M < 2 || M > 64) return false;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) {
         *status = s;
         return true;
     }
-    const SmallMKernel k = small_m_kernel(M, N, d->sms);
+    const SmallMKernel k = small_m_kernel(M, N, d->sms, t);
     if (k != SmallMKernel::kFragments && k != SmallMKernel::kLsu) return false;
-    *status = small_m_no_workspace(k, M, N, K, A, B, D, stream, bf16);
+    *status = small_m_no_workspace(k, M, N, K, A, B, D, stream, bf16, t);
     return true;
 }
 
-int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
-             void* stream) {
+// gemm_f16 / gemm_bf16 under tuning `t`: M = 1 the GEMV (or, with
+// m1_route = 1, the tile kernel), a few rows the register-fragment kernel,
+// otherwise the tile kernel with the plan for this shape.
+int gemm_impl(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D, void* stream,
+              bool bf16, const Tuning& t) {
     if (!A || !B || !D) return TMAGEMM_ERR_INVALID;
     if (int s = validate_common(M, N, K)) return s;
-    if (M == 1) return gemv_impl(N, K, A, B, D, stream);
+    if (M == 1 && t.m1_route == 0) return gemv_impl(N, K, A, B, D, stream, bf16, t);
     if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
         return TMAGEMM_ERR_ALIGN;
     // A few rows: the register-fragment kernel streams B fastest up to 16
     // rows (GB300, N = 4096, K = 14336: 21.5 us against 30 us for the tile
     // kernel); above that the tile kernel with its cluster split.
     int fr = TMAGEMM_OK;
-    if (few_rows(M, N, K, A, B, D, stream, false, &fr)) return fr;
+    if (few_rows(M, N, K, A, B, D, stream, bf16, t, &fr)) return fr;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    return run_gemm(plan_gemm(M, N, K, d->sms, 1, false, d->pairs, d->caps), d, M, N, K, A, B, D,
-                    nullptr, stream);
+    return run_gemm(plan_gemm(M, N, K, d->sms, t, 1, bf16, d->pairs, d->caps), d, M, N, K, A, B, D,
+                    nullptr, stream, t);
+}
+
+// The per-call options as a Tuning; TMAGEMM_ERR_INVALID for a value outside
+// its documented range.
+int tuning_from_options(const tmagemm_options* o, Tuning* t) {
+    if (!o) {
+        *t = process_tuning();
+        return TMAGEMM_OK;
+    }
+    const int32_t bn = o->tile_n, ck = o->cluster_split;
+    if ((bn != 0 && bn != 256 && bn != 224 && bn != 192 && bn != 128) || o->cta_pair < 0 ||
+        o->cta_pair > 2 || (ck != 0 && ck != 1 && ck != 2 && ck != 4 && ck != 8) ||
+        o->tail_split < 0 || o->tail_split > 1 || o->group_m < 0 || o->group_m > 64 ||
+        o->small_m_route < 0 || o->small_m_route > 3 || o->plain_launch < 0 ||
+        o->plain_launch > 1 || o->m1_route < 0 || o->m1_route > 1)
+        return TMAGEMM_ERR_INVALID;
+    t->tile_n = bn;
+    t->pair_mode = o->cta_pair;
+    t->cluster_split = ck;
+    t->tail_split = o->tail_split;
+    t->group_m = o->group_m;
+    t->small_m_route = o->small_m_route;
+    t->plain_launch = o->plain_launch;
+    t->m1_route = o->m1_route;
+    return TMAGEMM_OK;
+}
+
+// Columns of the tcgen05 swap-AB tile for M activation rows: 16, else 64.
+// Rows 17..32 run padded to 64: on GB300 the 64-wide configuration measured
+// 33 us against 37 us for the 32-wide one at N = 4096, K = 14336.
+int64_t small_m_tile_rows(int64_t M) { return M <= 16 ? M : 64; }
+
+}  // namespace
+
+extern "C" {
+
+int gemm_f16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+             void* stream) {
+    return gemm_impl(M, N, K, A, B, D, stream, false, process_tuning());
+}
+
+int gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+              void* stream) {
+    return gemm_impl(M, N, K, A, B, D, stream, true, process_tuning());
+}
+
+void tmagemm_options_init(tmagemm_options* opts) {
+    if (opts) *opts = tmagemm_options{};
+}
+
+int gemm_f16_ex(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+                const tmagemm_options* opts, void* stream) {
+    Tuning t;
+    if (int s = tuning_from_options(opts, &t)) return s;
+    return gemm_impl(M, N, K, A, B, D, stream, false, t);
+}
+
+int gemm_bf16_ex(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
+                 const tmagemm_options* opts, void* stream) {
+    Tuning t;
+    if (int s = tuning_from_options(opts, &t)) return s;
+    return gemm_impl(M, N, K, A, B, D, stream, true, t);
 }
 
 int64_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int64_t splits) {
@@ -291,7 +423,7 @@ int64_t gemm_f16_splitk_workspace_size(int64_t M, int64_t N, int64_t K, int64_t 
     if (M == 1) return 0;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    const GemmPlan p = plan_gemm(M, N, K, d->sms, splits == 0 ? 0 : splits);
+    const GemmPlan p = plan_gemm(M, N, K, d->sms, process_tuning(), splits == 0 ? 0 : splits);
     // No FP32 partials (one part, or gemm_f16's own plan): no workspace.
     if (!p.out_f32 || p.splits <= 1) return 0;
     return p.splits * M * N * 4;
@@ -302,22 +434,27 @@ int gemm_f16_splitk(int64_t M, int64_t N, int64_t K, const void* A, const void* 
     if (!A || !B || !D) return TMAGEMM_ERR_INVALID;
     if (splits < 0 || splits > 4096) return TMAGEMM_ERR_INVALID;
     if (int s = validate_common(M, N, K)) return s;
-    if (M == 1) return gemv_impl(N, K, A, B, D, stream);
+    const Tuning t = process_tuning();
+    if (M == 1) return gemv_impl(N, K, A, B, D, stream, false, t);
     if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
         return TMAGEMM_ERR_ALIGN;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    const GemmPlan p = plan_gemm(M, N, K, d->sms, splits == 0 ? 0 : splits);
+    const GemmPlan p = plan_gemm(M, N, K, d->sms, t, splits == 0 ? 0 : splits);
     if (!p.out_f32 || p.splits <= 1)   // no FP32 partials: gemm_f16's plan, no workspace
-        return run_gemm(plan_gemm(M, N, K, d->sms, 1, false, d->pairs, d->caps), d, M, N, K, A,
-                        B, D, nullptr, stream);
+        return run_gemm(plan_gemm(M, N, K, d->sms, t, 1, false, d->pairs, d->caps), d, M, N, K, A,
+                        B, D, nullptr, stream, t);
     if (!workspace || !aligned16(workspace) || workspace_bytes < p.splits * M * N * 4)
         return TMAGEMM_ERR_WORKSPACE;
-    return run_gemm(p, d, M, N, K, A, B, D, workspace, stream);
+    return run_gemm(p, d, M, N, K, A, B, D, workspace, stream, t);
 }
 
 int gemv_f16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream) {
-    return gemv_impl(N, K, x, W, y, stream);
+    return gemv_impl(N, K, x, W, y, stream, false, process_tuning());
+}
+
+int gemv_bf16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream) {
+    return gemv_impl(N, K, x, W, y, stream, true, process_tuning());
 }
 
 int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, const void* A,
@@ -333,6 +470,7 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
     if (G * N > (int64_t(1) << 31) - 1) return TMAGEMM_ERR_UNSUPPORTED;
     if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
         return TMAGEMM_ERR_ALIGN;
+    const Tuning t = process_tuning();
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
     GroupedLaunch g{};
@@ -340,7 +478,7 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
     g.groups = G;
     g.N = N;
     g.K = K;
-    g.bn = grouped_tile_n(m_offsets, G, N, d->sms, d->pairs, &g.pair);
+    g.bn = grouped_tile_n(m_offsets, G, N, d->sms, d->pairs, t, &g.pair);
     const int epi_cols = g.bn == 224 ? 32 : 64;
     if (int s = encode_2d(&g.tmA, A, K, rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
@@ -373,23 +511,20 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
     args.K = static_cast<int32_t>(K);
     args.wait_limit_ns = wait_limit_ns();
     args.err_word = d->err_word;
+    args.pdl = t.pdl();
     cudaError_t e = launch_grouped(g, d->sms, d->pairs, args, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
-
-// Columns of the tcgen05 swap-AB tile for M activation rows: 16, else 64.
-// Rows 17..32 run padded to 64: on GB300 the 64-wide configuration measured
-// 33 us against 37 us for the 32-wide one at N = 4096, K = 14336.
-static int64_t small_m_tile_rows(int64_t M) { return M <= 16 ? M : 64; }
 
 int64_t gemm_f16_small_m_workspace_size(int64_t M, int64_t N, int64_t K) {
     if (int s = validate_common(M, N, K)) return s;
     if (M < 2 || M > 64) return TMAGEMM_ERR_UNSUPPORTED;
     // Only swap-AB needs one (route 1, which does not depend on the shape).
-    if (small_m_kernel(M, N, 0) != SmallMKernel::kSwapAB) return 0;
+    const Tuning t = process_tuning();
+    if (small_m_kernel(M, N, 0, t) != SmallMKernel::kSwapAB) return 0;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    const GemmPlan p = plan_small_m(small_m_tile_rows(M), N, K, d->sms, 0);
+    const GemmPlan p = plan_small_m(small_m_tile_rows(M), N, K, d->sms, 0, t);
     return p.splits * N * p.bn * 4;
 }
 
@@ -400,15 +535,15 @@ int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void*
     if (M < 2 || M > 64) return TMAGEMM_ERR_UNSUPPORTED;
     if (!aligned16(X) || !aligned16(W) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
         return TMAGEMM_ERR_ALIGN;
-    DeviceState* dev = nullptr;
-    if (int s = device_state(&dev)) return s;
-    const SmallMKernel kern = small_m_kernel(M, N, dev->sms);
-    if (kern == SmallMKernel::kTile) return gemm_f16(M, N, K, X, W, D, stream);
-    if (kern != SmallMKernel::kSwapAB) return small_m_no_workspace(kern, M, N, K, X, W, D, stream);
-    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const Tuning t = process_tuning();
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    const GemmPlan p = plan_small_m(small_m_tile_rows(M), N, K, d->sms, 0);
+    const SmallMKernel kern = small_m_kernel(M, N, d->sms, t);
+    if (kern == SmallMKernel::kTile) return gemm_impl(M, N, K, X, W, D, stream, false, t);
+    if (kern != SmallMKernel::kSwapAB)
+        return small_m_no_workspace(kern, M, N, K, X, W, D, stream, false, t);
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const GemmPlan p = plan_small_m(small_m_tile_rows(M), N, K, d->sms, 0, t);
     const int64_t need = p.splits * N * p.bn * 4;
     if (!workspace || !aligned16(workspace) || workspace_bytes < need) return TMAGEMM_ERR_WORKSPACE;
     // Swapped roles: the weights are the 128-row operand, the activations the
@@ -427,28 +562,11 @@ int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void*
     args.K = static_cast<int32_t>(K);
     args.wait_limit_ns = wait_limit_ns();
     args.err_word = d->err_word;
+    args.pdl = t.pdl();
     cudaError_t e = launch_small_m(p, tmW, tmX, tmP, args, st);
-    if (e == cudaSuccess) e = launch_small_m_reduce(workspace, D, M, N, p.bn, p.splits, st);
+    if (e == cudaSuccess)
+        e = launch_small_m_reduce(workspace, D, M, N, p.bn, p.splits, t.pdl(), st);
     return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
-}
-
-int gemm_bf16(int64_t M, int64_t N, int64_t K, const void* A, const void* B, void* D,
-              void* stream) {
-    if (!A || !B || !D) return TMAGEMM_ERR_INVALID;
-    if (int s = validate_common(M, N, K)) return s;
-    if (M == 1) return gemv_impl(N, K, A, B, D, stream, true);
-    if (!aligned16(A) || !aligned16(B) || !aligned16(D) || (K % 8) != 0 || (N % 8) != 0)
-        return TMAGEMM_ERR_ALIGN;
-    int fr = TMAGEMM_OK;
-    if (few_rows(M, N, K, A, B, D, stream, true, &fr)) return fr;   // as in gemm_f16
-    DeviceState* d = nullptr;
-    if (int s = device_state(&d)) return s;
-    return run_gemm(plan_gemm(M, N, K, d->sms, 1, true, d->pairs, d->caps), d, M, N, K, A, B, D,
-                    nullptr, stream);
-}
-
-int gemv_bf16(int64_t N, int64_t K, const void* x, const void* W, void* y, void* stream) {
-    return gemv_impl(N, K, x, W, y, stream, true);
 }
 
 int tmagemm_check(void* stream) {
@@ -583,9 +701,9 @@ int plan_query(int64_t M, int64_t N, int64_t K, int64_t num_sms, int64_t num_pai
         // The plan gemm_f16 runs on the current device.
         DeviceState* d = nullptr;
         if (int s = device_state(&d)) return s;
-        *p = plan_gemm(M, N, K, d->sms, splits, false, d->pairs, d->caps);
+        *p = plan_gemm(M, N, K, d->sms, process_tuning(), splits, false, d->pairs, d->caps);
     } else {
-        *p = plan_gemm(M, N, K, static_cast<int>(num_sms), splits, false,
+        *p = plan_gemm(M, N, K, static_cast<int>(num_sms), process_tuning(), splits, false,
                        static_cast<int>(num_pairs));
     }
     return TMAGEMM_OK;

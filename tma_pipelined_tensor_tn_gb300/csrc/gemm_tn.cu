@@ -814,8 +814,8 @@ splitk_reduce_kernel(const float4* __restrict__ P, uint4* __restrict__ D, int64_
 constexpr int64_t kL2FitBytes = 96ll << 20;
 
 int choose_group_m(int64_t M, int64_t N, int64_t K, int64_t grid_m, int64_t slots, int tile_m,
-                   int bn) {
-    const int forced = __atomic_load_n(&g_force_group_m, __ATOMIC_ACQUIRE);
+                   int bn, const Tuning& t) {
+    const int forced = t.group_m;
     int64_t g = 1;
     if (forced > 0) {
         g = forced;
@@ -829,7 +829,7 @@ int choose_group_m(int64_t M, int64_t N, int64_t K, int64_t grid_m, int64_t slot
 }
 
 template <class C>
-GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) {
+GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits, const Tuning& t) {
     GemmPlan p{};
     p.m = M;
     p.n = N;
@@ -867,15 +867,14 @@ GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits) 
         // the time.  (A fuller last round would still need one whole round.)
         const int64_t full = p.tiles / slots * slots;
         const int64_t tail = p.tiles - full;
-        if (p.splits == 1 && tail > 0 && 2 * tail <= slots &&
-            __atomic_load_n(&g_tail_split, __ATOMIC_ACQUIRE) != 1) {
+        if (p.splits == 1 && tail > 0 && 2 * tail <= slots && t.tail_split != 1) {
             p.full_units = full;
             p.units = full + 2 * tail;
             p.narrow_cols = C::kNarrowCols;
             p.narrow_b_rows = C::kNarrowBRows;
         }
     }
-    p.group_m = choose_group_m(M, N, K, p.grid_m, slots, C::kTileM, C::BN);
+    p.group_m = choose_group_m(M, N, K, p.grid_m, slots, C::kTileM, C::BN, t);
     p.grid = static_cast<int>(p.units < slots ? p.units : slots) * (C::kPair ? 2 : 1);
     p.threads = C::kThreads;
     p.smem_bytes = static_cast<int>(C::kSmemBytes);
@@ -950,28 +949,11 @@ int64_t cluster_split_cost(const GemmPlan& p) {
     return std::max(compute, std::max(stream, hbm)) + reduce + (p.pair ? 4500 : 0);
 }
 
-// Per-device opt-in to > 48 KB dynamic shared memory for `kernel`, once per device.
-template <class K>
-cudaError_t smem_opt_in(K kernel, int bytes, std::atomic<bool> (&done)[64]) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    if (dev >= 0 && dev < 64 && done[dev].load(std::memory_order_acquire)) return cudaSuccess;
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    // The whole configurable L1/shared split goes to shared memory, so CTAs
-    // that ask for half of it can sit two to an SM.
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 static_cast<int>(cudaSharedmemCarveoutMaxShared));
-    if (e == cudaSuccess && dev >= 0 && dev < 64) done[dev].store(true, std::memory_order_release);
-    return e;
-}
-
 template <class C>
 cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
                        const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream) {
     auto kernel = gemm_tn_f16_kernel<C, DenseProblem>;
-    static std::atomic<bool> attr_done[64];
+    static ContextMarks attr_done;
     cudaError_t e = smem_opt_in(kernel, static_cast<int>(C::kSmemBytes), attr_done);
     if (e != cudaSuccess) return e;
     DenseProblem prob;
@@ -1003,14 +985,15 @@ cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUten
     prob.d_out = args.d_out;
     const unsigned cluster = static_cast<unsigned>((C::kPair ? 2 : 1) * (C::kClusterK ? C::kClusterK : 1));
     return launch_kernel(kernel, dim3(static_cast<unsigned>(plan.grid)), dim3(C::kThreads),
-                         C::kSmemBytes, stream, cluster, prob, args.wait_limit_ns, args.err_word);
+                         C::kSmemBytes, stream, cluster, args.pdl, prob, args.wait_limit_ns,
+                         args.err_word);
 }
 
 template <class C>
 cudaError_t launch_grouped_cfg(const GroupedLaunch& g, int num_sms, int num_pairs,
                                const GemmArgs& args, cudaStream_t stream) {
     auto kernel = gemm_tn_f16_kernel<C, GroupedProblem>;
-    static std::atomic<bool> attr_done[64];
+    static ContextMarks attr_done;
     cudaError_t e = smem_opt_in(kernel, static_cast<int>(C::kSmemBytes), attr_done);
     if (e != cudaSuccess) return e;
     GroupedProblem prob;
@@ -1033,19 +1016,19 @@ cudaError_t launch_grouped_cfg(const GroupedLaunch& g, int num_sms, int num_pair
     if (t == 0) return cudaSuccess;   // every group is empty
     const int grid = C::kPair ? 2 * (t < num_pairs ? t : num_pairs) : (t < num_sms ? t : num_sms);
     return launch_kernel(kernel, dim3(static_cast<unsigned>(grid)), dim3(C::kThreads),
-                         C::kSmemBytes, stream, C::kPair ? 2u : 1u, prob, args.wait_limit_ns,
-                         args.err_word);
+                         C::kSmemBytes, stream, C::kPair ? 2u : 1u, args.pdl, prob,
+                         args.wait_limit_ns, args.err_word);
 }
 
 }  // namespace
 
 int grouped_tile_n(const int64_t* m_offsets, int64_t groups, int64_t N, int num_sms, int num_pairs,
-                   bool* pair) {
+                   const Tuning& t, bool* pair) {
     // The width (and single CTAs or pairs) that minimises rounds x (BN + c)
     // over all groups' tiles, as for the dense plan.
     const int widths[3] = {256, 224, 192};
-    const int forced = __atomic_load_n(&g_force_tile_n, __ATOMIC_ACQUIRE);
-    const int pair_mode = __atomic_load_n(&g_pair_mode, __ATOMIC_ACQUIRE);
+    const int forced = t.tile_n;
+    const int pair_mode = t.pair_mode;
     int best = 256;
     bool best_pair = false;
     int64_t best_cost = -1;
@@ -1090,20 +1073,14 @@ cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, int num_pairs, c
     }
 }
 
-int g_force_tile_n = 0;
-int g_pair_mode = 0;
-int g_cluster_split = 0;
-int g_tail_split = 0;
-int g_force_group_m = 0;
-int g_pdl = 1;
-
 namespace {
 
 // A cluster split of CK: valid when all tiles x CK CTAs fit in one wave and K
 // has at least CK k-blocks (otherwise units == 0).
 template <class C>
-GemmPlan plan_cluster_split(int64_t M, int64_t N, int64_t K, int64_t slots, int max_clusters) {
-    GemmPlan p = plan_for<C>(M, N, K, slots, C::kClusterK);
+GemmPlan plan_cluster_split(int64_t M, int64_t N, int64_t K, int64_t slots, int max_clusters,
+                            const Tuning& t) {
+    GemmPlan p = plan_for<C>(M, N, K, slots, C::kClusterK, t);
     // One cluster per tile, all resident at once (a second wave would double
     // the time).
     const int64_t clusters_fit = max_clusters != 0 ? max_clusters : slots / C::kClusterK;
@@ -1118,43 +1095,43 @@ GemmPlan plan_cluster_split(int64_t M, int64_t N, int64_t K, int64_t slots, int 
 
 template <bool T>
 GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs, int64_t splits,
-                    const ClusterCaps& caps) {
+                    const ClusterCaps& caps, const Tuning& t) {
     // 3 single-CTA and 3 pair tile plans, up to 9 cluster splits.
     GemmPlan cands[15];
     int n = 0;
-    const int pair_mode = __atomic_load_n(&g_pair_mode, __ATOMIC_ACQUIRE);
-    const int forced = __atomic_load_n(&g_force_tile_n, __ATOMIC_ACQUIRE);
+    const int pair_mode = t.pair_mode;
+    const int forced = t.tile_n;
     const bool pairs_ok = splits == 1 && pairs > 0 && pair_mode != 1;
     const bool singles_ok = !(pairs_ok && pair_mode == 2);
     bool forced_ck = false;   // a forced cluster split size applies (the only candidate)
     if (splits == 1) {
         if (singles_ok) {
-            cands[n++] = plan_for<Cfg256<T>>(M, N, K, sms, 1);
-            cands[n++] = plan_for<Cfg224<T>>(M, N, K, sms, 1);
-            cands[n++] = plan_for<Cfg192<T>>(M, N, K, sms, 1);
+            cands[n++] = plan_for<Cfg256<T>>(M, N, K, sms, 1, t);
+            cands[n++] = plan_for<Cfg224<T>>(M, N, K, sms, 1, t);
+            cands[n++] = plan_for<Cfg192<T>>(M, N, K, sms, 1, t);
         }
         if (pairs_ok) {
-            cands[n++] = plan_for<CfgP256<T>>(M, N, K, pairs, 1);
-            cands[n++] = plan_for<CfgP224<T>>(M, N, K, pairs, 1);
-            cands[n++] = plan_for<CfgP192<T>>(M, N, K, pairs, 1);
+            cands[n++] = plan_for<CfgP256<T>>(M, N, K, pairs, 1, t);
+            cands[n++] = plan_for<CfgP224<T>>(M, N, K, pairs, 1, t);
+            cands[n++] = plan_for<CfgP192<T>>(M, N, K, pairs, 1, t);
         }
         // Few tiles and a long K: split K over clusters (no workspace).
-        const int ck_mode = __atomic_load_n(&g_cluster_split, __ATOMIC_ACQUIRE);
+        const int ck_mode = t.cluster_split;
         if (ck_mode != 1) {
             const bool pk = pairs > 0 && pair_mode != 1;
             // The narrower single-CTA tiles take the co-residency measured for
             // the 256-wide ones: all need one CTA per SM, so a cluster of CK
             // CTAs packs the same way.
             GemmPlan ck[9] = {
-                plan_cluster_split<CfgCK256<T, 2>>(M, N, K, sms, caps.single_ck[0]),
-                plan_cluster_split<CfgCK256<T, 4>>(M, N, K, sms, caps.single_ck[1]),
-                plan_cluster_split<CfgCK256<T, 8>>(M, N, K, sms, caps.single_ck[2]),
-                plan_cluster_split<CfgPCK256<T, 2>>(M, N, K, pairs, caps.pair_ck[0]),
-                plan_cluster_split<CfgPCK256<T, 4>>(M, N, K, pairs, caps.pair_ck[1]),
-                plan_cluster_split<CfgCK192<T, 2>>(M, N, K, sms, caps.single_ck[0]),
-                plan_cluster_split<CfgCK192<T, 4>>(M, N, K, sms, caps.single_ck[1]),
-                plan_cluster_split<CfgCK128<T, 4>>(M, N, K, sms, caps.single_ck[1]),
-                plan_cluster_split<CfgCK128<T, 8>>(M, N, K, sms, caps.single_ck[2])};
+                plan_cluster_split<CfgCK256<T, 2>>(M, N, K, sms, caps.single_ck[0], t),
+                plan_cluster_split<CfgCK256<T, 4>>(M, N, K, sms, caps.single_ck[1], t),
+                plan_cluster_split<CfgCK256<T, 8>>(M, N, K, sms, caps.single_ck[2], t),
+                plan_cluster_split<CfgPCK256<T, 2>>(M, N, K, pairs, caps.pair_ck[0], t),
+                plan_cluster_split<CfgPCK256<T, 4>>(M, N, K, pairs, caps.pair_ck[1], t),
+                plan_cluster_split<CfgCK192<T, 2>>(M, N, K, sms, caps.single_ck[0], t),
+                plan_cluster_split<CfgCK192<T, 4>>(M, N, K, sms, caps.single_ck[1], t),
+                plan_cluster_split<CfgCK128<T, 4>>(M, N, K, sms, caps.single_ck[1], t),
+                plan_cluster_split<CfgCK128<T, 8>>(M, N, K, sms, caps.single_ck[2], t)};
             static_assert(sizeof(ck) / sizeof(ck[0]) + 6 <= sizeof(cands) / sizeof(cands[0]),
                           "every candidate fits");
             if (!pk) ck[3].units = ck[4].units = 0;
@@ -1172,9 +1149,9 @@ GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs,
                     if (c.units > 0) cands[n++] = c;
         }
     } else {
-        cands[n++] = plan_for<Cfg256F<T>>(M, N, K, sms, splits);
-        cands[n++] = plan_for<Cfg224F<T>>(M, N, K, sms, splits);
-        cands[n++] = plan_for<Cfg192F<T>>(M, N, K, sms, splits);
+        cands[n++] = plan_for<Cfg256F<T>>(M, N, K, sms, splits, t);
+        cands[n++] = plan_for<Cfg224F<T>>(M, N, K, sms, splits, t);
+        cands[n++] = plan_for<Cfg192F<T>>(M, N, K, sms, splits, t);
     }
     GemmPlan best = cands[0];
     bool have = false;
@@ -1249,17 +1226,17 @@ cudaError_t launch_typed(const GemmPlan& plan, const CUtensorMap& tmA, const CUt
 
 }  // namespace
 
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits, bool bf16,
-                   int num_pairs, const ClusterCaps& caps) {
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, const Tuning& t, int64_t splits,
+                   bool bf16, int num_pairs, const ClusterCaps& caps) {
     const int64_t sms = num_sms > 0 ? num_sms : 1;
-    return bf16 ? plan_typed<true>(M, N, K, sms, num_pairs, splits, caps)
-                : plan_typed<false>(M, N, K, sms, num_pairs, splits, caps);
+    return bf16 ? plan_typed<true>(M, N, K, sms, num_pairs, splits, caps, t)
+                : plan_typed<false>(M, N, K, sms, num_pairs, splits, caps, t);
 }
 
 int max_resident_pairs() {
     // How many two-CTA clusters of the pair kernel can be resident at once.
     auto kernel = gemm_tn_f16_kernel<CfgP256<false>, DenseProblem>;
-    static std::atomic<bool> attr_done[64];
+    static ContextMarks attr_done;
     if (smem_opt_in(kernel, static_cast<int>(CfgP256<false>::kSmemBytes), attr_done) != cudaSuccess)
         return 0;
     cudaLaunchConfig_t cfg = {};
@@ -1284,7 +1261,7 @@ namespace {
 template <class C>
 int max_active_clusters(int ctas) {
     auto kernel = gemm_tn_f16_kernel<C, DenseProblem>;
-    static std::atomic<bool> attr_done[64];
+    static ContextMarks attr_done;
     if (smem_opt_in(kernel, static_cast<int>(C::kSmemBytes), attr_done) != cudaSuccess) return 0;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(ctas), 1, 1);
@@ -1326,12 +1303,13 @@ cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const C
                      : launch_typed<false>(plan, tmA, tmB, tmD, args, stream);
 }
 
-GemmPlan plan_small_m(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits) {
+GemmPlan plan_small_m(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits,
+                      const Tuning& t) {
     const int64_t sms = num_sms > 0 ? num_sms : 1;
     // The swapped problem: rows = N (weights), columns = Mp, same K.
-    if (M <= 16) return plan_for<CfgS16>(N, 16, K, sms, splits);
-    if (M <= 32) return plan_for<CfgS32>(N, 32, K, sms, splits);
-    return plan_for<CfgS64>(N, 64, K, sms, splits);
+    if (M <= 16) return plan_for<CfgS16>(N, 16, K, sms, splits, t);
+    if (M <= 32) return plan_for<CfgS32>(N, 32, K, sms, splits, t);
+    return plan_for<CfgS64>(N, 64, K, sms, splits, t);
 }
 
 cudaError_t launch_small_m(const GemmPlan& plan, const CUtensorMap& tmW, const CUtensorMap& tmX,
@@ -1383,24 +1361,26 @@ small_m_reduce_kernel(const float4* __restrict__ P, __half* __restrict__ D, int3
 }  // namespace
 
 cudaError_t launch_small_m_reduce(const void* partials, void* D, int64_t M, int64_t N, int64_t Mp,
-                                  int64_t splits, cudaStream_t stream) {
+                                  int64_t splits, bool pdl, cudaStream_t stream) {
     const int64_t threads = N * (Mp / 16);
     const int64_t blocks = (threads + 255) / 256;
     return launch_kernel(small_m_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0,
-                         stream, 1u, static_cast<const float4*>(partials), static_cast<__half*>(D),
+                         stream, 1u, pdl, static_cast<const float4*>(partials),
+                         static_cast<__half*>(D),
                          static_cast<int32_t>(M), static_cast<int32_t>(N),
                          static_cast<int32_t>(Mp), static_cast<int32_t>(splits));
 }
 
 cudaError_t launch_splitk_reduce(const void* partials, void* D, int64_t M, int64_t N,
-                                 int64_t splits, bool bf16, int num_sms, cudaStream_t stream) {
+                                 int64_t splits, bool bf16, int num_sms, bool pdl,
+                                 cudaStream_t stream) {
     const int64_t groups8 = M * N / 8;
     int64_t blocks = (groups8 + 255) / 256;
     const int64_t cap = static_cast<int64_t>(num_sms > 0 ? num_sms : 1) * 8;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) blocks = 1;
     auto kernel = bf16 ? splitk_reduce_kernel<true> : splitk_reduce_kernel<false>;
-    return launch_kernel(kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1u,
+    return launch_kernel(kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, stream, 1u, pdl,
                          static_cast<const float4*>(partials), static_cast<uint4*>(D), groups8,
                          M * N / 4, static_cast<int32_t>(splits));
 }

@@ -135,12 +135,12 @@ gemv_f16_kernel(const uint4* __restrict__ x, const uint4* __restrict__ W, uint16
 }  // namespace
 
 cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y, bool bf16,
-                        cudaStream_t stream, uint32_t* err) {
+                        cudaStream_t stream, uint32_t* err, bool pdl) {
     const int32_t K8 = static_cast<int32_t>(K / 8);
     const int64_t blocks = (N + kGvWarps - 1) / kGvWarps;
     auto kernel = bf16 ? gemv_f16_kernel<true> : gemv_f16_kernel<false>;
     return launch_kernel(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kGvWarps * 32), 0,
-                         stream, 1u, static_cast<const uint4*>(x), static_cast<const uint4*>(W),
+                         stream, 1u, pdl, static_cast<const uint4*>(x), static_cast<const uint4*>(W),
                          static_cast<uint16_t*>(y), static_cast<int32_t>(N), K8, err);
 }
 

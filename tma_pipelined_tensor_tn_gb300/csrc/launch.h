@@ -2,11 +2,36 @@
 // translation units.  Not installed; the public interface is include/tmagemm.h.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 namespace tmagemm {
+
+// The tuning choices of one call, fixed when the call starts: either the
+// caller's per-call options (gemm_f16_ex) or a snapshot of the process-wide
+// settings (tmagemm_set_*).  Every field 0 = the automatic choice.
+struct Tuning {
+    int tile_n = 0;          // 256, 224, 192 (128: cluster splits only) forces that width
+    int pair_mode = 0;       // 1 never CTA pairs, 2 pairs only
+    int cluster_split = 0;   // 1 never, 2/4/8 that cluster size wherever it applies
+    int tail_split = 0;      // 1 never
+    int group_m = 0;         // 1..64 forces GROUP_M of the tile order
+    int small_m_route = 0;   // 1 swap-AB, 2 register fragments (M <= 16), 3 LSU-fed tcgen05
+    int plain_launch = 0;    // 1: launch without programmatic dependent launch
+    int m1_route = 0;        // 1: M = 1 through the tile kernel instead of the GEMV
+    bool pdl() const { return plain_launch == 0; }
+};
+
+// Snapshot of the process-wide settings.
+Tuning process_tuning();
+
+// Unique id (cuCtxGetId) of the CUDA context current on this thread, 0 if
+// none is current.  Per-device set-up that lives in a context (function
+// attributes, the addresses of __device__ arrays) is keyed on it, so that it
+// is redone after cudaDeviceReset replaces the device's context.
+uint64_t current_context_id();
 
 // GEMM tile configuration used by the persistent tcgen05 kernel.
 struct GemmPlan {
@@ -43,11 +68,12 @@ struct ClusterCaps {
     int pair_ck[2] = {0, 0};
 };
 
-// Pure function of the problem shape and the SM count (no CUDA calls).
-// splits == 1: the plain GEMM; splits == 0: choose the split count; else that
-// many splits (clamped so that no split is empty).
-GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits = 1,
-                   bool bf16 = false, int num_pairs = 0, const ClusterCaps& caps = ClusterCaps{});
+// Pure function of the problem shape, the SM count and the tuning (no CUDA
+// calls).  splits == 1: the plain GEMM; splits == 0: choose the split count;
+// else that many splits (clamped so that no split is empty).
+GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, const Tuning& t,
+                   int64_t splits = 1, bool bf16 = false, int num_pairs = 0,
+                   const ClusterCaps& caps = ClusterCaps{});
 
 // The co-residency of the cluster-split kernels on the current device.
 ClusterCaps query_cluster_caps();
@@ -56,19 +82,10 @@ ClusterCaps query_cluster_caps();
 // (0 if clusters cannot be launched).
 int max_resident_pairs();
 
-// Pair-mode override for the plan: 0 automatic, 1 never pairs, 2 pairs only.
-extern int g_pair_mode;
-
-// Cluster split-K override for the plain GEMM: 0 automatic, 1 never, 2/4/8 that
-// cluster size whenever it applies (every tile x CK CTAs in one wave).
-extern int g_cluster_split;
-
-// Tail split of the plain GEMM: 0 automatic (wherever it applies), 1 never.
-extern int g_tail_split;
-
 // D = fp16/bf16(sum of `splits` FP32 partial M x N matrices laid out back to back).
 cudaError_t launch_splitk_reduce(const void* partials, void* D, int64_t M, int64_t N,
-                                 int64_t splits, bool bf16, int num_sms, cudaStream_t stream);
+                                 int64_t splits, bool bf16, int num_sms, bool pdl,
+                                 cudaStream_t stream);
 
 struct GemmArgs {
     int32_t M, N, K;
@@ -76,6 +93,7 @@ struct GemmArgs {
     uint32_t* err_word;   // device address of the sticky error word
     void* d_out = nullptr;   // D itself, for the cluster-split epilogue
     const CUtensorMap* tmBn = nullptr;   // B with box {bk, narrow_b_rows} (tail split only)
+    bool pdl = true;      // launch with programmatic dependent launch
 };
 
 // Enqueue the GEMM kernel.  Tensor maps: A {K, M} box {bk, bm}; B {K, N} box
@@ -87,11 +105,12 @@ cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const C
 // Skinny GEMM (2 <= M <= 64) as a swapped split-K problem: rows = N (weights),
 // columns = Mp = M rounded up to 16/32/64, same K.  Partials go to an FP32
 // workspace [splits][N][Mp]; launch_small_m_reduce transposes and sums them.
-GemmPlan plan_small_m(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits);
+GemmPlan plan_small_m(int64_t M, int64_t N, int64_t K, int num_sms, int64_t splits,
+                      const Tuning& t);
 cudaError_t launch_small_m(const GemmPlan& plan, const CUtensorMap& tmW, const CUtensorMap& tmX,
                            const CUtensorMap& tmP, const GemmArgs& args, cudaStream_t stream);
 cudaError_t launch_small_m_reduce(const void* partials, void* D, int64_t M, int64_t N, int64_t Mp,
-                                  int64_t splits, cudaStream_t stream);
+                                  int64_t splits, bool pdl, cudaStream_t stream);
 
 // Skinny GEMM (2 <= M <= small_m_mma_max_m()) on register fragments: the
 // weights stream from HBM straight into mma.sync operands; K is split over
@@ -102,7 +121,7 @@ int64_t small_m_mma_ctas(int64_t N, int num_sms);
 int64_t small_m_mma_wave(int num_sms);
 cudaError_t launch_small_m_mma(int64_t M, int64_t N, int64_t K, const void* X, const void* W,
                                void* D, cudaStream_t stream, bool bf16, int num_sms,
-                               uint32_t* err);
+                               uint32_t* err, bool pdl);
 
 // Skinny GEMM (2 <= M <= 64) on tcgen05 with the weights staged in shared
 // memory by the SMs' own 16-byte loads (X by TMA); K split over 8-CTA clusters
@@ -111,12 +130,7 @@ cudaError_t launch_small_m_mma(int64_t M, int64_t N, int64_t K, const void* X, c
 int64_t small_m_lsu_cols(int64_t M);
 cudaError_t launch_small_m_lsu(const CUtensorMap& tmX, int64_t M, int64_t N, int64_t K,
                                const void* W, void* D, uint64_t limit_ns, uint32_t* err,
-                               cudaStream_t stream, bool bf16 = false);
-
-// Route of gemm_f16_small_m: 0 automatic, 1 always the tcgen05 swap-AB
-// kernel, 2 the register-fragment kernel wherever it applies, 3 always the
-// LSU-fed tcgen05 kernel.
-extern int g_small_m_route;
+                               cudaStream_t stream, bool bf16, bool pdl);
 
 // Grouped GEMM: groups g < G with rows [m_offsets[g], m_offsets[g+1]) of A
 // and D and weights B[g] (N x K).  Maps: A {K, rows} box {64, 128}; B
@@ -132,34 +146,25 @@ struct GroupedLaunch {
     bool pair;                  // CTA-pair tiles (256 rows; B box bn / 2 rows)
 };
 int grouped_tile_n(const int64_t* m_offsets, int64_t groups, int64_t N, int num_sms, int num_pairs,
-                   bool* pair);
+                   const Tuning& t, bool* pair);
 cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, int num_pairs, const GemmArgs& args,
                            cudaStream_t stream);
 
 // Enqueue the GEMV kernel: y[n] = sum_k x[k] * W[n][k]; one warp per row;
 // fp16 or bf16 operands and output.
 cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y, bool bf16,
-                        cudaStream_t stream, uint32_t* err);
-
-// Tile-N override for the GEMM plan (0 = automatic); a tuning/test knob.
-extern int g_force_tile_n;
-
-// GROUP_M override for the dense tile order (0 = automatic); a tuning knob.
-extern int g_force_group_m;
-
-// Programmatic dependent launch: 1 (the default) launches every kernel with
-// the programmatic-stream-serialization attribute, so the next kernel on the
-// stream is scheduled while the previous one finishes and runs its set-up
-// (barrier initialisation, descriptor prefetch) meanwhile.  Every kernel of the
-// library executes griddepcontrol.wait before its first global memory access,
-// so stream order of results is unchanged.  0 launches them plainly.
-extern int g_pdl;
+                        cudaStream_t stream, uint32_t* err, bool pdl);
 
 // cudaLaunchKernelEx with a cluster of `cluster_x` CTAs along x (1 = none)
-// and, when g_pdl is set, the programmatic-stream-serialization attribute.
+// and, when `pdl` is set, the programmatic-stream-serialization attribute
+// (programmatic dependent launch): the next kernel on the stream is scheduled
+// while the previous one finishes and runs its set-up (barrier
+// initialisation, descriptor prefetch) meanwhile.  Every kernel of the
+// library executes griddepcontrol.wait before its first global memory access,
+// so the stream order of results is unchanged.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem_bytes,
-                          cudaStream_t stream, unsigned cluster_x, Args... args) {
+                          cudaStream_t stream, unsigned cluster_x, bool pdl, Args... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -174,7 +179,7 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
         attr[n].val.clusterDim.z = 1;
         ++n;
     }
-    if (__atomic_load_n(&g_pdl, __ATOMIC_ACQUIRE)) {
+    if (pdl) {
         attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attr[n].val.programmaticStreamSerializationAllowed = 1;
         ++n;
@@ -184,6 +189,30 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, args...);
     if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+// Per device, the context (current_context_id) in which a one-time set-up
+// was last done; 0 = never.
+using ContextMarks = std::atomic<uint64_t>[64];
+
+// Opt-in of `kernel` to `bytes` (> 48 KB) of dynamic shared memory on the
+// current device, once per context.  With `max_shared`, the whole
+// configurable L1/shared split also goes to shared memory, so CTAs that ask
+// for half of it can sit two to an SM.
+template <class K>
+cudaError_t smem_opt_in(K kernel, int bytes, ContextMarks& done, bool max_shared = true) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t ctx = current_context_id();
+    const bool tracked = dev >= 0 && dev < 64 && ctx != 0;
+    if (tracked && done[dev].load(std::memory_order_acquire) == ctx) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess && max_shared)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 static_cast<int>(cudaSharedmemCarveoutMaxShared));
+    if (e == cudaSuccess && tracked) done[dev].store(ctx, std::memory_order_release);
+    return e;
 }
 
 // Enqueue a one-block kernel that waits on an mbarrier nobody arrives on, with

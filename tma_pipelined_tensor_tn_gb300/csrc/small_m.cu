@@ -225,8 +225,6 @@ small_m_mma_kernel(const uint4* __restrict__ X, const uint4* __restrict__ W,
 
 }  // namespace
 
-int g_small_m_route = 0;
-
 int64_t small_m_mma_max_m() { return 16; }
 
 // CTAs the register-fragment kernel launches for N weight rows, and the wave
@@ -247,14 +245,14 @@ namespace {
 // ranges of whole 4-chunk (32-k) steps.
 template <int NT, int U, bool XB, int MIN_CTAS, int S, bool BF16>
 cudaError_t launch_variant(int64_t M, int64_t N, int64_t K, const void* X, const void* W, void* D,
-                           cudaStream_t stream, uint32_t* err) {
+                           cudaStream_t stream, uint32_t* err, bool pdl) {
     const int32_t K8 = static_cast<int32_t>(K / 8);
     const int32_t per = (K8 + S - 1) / S;
     const int32_t slice8 = (per + 3) / 4 * 4;
     const int64_t clusters = (N + kSmRows - 1) / kSmRows;
     return launch_kernel(small_m_mma_kernel<NT, U, XB, MIN_CTAS, S, BF16>,
                          dim3(static_cast<unsigned>(clusters * S)), dim3(kSmWarps * 32), 0,
-                         stream, static_cast<unsigned>(S), static_cast<const uint4*>(X),
+                         stream, static_cast<unsigned>(S), pdl, static_cast<const uint4*>(X),
                          static_cast<const uint4*>(W), static_cast<uint16_t*>(D),
                          static_cast<int32_t>(M), static_cast<int32_t>(N), K8, slice8, err);
 }
@@ -266,23 +264,23 @@ cudaError_t launch_variant(int64_t M, int64_t N, int64_t K, const void* X, const
 // wave (N = 28672: 448 CTAs).
 template <int NT, int U, bool BF16>
 cudaError_t launch_sliced(int64_t M, int64_t N, int64_t K, const void* X, const void* W, void* D,
-                          int num_sms, cudaStream_t stream, uint32_t* err) {
+                          int num_sms, cudaStream_t stream, uint32_t* err, bool pdl) {
     const int64_t clusters = (N + kSmRows - 1) / kSmRows;
     const int64_t wave = 4ll * (num_sms > 0 ? num_sms : 152);
     if (clusters * 8 <= wave)
-        return launch_variant<NT, U, true, 1, 8, BF16>(M, N, K, X, W, D, stream, err);
+        return launch_variant<NT, U, true, 1, 8, BF16>(M, N, K, X, W, D, stream, err, pdl);
     if (clusters * 4 <= wave)
-        return launch_variant<NT, U, true, 1, 4, BF16>(M, N, K, X, W, D, stream, err);
+        return launch_variant<NT, U, true, 1, 4, BF16>(M, N, K, X, W, D, stream, err, pdl);
     if (clusters * 2 <= wave)
-        return launch_variant<NT, U, true, 1, 2, BF16>(M, N, K, X, W, D, stream, err);
-    return launch_variant<NT, U, true, 1, 1, BF16>(M, N, K, X, W, D, stream, err);
+        return launch_variant<NT, U, true, 1, 2, BF16>(M, N, K, X, W, D, stream, err, pdl);
+    return launch_variant<NT, U, true, 1, 1, BF16>(M, N, K, X, W, D, stream, err, pdl);
 }
 
 template <bool BF16>
 cudaError_t launch_typed(int64_t M, int64_t N, int64_t K, const void* X, const void* W, void* D,
-                         int num_sms, cudaStream_t stream, uint32_t* err) {
-    if (M <= 8) return launch_sliced<1, 4, BF16>(M, N, K, X, W, D, num_sms, stream, err);
-    if (M <= 16) return launch_sliced<2, 2, BF16>(M, N, K, X, W, D, num_sms, stream, err);
+                         int num_sms, cudaStream_t stream, uint32_t* err, bool pdl) {
+    if (M <= 8) return launch_sliced<1, 4, BF16>(M, N, K, X, W, D, num_sms, stream, err, pdl);
+    if (M <= 16) return launch_sliced<2, 2, BF16>(M, N, K, X, W, D, num_sms, stream, err, pdl);
     return cudaErrorInvalidValue;
 }
 
@@ -296,9 +294,9 @@ cudaError_t launch_typed(int64_t M, int64_t N, int64_t K, const void* X, const v
 // compile time cost 2 us; above 16 tokens the tcgen05 kernel is faster.
 cudaError_t launch_small_m_mma(int64_t M, int64_t N, int64_t K, const void* X, const void* W,
                                void* D, cudaStream_t stream, bool bf16, int num_sms,
-                               uint32_t* err) {
-    return bf16 ? launch_typed<true>(M, N, K, X, W, D, num_sms, stream, err)
-                : launch_typed<false>(M, N, K, X, W, D, num_sms, stream, err);
+                               uint32_t* err, bool pdl) {
+    return bf16 ? launch_typed<true>(M, N, K, X, W, D, num_sms, stream, err, pdl)
+                : launch_typed<false>(M, N, K, X, W, D, num_sms, stream, err, pdl);
 }
 
 }  // namespace tmagemm

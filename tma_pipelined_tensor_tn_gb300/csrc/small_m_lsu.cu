@@ -303,20 +303,18 @@ small_m_lsu_kernel(const __grid_constant__ CUtensorMap tmX, const uint4* __restr
 
 template <int MP, bool BF16>
 cudaError_t launch_mp(const CUtensorMap& tmX, int64_t M, int64_t N, int64_t K, const void* W,
-                      void* D, uint64_t limit_ns, uint32_t* err, cudaStream_t stream) {
+                      void* D, uint64_t limit_ns, uint32_t* err, cudaStream_t stream, bool pdl) {
     auto kernel = small_m_lsu_kernel<MP, BF16>;
-    static std::atomic<bool> attr_done{false};
-    if (!attr_done.load(std::memory_order_acquire)) {
-        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(TmLayout<MP>::kSmemBytes));
-        if (e != cudaSuccess) return e;
-        attr_done.store(true, std::memory_order_release);
-    }
+    static ContextMarks attr_done;
+    cudaError_t e = smem_opt_in(kernel, static_cast<int>(TmLayout<MP>::kSmemBytes), attr_done,
+                                false);
+    if (e != cudaSuccess) return e;
     const int32_t kb_total = static_cast<int32_t>((K + 63) / 64);
     const int32_t kb_per_slice = (kb_total + kTmSlices - 1) / kTmSlices;
     const int64_t clusters = (N + kTmRows - 1) / kTmRows;
     return launch_kernel(kernel, dim3(static_cast<unsigned>(clusters * kTmSlices)), dim3(kTmThreads),
-                         TmLayout<MP>::kSmemBytes, stream, static_cast<unsigned>(kTmSlices), tmX,
+                         TmLayout<MP>::kSmemBytes, stream, static_cast<unsigned>(kTmSlices), pdl,
+                         tmX,
                          static_cast<const uint4*>(W), static_cast<uint16_t*>(D),
                          static_cast<int32_t>(M), static_cast<int32_t>(N),
                          static_cast<int32_t>(K / 8), kb_total, kb_per_slice, limit_ns, err);
@@ -328,14 +326,14 @@ int64_t small_m_lsu_cols(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
 
 cudaError_t launch_small_m_lsu(const CUtensorMap& tmX, int64_t M, int64_t N, int64_t K,
                                const void* W, void* D, uint64_t limit_ns, uint32_t* err,
-                               cudaStream_t stream, bool bf16) {
+                               cudaStream_t stream, bool bf16, bool pdl) {
     switch (small_m_lsu_cols(M) * (bf16 ? -1 : 1)) {
-        case 16: return launch_mp<16, false>(tmX, M, N, K, W, D, limit_ns, err, stream);
-        case 32: return launch_mp<32, false>(tmX, M, N, K, W, D, limit_ns, err, stream);
-        case 64: return launch_mp<64, false>(tmX, M, N, K, W, D, limit_ns, err, stream);
-        case -16: return launch_mp<16, true>(tmX, M, N, K, W, D, limit_ns, err, stream);
-        case -32: return launch_mp<32, true>(tmX, M, N, K, W, D, limit_ns, err, stream);
-        default: return launch_mp<64, true>(tmX, M, N, K, W, D, limit_ns, err, stream);
+        case 16: return launch_mp<16, false>(tmX, M, N, K, W, D, limit_ns, err, stream, pdl);
+        case 32: return launch_mp<32, false>(tmX, M, N, K, W, D, limit_ns, err, stream, pdl);
+        case 64: return launch_mp<64, false>(tmX, M, N, K, W, D, limit_ns, err, stream, pdl);
+        case -16: return launch_mp<16, true>(tmX, M, N, K, W, D, limit_ns, err, stream, pdl);
+        case -32: return launch_mp<32, true>(tmX, M, N, K, W, D, limit_ns, err, stream, pdl);
+        default: return launch_mp<64, true>(tmX, M, N, K, W, D, limit_ns, err, stream, pdl);
     }
 }
 

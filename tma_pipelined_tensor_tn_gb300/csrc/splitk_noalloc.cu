@@ -18,6 +18,7 @@
 #include <mutex>
 
 #include "../../include/tmagemm.h"
+#include "launch.h"
 
 namespace tmagemm {
 namespace {
@@ -29,23 +30,33 @@ static __device__ __align__(256) float g_splitk_scratch[kSplitkScratchBytes / 4]
 
 constexpr int kMaxDevices = 64;
 std::mutex g_scratch_mutex;
-void* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchAddress {
+    uint64_t ctx = 0;      // the context the address was looked up in
+    void* ptr = nullptr;
+};
+ScratchAddress g_scratch[kMaxDevices];
 
 // The array's device address on the current device.  In host code the name
 // g_splitk_scratch is a host-side stand-in, not a device address, so the
-// address is looked up once per device, with that device current.
+// address is looked up with the device current: on the first call in each
+// context of the device (after cudaDeviceReset the device's next context
+// loads this module anew, and the array may sit elsewhere).
 int scratch_for_current_device(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return TMAGEMM_ERR_CUDA;
     if (dev < 0 || dev >= kMaxDevices) return TMAGEMM_ERR_UNSUPPORTED;
     std::lock_guard<std::mutex> lock(g_scratch_mutex);
-    if (g_scratch_ptr[dev] == nullptr) {
+    ScratchAddress& a = g_scratch[dev];
+    const uint64_t ctx = current_context_id();
+    if (a.ptr == nullptr || ctx == 0 || a.ctx != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_splitk_scratch) != cudaSuccess || p == nullptr)
             return TMAGEMM_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
+        a.ptr = p;
+        // The look-up creates the primary context if there was none yet.
+        a.ctx = ctx != 0 ? ctx : current_context_id();
     }
-    *out = g_scratch_ptr[dev];
+    *out = a.ptr;
     return TMAGEMM_OK;
 }
 
