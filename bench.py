@@ -843,10 +843,20 @@ def run_case(args, name):
             fn = lambda: tg.gemm_f16(M, N, K, a.data_ptr(), b.data_ptr(), d.data_ptr(), sh)
         unit = ("TFLOP/s", fl / 1e12)
     elif name in ("gemv", "bf16_gemv", "small_m8", "small_m16", "small_m32", "small_m64"):
+        # Weight sets rotated past L2: consecutive launches read HBM.
         x, W = inputs.gemv_inputs(GEMV_N, GEMV_K, seed=0)
         if name == "bf16_gemv":
             x, W = x.to(torch.bfloat16), W.to(torch.bfloat16)
-        w = W.to(dev)
+        l2 = int(getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0) or 129 << 20)
+        nw = inputs.l2_rotation_count(int(gemv_bytes()), l2)
+        ws_rot = [W.to(dev)]
+        ws_rot += [ws_rot[0].clone() for _ in range(nw - 1)]
+        turn = [0]
+
+        def w_next():
+            turn[0] += 1
+            return ws_rot[turn[0] % nw].data_ptr()
+
         if name.startswith("small_m"):
             Ms = int(name[7:])
             X = (torch.randn((Ms, GEMV_K), generator=torch.Generator().manual_seed(1)) * 0.02).half()
@@ -854,14 +864,14 @@ def run_case(args, name):
             y = torch.empty((Ms, GEMV_N), dtype=torch.float16, device=dev)
             need = tg.gemm_f16_small_m_workspace_size(Ms, GEMV_N, GEMV_K)
             ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=dev)
-            fn = lambda: tg.gemm_f16_small_m(Ms, GEMV_N, GEMV_K, xv.data_ptr(), w.data_ptr(),
+            fn = lambda: tg.gemm_f16_small_m(Ms, GEMV_N, GEMV_K, xv.data_ptr(), w_next(),
                                              y.data_ptr(), ws.data_ptr(), need, sh)
             by = 2.0 * (GEMV_N * GEMV_K + Ms * GEMV_K + Ms * GEMV_N)
         else:
             xv = x.to(dev)
-            y = torch.empty((GEMV_N,), dtype=w.dtype, device=dev)
+            y = torch.empty((GEMV_N,), dtype=x.dtype, device=dev)
             g = tg.gemv_bf16 if name == "bf16_gemv" else tg.gemv_f16
-            fn = lambda: g(GEMV_N, GEMV_K, xv.data_ptr(), w.data_ptr(), y.data_ptr(), sh)
+            fn = lambda: g(GEMV_N, GEMV_K, xv.data_ptr(), w_next(), y.data_ptr(), sh)
             by = gemv_bytes()
         unit = ("GB/s", by / 1e9)
     elif name == "grouped":

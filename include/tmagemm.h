@@ -386,6 +386,27 @@ int tmagemm_set_cluster_split(int mode);
 int tmagemm_set_tail_split(int mode);
 
 /*
+ * Formulation of gemm_f16_grouped, process-wide: 0 = automatic, 1 = always
+ * row tiles (tiles of 128 or 256 rows of one group), 2 = always transposed
+ * (each group computed as D_g^T = B_g A_g^T: tiles of 256 or 128 weight rows
+ * by blocks of up to 256 rows of the group, so a group's rows are padded to
+ * a multiple of 16 instead of 128 or 256; the accumulator is stored
+ * transposed).  Results agree up to FP32 accumulation order.  Returns
+ * TMAGEMM_ERR_INVALID for other values.
+ */
+int tmagemm_set_grouped_transposed(int mode);
+
+/*
+ * The plan gemm_f16_grouped runs for these groups (G, m_offsets and N as for
+ * gemm_f16_grouped) on `num_sms` SMs with `num_pairs` co-resident CTA pairs:
+ * out[0] = 1 if transposed, out[1] = 1 if CTA pairs, out[2] = tile width of
+ * the row tiles (256 when transposed), out[3] = the widest block of a group's
+ * rows when transposed (else 0).  `out` holds 4 values.  No GPU needed.
+ */
+int tmagemm_grouped_plan(int64_t G, const int64_t* m_offsets, int64_t N, int64_t num_sms,
+                         int64_t num_pairs, int64_t* out);
+
+/*
  * Programmatic dependent launch of the library's kernels: 1 (the default)
  * launches each kernel with CUDA's programmatic-stream-serialization
  * attribute, so a kernel queued behind another on the same stream is

@@ -71,6 +71,7 @@ plain("cluster_auto", 1024, 1024, 16384)
 for ck in (2, 4, 8):
     plain(f"cluster_{ck}", 512, 1000, 4160, knobs=((tg.tmagemm_set_cluster_split, ck),))
 plain("decode_32x4096x14336", 32, 4096, 14336)
+plain("decode_48x4096x14336", 48, 4096, 14336)
 plain("decode_64x14336x4096", 64, 14336, 4096)
 plain("group_m_8", 8192, 8192, 1024)
 
@@ -93,7 +94,39 @@ D = tg.gemm_grouped(A, B, offsets)
 ref = torch.cat([torch.matmul(A[offsets[g]:offsets[g + 1]], B[g].T) for g in range(len(counts_g))])
 exp = [sum(ceil_div(c, tm) for c in counts_g) * ceil_div(Ng, bn)
        for tm in (128, 256) for bn in (256, 224, 192)]
-verify("grouped", tg.checked_unit_counts(4000), exp, ref, D)
+
+
+def transposed_units(counts, N, tile_m, maxw):
+    """Units of the transposed grouped schedule: weight blocks x row blocks."""
+    return ceil_div(N, tile_m) * sum(ceil_div(ceil_div(c, 16), maxw // 16) for c in counts if c)
+
+
+exp_t = [transposed_units(counts_g, Ng, tm, w) for tm in (128, 256) for w in range(128, 257, 16)]
+verify("grouped", tg.checked_unit_counts(4000), exp + exp_t, ref, D)
+# Both formulations forced, single CTAs and pairs, with empty and 1-row groups.
+counts_t = [0, 1, 129, 0, 16, 17, 700]
+offs_t = [0]
+for c in counts_t:
+    offs_t.append(offs_t[-1] + c)
+A_t = rnd((offs_t[-1], 520), seed=15)
+B_t = rnd((len(counts_t), 1000, 520), seed=16)
+ref_t = torch.cat([torch.matmul(A_t[offs_t[g]:offs_t[g + 1]], B_t[g].T) for g in range(len(counts_t))])
+for mode in (1, 2):
+    for pair in (1, 2):
+        assert tg.tmagemm_set_grouped_transposed(mode) == tg.TMAGEMM_OK
+        assert tg.tmagemm_set_cta_pair(pair) == tg.TMAGEMM_OK
+        try:
+            D_t = tg.gemm_grouped(A_t, B_t, offs_t)
+            counts = tg.checked_unit_counts(4000)
+        finally:
+            tg.tmagemm_set_grouped_transposed(0)
+            tg.tmagemm_set_cta_pair(0)
+        tm = 256 if pair == 2 else 128
+        if mode == 2:
+            units = [transposed_units(counts_t, 1000, tm, w) for w in range(128, 257, 16)]
+        else:
+            units = [sum(ceil_div(c, tm) for c in counts_t) * ceil_div(1000, bn) for bn in (256, 224, 192)]
+        verify(f"grouped_mode{mode}_pair{pair}", counts, units, ref_t, D_t)
 
 # Swap-AB small-M (route 1): tile kernel units with FP32 partials.
 assert tg.tmagemm_set_small_m_route(1) == tg.TMAGEMM_OK

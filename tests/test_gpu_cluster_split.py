@@ -44,7 +44,7 @@ def test_auto_plan_uses_cluster_split(tg):
 def test_auto_parity_1024x1024x16384(tg):
     M, N, K = 1024, 1024, 16384
     A, B = inputs.gemm_inputs(M, N, K, seed=600)
-    compare(gemm_with(tg, A, B, 0), oracle.gemm_f16(A.numpy(), B.numpy()), "cluster split auto")
+    compare(gemm_with(tg, A, B, 0), oracle.gemm_f16(A.numpy(), B.numpy()), "cluster split auto", k=A.shape[1])
 
 
 @pytest.fixture(params=[0, 1], ids=["pairs_allowed", "single_ctas"])
@@ -71,7 +71,7 @@ def test_forced_sizes_parity(tg, pair_mode, ck, M, N, K):
         assert p["cluster_k"] == ck, p
     A, B = inputs.gemm_inputs(M, N, K, seed=M + N + ck)
     compare(gemm_with(tg, A, B, ck), oracle.gemm_f16(A.numpy(), B.numpy()),
-            f"cluster split {ck} {M}x{N}x{K} pair mode {pair_mode}")
+            f"cluster split {ck} {M}x{N}x{K} pair mode {pair_mode}", k=A.shape[1])
 
 
 @pytest.mark.parametrize("ck", [2, 4, 8])
@@ -116,7 +116,7 @@ def test_output_guard(tg):
     assert np.all(host[:guard] == sentinel) and np.all(host[guard + M * N:] == sentinel)
     body = host[guard:guard + M * N]
     assert not np.any(body == sentinel)
-    compare(body.view(np.float16).reshape(M, N), oracle.gemm_f16(A.numpy(), B.numpy()), "guarded")
+    compare(body.view(np.float16).reshape(M, N), oracle.gemm_f16(A.numpy(), B.numpy()), "guarded", k=A.shape[1])
 
 
 def forced_plan_and_gemm(tg, A, B, bn, ck):
@@ -146,7 +146,7 @@ def test_narrow_tiles_parity(tg, bn, ck, M, N, K):
     A, B = inputs.gemm_inputs(M, N, K, seed=M + N + bn + ck)
     p, D = forced_plan_and_gemm(tg, A, B, bn, ck)
     assert (p["BN"], p["cluster_k"], p["pair"]) == (bn, ck, 0), p
-    compare(D, oracle.gemm_f16(A.numpy(), B.numpy()), f"cluster split {bn}x{ck} {M}x{N}x{K}")
+    compare(D, oracle.gemm_f16(A.numpy(), B.numpy()), f"cluster split {bn}x{ck} {M}x{N}x{K}", k=A.shape[1])
 
 
 @pytest.mark.parametrize("bn,ck", [(128, 4), (128, 8), (192, 2), (192, 4)])
@@ -172,4 +172,25 @@ def test_decode_shapes_fill_the_sms(tg, M, N, K):
     D = tg.gemm(X.cuda(), W.cuda()).cpu().numpy()
     tg.check()
     rows = np.arange(0, N, 97)
-    compare(D[:, rows], oracle.gemm_f16(X.numpy(), W.numpy()[rows]), f"decode {M}x{N}x{K}")
+    compare(D[:, rows], oracle.gemm_f16(X.numpy(), W.numpy()[rows]), f"decode {M}x{N}x{K}", k=X.shape[1])
+
+
+@pytest.mark.parametrize("M,N,K", [(17, 4096, 14336), (64, 4096, 14336), (40, 1000, 4160),
+                                   (2, 520, 1032), (64, 4104, 200)])
+def test_decode_cluster_split(tg, M, N, K):
+    """The decode split (at most 64 rows; a stage holds a 64-row A box, so the
+    128-row MMA's rows past it read the stage's own B box and reach only
+    unstored accumulator rows; 9 stages): 4-CTA clusters of 128-wide tiles,
+    forced per call, ragged N and K included.  The oracle's result; integer
+    inputs bit-exact."""
+    # small_m_route = 1 keeps every M on the tile kernel in gemm_f16_ex
+    opts = tg.options(cluster_split=4, tile_n=128, small_m_route=1)
+    A, B = inputs.gemm_inputs(M, N, K, seed=700 + M)
+    D = tg.gemm(A.cuda(), B.cuda(), opts=opts)
+    tg.check()
+    compare(D.cpu().numpy(), oracle.gemm_f16(A.numpy(), B.numpy()), f"decode {M}x{N}x{K}", k=K)
+    Ai = inputs.integer_f16((M, K), seed=M)
+    Bi = inputs.integer_f16((N, K), seed=N)
+    Di = tg.gemm(Ai.cuda(), Bi.cuda(), opts=opts)
+    tg.check()
+    assert_bitexact(Di.cpu().numpy(), oracle.gemm_f16(Ai.numpy(), Bi.numpy()), f"decode {M} int")

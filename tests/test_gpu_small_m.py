@@ -47,14 +47,14 @@ def decode_inputs(M, N, K, seed):
 def test_small_m_parity_down_projection(tg, route, M):
     N, K = 4096, 14336
     X, W = decode_inputs(M, N, K, seed=M)
-    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M M={M} route {route}")
+    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M M={M} route {route}", k=X.shape[1])
 
 
 @pytest.mark.parametrize("M", [33, 64])
 def test_small_m_parity_down_projection_wide(tg, route, M):
     N, K = 4096, 14336
     X, W = decode_inputs(M, N, K, seed=M)
-    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M M={M} route {route}")
+    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M M={M} route {route}", k=X.shape[1])
 
 
 # Ragged N (not a multiple of the 64 weight rows of a cluster), K shorter than
@@ -64,13 +64,13 @@ def test_small_m_parity_down_projection_wide(tg, route, M):
 def test_small_m_edge_shapes(tg, route, M, N, K):
     X, W = inputs.gemm_inputs(M, N, K, seed=M + N)
     compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()),
-            f"small-M {M}x{N}x{K} route {route}")
+            f"small-M {M}x{N}x{K} route {route}", k=X.shape[1])
 
 
 @pytest.mark.parametrize("M,N,K", [(40, 264, 8), (64, 1000, 4160), (47, 136, 72), (33, 4104, 1000)])
 def test_small_m_edge_shape_wide(tg, route, M, N, K):
     X, W = inputs.gemm_inputs(M, N, K, seed=M + N + K)
-    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M {M}x{N}x{K} route {route}")
+    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M {M}x{N}x{K} route {route}", k=X.shape[1])
 
 
 @pytest.mark.parametrize("M", [12, 32, 64])
@@ -107,7 +107,7 @@ def test_small_m_auto_route(tg, M):
     N, K = 1032, 2056
     X, W = inputs.gemm_inputs(M, N, K, seed=400 + M)
     d = run(tg, X, W)
-    compare(d, oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M auto M={M}")
+    compare(d, oracle.gemm_f16(X.numpy(), W.numpy()), f"small-M auto M={M}", k=X.shape[1])
     assert tg.gemm_f16_small_m_workspace_size(M, N, K) == 0
     assert_bitexact(d, tg.gemm(X.cuda(), W.cuda()).cpu().numpy(), f"small-M auto vs gemm_f16 M={M}")
 
@@ -142,7 +142,7 @@ def test_fragments_wide_n_without_k_split(tg, M):
     whole K (clusters of one CTA).  Parity, and integer inputs bit for bit."""
     N, K = 28672, 1032
     X, W = decode_inputs(M, N, K, seed=500 + M)
-    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"wide N M={M}")
+    compare(run(tg, X, W), oracle.gemm_f16(X.numpy(), W.numpy()), f"wide N M={M}", k=X.shape[1])
     Xi = inputs.integer_f16((M, K), seed=502 + M)
     Wi = inputs.integer_f16((N, K), seed=503 + M)
     assert_bitexact(run(tg, Xi, Wi), oracle.gemm_f16(Xi.numpy(), Wi.numpy()), f"wide N integer M={M}")

@@ -37,7 +37,7 @@ def run_splitk(tg, A, B, splits, ws=None):
 def test_splitk_parity(tg, M, N, K, splits):
     A, B = inputs.gemm_inputs(M, N, K, seed=M + K)
     compare(run_splitk(tg, A, B, splits), oracle.gemm_f16(A.numpy(), B.numpy()),
-            f"split-K {M}x{N}x{K} s={splits}")
+            f"split-K {M}x{N}x{K} s={splits}", k=A.shape[1])
 
 
 def test_splitk_integer_bitexact(tg):
@@ -56,7 +56,7 @@ def test_splitk_each_tile_width(tg, bn):
         D = run_splitk(tg, A, B, 3)
     finally:
         tg.tmagemm_set_tile_n(0)
-    compare(D, oracle.gemm_f16(A.numpy(), B.numpy()), f"split-K BN={bn}")
+    compare(D, oracle.gemm_f16(A.numpy(), B.numpy()), f"split-K BN={bn}", k=A.shape[1])
 
 
 def test_splitk_deterministic_and_one_part_equals_plain(tg):
@@ -68,7 +68,7 @@ def test_splitk_deterministic_and_one_part_equals_plain(tg):
     plain = tg.gemm(A.cuda(), B.cuda())
     tg.check()
     assert_bitexact(run_splitk(tg, A, B, 1), plain.cpu().numpy(), "splits=1 is the plain GEMM")
-    compare(d1, oracle.gemm_f16(A.numpy(), B.numpy()), "split-K 6 parts")
+    compare(d1, oracle.gemm_f16(A.numpy(), B.numpy()), "split-K 6 parts", k=A.shape[1])
 
 
 def test_splitk_workspace_rules(tg):

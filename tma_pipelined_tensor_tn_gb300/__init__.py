@@ -46,6 +46,8 @@ from ._binding import (  # noqa: F401
     tmagemm_last_error_detail,
     tmagemm_ring_position,
     tmagemm_selftest_wait_timeout,
+    tmagemm_set_grouped_transposed,
+    tmagemm_grouped_plan,
     tmagemm_set_cluster_split,
     tmagemm_set_cta_pair,
     tmagemm_set_group_m,

@@ -71,6 +71,8 @@ SIGNATURES = {
     "tmagemm_set_cluster_split": ([_int], _int),
     "tmagemm_set_tail_split": ([_int], _int),
     "tmagemm_set_group_m": ([_int], _int),
+    "tmagemm_set_grouped_transposed": ([_int], _int),
+    "tmagemm_grouped_plan": ([_i64, _P64, _i64, _i64, _i64, _P64], _int),
     "tmagemm_host_pipeline_create": ([_i64, _i64, _i64, _int, _int, ctypes.POINTER(_p)], _int),
     "tmagemm_host_pipeline_run": ([_p, _i64, _p, _p, _p], _int),
     "tmagemm_host_pipeline_synchronize": ([_p], _int),
@@ -294,6 +296,20 @@ def tmagemm_set_cluster_split(mode) -> int:
 
 def tmagemm_set_tail_split(mode) -> int:
     return lib().tmagemm_set_tail_split(mode)
+
+
+def tmagemm_set_grouped_transposed(mode) -> int:
+    return lib().tmagemm_set_grouped_transposed(mode)
+
+
+def tmagemm_grouped_plan(m_offsets, N, num_sms, num_pairs=0):
+    G = len(m_offsets) - 1
+    offs = (ctypes.c_int64 * (G + 1))(*[int(v) for v in m_offsets])
+    out = (ctypes.c_int64 * 4)()
+    s = lib().tmagemm_grouped_plan(G, offs, N, num_sms, num_pairs, out)
+    if s != TMAGEMM_OK:
+        raise TmaGemmError(s, "tmagemm_grouped_plan")
+    return dict(zip(("transposed", "pair", "bn", "maxw"), list(out)))
 
 
 def tmagemm_set_group_m(g) -> int:

@@ -45,6 +45,7 @@ int g_tail_split = 0;
 int g_force_group_m = 0;
 int g_small_m_route = 0;
 int g_pdl = 1;
+int g_grouped_t = 0;
 
 struct DeviceState {
     bool ready = false;
@@ -85,6 +86,7 @@ Tuning process_tuning() {
     t.group_m = __atomic_load_n(&g_force_group_m, __ATOMIC_ACQUIRE);
     t.small_m_route = __atomic_load_n(&g_small_m_route, __ATOMIC_ACQUIRE);
     t.plain_launch = __atomic_load_n(&g_pdl, __ATOMIC_ACQUIRE) ? 0 : 1;
+    t.grouped_t = __atomic_load_n(&g_grouped_t, __ATOMIC_ACQUIRE);
     return t;
 }
 
@@ -478,16 +480,15 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
     g.groups = G;
     g.N = N;
     g.K = K;
-    g.bn = grouped_tile_n(m_offsets, G, N, d->sms, d->pairs, t, &g.pair);
-    const int epi_cols = g.bn == 224 ? 32 : 64;
-    if (int s = encode_2d(&g.tmA, A, K, rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
-        return s;
+    plan_grouped(m_offsets, G, N, d->sms, d->pairs, t, &g);
+    // The weights B as {K, N, G}: the narrow operand of row tiles (box of bn
+    // rows, bn / 2 per CTA of a pair), the 128-row operand of transposed ones.
     {
+        const uint32_t b_rows = g.transposed ? 128u : static_cast<uint32_t>(g.pair ? g.bn / 2 : g.bn);
         cuuint64_t dims[3] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(N),
                               static_cast<cuuint64_t>(G)};
         cuuint64_t strides[2] = {static_cast<cuuint64_t>(K) * 2, static_cast<cuuint64_t>(N * K) * 2};
-        cuuint32_t box[3] = {64, static_cast<cuuint32_t>(g.pair ? g.bn / 2 : g.bn), 1};
+        cuuint32_t box[3] = {64, b_rows, 1};
         cuuint32_t estr[3] = {1, 1, 1};
         if (g_encode(&g.tmB, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3, const_cast<void*>(B), dims, strides,
                      box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -495,15 +496,38 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
             return TMAGEMM_ERR_CUDA;
     }
-    const CUtensorMapSwizzle dswz =
-        epi_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-    for (int64_t i = 0; i < G; ++i) {
-        const int64_t mg = m_offsets[i + 1] - m_offsets[i];
-        if (mg == 0) continue;   // an empty group has no tiles and no map
-        const void* base = static_cast<const uint16_t*>(D) + m_offsets[i] * N;
-        if (int s = encode_2d(&g.tmD[i], base, N, mg, epi_cols, 128, dswz,
-                              CU_TENSOR_MAP_L2_PROMOTION_NONE))
+    if (g.transposed) {
+        // A's rows are the narrow operand: a box of bn / (CTAs per tile) rows
+        // (each CTA of a pair loads its half of a block); the weights are "A".
+        const CUtensorMap weights = g.tmB;
+        if (int s = encode_2d(&g.tmB, A, K, rows, 64, g.pair ? g.bn / 2 : g.bn,
+                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
             return s;
+        g.tmA = weights;
+        // D rows of each group, stored 16 rows x 128 columns at a time (unswizzled).
+        for (int64_t i = 0; i < G; ++i) {
+            const int64_t mg = m_offsets[i + 1] - m_offsets[i];
+            if (mg == 0) continue;   // an empty group has no tiles and no map
+            const void* base = static_cast<const uint16_t*>(D) + m_offsets[i] * N;
+            if (int s = encode_2d(&g.tmD[i], base, N, mg, 128, 16, CU_TENSOR_MAP_SWIZZLE_NONE,
+                                  CU_TENSOR_MAP_L2_PROMOTION_NONE))
+                return s;
+        }
+    } else {
+        const int epi_cols = g.bn == 224 ? 32 : 64;
+        if (int s = encode_2d(&g.tmA, A, K, rows, 64, 128, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+            return s;
+        const CUtensorMapSwizzle dswz =
+            epi_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+        for (int64_t i = 0; i < G; ++i) {
+            const int64_t mg = m_offsets[i + 1] - m_offsets[i];
+            if (mg == 0) continue;   // an empty group has no tiles and no map
+            const void* base = static_cast<const uint16_t*>(D) + m_offsets[i] * N;
+            if (int s = encode_2d(&g.tmD[i], base, N, mg, epi_cols, 128, dswz,
+                                  CU_TENSOR_MAP_L2_PROMOTION_NONE))
+                return s;
+        }
     }
     GemmArgs args;
     args.M = static_cast<int32_t>(rows);
@@ -660,6 +684,29 @@ int tmagemm_set_cluster_split(int mode) {
 int tmagemm_set_tail_split(int mode) {
     if (mode != 0 && mode != 1) return TMAGEMM_ERR_INVALID;
     __atomic_store_n(&g_tail_split, mode, __ATOMIC_RELEASE);
+    return TMAGEMM_OK;
+}
+
+int tmagemm_set_grouped_transposed(int mode) {
+    if (mode < 0 || mode > 2) return TMAGEMM_ERR_INVALID;
+    __atomic_store_n(&g_grouped_t, mode, __ATOMIC_RELEASE);
+    return TMAGEMM_OK;
+}
+
+int tmagemm_grouped_plan(int64_t G, const int64_t* m_offsets, int64_t N, int64_t num_sms,
+                         int64_t num_pairs, int64_t* out) {
+    if (!out || !m_offsets || G <= 0 || G > kMaxGroupsHost || N <= 0 || num_sms <= 0 ||
+        num_pairs < 0 || num_pairs > num_sms / 2 || m_offsets[0] != 0)
+        return TMAGEMM_ERR_INVALID;
+    for (int64_t g = 0; g < G; ++g)
+        if (m_offsets[g + 1] < m_offsets[g]) return TMAGEMM_ERR_INVALID;
+    GroupedLaunch gl{};
+    plan_grouped(m_offsets, G, N, static_cast<int>(num_sms), static_cast<int>(num_pairs),
+                 process_tuning(), &gl);
+    out[0] = gl.transposed ? 1 : 0;
+    out[1] = gl.pair ? 1 : 0;
+    out[2] = gl.bn;
+    out[3] = gl.maxw;
     return TMAGEMM_OK;
 }
 

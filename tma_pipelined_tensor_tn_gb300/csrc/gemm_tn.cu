@@ -70,7 +70,7 @@ namespace {
 constexpr bool kL2WarmUp = TMAGEMM_L2_WARMUP != 0;
 
 template <int BN_, int EPI_COLS_, int STAGES_, bool OUT_F32_, bool BF16_, int TMEM_COLS_ = 512,
-          int CTAS_PER_SM_ = 1, bool PAIR_ = false, int CK_ = 0>
+          int CTAS_PER_SM_ = 1, bool PAIR_ = false, int CK_ = 0, int A_ROWS_ = 128>
 struct Cfg {
     static constexpr int BM = 128, BN = BN_, BK = 64, STAGES = STAGES_;
     // PAIR: a cluster of two CTAs runs one 256 x BN tile with cta_group::2
@@ -93,7 +93,13 @@ struct Cfg {
     static constexpr uint32_t kEpiRowBytes = kEpiCols * kEpiElemBytes;
     static constexpr uint32_t kEpiChunks = kEpiRowBytes / 16;    // 16-byte chunks per box row
     static constexpr int kGroupM = 8;   // L2 group height in tiles (grouped GEMM; dense: per plan)
-    static constexpr uint32_t kABytes = BM * BK * 2;
+    // A_ROWS < 128 (problems of at most A_ROWS rows): a stage holds only
+    // A_ROWS rows of A, so more stages fit.  The 128-row MMA still reads 128
+    // rows from the stage's A address; rows past A_ROWS fall on the start of
+    // the same stage's B box (landed with it) and reach only accumulator rows
+    // >= M, which are never stored.
+    static constexpr int kARows = A_ROWS_;
+    static constexpr uint32_t kABytes = kARows * BK * 2;
     static constexpr uint32_t kBBytes = kBRows * BK * 2;
     static constexpr uint32_t kStageBytes = kABytes + kBBytes;
     static constexpr uint32_t kEpiBufBytes = BM * kEpiRowBytes;
@@ -103,9 +109,9 @@ struct Cfg {
     static constexpr uint32_t kTmemCols = TMEM_COLS_;
     static constexpr uint32_t kAccStride = TMEM_COLS_ / 2;
     static constexpr int kCtasPerSm = CTAS_PER_SM_;
+    // Stage s: its A box at kOffA + s * kStageBytes, its B box right after.
     static constexpr uint32_t kOffA = 0;
-    static constexpr uint32_t kOffB = kOffA + STAGES * kABytes;
-    static constexpr uint32_t kOffD = kOffB + STAGES * kBBytes;
+    static constexpr uint32_t kOffD = kOffA + STAGES * kStageBytes;
     static constexpr uint32_t kOffBar = kOffD + kEpiBufs * kEpiBufBytes;
     static constexpr uint32_t kNumBars = 2 * STAGES + 5;
     static constexpr uint32_t kOffMisc = kOffBar + kNumBars * 8;
@@ -126,13 +132,20 @@ struct Cfg {
     static constexpr bool kTailSplit = !OUT_F32_ && CK_ == 0 && kNarrowCols < BN_ &&
                                        kNarrowBRows % 8 == 0 &&
                                        ((BN_ - kNarrowCols) / (PAIR_ ? 2 : 1)) % 8 == 0;
+    // Units narrower than BN (tail-split parts, transposed grouped blocks):
+    // their MMA N and store boxes follow the unit.
+    static constexpr bool kVarCols = !OUT_F32_ && CK_ == 0;
 
     static_assert(BK * 2 == 128, "a K-major row of one k-block is one 128-byte swizzle atom");
     static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "UMMA N for M = 128");
-    static_assert(kEpiRowBytes == 64 || kEpiRowBytes == 128, "store boxes are 64 or 128 bytes wide");
+    static_assert(CK_ != 0 || kEpiRowBytes == 64 || kEpiRowBytes == 128,
+                  "store boxes are 64 or 128 bytes wide (cluster splits store without them)");
     static_assert(kEpiCols % 16 == 0 && BN % kEpiCols == 0, "epilogue boxes tile BN");
     static_assert(kAccStride + BN <= kTmemCols, "two accumulators fit in TMEM");
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "stages stay 1024-B aligned");
+    static_assert(kARows == BM || (kARows % 16 == 0 && kARows < BM && !PAIR_ &&
+                                   uint32_t(BM - kARows) * BK * 2 <= kBBytes),
+                  "a short A box: the MMA's rows past it stay inside the stage");
     static_assert(kEpiBufBytes % 1024 == 0, "epilogue boxes stay 1024-B aligned");
     static_assert(kSmemBytes <= 232448, "fits the 227 KB opt-in shared memory");
     static_assert(kTmemCols * CTAS_PER_SM_ <= 512, "resident CTAs share the SM's 512 TMEM columns");
@@ -174,6 +187,10 @@ template <bool T, int CK> using CfgPCK256 = Cfg<256, 64, 6, false, T, 512, 1, tr
 // clusters of 8 CTAs at ~200 KB each, 36 of 4, 76 of 2), with deeper rings.
 template <bool T, int CK> using CfgCK128 = Cfg<128, 64, 6, false, T, 256, 1, false, CK>;
 template <bool T, int CK> using CfgCK192 = Cfg<192, 64, 5, false, T, 512, 1, false, CK>;
+// Decode-sized cluster split (at most 64 rows of A, so a stage holds a
+// 64-row A box): the 128-wide 4-CTA tiles with a 9-stage ring instead of 6,
+// half again as many weight bytes in flight per SM.
+template <bool T> using CfgCKD128 = Cfg<128, 64, 9, false, T, 256, 1, false, 4, 64>;
 
 // Two CTAs per SM (each with half the ring and 128 TMEM columns) keep two
 // independent weight streams per SM in flight.
@@ -208,15 +225,20 @@ struct Work {
     // [narrow_cols, BN) for p = 1.  narrow_cols = 0 (and full_units =
     // num_units): no tail split.
     int32_t full_units, narrow_cols;
+    int32_t narrow_b_bytes;   // bytes of one stage's B box for a narrow unit (per CTA)
 };
 
 struct DenseProblem {
+    static constexpr bool kTransposed = false;   // D tiles stored as computed
     CUtensorMap tmA, tmB, tmD;
     CUtensorMap tmBn;   // B with the narrow box of tail-split parts
     Work w;
     void* d_out;   // D itself (M x N, row-major), for the cluster-split epilogue
 
     __device__ __forceinline__ int32_t num_units() const { return w.num_units; }
+    __device__ __forceinline__ uint32_t narrow_b_bytes() const {
+        return static_cast<uint32_t>(w.narrow_b_bytes);
+    }
     // Bytes one stage's A box brings (the rest of the A stage is not written).
     __device__ __forceinline__ uint32_t a_box_bytes(int BK) const {
         return static_cast<uint32_t>(w.a_box_rows) * static_cast<uint32_t>(BK) * 2u;
@@ -295,6 +317,7 @@ struct DenseProblem {
 constexpr int kMaxGroups = 64;
 
 struct GroupedProblem {
+    static constexpr bool kTransposed = false;
     CUtensorMap tmA, tmB;
     CUtensorMap tmD[kMaxGroups];
     int32_t tile_start[kMaxGroups + 1];   // prefix sums of the groups' tile counts
@@ -302,6 +325,7 @@ struct GroupedProblem {
     int32_t groups, grid_n, N, k_blocks;
 
     __device__ __forceinline__ int32_t num_units() const { return tile_start[groups]; }
+    __device__ __forceinline__ uint32_t narrow_b_bytes() const { return 0; }   // no narrow units
     __device__ __forceinline__ uint32_t a_box_bytes(int BK) const {
         return 128u * static_cast<uint32_t>(BK) * 2u;
     }
@@ -353,6 +377,85 @@ struct GroupedProblem {
     template <bool kOutF32>
     __device__ __forceinline__ void store(uint32_t buf, int32_t x, const UnitInfo& ui) const {
         tma_store_2d(&tmD[ui.store_z], buf, x, ui.store_y);
+    }
+};
+
+// Grouped problem, transposed: each group is computed as D_g^T = B_g A_g^T,
+// so that its run-time row count becomes the MMA's N (whole 16-row steps)
+// instead of a tile's 128 or 256 rows.  The weights B_g (N x K) are the
+// 128-row (per CTA) operand, the group's rows of A the narrow one; the
+// accumulator of a tile holds [weight row n][row t of A] and is stored
+// transposed, as rows t, columns n of D.  A group's rows are cut into
+// tb_count(g) blocks of nearly equal width (multiples of 16, at most maxw16 *
+// 16): no block is padded by more than 15 rows.  Units run group by group,
+// and within a group a block of rows against every weight block in turn, so
+// a group's weights and rows are reused from L2 while the group runs.
+struct GroupedTProblem {
+    static constexpr bool kTransposed = true;
+    CUtensorMap tmW;                      // B as {K, N, G}, box {64, 128, 1}
+    CUtensorMap tmX;                      // A as {K, rows}, box {64, BN / CTAs per tile}
+    CUtensorMap tmD[kMaxGroups];          // D rows of group g as {N, M_g}, box {128, 16}
+    int32_t tile_start[kMaxGroups + 1];   // prefix sums of the groups' unit counts
+    int32_t m_off[kMaxGroups + 1];        // row offsets; m_off[groups] = all rows
+    int32_t groups, n_blocks, N, k_blocks, maxw16;
+
+    __device__ __forceinline__ int32_t num_units() const { return tile_start[groups]; }
+    __device__ __forceinline__ uint32_t narrow_b_bytes() const { return 0; }   // one B box
+    __device__ __forceinline__ uint32_t a_box_bytes(int BK) const {
+        return 128u * static_cast<uint32_t>(BK) * 2u;
+    }
+    __device__ __forceinline__ void prefetch() const {
+        tma_prefetch_desc(&tmW);
+        tma_prefetch_desc(&tmX);
+    }
+    __device__ __forceinline__ void prefetch_l2(int32_t k, const UnitInfo& ui, int32_t row_a,
+                                                int32_t row_b) const {
+        tma_prefetch_l2_3d(&tmW, k, ui.a_row + row_a, ui.store_z);
+        tma_prefetch_l2_2d(&tmX, k, ui.b_row + row_b);
+    }
+    __device__ __forceinline__ UnitInfo unit(int32_t u, int BM, int, int) const {
+        int32_t g = 0;
+        while (g + 1 < groups && tile_start[g + 1] <= u) ++g;
+        const int32_t local = u - tile_start[g];
+        const int32_t rows = m_off[g + 1] - m_off[g];
+        // rows in 16-row steps, cut into tb blocks of q or q + 1 steps
+        const int32_t steps = (rows + 15) / 16;
+        const int32_t tb_count = (steps + maxw16 - 1) / maxw16;
+        const int32_t q = steps / tb_count, extra = steps % tb_count;
+        const int32_t tb = local / n_blocks, nb = local % n_blocks;
+        UnitInfo ui;
+        ui.a_row = nb * BM;                                       // weight rows (D columns)
+        const int32_t t0 = 16 * (tb * q + min(tb, extra));         // first row of the block
+        ui.b_row = m_off[g] + t0;
+        ui.cols = 16 * (q + (tb < extra ? 1 : 0));
+        ui.narrow = 0;
+        ui.kb0 = 0;
+        ui.kb1 = k_blocks;
+        ui.store_y = t0;                                          // row in group g's D map
+        ui.store_z = g;
+        ui.n_limit = N;
+        ui.m_limit = rows;
+        return ui;
+    }
+    __device__ __forceinline__ void load_a(uint32_t dst, int32_t k, const UnitInfo& ui,
+                                           uint32_t bar) const {
+        tma_load_3d(dst, &tmW, k, ui.a_row, ui.store_z, bar);
+    }
+    __device__ __forceinline__ void load_b(uint32_t dst, int32_t k, const UnitInfo& ui,
+                                           uint32_t bar) const {
+        tma_load_2d(dst, &tmX, k, ui.b_row, bar);
+    }
+    __device__ __forceinline__ void load_a_pair(uint32_t dst, int32_t k, const UnitInfo& ui,
+                                                int32_t row_off, uint32_t bar_cluster) const {
+        tma_load_3d_pair(dst, &tmW, k, ui.a_row + row_off, ui.store_z, bar_cluster);
+    }
+    __device__ __forceinline__ void load_b_pair(uint32_t dst, int32_t k, const UnitInfo& ui,
+                                                int32_t row_off, uint32_t bar_cluster) const {
+        tma_load_2d_pair(dst, &tmX, k, ui.b_row + row_off, bar_cluster);
+    }
+    // A 16-row x 128-column box of D (rows y.., columns x..) of group z.
+    __device__ __forceinline__ void store_t(uint32_t buf, int32_t x, int32_t y, int32_t z) const {
+        tma_store_2d(&tmD[z], buf, x, y);
     }
 };
 
@@ -467,8 +570,8 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
             for (int32_t u = unit0; ok && u < prob.num_units(); u += unit_step) {
                 const UnitInfo ui = prob.unit(u, C::kTileM, C::BN, C::kGroupM);
                 // A pair's B rows: this CTA's half of the unit's columns.
-                const bool narrow = C::kTailSplit && ui.narrow != 0;
-                const uint32_t b_bytes = narrow ? C::kNarrowBBytes : C::kBBytes;
+                const bool narrow = C::kVarCols && ui.narrow != 0;
+                const uint32_t b_bytes = narrow ? prob.narrow_b_bytes() : C::kBBytes;
                 const int32_t b_off = static_cast<int32_t>(rank) * (ui.cols / 2);
                 for (int32_t kb = ui.kb0; kb < ui.kb1; ++kb) {
                     const uint32_t s = ring_stage(it, C::STAGES);
@@ -492,14 +595,15 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                             mbar_arrive_expect_tx(full_bar(s),
                                                   2 * (prob.a_box_bytes(C::BK) + b_bytes));
                         const uint32_t leader_full = map_to_rank(full_bar(s), pair_leader);
-                        prob.load_a_pair(sbase + C::kOffA + s * C::kABytes, kb * C::BK, ui,
+                        const uint32_t stage = sbase + C::kOffA + s * C::kStageBytes;
+                        prob.load_a_pair(stage, kb * C::BK, ui,
                                          static_cast<int32_t>(rank) * C::BM, leader_full);
-                        prob.load_b_pair(sbase + C::kOffB + s * C::kBBytes, kb * C::BK, ui, b_off,
-                                         leader_full);
+                        prob.load_b_pair(stage + C::kABytes, kb * C::BK, ui, b_off, leader_full);
                     } else {
                         mbar_arrive_expect_tx(full_bar(s), prob.a_box_bytes(C::BK) + b_bytes);
-                        prob.load_a(sbase + C::kOffA + s * C::kABytes, kb * C::BK, ui, full_bar(s));
-                        prob.load_b(sbase + C::kOffB + s * C::kBBytes, kb * C::BK, ui, full_bar(s));
+                        const uint32_t stage = sbase + C::kOffA + s * C::kStageBytes;
+                        prob.load_a(stage, kb * C::BK, ui, full_bar(s));
+                        prob.load_b(stage + C::kABytes, kb * C::BK, ui, full_bar(s));
                     }
                     ++it;
                 }
@@ -526,9 +630,9 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 const UnitInfo ui = prob.unit(u, C::kTileM, C::BN, C::kGroupM);
                 const int32_t kb0 = ui.kb0;
                 const int32_t kb1 = ui.kb1;
-                // A tail-split part is an MMA of its own width (N = its columns).
+                // A narrow unit is an MMA of its own width (N = its columns).
                 const uint32_t idesc =
-                    C::kTailSplit && ui.narrow
+                    C::kVarCols && ui.cols != C::BN
                         ? umma_idesc_16bit_f32(C::kTileM, static_cast<uint32_t>(ui.cols), C::kBF16)
                         : C::kIdesc;
                 const uint32_t acc = tcount & 1u;
@@ -546,8 +650,8 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a_addr = sbase + C::kOffA + s * C::kABytes;
-                    const uint32_t b_addr = sbase + C::kOffB + s * C::kBBytes;
+                    const uint32_t a_addr = sbase + C::kOffA + s * C::kStageBytes;
+                    const uint32_t b_addr = a_addr + C::kABytes;
 #pragma unroll
                     for (int j = 0; j < C::BK / 16; ++j) {
                         const uint64_t ad = umma_desc_sw128_kmajor(a_addr + 32u * j);
@@ -606,6 +710,17 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                     st_shared_v4(p_row + (32u * c + 4u * j) * 4u, v[4 * j], v[4 * j + 1],
                                  v[4 * j + 2], v[4 * j + 3]);
             }
+            if constexpr (C::BN % 32 != 0) {
+                // The last 16 columns of a tile whose width is an odd multiple of 16.
+                constexpr uint32_t c0 = C::BN / 32 * 32;
+                uint32_t v[16];
+                tmem_ld_32x32b_x16(t_row + c0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    st_shared_v4(p_row + (c0 + 4u * j) * 4u, v[4 * j], v[4 * j + 1], v[4 * j + 2],
+                                 v[4 * j + 3]);
+            }
         }
     } else {
         // ================= epilogue (warps 2..5) =================
@@ -615,7 +730,8 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
         uint32_t tcount = 0, box = 0;
         for (int32_t u = unit0; u < prob.num_units(); u += unit_step, ++tcount) {
             UnitInfo ui = prob.unit(u, C::kTileM, C::BN, C::kGroupM);
-            ui.store_y += static_cast<int32_t>(rank) * C::BM;   // this CTA's 128 rows
+            if constexpr (!P::kTransposed)
+                ui.store_y += static_cast<int32_t>(rank) * C::BM;   // this CTA's 128 rows
             const int32_t n0 = ui.b_row;
             const uint32_t acc = tcount & 1u;
             const uint32_t acc_ph = (tcount >> 1) & 1u;
@@ -625,7 +741,49 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
             if (!named_bar_and(1, C::kEpiThreads, ok)) break;
             tc_fence_after();
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16) + acc * C::kAccStride;
-            const int chunks = (C::kTailSplit && ui.narrow ? ui.cols : C::BN) / C::kEpiCols;
+            // Whole accumulator read: give it back to the MMA warp.
+            auto release_acc = [&]() {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if constexpr (C::kPair)
+                        mbar_arrive_cluster(map_to_rank(acc_empty_bar(acc), pair_leader));
+                    else
+                        mbar_arrive(acc_empty_bar(acc));
+                }
+            };
+            if constexpr (P::kTransposed) {
+                // The accumulator is [weight row n][row t of A]: each box is
+                // 16 rows of D by this CTA's 128 columns, row t of the box
+                // (256 bytes, unswizzled) holding column n = `row` at byte
+                // 2n, written by this thread from its accumulator column t.
+                const int tchunks = ui.cols / 16;
+                const int32_t x = ui.a_row + static_cast<int32_t>(rank) * C::BM;
+#pragma unroll 1
+                for (int c = 0; c < tchunks; ++c, ++box) {
+                    uint32_t v[16];
+                    tmem_ld_32x32b_x16(t_row + 16 * c, v);
+                    tmem_ld_wait();
+                    if (c == tchunks - 1) release_acc();
+                    const uint32_t buf = sbase + C::kOffD + (box & 1u) * C::kEpiBufBytes;
+                    if (store_thread) bulk_wait_group_read<1>();
+                    named_bar_sync(1, C::kEpiThreads);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t)
+                        st_shared_u16(buf + static_cast<uint32_t>(t) * 256u + row * 2u,
+                                      cvt16_rn<C::kBF16>(v[t]));
+                    fence_proxy_async_smem();
+                    named_bar_sync(1, C::kEpiThreads);
+                    if (store_thread) {
+                        const int32_t y = ui.store_y + 16 * c;
+                        if (x < ui.n_limit && y < ui.m_limit &&
+                            check_ok((x & 7) == 0 && x >= 0 && y >= 0, err, kSiteCheckTma))
+                            prob.store_t(buf, x, y, ui.store_z);
+                        bulk_commit_group();
+                    }
+                }
+            } else {
+            const int chunks = (C::kVarCols ? ui.cols : C::BN) / C::kEpiCols;
 #pragma unroll 1
             for (int c = 0; c < chunks; ++c, ++box) {
                 uint32_t v[C::kEpiCols];
@@ -639,17 +797,7 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                                            *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
                 }
                 tmem_ld_wait();
-                if (c == chunks - 1) {
-                    // Whole accumulator read: give it back to the MMA warp.
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        if constexpr (C::kPair)
-                            mbar_arrive_cluster(map_to_rank(acc_empty_bar(acc), pair_leader));
-                        else
-                            mbar_arrive(acc_empty_bar(acc));
-                    }
-                }
+                if (c == chunks - 1) release_acc();
                 const uint32_t buf = sbase + C::kOffD + (box & 1u) * C::kEpiBufBytes;
                 // The store that last read this buffer (two boxes ago) must be done.
                 if (store_thread) bulk_wait_group_read<1>();
@@ -683,6 +831,7 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                     bulk_commit_group();
                 }
             }
+            }   // not transposed
             if (store_thread && rank == 0) check_count_unit(err, u);
         }
         if (store_thread) bulk_wait_group<0>();
@@ -881,6 +1030,7 @@ GemmPlan plan_for(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t splits, 
     p.out_f32 = C::kOutF32;
     p.bf16 = C::kBF16;
     p.pair = C::kPair;
+    p.a_rows = C::kARows;
     p.b_box_rows = C::kBRows;
     // With fewer than 128 rows, a box only as tall as the rows that exist
     // (16-row multiples: whole 8-row swizzle atoms) spares the TMA unit the
@@ -970,12 +1120,21 @@ cudaError_t launch_cfg(const GemmPlan& plan, const CUtensorMap& tmA, const CUten
     prob.w.kb_per_unit = static_cast<int32_t>(plan.kb_per_unit);
     prob.w.group_m = static_cast<int32_t>(plan.group_m);
     prob.w.a_box_rows = plan.a_box_rows;
+    if (plan.a_box_rows > C::kARows || plan.a_rows != C::kARows) return cudaErrorInvalidValue;
     prob.w.full_units = static_cast<int32_t>(plan.full_units);
     prob.w.narrow_cols = plan.narrow_cols;
+    prob.w.narrow_b_bytes = plan.narrow_b_rows * C::BK * 2;
     if (plan.narrow_cols > 0) {
-        // The parts' B box must be the one the kernel counts bytes for.
-        if (!C::kTailSplit || args.tmBn == nullptr || plan.narrow_cols != C::kNarrowCols ||
-            plan.narrow_b_rows != C::kNarrowBRows || plan.full_units > plan.units)
+        // Tail-split parts: whole store boxes, an MMA N of 16s, whole 8-row
+        // swizzle atoms of B in each CTA, and B read through the narrow box
+        // whose bytes the kernel counts (narrow_b_rows rows per CTA).
+        const int per_cta = C::kPair ? 2 : 1;
+        const int second = C::BN - plan.narrow_cols;   // the second part
+        if (!C::kTailSplit || args.tmBn == nullptr || plan.narrow_cols >= C::BN ||
+            plan.narrow_cols % 16 != 0 || plan.narrow_cols % C::kEpiCols != 0 ||
+            plan.narrow_b_rows * per_cta != plan.narrow_cols || plan.narrow_b_rows % 8 != 0 ||
+            plan.full_units > plan.units || second % C::kEpiCols != 0 ||
+            (second / per_cta) % 8 != 0)
             return cudaErrorInvalidValue;
         prob.tmBn = *args.tmBn;
     } else {
@@ -1020,6 +1179,41 @@ cudaError_t launch_grouped_cfg(const GroupedLaunch& g, int num_sms, int num_pair
                          args.wait_limit_ns, args.err_word);
 }
 
+template <class C>
+cudaError_t launch_grouped_t_cfg(const GroupedLaunch& g, int num_sms, int num_pairs,
+                                 const GemmArgs& args, cudaStream_t stream) {
+    static_assert(C::BN == 256 && C::kEpiBufBytes >= 16 * 256 && !C::kOutF32 && C::kClusterK == 0,
+                  "transposed grouped tiles: blocks of up to 256 rows, 16 x 128 store boxes");
+    auto kernel = gemm_tn_f16_kernel<C, GroupedTProblem>;
+    static ContextMarks attr_done;
+    cudaError_t e = smem_opt_in(kernel, static_cast<int>(C::kSmemBytes), attr_done);
+    if (e != cudaSuccess) return e;
+    if (g.maxw < 16 || g.maxw > C::BN || g.maxw % 16 != 0) return cudaErrorInvalidValue;
+    GroupedTProblem prob;
+    prob.tmW = g.tmA;
+    prob.tmX = g.tmB;
+    prob.groups = static_cast<int32_t>(g.groups);
+    prob.n_blocks = static_cast<int32_t>(ceil_div(g.N, C::kTileM));
+    prob.N = static_cast<int32_t>(g.N);
+    prob.k_blocks = static_cast<int32_t>(ceil_div(g.K, C::BK));
+    prob.maxw16 = g.maxw / 16;
+    int32_t t = 0;
+    for (int64_t i = 0; i <= g.groups; ++i) {
+        prob.m_off[i] = static_cast<int32_t>(g.m_offsets[i]);
+        prob.tile_start[i] = t;
+        if (i < g.groups) {
+            prob.tmD[i] = g.tmD[i];
+            const int64_t steps = ceil_div(g.m_offsets[i + 1] - g.m_offsets[i], 16);
+            t += static_cast<int32_t>(ceil_div(steps, prob.maxw16) * prob.n_blocks);
+        }
+    }
+    if (t == 0) return cudaSuccess;   // every group is empty
+    const int grid = C::kPair ? 2 * (t < num_pairs ? t : num_pairs) : (t < num_sms ? t : num_sms);
+    return launch_kernel(kernel, dim3(static_cast<unsigned>(grid)), dim3(C::kThreads),
+                         C::kSmemBytes, stream, C::kPair ? 2u : 1u, args.pdl, prob,
+                         args.wait_limit_ns, args.err_word);
+}
+
 }  // namespace
 
 int grouped_tile_n(const int64_t* m_offsets, int64_t groups, int64_t N, int num_sms, int num_pairs,
@@ -1055,8 +1249,80 @@ int grouped_tile_n(const int64_t* m_offsets, int64_t groups, int64_t N, int num_
     return best;
 }
 
+namespace {
+
+// Largest per-slot load of the transposed grouped schedule (units in the
+// order GroupedTProblem numbers them, slot = unit mod slots): the sum over a
+// slot's units of (block width + c).
+int64_t grouped_t_max_load(const int64_t* m_offsets, int64_t groups, int64_t n_blocks,
+                           int64_t maxw, int64_t c, int64_t slots) {
+    int64_t loads[1024] = {};
+    if (slots > 1024) return -1;
+    int64_t u = 0;
+    for (int64_t g = 0; g < groups; ++g) {
+        const int64_t steps = ceil_div(m_offsets[g + 1] - m_offsets[g], 16);
+        if (steps == 0) continue;
+        const int64_t tb_count = ceil_div(steps, maxw / 16);
+        const int64_t q = steps / tb_count, extra = steps % tb_count;
+        for (int64_t tb = 0; tb < tb_count; ++tb)
+            for (int64_t nb = 0; nb < n_blocks; ++nb, ++u)
+                loads[u % slots] += 16 * (q + (tb < extra ? 1 : 0)) + c;
+    }
+    int64_t worst = 0;
+    for (int64_t s = 0; s < slots; ++s) worst = std::max(worst, loads[s]);
+    return worst;
+}
+
+}  // namespace
+
+void plan_grouped(const int64_t* m_offsets, int64_t groups, int64_t N, int num_sms, int num_pairs,
+                  const Tuning& t, GroupedLaunch* g) {
+    // Row-tiled: rounds x (BN + c) per k-block.
+    bool pair = false;
+    g->bn = grouped_tile_n(m_offsets, groups, N, num_sms, num_pairs, t, &pair);
+    g->pair = pair;
+    g->transposed = false;
+    g->maxw = 0;
+    if (t.grouped_t == 1) return;
+    int64_t best = -1;
+    {
+        const int64_t tile_m = pair ? 256 : 128;
+        const int64_t slots = pair ? num_pairs : (num_sms > 0 ? num_sms : 1);
+        int64_t tiles = 0;
+        for (int64_t i = 0; i < groups; ++i)
+            tiles += ceil_div(m_offsets[i + 1] - m_offsets[i], tile_m) * ceil_div(N, g->bn);
+        const int64_t used = tiles < slots ? (tiles > 0 ? tiles : 1) : slots;
+        best = t.grouped_t == 2 ? -1 : ceil_div(tiles, used) * (g->bn + (pair ? 16 : 32));
+    }
+    // Transposed: 256 weight rows per CTA pair (128 per single CTA) by blocks
+    // of a group's rows of at most maxw, for the maxw whose schedule is best.
+    const int pair_mode = t.pair_mode;
+    for (int use_pair = 0; use_pair < 2; ++use_pair) {
+        if (use_pair && (num_pairs <= 0 || pair_mode == 1)) continue;
+        if (!use_pair && num_pairs > 0 && pair_mode == 2) continue;
+        if (t.tile_n != 0 && t.tile_n != 256) continue;
+        const int64_t tile_m = use_pair ? 256 : 128;
+        const int64_t slots = use_pair ? num_pairs : (num_sms > 0 ? num_sms : 1);
+        for (int64_t maxw = 256; maxw >= 128; maxw -= 16) {
+            const int64_t load = grouped_t_max_load(m_offsets, groups, ceil_div(N, tile_m), maxw,
+                                                    use_pair ? 16 : 32, slots);
+            if (load < 0) continue;
+            if (best < 0 || load < best) {
+                best = load;
+                g->transposed = true;
+                g->pair = use_pair != 0;
+                g->bn = 256;
+                g->maxw = static_cast<int>(maxw);
+            }
+        }
+    }
+}
+
 cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, int num_pairs, const GemmArgs& args,
                            cudaStream_t stream) {
+    if (g.transposed)
+        return g.pair ? launch_grouped_t_cfg<CfgP256<false>>(g, num_sms, num_pairs, args, stream)
+                      : launch_grouped_t_cfg<Cfg256<false>>(g, num_sms, num_pairs, args, stream);
     if (g.pair) {
         switch (g.bn) {
             case 256: return launch_grouped_cfg<CfgP256<false>>(g, num_sms, num_pairs, args, stream);
@@ -1096,8 +1362,8 @@ GemmPlan plan_cluster_split(int64_t M, int64_t N, int64_t K, int64_t slots, int 
 template <bool T>
 GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs, int64_t splits,
                     const ClusterCaps& caps, const Tuning& t) {
-    // 3 single-CTA and 3 pair tile plans, up to 9 cluster splits.
-    GemmPlan cands[15];
+    // 3 single-CTA and 3 pair tile plans, up to 10 cluster splits.
+    GemmPlan cands[16];
     int n = 0;
     const int pair_mode = t.pair_mode;
     const int forced = t.tile_n;
@@ -1115,6 +1381,7 @@ GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs,
             cands[n++] = plan_for<CfgP224<T>>(M, N, K, pairs, 1, t);
             cands[n++] = plan_for<CfgP192<T>>(M, N, K, pairs, 1, t);
         }
+
         // Few tiles and a long K: split K over clusters (no workspace).
         const int ck_mode = t.cluster_split;
         if (ck_mode != 1) {
@@ -1122,7 +1389,7 @@ GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs,
             // The narrower single-CTA tiles take the co-residency measured for
             // the 256-wide ones: all need one CTA per SM, so a cluster of CK
             // CTAs packs the same way.
-            GemmPlan ck[9] = {
+            GemmPlan ck[10] = {
                 plan_cluster_split<CfgCK256<T, 2>>(M, N, K, sms, caps.single_ck[0], t),
                 plan_cluster_split<CfgCK256<T, 4>>(M, N, K, sms, caps.single_ck[1], t),
                 plan_cluster_split<CfgCK256<T, 8>>(M, N, K, sms, caps.single_ck[2], t),
@@ -1131,12 +1398,17 @@ GemmPlan plan_typed(int64_t M, int64_t N, int64_t K, int64_t sms, int64_t pairs,
                 plan_cluster_split<CfgCK192<T, 2>>(M, N, K, sms, caps.single_ck[0], t),
                 plan_cluster_split<CfgCK192<T, 4>>(M, N, K, sms, caps.single_ck[1], t),
                 plan_cluster_split<CfgCK128<T, 4>>(M, N, K, sms, caps.single_ck[1], t),
-                plan_cluster_split<CfgCK128<T, 8>>(M, N, K, sms, caps.single_ck[2], t)};
+                plan_cluster_split<CfgCK128<T, 8>>(M, N, K, sms, caps.single_ck[2], t),
+                plan_cluster_split<CfgCKD128<T>>(M, N, K, sms, caps.decode_ck, t)};
+            // The decode split takes problems of at most 64 rows; where it
+            // applies, its 9-stage ring replaces the 6-stage one of the same tile.
+            if (M > 64) ck[9].units = 0;
+            if (M <= 64 && ck[9].units > 0) ck[7].units = 0;
             static_assert(sizeof(ck) / sizeof(ck[0]) + 6 <= sizeof(cands) / sizeof(cands[0]),
                           "every candidate fits");
             if (!pk) ck[3].units = ck[4].units = 0;
             if (pair_mode == 2)
-                for (int i : {0, 1, 2, 5, 6, 7, 8}) ck[i].units = 0;
+                for (int i : {0, 1, 2, 5, 6, 7, 8, 9}) ck[i].units = 0;
             for (const GemmPlan& c : ck)
                 if (c.units > 0 && ck_mode == c.cluster_k && (forced == 0 || c.bn == forced) &&
                     (!forced_ck || plan_cost(c) < plan_cost(cands[0]))) {
@@ -1188,6 +1460,12 @@ cudaError_t launch_typed(const GemmPlan& plan, const CUtensorMap& tmA, const CUt
             default: return cudaErrorInvalidValue;
         }
     }
+    if (plan.cluster_k > 0 && plan.a_rows == 64) {
+        switch (plan.bn * 16 + plan.cluster_k) {
+            case 128 * 16 + 4: return launch_cfg<CfgCKD128<T>>(plan, tmA, tmB, tmD, args, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     if (plan.cluster_k > 0) {
         switch (plan.bn * 16 + plan.cluster_k) {
             case 256 * 16 + 2: return launch_cfg<CfgCK256<T, 2>>(plan, tmA, tmB, tmD, args, stream);
@@ -1226,11 +1504,55 @@ cudaError_t launch_typed(const GemmPlan& plan, const CUtensorMap& tmA, const CUt
 
 }  // namespace
 
+namespace {
+
+// Everything a plan depends on.
+struct PlanKey {
+    int64_t m, n, k, splits;
+    int sms, pairs, bf16;
+    ClusterCaps caps;
+    Tuning t;
+    bool operator==(const PlanKey& o) const {
+        return m == o.m && n == o.n && k == o.k && splits == o.splits && sms == o.sms &&
+               pairs == o.pairs && bf16 == o.bf16 &&
+               std::equal(caps.single_ck, caps.single_ck + 3, o.caps.single_ck) &&
+               std::equal(caps.pair_ck, caps.pair_ck + 2, o.caps.pair_ck) &&
+               caps.decode_ck == o.caps.decode_ck &&
+               t.tile_n == o.t.tile_n && t.pair_mode == o.t.pair_mode &&
+               t.cluster_split == o.t.cluster_split && t.tail_split == o.t.tail_split &&
+               t.group_m == o.t.group_m && t.small_m_route == o.t.small_m_route &&
+               t.plain_launch == o.t.plain_launch && t.m1_route == o.t.m1_route &&
+               t.grouped_t == o.t.grouped_t;
+    }
+};
+
+// The last few plans of this host thread (round-robin replacement): a shape
+// that repeats skips the search over candidate plans.
+struct PlanCache {
+    static constexpr int kEntries = 8;
+    PlanKey key[kEntries];
+    GemmPlan plan[kEntries];
+    bool used[kEntries] = {};
+    int next = 0;
+};
+thread_local PlanCache t_plan_cache;
+
+}  // namespace
+
 GemmPlan plan_gemm(int64_t M, int64_t N, int64_t K, int num_sms, const Tuning& t, int64_t splits,
                    bool bf16, int num_pairs, const ClusterCaps& caps) {
     const int64_t sms = num_sms > 0 ? num_sms : 1;
-    return bf16 ? plan_typed<true>(M, N, K, sms, num_pairs, splits, caps, t)
-                : plan_typed<false>(M, N, K, sms, num_pairs, splits, caps, t);
+    const PlanKey key{M, N, K, splits, static_cast<int>(sms), num_pairs, bf16 ? 1 : 0, caps, t};
+    PlanCache& c = t_plan_cache;
+    for (int i = 0; i < PlanCache::kEntries; ++i)
+        if (c.used[i] && c.key[i] == key) return c.plan[i];
+    const GemmPlan p = bf16 ? plan_typed<true>(M, N, K, sms, num_pairs, splits, caps, t)
+                            : plan_typed<false>(M, N, K, sms, num_pairs, splits, caps, t);
+    c.key[c.next] = key;
+    c.plan[c.next] = p;
+    c.used[c.next] = true;
+    c.next = (c.next + 1) % PlanCache::kEntries;
+    return p;
 }
 
 int max_resident_pairs() {
@@ -1291,9 +1613,11 @@ ClusterCaps query_cluster_caps() {
     c.single_ck[2] = max_active_clusters<CfgCK256<false, 8>>(8);
     c.pair_ck[0] = max_active_clusters<CfgPCK256<false, 2>>(4);
     c.pair_ck[1] = max_active_clusters<CfgPCK256<false, 4>>(8);
+    c.decode_ck = max_active_clusters<CfgCKD128<false>>(4);
     // A query that failed must not read as "unknown" (ideal packing): forbid.
     for (int& v : c.single_ck) v = v > 0 ? v : -1;
     for (int& v : c.pair_ck) v = v > 0 ? v : -1;
+    c.decode_ck = c.decode_ck > 0 ? c.decode_ck : -1;
     return c;
 }
 

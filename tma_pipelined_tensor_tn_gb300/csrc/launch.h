@@ -21,6 +21,7 @@ struct Tuning {
     int small_m_route = 0;   // 1 swap-AB, 2 register fragments (M <= 16), 3 LSU-fed tcgen05
     int plain_launch = 0;    // 1: launch without programmatic dependent launch
     int m1_route = 0;        // 1: M = 1 through the tile kernel instead of the GEMV
+    int grouped_t = 0;       // grouped GEMM: 1 never transposed, 2 always transposed
     bool pdl() const { return plain_launch == 0; }
 };
 
@@ -49,6 +50,7 @@ struct GemmPlan {
     int b_box_rows;        // rows of B per CTA (bn, or bn / 2 for a pair)
     int a_box_rows;        // rows of A per TMA box: 128, or M rounded up to 16 when M < 128
     int cluster_k;         // > 0: K split over clusters of this many CTAs (one unit per CTA)
+    int a_rows;            // rows of A a stage holds (128; 64 for the decode cluster splits)
     int group_m;           // L2 group height of the tile order, in tiles
     // Tail split: the tiles of the last, partly filled round run as two units
     // each (narrow_cols and bn - narrow_cols columns), when that round is at
@@ -66,6 +68,7 @@ struct GemmPlan {
 struct ClusterCaps {
     int single_ck[3] = {0, 0, 0};
     int pair_ck[2] = {0, 0};
+    int decode_ck = 0;             // the decode split (4 CTAs, 128 wide, 9 stages)
 };
 
 // Pure function of the problem shape, the SM count and the tuning (no CUDA
@@ -144,9 +147,19 @@ struct GroupedLaunch {
     int64_t groups, N, K;
     int bn;
     bool pair;                  // CTA-pair tiles (256 rows; B box bn / 2 rows)
+    // Transposed (D_g^T = B_g A_g^T): tmA = B {K, N, G} box {64, 128, 1},
+    // tmB = A {K, rows} box {64, bn / CTAs per tile}, tmD[g] = D rows of group
+    // g {N, M_g} box {128, 16} unswizzled; a group's rows in blocks of at
+    // most maxw (a multiple of 16 up to bn).
+    bool transposed;
+    int maxw;
 };
-int grouped_tile_n(const int64_t* m_offsets, int64_t groups, int64_t N, int num_sms, int num_pairs,
-                   const Tuning& t, bool* pair);
+// The grouped GEMM's formulation and tiles for these groups: the row-tiled
+// form (tiles of 128 or 256 rows of a group by bn columns) or the transposed
+// one (256 or 128 weight rows by blocks of up to maxw rows of a group), the
+// one whose busiest CTA (pair) of the persistent schedule has the least work.
+void plan_grouped(const int64_t* m_offsets, int64_t groups, int64_t N, int num_sms, int num_pairs,
+                  const Tuning& t, GroupedLaunch* g);
 cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, int num_pairs, const GemmArgs& args,
                            cudaStream_t stream);
 

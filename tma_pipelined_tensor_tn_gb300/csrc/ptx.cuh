@@ -521,6 +521,16 @@ __device__ __forceinline__ uint32_t pack2_rn(uint32_t lo_bits, uint32_t hi_bits)
         return pack_half2_rn(lo_bits, hi_bits);
 }
 
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint16_t v) {
+    asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(v) : "memory");
+}
+
+// fp32 bits -> one fp16 or bf16, round to nearest even.
+template <bool BF16>
+__device__ __forceinline__ uint16_t cvt16_rn(uint32_t f_bits) {
+    return static_cast<uint16_t>(pack2_rn<BF16>(f_bits, 0u) & 0xffffu);
+}
+
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};"
