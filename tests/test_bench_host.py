@@ -30,12 +30,14 @@ def test_whole_job_value_counts_every_rank():
     assert bench.whole_job_value(5, 10, 2, 4.0) == 25.0
 
 
-def test_l2_rotation_exceeds_twice_l2():
+def test_l2_rotation_exceeds_four_times_l2():
+    """A set is read again only after at least 4 x L2 bytes of sets (the
+    smallest such count)."""
     l2 = 129 * 2 ** 20
     for per_set in (int(bench.gemm_bytes()), int(bench.gemv_bytes()), 10 ** 6):
         n = inputs.l2_rotation_count(per_set, l2)
-        assert n >= 2 and n * per_set >= 2 * l2
-        assert (n - 1) * per_set < 2 * l2 or n == 2
+        assert n >= 2 and n * per_set >= 4 * l2
+        assert (n - 1) * per_set < 4 * l2 or n == 2
 
 
 def _free_port():

@@ -504,7 +504,11 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
                               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
             return s;
         g.tmA = weights;
-        // D rows of each group, stored 16 rows x 128 columns at a time (unswizzled).
+        // D as one map (64 rows x 128 columns per store, inside a group) and
+        // per group (16 x 128, clipped at the group's last row); unswizzled.
+        if (int s = encode_2d(&g.tmD64, D, N, rows, 128, 64, CU_TENSOR_MAP_SWIZZLE_NONE,
+                              CU_TENSOR_MAP_L2_PROMOTION_NONE))
+            return s;
         for (int64_t i = 0; i < G; ++i) {
             const int64_t mg = m_offsets[i + 1] - m_offsets[i];
             if (mg == 0) continue;   // an empty group has no tiles and no map

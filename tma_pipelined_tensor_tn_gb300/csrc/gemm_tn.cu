@@ -69,6 +69,7 @@ namespace {
 // Prefetch of each CTA's first k-blocks into L2 before the dependency wait.
 constexpr bool kL2WarmUp = TMAGEMM_L2_WARMUP != 0;
 
+
 template <int BN_, int EPI_COLS_, int STAGES_, bool OUT_F32_, bool BF16_, int TMEM_COLS_ = 512,
           int CTAS_PER_SM_ = 1, bool PAIR_ = false, int CK_ = 0, int A_ROWS_ = 128>
 struct Cfg {
@@ -385,7 +386,9 @@ struct GroupedProblem {
 // instead of a tile's 128 or 256 rows.  The weights B_g (N x K) are the
 // 128-row (per CTA) operand, the group's rows of A the narrow one; the
 // accumulator of a tile holds [weight row n][row t of A] and is stored
-// transposed, as rows t, columns n of D.  A group's rows are cut into
+// transposed, as rows t, columns n of D: 64 rows at a time through one map
+// over all of D where those rows lie inside the group, else 16 rows at a
+// time through the group's own map, which clips at the group's last row.  A group's rows are cut into
 // tb_count(g) blocks of nearly equal width (multiples of 16, at most maxw16 *
 // 16): no block is padded by more than 15 rows.  Units run group by group,
 // and within a group a block of rows against every weight block in turn, so
@@ -395,6 +398,7 @@ struct GroupedTProblem {
     CUtensorMap tmW;                      // B as {K, N, G}, box {64, 128, 1}
     CUtensorMap tmX;                      // A as {K, rows}, box {64, BN / CTAs per tile}
     CUtensorMap tmD[kMaxGroups];          // D rows of group g as {N, M_g}, box {128, 16}
+    CUtensorMap tmD64;                    // all of D as {N, rows}, box {128, 64}
     int32_t tile_start[kMaxGroups + 1];   // prefix sums of the groups' unit counts
     int32_t m_off[kMaxGroups + 1];        // row offsets; m_off[groups] = all rows
     int32_t groups, n_blocks, N, k_blocks, maxw16;
@@ -407,6 +411,7 @@ struct GroupedTProblem {
     __device__ __forceinline__ void prefetch() const {
         tma_prefetch_desc(&tmW);
         tma_prefetch_desc(&tmX);
+        tma_prefetch_desc(&tmD64);
     }
     __device__ __forceinline__ void prefetch_l2(int32_t k, const UnitInfo& ui, int32_t row_a,
                                                 int32_t row_b) const {
@@ -453,9 +458,14 @@ struct GroupedTProblem {
                                                 int32_t row_off, uint32_t bar_cluster) const {
         tma_load_2d_pair(dst, &tmX, k, ui.b_row + row_off, bar_cluster);
     }
-    // A 16-row x 128-column box of D (rows y.., columns x..) of group z.
-    __device__ __forceinline__ void store_t(uint32_t buf, int32_t x, int32_t y, int32_t z) const {
+    // A 16-row x 128-column box of D: rows y.. of group z, columns x...
+    __device__ __forceinline__ void store_t16(uint32_t buf, int32_t x, int32_t y,
+                                              int32_t z) const {
         tma_store_2d(&tmD[z], buf, x, y);
+    }
+    // A 64-row x 128-column box of D: rows y.. of all of D, columns x...
+    __device__ __forceinline__ void store_t64(uint32_t buf, int32_t x, int32_t y) const {
+        tma_store_2d(&tmD64, buf, x, y);
     }
 };
 
@@ -753,32 +763,44 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 }
             };
             if constexpr (P::kTransposed) {
-                // The accumulator is [weight row n][row t of A]: each box is
-                // 16 rows of D by this CTA's 128 columns, row t of the box
-                // (256 bytes, unswizzled) holding column n = `row` at byte
-                // 2n, written by this thread from its accumulator column t.
-                const int tchunks = ui.cols / 16;
+                // The accumulator is [weight row n][row t of A]: a chunk is up
+                // to 64 rows of D by this CTA's 128 columns, staged as rows of
+                // 256 bytes (unswizzled), row t holding column n = `row` at
+                // byte 2n, written by this thread from accumulator column t.
+                static_assert(C::kEpiBufBytes >= 64 * 256, "a 64-row chunk fits a store buffer");
                 const int32_t x = ui.a_row + static_cast<int32_t>(rank) * C::BM;
 #pragma unroll 1
-                for (int c = 0; c < tchunks; ++c, ++box) {
-                    uint32_t v[16];
-                    tmem_ld_32x32b_x16(t_row + 16 * c, v);
+                for (int c0 = 0; c0 < ui.cols; c0 += 64, ++box) {
+                    const int n16 = min(64, ui.cols - c0) / 16;   // 16-row parts of the chunk
+                    uint32_t v[64];
+#pragma unroll
+                    for (int h = 0; h < 4; ++h)
+                        if (h < n16)
+                            tmem_ld_32x32b_x16(t_row + c0 + 16 * h,
+                                               *reinterpret_cast<uint32_t(*)[16]>(&v[16 * h]));
                     tmem_ld_wait();
-                    if (c == tchunks - 1) release_acc();
+                    if (c0 + 64 >= ui.cols) release_acc();
                     const uint32_t buf = sbase + C::kOffD + (box & 1u) * C::kEpiBufBytes;
                     if (store_thread) bulk_wait_group_read<1>();
                     named_bar_sync(1, C::kEpiThreads);
 #pragma unroll
-                    for (int t = 0; t < 16; ++t)
-                        st_shared_u16(buf + static_cast<uint32_t>(t) * 256u + row * 2u,
-                                      cvt16_rn<C::kBF16>(v[t]));
+                    for (int t = 0; t < 64; ++t)
+                        if (t < 16 * n16)
+                            st_shared_u16(buf + static_cast<uint32_t>(t) * 256u + row * 2u,
+                                          cvt16_rn<C::kBF16>(v[t]));
                     fence_proxy_async_smem();
                     named_bar_sync(1, C::kEpiThreads);
                     if (store_thread) {
-                        const int32_t y = ui.store_y + 16 * c;
-                        if (x < ui.n_limit && y < ui.m_limit &&
-                            check_ok((x & 7) == 0 && x >= 0 && y >= 0, err, kSiteCheckTma))
-                            prob.store_t(buf, x, y, ui.store_z);
+                        const int32_t y = ui.store_y + c0;        // row in the group
+                        if (x < ui.n_limit &&
+                            check_ok((x & 7) == 0 && x >= 0 && y >= 0, err, kSiteCheckTma)) {
+                            if (n16 == 4 && y + 64 <= ui.m_limit) {
+                                prob.store_t64(buf, x, ui.b_row + c0);   // inside the group
+                            } else {
+                                for (int j = 0; j < n16 && y + 16 * j < ui.m_limit; ++j)
+                                    prob.store_t16(buf + 4096u * j, x, y + 16 * j, ui.store_z);
+                            }
+                        }
                         bulk_commit_group();
                     }
                 }
@@ -1192,6 +1214,7 @@ cudaError_t launch_grouped_t_cfg(const GroupedLaunch& g, int num_sms, int num_pa
     GroupedTProblem prob;
     prob.tmW = g.tmA;
     prob.tmX = g.tmB;
+    prob.tmD64 = g.tmD64;
     prob.groups = static_cast<int32_t>(g.groups);
     prob.n_blocks = static_cast<int32_t>(ceil_div(g.N, C::kTileM));
     prob.N = static_cast<int32_t>(g.N);

@@ -62,8 +62,11 @@ def integer_f16(shape, seed: int, lo: int = -2, hi: int = 2) -> torch.Tensor:
     return torch.randint(lo, hi + 1, shape, generator=g, dtype=torch.int32).to(torch.float16)
 
 
-def l2_rotation_count(bytes_per_set: int, l2_bytes: int, factor: float = 2.0) -> int:
-    """How many distinct input sets to rotate so that each launch misses L2."""
+def l2_rotation_count(bytes_per_set: int, l2_bytes: int, factor: float = 4.0) -> int:
+    """How many distinct input sets to rotate so that each launch misses L2:
+    enough that a set is read again only after `factor` x L2 bytes of other
+    sets (at 2 x L2, ncu still counted 10-30 % of a 117 MB weight set as L2
+    hits on the next pass)."""
     if bytes_per_set <= 0:
         return 1
     n = 1
