@@ -566,9 +566,9 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
     }
     tc_fence_before();
     __syncthreads();
-    // A pair's barriers must be initialised before the peer's TMA or MMA
-    // commits can reach them.
-    if constexpr (C::kPair) cluster_sync();
+    // A pair's barriers must be initialised, and both CTAs' TMEM allocated,
+    // before the peer's TMA, MMA or commits can reach them.
+    if constexpr (C::kPair) cluster_sync_after_init();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
@@ -806,9 +806,11 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 }
             } else {
             const int chunks = (C::kVarCols ? ui.cols : C::BN) / C::kEpiCols;
-#pragma unroll 1
-            for (int c = 0; c < chunks; ++c, ++box) {
-                uint32_t v[C::kEpiCols];
+            // Box c's accumulator columns are read from TMEM one box ahead:
+            // the read of box c + 1 is issued once box c's registers are in
+            // shared memory, so it runs under box c's barrier and store.
+            uint32_t v[C::kEpiCols];
+            auto load_box = [&](int c) {
                 if constexpr (C::kEpiCols == 16) {
                     tmem_ld_32x32b_x16(t_row + c * C::kEpiCols,
                                        *reinterpret_cast<uint32_t(*)[16]>(&v[0]));
@@ -818,6 +820,10 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                         tmem_ld_32x32b_x32(t_row + c * C::kEpiCols + 32 * h,
                                            *reinterpret_cast<uint32_t(*)[32]>(&v[32 * h]));
                 }
+            };
+            load_box(0);
+#pragma unroll 1
+            for (int c = 0; c < chunks; ++c, ++box) {
                 tmem_ld_wait();
                 if (c == chunks - 1) release_acc();
                 const uint32_t buf = sbase + C::kOffD + (box & 1u) * C::kEpiBufBytes;
@@ -844,6 +850,7 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                     }
                 }
                 fence_proxy_async_smem();
+                if (c + 1 < chunks) load_box(c + 1);
                 named_bar_sync(1, C::kEpiThreads);
                 if (store_thread) {
                     const int32_t x = n0 + c * C::kEpiCols;

@@ -395,6 +395,17 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Cluster barrier whose arrive carries no release: for the set-up barrier of
+// a CTA pair, where the only writes the peer must see are mbarrier
+// initialisations already released to the cluster by fence.mbarrier_init,
+// and the TMEM allocation, ordered by the tcgen05 fences around it.  (An
+// arrive with release waits for the thread's outstanding memory operations;
+// on GB300 that cost the pair set-up about 1.3 us.)
+__device__ __forceinline__ void cluster_sync_after_init() {
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Four floats from shared memory at a shared::cluster address (any CTA of
 // the cluster); 16-byte aligned.
 __device__ __forceinline__ void ld_shared_cluster_v4(uint32_t cluster_addr, float (&v)[4]) {
