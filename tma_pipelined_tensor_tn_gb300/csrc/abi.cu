@@ -227,13 +227,14 @@ int run_gemm(const GemmPlan& plan, DeviceState* d, int64_t M, int64_t N, int64_t
     if (int s = encode_2d(&tmB, B, K, N, plan.bk, plan.b_box_rows, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, plan.bf16))
         return s;
+    // Store boxes: 32 rows (each epilogue warp stores its own rows) by one
+    // swizzle span: 64 columns (128 B) or 32 columns (64 B) of fp16, 32 of fp32.
     if (plan.out_f32) {
-        if (int s = encode_ws_3d(&tmD, workspace, N, M, plan.splits, plan.bm)) return s;
+        if (int s = encode_ws_3d(&tmD, workspace, N, M, plan.splits, kEpiWarpRows)) return s;
     } else {
-        // Store boxes are one swizzle span wide: 64 columns (128 B) or 32 columns (64 B).
         const CUtensorMapSwizzle dswz =
             plan.epi_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-        if (int s = encode_2d(&tmD, D, N, M, plan.epi_cols, plan.bm, dswz,
+        if (int s = encode_2d(&tmD, D, N, M, plan.epi_cols, kEpiWarpRows, dswz,
                               CU_TENSOR_MAP_L2_PROMOTION_NONE, plan.bf16))
             return s;
     }
@@ -528,7 +529,7 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
             const int64_t mg = m_offsets[i + 1] - m_offsets[i];
             if (mg == 0) continue;   // an empty group has no tiles and no map
             const void* base = static_cast<const uint16_t*>(D) + m_offsets[i] * N;
-            if (int s = encode_2d(&g.tmD[i], base, N, mg, epi_cols, 128, dswz,
+            if (int s = encode_2d(&g.tmD[i], base, N, mg, epi_cols, kEpiWarpRows, dswz,
                                   CU_TENSOR_MAP_L2_PROMOTION_NONE))
                 return s;
         }
@@ -583,7 +584,8 @@ int gemm_f16_small_m(int64_t M, int64_t N, int64_t K, const void* X, const void*
     if (int s = encode_2d(&tmX, X, K, M, p.bk, p.bn, CU_TENSOR_MAP_SWIZZLE_128B,
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
         return s;
-    if (int s = encode_ws_3d(&tmP, workspace, p.bn, N, p.splits, p.bm, p.epi_cols)) return s;
+    if (int s = encode_ws_3d(&tmP, workspace, p.bn, N, p.splits, kEpiWarpRows, p.epi_cols))
+        return s;
     GemmArgs args;
     args.M = static_cast<int32_t>(N);
     args.N = static_cast<int32_t>(p.bn);

@@ -299,11 +299,12 @@ struct DenseProblem {
         tma_load_2d_pair(dst, ui.narrow ? &tmBn : &tmB, k, ui.b_row + row_off, bar_cluster);
     }
     template <bool kOutF32>
-    __device__ __forceinline__ void store(uint32_t buf, int32_t x, const UnitInfo& ui) const {
+    __device__ __forceinline__ void store(uint32_t buf, int32_t x, int32_t y,
+                                          const UnitInfo& ui) const {
         if constexpr (kOutF32)
-            tma_store_3d(&tmD, buf, x, ui.store_y, ui.store_z);
+            tma_store_3d(&tmD, buf, x, y, ui.store_z);
         else
-            tma_store_2d(&tmD, buf, x, ui.store_y);
+            tma_store_2d(&tmD, buf, x, y);
     }
 };
 
@@ -376,8 +377,9 @@ struct GroupedProblem {
         tma_load_3d_pair(dst, &tmB, k, ui.b_row + row_off, ui.store_z, bar_cluster);
     }
     template <bool kOutF32>
-    __device__ __forceinline__ void store(uint32_t buf, int32_t x, const UnitInfo& ui) const {
-        tma_store_2d(&tmD[ui.store_z], buf, x, ui.store_y);
+    __device__ __forceinline__ void store(uint32_t buf, int32_t x, int32_t y,
+                                          const UnitInfo& ui) const {
+        tma_store_2d(&tmD[ui.store_z], buf, x, y);
     }
 };
 
@@ -736,7 +738,7 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
         // ================= epilogue (warps 2..5) =================
         const uint32_t quarter = static_cast<uint32_t>(warp) & 3u;   // TMEM lane quarter
         const uint32_t row = quarter * 32u + static_cast<uint32_t>(lane);  // row in tile
-        const bool store_thread = threadIdx.x == 64;   // issues the TMA stores
+        const bool store_thread = threadIdx.x == 64;   // the transposed form's store thread
         uint32_t tcount = 0, box = 0;
         for (int32_t u = unit0; u < prob.num_units(); u += unit_step, ++tcount) {
             UnitInfo ui = prob.unit(u, C::kTileM, C::BN, C::kGroupM);
@@ -826,15 +828,20 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
             for (int c = 0; c < chunks; ++c, ++box) {
                 tmem_ld_wait();
                 if (c == chunks - 1) release_acc();
-                const uint32_t buf = sbase + C::kOffD + (box & 1u) * C::kEpiBufBytes;
-                // The store that last read this buffer (two boxes ago) must be done.
-                if (store_thread) bulk_wait_group_read<1>();
-                named_bar_sync(1, C::kEpiThreads);
-                // Row `row` of the box holds kEpiChunks 16-byte chunks.  The
+                // Each epilogue warp stages and stores its own 32 rows: a
+                // 32-row slice of the box buffer (whole 1024-byte swizzle
+                // atoms) and one TMA store of 32 rows issued by its lane 0,
+                // so the warps synchronise with nothing but themselves.
+                const uint32_t buf = sbase + C::kOffD + (box & 1u) * C::kEpiBufBytes +
+                                     quarter * 32u * C::kEpiRowBytes;
+                // The store that last read this slice (two boxes ago) must be done.
+                if (lane == 0) bulk_wait_group_read<1>();
+                __syncwarp();
+                // Row `lane` of the slice holds kEpiChunks 16-byte chunks.  The
                 // TMA swizzle whose span equals the row width (64B or 128B)
                 // XORs the chunk index with address bits 7.. of the row start:
                 // chunk j of row r lands at j ^ ((r * row_bytes / 128) % chunks).
-                const uint32_t row_addr = buf + row * C::kEpiRowBytes;
+                const uint32_t row_addr = buf + static_cast<uint32_t>(lane) * C::kEpiRowBytes;
                 const uint32_t xr = ((row * C::kEpiRowBytes) >> 7) & (C::kEpiChunks - 1);
 #pragma unroll
                 for (uint32_t j = 0; j < C::kEpiChunks; ++j) {
@@ -851,19 +858,20 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 }
                 fence_proxy_async_smem();
                 if (c + 1 < chunks) load_box(c + 1);
-                named_bar_sync(1, C::kEpiThreads);
-                if (store_thread) {
+                __syncwarp();
+                if (lane == 0) {
                     const int32_t x = n0 + c * C::kEpiCols;
-                    if (x < ui.n_limit && ui.store_y < ui.m_limit &&
-                        check_ok((x & 7) == 0 && x >= 0 && ui.store_y >= 0, err, kSiteCheckTma))
-                        prob.template store<C::kOutF32>(buf, x, ui);
+                    const int32_t y = ui.store_y + static_cast<int32_t>(quarter) * 32;
+                    if (x < ui.n_limit && y < ui.m_limit &&
+                        check_ok((x & 7) == 0 && x >= 0 && y >= 0, err, kSiteCheckTma))
+                        prob.template store<C::kOutF32>(buf, x, y, ui);
                     bulk_commit_group();
                 }
             }
             }   // not transposed
             if (store_thread && rank == 0) check_count_unit(err, u);
         }
-        if (store_thread) bulk_wait_group<0>();
+        if (lane == 0) bulk_wait_group<0>();   // every lane 0 that issued stores
     }
 
     if constexpr (C::kClusterK != 0) {

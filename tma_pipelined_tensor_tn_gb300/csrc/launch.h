@@ -34,6 +34,10 @@ Tuning process_tuning();
 // is redone after cudaDeviceReset replaces the device's context.
 uint64_t current_context_id();
 
+// Rows of a D store box: each of the four epilogue warps stores its own 32
+// rows of a tile.
+constexpr int kEpiWarpRows = 32;
+
 // GEMM tile configuration used by the persistent tcgen05 kernel.
 struct GemmPlan {
     int bm, bn, bk, stages;
@@ -100,8 +104,8 @@ struct GemmArgs {
 };
 
 // Enqueue the GEMM kernel.  Tensor maps: A {K, M} box {bk, bm}; B {K, N} box
-// {bk, bn}; D {N, M} box {epi_cols, bm} (fp16), or for split-K the FP32
-// workspace {N, M, splits} box {32, bm, 1}.
+// {bk, bn}; D {N, M} box {epi_cols, 32} (fp16), or for split-K the FP32
+// workspace {N, M, splits} box {32, 32, 1}.
 cudaError_t launch_gemm_tn(const GemmPlan& plan, const CUtensorMap& tmA, const CUtensorMap& tmB,
                            const CUtensorMap& tmD, const GemmArgs& args, cudaStream_t stream);
 
@@ -138,7 +142,7 @@ cudaError_t launch_small_m_lsu(const CUtensorMap& tmX, int64_t M, int64_t N, int
 // Grouped GEMM: groups g < G with rows [m_offsets[g], m_offsets[g+1]) of A
 // and D and weights B[g] (N x K).  Maps: A {K, rows} box {64, 128}; B
 // {K, N, G} box {64, bn, 1}; tmD[g] = D rows of group g, {N, M_g} box
-// {epi_cols(bn), 128} (unused for empty groups).
+// {epi_cols(bn), 32} (unused for empty groups).
 constexpr int kMaxGroupsHost = 64;
 struct GroupedLaunch {
     CUtensorMap tmA, tmB;
