@@ -134,6 +134,22 @@ def test_grouped_transposed_tiny_groups_integer_bitexact(tg, formulation):
                     f"grouped integer {formulation}")
 
 
+def test_grouped_every_block_width_integer_bitexact(tg, formulation):
+    """Groups of 1..15 whole 16-row steps (each a single block of that width
+    in the transposed form, which loads exactly a block's rows of A through
+    the map for its width) and a 500-row group cut into blocks of two widths:
+    integer inputs match the oracle bit for bit in every formulation."""
+    counts = [16 * j - (j % 5) for j in range(1, 16)] + [500]
+    offs = [0]
+    for c in counts:
+        offs.append(offs[-1] + c)
+    G, N, K = len(counts), 264, 192
+    A = inputs.integer_f16((offs[-1], K), seed=94)
+    B = inputs.integer_f16((G, N, K), seed=95)
+    assert_bitexact(run(tg, A, B, offs), oracle.gemm_f16_grouped(A.numpy(), B.numpy(), offs),
+                    f"grouped widths {formulation}")
+
+
 def test_grouped_transposed_writes_only_group_rows(tg):
     """Transposed stores clip at each group's last row and at N: rows of D
     past the groups keep their contents, and every group row is written."""

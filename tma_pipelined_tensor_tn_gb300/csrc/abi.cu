@@ -498,13 +498,29 @@ int gemm_f16_grouped(int64_t G, const int64_t* m_offsets, int64_t N, int64_t K, 
             return TMAGEMM_ERR_CUDA;
     }
     if (g.transposed) {
-        // A's rows are the narrow operand: a box of bn / (CTAs per tile) rows
-        // (each CTA of a pair loads its half of a block); the weights are "A".
-        const CUtensorMap weights = g.tmB;
-        if (int s = encode_2d(&g.tmB, A, K, rows, 64, g.pair ? g.bn / 2 : g.bn,
-                              CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
-            return s;
-        g.tmA = weights;
+        // A's rows are the narrow operand, the weights "A".  A block of w rows
+        // loads exactly its rows (w / 2 per CTA of a pair): one map per block
+        // width in use, box {64, w / CTAs per tile}.  A group of `steps`
+        // 16-row steps has blocks of q and (if the division leaves a
+        // remainder) q + 1 steps.
+        g.tmA = g.tmB;
+        g.x_used = 0;
+        const int64_t maxw16 = g.maxw / 16;
+        for (int64_t i = 0; i < G; ++i) {
+            const int64_t steps = (m_offsets[i + 1] - m_offsets[i] + 15) / 16;
+            if (steps == 0) continue;
+            const int64_t tb = (steps + maxw16 - 1) / maxw16;
+            const int64_t q = steps / tb;
+            g.x_used |= 1u << (q - 1);
+            if (steps % tb != 0) g.x_used |= 1u << q;
+        }
+        for (int j = 0; j < 16; ++j) {
+            if (!(g.x_used & (1u << j))) continue;
+            const int64_t box_rows = 16 * (j + 1) / (g.pair ? 2 : 1);
+            if (int s = encode_2d(&g.tmXw[j], A, K, rows, 64, box_rows, CU_TENSOR_MAP_SWIZZLE_128B,
+                                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B))
+                return s;
+        }
         // D as one map (64 rows x 128 columns per store, inside a group) and
         // per group (16 x 128, clipped at the group's last row); unswizzled.
         if (int s = encode_2d(&g.tmD64, D, N, rows, 128, 64, CU_TENSOR_MAP_SWIZZLE_NONE,

@@ -237,8 +237,10 @@ struct DenseProblem {
     void* d_out;   // D itself (M x N, row-major), for the cluster-split epilogue
 
     __device__ __forceinline__ int32_t num_units() const { return w.num_units; }
-    __device__ __forceinline__ uint32_t narrow_b_bytes() const {
-        return static_cast<uint32_t>(w.narrow_b_bytes);
+    // Bytes one stage's B box brings for this unit (per CTA); `full` for a whole box.
+    __device__ __forceinline__ uint32_t b_box_bytes(const UnitInfo& ui, int,
+                                                    uint32_t full) const {
+        return ui.narrow ? static_cast<uint32_t>(w.narrow_b_bytes) : full;
     }
     // Bytes one stage's A box brings (the rest of the A stage is not written).
     __device__ __forceinline__ uint32_t a_box_bytes(int BK) const {
@@ -327,7 +329,9 @@ struct GroupedProblem {
     int32_t groups, grid_n, N, k_blocks;
 
     __device__ __forceinline__ int32_t num_units() const { return tile_start[groups]; }
-    __device__ __forceinline__ uint32_t narrow_b_bytes() const { return 0; }   // no narrow units
+    __device__ __forceinline__ uint32_t b_box_bytes(const UnitInfo&, int, uint32_t full) const {
+        return full;   // no narrow units
+    }
     __device__ __forceinline__ uint32_t a_box_bytes(int BK) const {
         return 128u * static_cast<uint32_t>(BK) * 2u;
     }
@@ -392,33 +396,45 @@ struct GroupedProblem {
 // over all of D where those rows lie inside the group, else 16 rows at a
 // time through the group's own map, which clips at the group's last row.  A group's rows are cut into
 // tb_count(g) blocks of nearly equal width (multiples of 16, at most maxw16 *
-// 16): no block is padded by more than 15 rows.  Units run group by group,
+// 16): no block is padded by more than 15 rows.  A block of w rows loads
+// only those rows of A (w / CTAs per tile per CTA), through the map for its
+// width: below 256 the loads, not the MMAs, set a unit's time, so a box of
+// the full 256 (128 per CTA) rows would cost a narrow block as much as a
+// wide one.  Units run group by group,
 // and within a group a block of rows against every weight block in turn, so
 // a group's weights and rows are reused from L2 while the group runs.
 struct GroupedTProblem {
     static constexpr bool kTransposed = true;
     CUtensorMap tmW;                      // B as {K, N, G}, box {64, 128, 1}
-    CUtensorMap tmX;                      // A as {K, rows}, box {64, BN / CTAs per tile}
+    CUtensorMap tmX[16];                  // A as {K, rows}, box {64, 16 (j + 1) / x_ctas}
     CUtensorMap tmD[kMaxGroups];          // D rows of group g as {N, M_g}, box {128, 16}
     CUtensorMap tmD64;                    // all of D as {N, rows}, box {128, 64}
     int32_t tile_start[kMaxGroups + 1];   // prefix sums of the groups' unit counts
     int32_t m_off[kMaxGroups + 1];        // row offsets; m_off[groups] = all rows
     int32_t groups, n_blocks, N, k_blocks, maxw16;
+    int32_t x_ctas;                       // CTAs per tile (2 for a pair): A rows per CTA = w / x_ctas
+    uint32_t x_used;                      // bit j: tmX[j] (blocks of 16 (j + 1) rows) is encoded
 
     __device__ __forceinline__ int32_t num_units() const { return tile_start[groups]; }
-    __device__ __forceinline__ uint32_t narrow_b_bytes() const { return 0; }   // one B box
+    // The map of A for this unit's block width (a multiple of 16, at most 256).
+    __device__ __forceinline__ const CUtensorMap* x_map(const UnitInfo& ui) const {
+        return &tmX[ui.cols / 16 - 1];
+    }
+    __device__ __forceinline__ uint32_t b_box_bytes(const UnitInfo& ui, int BK, uint32_t) const {
+        return static_cast<uint32_t>(ui.cols / x_ctas) * static_cast<uint32_t>(BK) * 2u;
+    }
     __device__ __forceinline__ uint32_t a_box_bytes(int BK) const {
         return 128u * static_cast<uint32_t>(BK) * 2u;
     }
     __device__ __forceinline__ void prefetch() const {
         tma_prefetch_desc(&tmW);
-        tma_prefetch_desc(&tmX);
+        for (uint32_t m = x_used; m != 0; m &= m - 1) tma_prefetch_desc(&tmX[__ffs(m) - 1]);
         tma_prefetch_desc(&tmD64);
     }
     __device__ __forceinline__ void prefetch_l2(int32_t k, const UnitInfo& ui, int32_t row_a,
                                                 int32_t row_b) const {
         tma_prefetch_l2_3d(&tmW, k, ui.a_row + row_a, ui.store_z);
-        tma_prefetch_l2_2d(&tmX, k, ui.b_row + row_b);
+        tma_prefetch_l2_2d(x_map(ui), k, ui.b_row + row_b);
     }
     __device__ __forceinline__ UnitInfo unit(int32_t u, int BM, int, int) const {
         int32_t g = 0;
@@ -450,7 +466,7 @@ struct GroupedTProblem {
     }
     __device__ __forceinline__ void load_b(uint32_t dst, int32_t k, const UnitInfo& ui,
                                            uint32_t bar) const {
-        tma_load_2d(dst, &tmX, k, ui.b_row, bar);
+        tma_load_2d(dst, x_map(ui), k, ui.b_row, bar);
     }
     __device__ __forceinline__ void load_a_pair(uint32_t dst, int32_t k, const UnitInfo& ui,
                                                 int32_t row_off, uint32_t bar_cluster) const {
@@ -458,7 +474,7 @@ struct GroupedTProblem {
     }
     __device__ __forceinline__ void load_b_pair(uint32_t dst, int32_t k, const UnitInfo& ui,
                                                 int32_t row_off, uint32_t bar_cluster) const {
-        tma_load_2d_pair(dst, &tmX, k, ui.b_row + row_off, bar_cluster);
+        tma_load_2d_pair(dst, x_map(ui), k, ui.b_row + row_off, bar_cluster);
     }
     // A 16-row x 128-column box of D: rows y.. of group z, columns x...
     __device__ __forceinline__ void store_t16(uint32_t buf, int32_t x, int32_t y,
@@ -582,8 +598,8 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
             for (int32_t u = unit0; ok && u < prob.num_units(); u += unit_step) {
                 const UnitInfo ui = prob.unit(u, C::kTileM, C::BN, C::kGroupM);
                 // A pair's B rows: this CTA's half of the unit's columns.
-                const bool narrow = C::kVarCols && ui.narrow != 0;
-                const uint32_t b_bytes = narrow ? prob.narrow_b_bytes() : C::kBBytes;
+                const uint32_t b_bytes =
+                    C::kVarCols ? prob.b_box_bytes(ui, C::BK, C::kBBytes) : C::kBBytes;
                 const int32_t b_off = static_cast<int32_t>(rank) * (ui.cols / 2);
                 for (int32_t kb = ui.kb0; kb < ui.kb1; ++kb) {
                     const uint32_t s = ring_stage(it, C::STAGES);
@@ -712,15 +728,26 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
             tc_fence_after();
             const uint32_t t_row = tmem_base + ((quarter * 32u) << 16);
             const uint32_t p_row = sbase + C::kOffA + row * C::kPartStride * 4u;
+            // Up to four 32-column loads in flight per wait: the copy sits
+            // between the last MMA and the cluster's reduction.
+            constexpr int kLoads = C::BN / 32;
+            constexpr int kBatch = kLoads < 4 ? kLoads : 4;
 #pragma unroll 1
-            for (int c = 0; c < C::BN / 32; ++c) {
-                uint32_t v[32];
-                tmem_ld_32x32b_x32(t_row + 32 * c, v);
+            for (int c0 = 0; c0 < kLoads; c0 += kBatch) {
+                uint32_t v[kBatch][32];
+#pragma unroll
+                for (int b = 0; b < kBatch; ++b)
+                    if (c0 + b < kLoads) tmem_ld_32x32b_x32(t_row + 32 * (c0 + b), v[b]);
                 tmem_ld_wait();
 #pragma unroll
-                for (int j = 0; j < 8; ++j)
-                    st_shared_v4(p_row + (32u * c + 4u * j) * 4u, v[4 * j], v[4 * j + 1],
-                                 v[4 * j + 2], v[4 * j + 3]);
+                for (int b = 0; b < kBatch; ++b) {
+                    if (c0 + b >= kLoads) break;
+                    const uint32_t c = static_cast<uint32_t>(c0 + b);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j)
+                        st_shared_v4(p_row + (32u * c + 4u * j) * 4u, v[b][4 * j],
+                                     v[b][4 * j + 1], v[b][4 * j + 2], v[b][4 * j + 3]);
+                }
             }
             if constexpr (C::BN % 32 != 0) {
                 // The last 16 columns of a tile whose width is an odd multiple of 16.
@@ -885,6 +912,14 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
         // per thread have their loads in flight at once.
         tc_fence_before();
         cluster_sync();
+        // The accumulator is in shared memory now: a single CTA gives its
+        // TMEM back before the reduction rather than at exit.
+        if constexpr (!C::kPair) {
+            if (warp == 1) {
+                tc_fence_after();
+                tmem_dealloc(tmem_base, C::kTmemCols);
+            }
+        }
         constexpr int kGroups = C::BN / 8;
         constexpr int kItems = C::kClusterK <= 4 ? 2 : 1;
         constexpr uint32_t kPeerStride = C::kPair ? 2u : 1u;
@@ -940,7 +975,11 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
             }
         }
         if (threadIdx.x == 0 && rank == 0 && !*abort_flag) check_count_unit(err, unit0);
-        cluster_sync();   // peers' shared memory stays alive until every CTA has read it
+        // This CTA has read its peers' partials (the loads above returned
+        // before their sums were stored): arrive now; the matching wait, just
+        // before exit, keeps every CTA's shared memory alive until all have
+        // read it, and the stores and teardown run meanwhile.
+        cluster_arrive_release();
     }
 
     // ---- teardown ----
@@ -951,9 +990,13 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
             check_ok(ring_count[0] == ring_count[1], err, kSiteCheckRing);
     }
     // A pair stays alive until both CTAs are done with each other's shared
-    // memory and barriers.
-    if constexpr (C::kPair) cluster_sync();
-    if (warp == 1) {
+    // memory and barriers (with a cluster split, the wait that completes the
+    // barrier arrived at after the reduction).
+    if constexpr (C::kClusterK != 0)
+        cluster_wait_acquire();
+    else if constexpr (C::kPair)
+        cluster_sync();
+    if (warp == 1 && (C::kPair || C::kClusterK == 0)) {
         tc_fence_after();
         if constexpr (C::kPair)
             tmem_dealloc_pair(tmem_base, C::kTmemCols);
@@ -1228,7 +1271,9 @@ cudaError_t launch_grouped_t_cfg(const GroupedLaunch& g, int num_sms, int num_pa
     if (g.maxw < 16 || g.maxw > C::BN || g.maxw % 16 != 0) return cudaErrorInvalidValue;
     GroupedTProblem prob;
     prob.tmW = g.tmA;
-    prob.tmX = g.tmB;
+    for (int j = 0; j < 16; ++j) prob.tmX[j] = g.tmXw[j];
+    prob.x_used = g.x_used;
+    prob.x_ctas = C::kPair ? 2 : 1;
     prob.tmD64 = g.tmD64;
     prob.groups = static_cast<int32_t>(g.groups);
     prob.n_blocks = static_cast<int32_t>(ceil_div(g.N, C::kTileM));
@@ -1242,7 +1287,14 @@ cudaError_t launch_grouped_t_cfg(const GroupedLaunch& g, int num_sms, int num_pa
         if (i < g.groups) {
             prob.tmD[i] = g.tmD[i];
             const int64_t steps = ceil_div(g.m_offsets[i + 1] - g.m_offsets[i], 16);
-            t += static_cast<int32_t>(ceil_div(steps, prob.maxw16) * prob.n_blocks);
+            const int64_t tb = ceil_div(steps, prob.maxw16);
+            t += static_cast<int32_t>(tb * prob.n_blocks);
+            // Every block width of the group (q or q + 1 steps) has its map.
+            if (steps > 0) {
+                const int64_t q = steps / tb;
+                const uint32_t need = (1u << (q - 1)) | (steps % tb != 0 ? 1u << q : 0u);
+                if ((g.x_used & need) != need) return cudaErrorInvalidValue;
+            }
         }
     }
     if (t == 0) return cudaSuccess;   // every group is empty
@@ -1291,9 +1343,13 @@ namespace {
 
 // Largest per-slot load of the transposed grouped schedule (units in the
 // order GroupedTProblem numbers them, slot = unit mod slots): the sum over a
-// slot's units of (block width + c).
+// slot's units of (cost of a block of width w + c), in the row-tiled plan's
+// unit (one column of a 256-row pair tile per k-block).  A k-block of a block
+// costs the larger of its MMA (w) and its loads: 128 weight rows and w / 2
+// rows of A per CTA of a pair (w for a single CTA), where 256 rows' bytes
+// take as long as a 256-column MMA.
 int64_t grouped_t_max_load(const int64_t* m_offsets, int64_t groups, int64_t n_blocks,
-                           int64_t maxw, int64_t c, int64_t slots) {
+                           int64_t maxw, int64_t c, int64_t slots, bool pair) {
     int64_t loads[1024] = {};
     if (slots > 1024) return -1;
     int64_t u = 0;
@@ -1302,9 +1358,11 @@ int64_t grouped_t_max_load(const int64_t* m_offsets, int64_t groups, int64_t n_b
         if (steps == 0) continue;
         const int64_t tb_count = ceil_div(steps, maxw / 16);
         const int64_t q = steps / tb_count, extra = steps % tb_count;
-        for (int64_t tb = 0; tb < tb_count; ++tb)
-            for (int64_t nb = 0; nb < n_blocks; ++nb, ++u)
-                loads[u % slots] += 16 * (q + (tb < extra ? 1 : 0)) + c;
+        for (int64_t tb = 0; tb < tb_count; ++tb) {
+            const int64_t w = 16 * (q + (tb < extra ? 1 : 0));
+            const int64_t cost = pair ? std::max(w, 128 + w / 2) : 128 + w;
+            for (int64_t nb = 0; nb < n_blocks; ++nb, ++u) loads[u % slots] += cost + c;
+        }
     }
     int64_t worst = 0;
     for (int64_t s = 0; s < slots; ++s) worst = std::max(worst, loads[s]);
@@ -1343,7 +1401,7 @@ void plan_grouped(const int64_t* m_offsets, int64_t groups, int64_t N, int num_s
         const int64_t slots = use_pair ? num_pairs : (num_sms > 0 ? num_sms : 1);
         for (int64_t maxw = 256; maxw >= 128; maxw -= 16) {
             const int64_t load = grouped_t_max_load(m_offsets, groups, ceil_div(N, tile_m), maxw,
-                                                    use_pair ? 16 : 32, slots);
+                                                    use_pair ? 16 : 32, slots, use_pair != 0);
             if (load < 0) continue;
             if (best < 0 || load < best) {
                 best = load;

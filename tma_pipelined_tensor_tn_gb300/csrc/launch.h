@@ -152,12 +152,16 @@ struct GroupedLaunch {
     int bn;
     bool pair;                  // CTA-pair tiles (256 rows; B box bn / 2 rows)
     // Transposed (D_g^T = B_g A_g^T): tmA = B {K, N, G} box {64, 128, 1},
-    // tmB = A {K, rows} box {64, bn / CTAs per tile}, tmD[g] = D rows of group
+    // tmXw (below) = A by block width, tmD[g] = D rows of group
     // g {N, M_g} box {128, 16} unswizzled (and tmD64); a group's rows in
     // blocks of at most maxw (a multiple of 16 up to bn).
     bool transposed;
     int maxw;
     CUtensorMap tmD64;          // transposed: all of D {N, rows} box {128, 64} unswizzled
+    // Transposed: A {K, rows} once per block width 16 (j + 1) in use (bit j of
+    // x_used), box {64, 16 (j + 1) / CTAs per tile}; tmB is then unused.
+    CUtensorMap tmXw[16];
+    uint32_t x_used;
 };
 // The grouped GEMM's formulation and tiles for these groups: the row-tiled
 // form (tiles of 128 or 256 rows of a group by bn columns) or the transposed

@@ -395,6 +395,15 @@ __device__ __forceinline__ void cluster_sync() {
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// The two halves of cluster_sync, for work placed between them.  Every
+// thread of the cluster arrives once and then waits once.
+__device__ __forceinline__ void cluster_arrive_release() {
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Cluster barrier whose arrive carries no release: for the set-up barrier of
 // a CTA pair, where the only writes the peer must see are mbarrier
 // initialisations already released to the cluster by fence.mbarrier_init,
