@@ -570,9 +570,10 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
         }
         __syncwarp();
     }
-    // A, B and D (and the previous grid's TMEM) are only touched once the
-    // grid before this one on the stream has completed.
-    grid_dependency_wait();
+    // TMEM is this CTA's own: allocating it before the previous grid has
+    // completed is safe (a CTA of that grid still on this SM only delays the
+    // allocation until it frees its columns; it never waits on this grid), so
+    // the whole set-up runs under the previous grid's tail.
     if (warp == 1) {
         if constexpr (C::kPair) {
             tmem_alloc_pair(smem_u32(tmem_holder), C::kTmemCols);
@@ -589,6 +590,9 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
     if constexpr (C::kPair) cluster_sync_after_init();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
+    // A, B and D are only touched once the grid before this one on the
+    // stream has completed.
+    grid_dependency_wait();
 
     if (warp == 0) {
         // ================= TMA producer =================
@@ -903,13 +907,15 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
 
     if constexpr (C::kClusterK != 0) {
         // Every CTA's partial tile is complete and visible cluster-wide.  The
-        // outputs of the tile that exist (rows below M, 8-column groups left of
+        // outputs of the tile that exist (rows below M, 4-column groups left of
         // N) are dealt out evenly over the CK CTAs (a pair's halves reduce
         // separately: CTA (pair p, half h) adds the partials of ranks 2q + h),
         // so with a few rows every CTA of the cluster still takes a share.
-        // Each 8-column group: the CK partials loaded together and added in
-        // slice order (deterministic), one 16-byte store of D; kItems groups
-        // per thread have their loads in flight at once.
+        // Each 4-column group: the CK partials loaded together (consecutive
+        // threads read consecutive 16 bytes of a peer's partial row, whole
+        // 128-byte lines per quarter warp) and added in slice order
+        // (deterministic), one 8-byte store of D; kItems groups per thread
+        // have their loads in flight at once.
         tc_fence_before();
         cluster_sync();
         // The accumulator is in shared memory now: a single CTA gives its
@@ -920,32 +926,31 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 tmem_dealloc(tmem_base, C::kTmemCols);
             }
         }
-        constexpr int kGroups = C::BN / 8;
-        constexpr int kItems = C::kClusterK <= 4 ? 2 : 1;
+        constexpr int kGroups = C::BN / 4;
+        constexpr int kItems = C::kClusterK <= 4 ? 4 : 2;
         constexpr uint32_t kPeerStride = C::kPair ? 2u : 1u;
         const UnitInfo ui = prob.unit(unit0, C::kTileM, C::BN, C::kGroupM);
         uint16_t* dout = static_cast<uint16_t*>(prob.d_out);
         const int32_t m0 = ui.a_row + static_cast<int32_t>(rank) * C::BM;
         const int rows = max(0, min(C::BM, prob.w.M - m0));
         // (N is a multiple of 8, so a group is either whole or outside.)
-        const int groups = max(0, min(kGroups, (prob.w.N - ui.b_row + 7) / 8));
+        const int groups = max(0, min(kGroups, (prob.w.N - ui.b_row + 3) / 4));
         const int total = rows * groups;
         const int f_begin = static_cast<int>(ck_rank) * total / C::kClusterK;
         const int f_end = (static_cast<int>(ck_rank) + 1) * total / C::kClusterK;
         for (int f0 = f_begin + static_cast<int>(threadIdx.x); f0 < f_end;
              f0 += kItems * C::kThreads) {
-            float lo[kItems][C::kClusterK][4], hi[kItems][C::kClusterK][4];
+            float part[kItems][C::kClusterK][4];
 #pragma unroll
             for (int it = 0; it < kItems; ++it) {
                 const int f = f0 + it * C::kThreads;
                 if (f >= f_end) break;
                 const int rl = f / groups, g = f % groups;
-                const uint32_t local = sbase + C::kOffA + (rl * C::kPartStride + 8u * g) * 4u;
+                const uint32_t local = sbase + C::kOffA + (rl * C::kPartStride + 4u * g) * 4u;
 #pragma unroll
                 for (int q = 0; q < C::kClusterK; ++q) {
                     const uint32_t peer = kPeerStride * static_cast<uint32_t>(q) + rank;
-                    ld_shared_cluster_v4(map_to_rank(local, peer), lo[it][q]);
-                    ld_shared_cluster_v4(map_to_rank(local + 16u, peer), hi[it][q]);
+                    ld_shared_cluster_v4(map_to_rank(local, peer), part[it][q]);
                 }
             }
 #pragma unroll
@@ -953,25 +958,19 @@ gemm_tn_f16_kernel(const __grid_constant__ P prob, const uint64_t limit_ns,
                 const int f = f0 + it * C::kThreads;
                 if (f >= f_end) break;
                 const int rl = f / groups, g = f % groups;
-                float a[8] = {lo[it][0][0], lo[it][0][1], lo[it][0][2], lo[it][0][3],
-                              hi[it][0][0], hi[it][0][1], hi[it][0][2], hi[it][0][3]};
+                float a[4] = {part[it][0][0], part[it][0][1], part[it][0][2], part[it][0][3]};
 #pragma unroll
                 for (int q = 1; q < C::kClusterK; ++q) {
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        a[e] += lo[it][q][e];
-                        a[4 + e] += hi[it][q][e];
-                    }
+                    for (int e = 0; e < 4; ++e) a[e] += part[it][q][e];
                 }
-                uint4 o;
+                uint2 o;
                 o.x = pack2_rn<C::kBF16>(__float_as_uint(a[0]), __float_as_uint(a[1]));
                 o.y = pack2_rn<C::kBF16>(__float_as_uint(a[2]), __float_as_uint(a[3]));
-                o.z = pack2_rn<C::kBF16>(__float_as_uint(a[4]), __float_as_uint(a[5]));
-                o.w = pack2_rn<C::kBF16>(__float_as_uint(a[6]), __float_as_uint(a[7]));
-                const int32_t m = m0 + rl, n = ui.b_row + 8 * g;
-                if (check_ok(rl < C::BM && g < kGroups && m < prob.w.M && n + 8 <= prob.w.N, err,
+                const int32_t m = m0 + rl, n = ui.b_row + 4 * g;
+                if (check_ok(rl < C::BM && g < kGroups && m < prob.w.M && n + 4 <= prob.w.N, err,
                              kSiteCheckBounds))
-                    *reinterpret_cast<uint4*>(dout + static_cast<int64_t>(m) * prob.w.N + n) = o;
+                    *reinterpret_cast<uint2*>(dout + static_cast<int64_t>(m) * prob.w.N + n) = o;
             }
         }
         if (threadIdx.x == 0 && rank == 0 && !*abort_flag) check_count_unit(err, unit0);
