@@ -55,10 +55,23 @@ def test_gemv_unit_vector(tg):
 
 
 @pytest.mark.parametrize("N,K", [(1, 8), (3, 72), (4097, 256), (100, 264), (513, 1000),
-                                 (64, 14344), (5, 2048 * 8 + 8)])
+                                 (64, 14344), (5, 2048 * 8 + 8),
+                                 # one row per CTA on 152 SMs; more rows per CTA than
+                                 # the pieces kernel's table (one warp per row); many
+                                 # pieces with a partial last one
+                                 (152, 4096), (10000, 1024), (2048, 65536 + 8)])
 def test_gemv_edge_shapes(tg, N, K):
     x, W = inputs.gemv_inputs(N, K, seed=N * 7 + K)
     compare(run_gemv(tg, x, W), oracle.gemv_f16(x.numpy(), W.numpy()), f"gemv {N}x{K}")
+
+
+def test_gemv_partial_piece_integer_bitexact(tg):
+    # Rows of 375 16-byte chunks: one whole piece and a partial one per row.
+    N, K = 1000, 3000
+    x = inputs.integer_f16((K,), seed=32)
+    W = inputs.integer_f16((N, K), seed=33)
+    assert_bitexact(run_gemv(tg, x, W), oracle.gemv_f16(x.numpy(), W.numpy()),
+                    "integer gemv, partial piece")
 
 
 def test_gemv_fp32_accumulation(tg):

@@ -211,8 +211,8 @@ int gemv_impl(int64_t N, int64_t K, const void* x, const void* W, void* y, void*
     if (!aligned16(x) || !aligned16(W) || !aligned16(y) || (K % 8) != 0) return TMAGEMM_ERR_ALIGN;
     DeviceState* d = nullptr;
     if (int s = device_state(&d)) return s;
-    cudaError_t e = launch_gemv(N, K, x, W, y, bf16, static_cast<cudaStream_t>(stream), d->err_word,
-                                t.pdl());
+    cudaError_t e = launch_gemv(N, K, x, W, y, bf16, d->sms, static_cast<cudaStream_t>(stream),
+                                d->err_word, t.pdl());
     return e == cudaSuccess ? TMAGEMM_OK : TMAGEMM_ERR_CUDA;
 }
 

@@ -54,6 +54,7 @@
 #include <atomic>
 #include <cmath>
 #include <cstdint>
+#include <vector>
 
 #include "launch.h"
 #include "ptx.cuh"
@@ -440,12 +441,12 @@ struct GroupedTProblem {
         int32_t g = 0;
         while (g + 1 < groups && tile_start[g + 1] <= u) ++g;
         const int32_t local = u - tile_start[g];
+        const int32_t tb = local / n_blocks, nb = local % n_blocks;
         const int32_t rows = m_off[g + 1] - m_off[g];
         // rows in 16-row steps, cut into tb blocks of q or q + 1 steps
         const int32_t steps = (rows + 15) / 16;
         const int32_t tb_count = (steps + maxw16 - 1) / maxw16;
         const int32_t q = steps / tb_count, extra = steps % tb_count;
-        const int32_t tb = local / n_blocks, nb = local % n_blocks;
         UnitInfo ui;
         ui.a_row = nb * BM;                                       // weight rows (D columns)
         const int32_t t0 = 16 * (tb * q + min(tb, extra));         // first row of the block
@@ -1351,7 +1352,8 @@ int64_t grouped_t_max_load(const int64_t* m_offsets, int64_t groups, int64_t n_b
                            int64_t maxw, int64_t c, int64_t slots, bool pair) {
     int64_t loads[1024] = {};
     if (slots > 1024) return -1;
-    int64_t u = 0;
+    // The cost of each row block, in the kernel's order of units.
+    std::vector<int64_t> costs;
     for (int64_t g = 0; g < groups; ++g) {
         const int64_t steps = ceil_div(m_offsets[g + 1] - m_offsets[g], 16);
         if (steps == 0) continue;
@@ -1359,10 +1361,12 @@ int64_t grouped_t_max_load(const int64_t* m_offsets, int64_t groups, int64_t n_b
         const int64_t q = steps / tb_count, extra = steps % tb_count;
         for (int64_t tb = 0; tb < tb_count; ++tb) {
             const int64_t w = 16 * (q + (tb < extra ? 1 : 0));
-            const int64_t cost = pair ? std::max(w, 128 + w / 2) : 128 + w;
-            for (int64_t nb = 0; nb < n_blocks; ++nb, ++u) loads[u % slots] += cost + c;
+            costs.push_back((pair ? std::max(w, 128 + w / 2) : 128 + w) + c);
         }
     }
+    int64_t u = 0;
+    for (const int64_t cost : costs)
+        for (int64_t nb = 0; nb < n_blocks; ++nb, ++u) loads[u % slots] += cost;
     int64_t worst = 0;
     for (int64_t s = 0; s < slots; ++s) worst = std::max(worst, loads[s]);
     return worst;

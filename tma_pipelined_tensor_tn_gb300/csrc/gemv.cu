@@ -5,9 +5,9 @@
 // algorithmic bytes at N = 4096, K = 14336), so the bound is HBM bandwidth, not
 // arithmetic ("Learning TileLang with GEMV", §02 Bandwidth Bound).  The page's
 // rules for a bandwidth-bound kernel (§07 Summary) decide the design:
-//   - enough independent work: one warp per output row gives N warps (4096 at
-//     the Llama-3-8B down-projection shape, about 27 per SM), all resident at
-//     once, so every warp gets the same HBM share and no SM tail remains;
+//   - enough independent work: N rows of K / 8 independent 16-byte loads
+//     (4096 rows of 1792 at the Llama-3-8B down-projection shape), spread over
+//     every SM at once;
 //   - coalesced: at every step the 32 lanes of a warp read 32 adjacent 16-byte
 //     chunks of the row, 512 contiguous bytes (§4.3 Coalescing);
 //   - wide: every load is 128 bits = 8 fp16 (§4.5 thread_vectorized_split_k).
@@ -20,6 +20,18 @@
 // Reduction: thread all-reduce lowered to shuffles) and y[n] is written once
 // with cvt.rn.  W is streamed with L1::no_allocate so it does not evict x,
 // which every warp re-reads from L1.  No atomics: results are deterministic.
+//
+// Two kernels share these rules.  gemv_pieces_kernel (the default wherever a
+// CTA's rows and a row's pieces fit its shared-memory table): one CTA per SM
+// takes N / SMs contiguous rows and cuts them into pieces of 3.5 KB that its
+// warps take in turn from a shared-memory counter, each warp issuing the next
+// piece's loads before it sums the current one (a row's last, shorter part is
+// summed after, by one warp per row).  A warp's share of the SM's
+// bandwidth varies from warp to warp, so a static one-row-per-warp split ends
+// when its slowest warp does; taking pieces in turn ends all warps of a CTA
+// together.  Each piece's sum goes to a fixed slot and a row adds its slots in
+// order, so which warp took which piece does not change the result.
+// gemv_f16_kernel (one warp per row, all resident at once) covers the rest.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
@@ -132,11 +144,108 @@ gemv_f16_kernel(const uint4* __restrict__ x, const uint4* __restrict__ W, uint16
     }
 }
 
+// ---- pieces: one CTA per SM, warps take 3.5 KB pieces of the CTA's rows ----
+constexpr int kPcWarps = 24;        // warps per CTA
+constexpr int kPcLoads = 7;         // 16-byte loads per lane per piece
+constexpr int32_t kPcChunks = 32 * kPcLoads;   // 16-byte chunks per piece (3.5 KB)
+constexpr int kPcMaxRows = 64;      // rows per CTA the slot table holds
+constexpr int kPcMaxPieces = 64;    // pieces per row the slot table holds
+
+template <bool BF16>
+__global__ void __launch_bounds__(kPcWarps * 32, 1)
+gemv_pieces_kernel(const uint4* __restrict__ x, const uint4* __restrict__ W,
+                   uint16_t* __restrict__ y, int32_t N, int32_t K8, uint32_t* __restrict__ err) {
+    grid_launch_dependents();
+    __shared__ int next_piece;
+    __shared__ float slot[kPcMaxRows][kPcMaxPieces];
+    const int lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
+    const int32_t r0 = static_cast<int32_t>(static_cast<int64_t>(blockIdx.x) * N / gridDim.x);
+    const int32_t r1 = static_cast<int32_t>(static_cast<int64_t>(blockIdx.x + 1) * N / gridDim.x);
+    const int32_t rows = r1 - r0;
+    // Whole pieces of a row, taken in turn; the rest of the row (fewer than
+    // kPcChunks chunks) is one more slot, summed by one warp per row after.
+    const int32_t pieces = K8 / kPcChunks;
+    const int32_t tail0 = pieces * kPcChunks;
+    const int32_t items = rows * pieces;
+    if (threadIdx.x == 0) next_piece = 0;
+    // While the previous grid finishes, pull the head of each of this CTA's
+    // rows into L2 (a prefetch cannot see stale data).
+    if (kGvPrefetchChunks > 0 && threadIdx.x < rows)
+        prefetch_l2_bytes(W + static_cast<int64_t>(r0 + threadIdx.x) * K8,
+                          static_cast<uint32_t>(min(K8, kGvPrefetchChunks)) * 16u);
+    __syncthreads();
+    grid_dependency_wait();   // x and W may come from the grid before this one
+    auto take = [&]() {
+        int v = 0;
+        if (lane == 0) v = atomicAdd(&next_piece, 1);
+        return __shfl_sync(0xffffffffu, v, 0);
+    };
+    // Piece `it` = row it / pieces, chunks [pc * kPcChunks, +kPcChunks) of it;
+    // lane l holds chunks pc * kPcChunks + l + 32 u.
+    auto load = [&](int it, uint4 (&w)[kPcLoads]) {
+        const int32_t row = it / pieces, pc = it % pieces;
+        const uint4* p = W + static_cast<int64_t>(r0 + row) * K8 + pc * kPcChunks + lane;
+#pragma unroll
+        for (int u = 0; u < kPcLoads; ++u) w[u] = ld_stream_v4(p + 32 * u);
+    };
+    uint4 wa[kPcLoads], wb[kPcLoads];
+    int cur = take();
+    if (cur < items) load(cur, wa);
+    while (cur < items) {
+        const int nxt = take();
+        if (nxt < items) load(nxt, wb);
+        const int32_t row = cur / pieces, pc = cur % pieces;
+        const int32_t base = pc * kPcChunks + lane;
+        float acc = 0.f;
+#pragma unroll
+        for (int u = 0; u < kPcLoads; ++u) acc = dot8<BF16>(wa[u], __ldg(x + base + 32 * u), acc);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+        if (lane == 0) slot[row][pc] = acc;
+#pragma unroll
+        for (int u = 0; u < kPcLoads; ++u) wa[u] = wb[u];
+        cur = nxt;
+    }
+    if (tail0 < K8) {
+        for (int32_t row = warp; row < rows; row += kPcWarps) {
+            const uint4* wrow = W + static_cast<int64_t>(r0 + row) * K8;
+            float acc = 0.f;
+            for (int32_t c = tail0 + lane; c < K8; c += 32)
+                acc = dot8<BF16>(ld_stream_v4(wrow + c), __ldg(x + c), acc);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+            if (lane == 0) slot[row][pieces] = acc;
+        }
+    }
+    __syncthreads();
+    if (threadIdx.x < rows) {
+        const int32_t slots = pieces + (tail0 < K8 ? 1 : 0);
+        float s = slot[threadIdx.x][0];
+        for (int32_t pc = 1; pc < slots; ++pc) s += slot[threadIdx.x][pc];
+        const int32_t n = r0 + static_cast<int32_t>(threadIdx.x);
+        if constexpr (BF16)
+            y[n] = __bfloat16_as_ushort(__float2bfloat16_rn(s));
+        else
+            y[n] = __half_as_ushort(__float2half_rn(s));
+        check_count_unit(err, n);   // checked build: output rows written
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y, bool bf16,
-                        cudaStream_t stream, uint32_t* err, bool pdl) {
+                        int num_sms, cudaStream_t stream, uint32_t* err, bool pdl) {
     const int32_t K8 = static_cast<int32_t>(K / 8);
+    const int64_t pieces = K8 / kPcChunks + (K8 % kPcChunks != 0 ? 1 : 0);   // slots per row
+    if (num_sms > 0 && N >= num_sms && (N + num_sms - 1) / num_sms <= kPcMaxRows &&
+        pieces <= kPcMaxPieces) {
+        auto kernel = bf16 ? gemv_pieces_kernel<true> : gemv_pieces_kernel<false>;
+        return launch_kernel(kernel, dim3(static_cast<unsigned>(num_sms)), dim3(kPcWarps * 32), 0,
+                             stream, 1u, pdl, static_cast<const uint4*>(x),
+                             static_cast<const uint4*>(W), static_cast<uint16_t*>(y),
+                             static_cast<int32_t>(N), K8, err);
+    }
     const int64_t blocks = (N + kGvWarps - 1) / kGvWarps;
     auto kernel = bf16 ? gemv_f16_kernel<true> : gemv_f16_kernel<false>;
     return launch_kernel(kernel, dim3(static_cast<unsigned>(blocks)), dim3(kGvWarps * 32), 0,

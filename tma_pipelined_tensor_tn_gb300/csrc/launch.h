@@ -172,10 +172,11 @@ void plan_grouped(const int64_t* m_offsets, int64_t groups, int64_t N, int num_s
 cudaError_t launch_grouped(const GroupedLaunch& g, int num_sms, int num_pairs, const GemmArgs& args,
                            cudaStream_t stream);
 
-// Enqueue the GEMV kernel: y[n] = sum_k x[k] * W[n][k]; one warp per row;
-// fp16 or bf16 operands and output.
+// Enqueue the GEMV: y[n] = sum_k x[k] * W[n][k]; fp16 or bf16 operands and
+// output.  One CTA per SM taking pieces of its rows where N / num_sms rows and
+// their pieces fit the CTA's slot table, else one warp per row.
 cudaError_t launch_gemv(int64_t N, int64_t K, const void* x, const void* W, void* y, bool bf16,
-                        cudaStream_t stream, uint32_t* err, bool pdl);
+                        int num_sms, cudaStream_t stream, uint32_t* err, bool pdl);
 
 // cudaLaunchKernelEx with a cluster of `cluster_x` CTAs along x (1 = none)
 // and, when `pdl` is set, the programmatic-stream-serialization attribute
