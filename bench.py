@@ -484,9 +484,9 @@ def run_ours(args, rank, world, local_rank):
                      "traffic": load_traffic("gemm_tn_f16_kernel@gemm_4096"),
                      "peak_source": f"{peak_src} bf16_tflops (burst; fp16 dense = bf16 dense)",
                      "flops_per_launch": gemm_flops()},
-        "roofline_gemv": {"bound": "hbm", "kernel": "gemv_f16_kernel", "achieved": gemv_gbs,
+        "roofline_gemv": {"bound": "hbm", "kernel": "gemv_pieces_kernel", "achieved": gemv_gbs,
                           "peak": peak_h, "unit": "GB/s", "frac": gemv_gbs / peak_h,
-                          "traffic": load_traffic("gemv_f16_kernel@gemv_4096x14336"),
+                          "traffic": load_traffic("gemv_pieces_kernel@gemv_4096x14336"),
                           "peak_source": f"{peak_src} hbm_gbs",
                           "bytes_per_launch": gemv_bytes()},
         "e2e": {"value": e2e_steps * gemm_flops() / (e2e_ms / 1e3) / 1e12 * world, "unit": "TFLOP/s",
