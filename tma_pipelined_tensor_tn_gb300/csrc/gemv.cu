@@ -145,7 +145,7 @@ gemv_f16_kernel(const uint4* __restrict__ x, const uint4* __restrict__ W, uint16
 }
 
 // ---- pieces: one CTA per SM, warps take 3.5 KB pieces of the CTA's rows ----
-constexpr int kPcWarps = 24;        // warps per CTA
+constexpr int kPcWarps = 28;        // warps per CTA
 constexpr int kPcLoads = 7;         // 16-byte loads per lane per piece
 constexpr int32_t kPcChunks = 32 * kPcLoads;   // 16-byte chunks per piece (3.5 KB)
 constexpr int kPcMaxRows = 64;      // rows per CTA the slot table holds
