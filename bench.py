@@ -15,6 +15,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -33,10 +34,14 @@ GEMV_N, GEMV_K = 4096, 14336
 WORKLOAD = ("gemm_f16 TN D=A*B^T M=N=K=4096, A,B ~ U[-1,1] fp16, fp32 accumulate, fp16 out; "
             "+ gemv_f16 y=x*W^T N=4096 K=14336, x,W ~ N(0,0.02) fp16")
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-KERNEL_SOURCES = ["tma_pipelined_tensor_tn_gb300/csrc/gemm_tn.cu",
-                  "tma_pipelined_tensor_tn_gb300/csrc/gemv.cu",
-                  "tma_pipelined_tensor_tn_gb300/csrc/ptx.cuh",
-                  "tma_pipelined_tensor_tn_gb300/csrc/tile_sched.cuh"]
+# The sources each committed DRAM-traffic capture depends on (by key prefix).
+KERNEL_SOURCES = {
+    "gemm_tn_f16_kernel": ["tma_pipelined_tensor_tn_gb300/csrc/gemm_tn.cu",
+                           "tma_pipelined_tensor_tn_gb300/csrc/ptx.cuh",
+                           "tma_pipelined_tensor_tn_gb300/csrc/tile_sched.cuh"],
+    "gemv_pieces_kernel": ["tma_pipelined_tensor_tn_gb300/csrc/gemv.cu",
+                           "tma_pipelined_tensor_tn_gb300/csrc/ptx.cuh"],
+}
 
 
 def gemm_flops(M=GEMM_M, N=GEMM_N, K=GEMM_K):
@@ -71,11 +76,19 @@ def whole_job_value(units_per_step, steps, world, total_seconds):
     return world * steps * units_per_step / total_seconds
 
 
-def sources_hash():
+def _code_only(text):
+    """C/C++ source without comments and whitespace: a capture stays valid
+    across comment edits, not across code changes."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
+def sources_hash(kernel):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -99,7 +112,8 @@ def load_traffic(key):
     except (OSError, ValueError):
         return None
     e = d.get(key)
-    if not e or e.get("sources_hash") != sources_hash():
+    kernel = key.split("@")[0]
+    if not e or kernel not in KERNEL_SOURCES or e.get("sources_hash") != sources_hash(kernel):
         return None
     return e.get("bytes_per_launch")
 

@@ -61,6 +61,18 @@ def _rank_main(rank, world, port, out_dir):
         dist.destroy_process_group()
 
 
+def test_traffic_capture_survives_comment_edits_not_code_edits():
+    src = 'int f(int a) {  // sum\n  /* the body */\n  return a + 1;\n}\n'
+    reworded = 'int f(int a) {  // the sum, reworded\n  return a + 1;  /* note */\n}\n'
+    changed = 'int f(int a) {  // sum\n  return a + 2;\n}\n'
+    assert bench._code_only(src) == bench._code_only(reworded)
+    assert bench._code_only(src) != bench._code_only(changed)
+    # every committed capture names a kernel whose sources the bench knows
+    with open(os.path.join(os.path.dirname(bench.__file__), "profiles", "dram_traffic.json")) as f:
+        keys = json.load(f)
+    assert keys and all(k.split("@")[0] in bench.KERNEL_SOURCES for k in keys)
+
+
 def test_max_over_ranks_two_gloo_ranks(tmp_path):
     mp = pytest.importorskip("torch.multiprocessing")
     port = _free_port()

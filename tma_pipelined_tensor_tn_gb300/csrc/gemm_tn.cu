@@ -399,9 +399,8 @@ struct GroupedProblem {
 // tb_count(g) blocks of nearly equal width (multiples of 16, at most maxw16 *
 // 16): no block is padded by more than 15 rows.  A block of w rows loads
 // only those rows of A (w / CTAs per tile per CTA), through the map for its
-// width: below 256 the loads, not the MMAs, set a unit's time, so a box of
-// the full 256 (128 per CTA) rows would cost a narrow block as much as a
-// wide one.  Units run group by group,
+// width, so a narrow block moves no more bytes than it uses.  Units run group
+// by group,
 // and within a group a block of rows against every weight block in turn, so
 // a group's weights and rows are reused from L2 while the group runs.
 struct GroupedTProblem {
@@ -1344,10 +1343,10 @@ namespace {
 // Largest per-slot load of the transposed grouped schedule (units in the
 // order GroupedTProblem numbers them, slot = unit mod slots): the sum over a
 // slot's units of (cost of a block of width w + c), in the row-tiled plan's
-// unit (one column of a 256-row pair tile per k-block).  A k-block of a block
-// costs the larger of its MMA (w) and its loads: 128 weight rows and w / 2
-// rows of A per CTA of a pair (w for a single CTA), where 256 rows' bytes
-// take as long as a 256-column MMA.
+// unit (one column of a 256-row pair tile per k-block).  The model charges a
+// k-block of a block the larger of its MMA (w) and its loads: 128 weight rows
+// and w / 2 rows of A per CTA of a pair (w for a single CTA), counting 256
+// rows' bytes as long as a 256-column MMA.
 int64_t grouped_t_max_load(const int64_t* m_offsets, int64_t groups, int64_t n_blocks,
                            int64_t maxw, int64_t c, int64_t slots, bool pair) {
     int64_t loads[1024] = {};
