@@ -65,6 +65,18 @@ def test_gemv_edge_shapes(tg, N, K):
     compare(run_gemv(tg, x, W), oracle.gemv_f16(x.numpy(), W.numpy()), f"gemv {N}x{K}")
 
 
+def test_gemv_pieces_table_limits(tg):
+    # The pieces kernel holds up to 64 rows per CTA (one CTA per SM) and 64
+    # slots per row (pieces of 224 16-byte chunks and a shorter last part):
+    # exactly at each limit, and one past it (where the one-warp-per-row
+    # kernel takes over).
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    for N, K in [(64 * sms, 1024), (64 * sms + 1, 1024), (256, 64 * 224 * 8),
+                 (256, 63 * 224 * 8 + 8), (256, 64 * 224 * 8 + 8)]:
+        x, W = inputs.gemv_inputs(N, K, seed=N + K)
+        compare(run_gemv(tg, x, W), oracle.gemv_f16(x.numpy(), W.numpy()), f"gemv {N}x{K}")
+
+
 def test_gemv_partial_piece_integer_bitexact(tg):
     # Rows of 375 16-byte chunks: one whole piece and a partial one per row.
     N, K = 1000, 3000
