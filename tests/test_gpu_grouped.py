@@ -150,6 +150,21 @@ def test_grouped_every_block_width_integer_bitexact(tg, formulation):
                     f"grouped widths {formulation}")
 
 
+def test_grouped_full_width_blocks_integer_bitexact(tg, formulation):
+    """Groups of exactly 256 rows (in the transposed form a block as wide as a
+    tile, through the widest map of A), next to 250-, 17-, 512- and 1-row
+    groups: integer inputs match the oracle bit for bit in every formulation."""
+    counts = [256, 256, 256, 256, 250, 17, 512, 1]
+    offs = [0]
+    for c in counts:
+        offs.append(offs[-1] + c)
+    G, N, K = len(counts), 2048, 256
+    A = inputs.integer_f16((offs[-1], K), seed=96)
+    B = inputs.integer_f16((G, N, K), seed=97)
+    assert_bitexact(run(tg, A, B, offs), oracle.gemm_f16_grouped(A.numpy(), B.numpy(), offs),
+                    f"grouped 256-row blocks {formulation}")
+
+
 def test_grouped_transposed_writes_only_group_rows(tg):
     """Transposed stores clip at each group's last row and at N: rows of D
     past the groups keep their contents, and every group row is written."""
